@@ -1,1 +1,166 @@
-"""GB300-native chunkwise Gated DeltaNet prefill (placeholder, binding added with the C-ABI)."""
+"""GB300-native chunkwise Gated DeltaNet (GDN) prefill.
+
+Python binding of the C ABI in include/gdn.h. Argument marshalling only: every
+step of the computation runs in the CUDA kernels of libgdn_gb300.so, and there
+is no CPU or PyTorch fallback (a missing library raises).
+
+The entry point mirrors ``gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias,
+state_pool, cache_indices, cu_seqlens, chunk_size=64)`` of the pymllm page
+"pymllm.layers.attention.gdn_chunkwise" (Module Contents): same arguments, same
+shapes, state_pool updated in place, output returned in v's dtype.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import GdnError
+
+__all__ = ["gdn_extend_chunkwise", "gdn_workspace_size", "gdn_get_device_status", "GdnError",
+           "library_path", "version"]
+
+_ws_cache: dict = {}
+
+
+def library_path() -> str:
+    return _lib.lib_path()
+
+
+def version() -> int:
+    return int(_lib.load().gdn_version())
+
+
+def gdn_workspace_size(total_tokens: int, batch: int, H: int, HV: int, K: int, V: int, chunk_size: int) -> int:
+    return int(_lib.load().gdn_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size))
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    key = (device.index,)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _aligned_ptr(buf: torch.Tensor) -> int:
+    p = buf.data_ptr()
+    return (p + 255) & ~255
+
+
+def _req(t: torch.Tensor, name: str, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, cu_seqlens,
+                         chunk_size: int = 64, *, scale: float = 1.0, out: torch.Tensor = None,
+                         workspace: torch.Tensor = None, check: bool = False, stream=None) -> torch.Tensor:
+    """Chunkwise GDN prefill; returns ``out [total_tokens, HV, V]`` in v's dtype.
+
+    q, k ``[T, H, K]``, v ``[T, HV, V]`` bf16 on one CUDA device; a, b ``[T, HV]``,
+    A_log, dt_bias ``[HV]`` fp32; state_pool ``[pool, HV, V, K]`` fp32 (updated in
+    place); cache_indices ``[B]`` and cu_seqlens ``[B+1]`` int64 on the same device.
+    ``check=True`` waits for the device and raises on a device-detected error
+    (bad cache index or cu_seqlens).
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_extend_chunkwise runs on a CUDA device; move the inputs there first")
+    act = (torch.bfloat16, torch.float16)
+    _req(q, "q", act, dev)
+    _req(k, "k", q.dtype, dev)
+    _req(v, "v", q.dtype, dev)
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias), ("state_pool", state_pool)):
+        _req(t, name, torch.float32, dev)
+    _req(cache_indices, "cache_indices", torch.int64, dev)
+    _req(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
+        raise ValueError(f"bad q/k/v shapes {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    if a.shape != (T, HV) or b.shape != (T, HV) or A_log.shape != (HV,) or dt_bias.shape != (HV,):
+        raise ValueError("a, b must be [T, HV] and A_log, dt_bias [HV]")
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, V, K):
+        raise ValueError(f"state_pool must be [pool, {HV}, {V}, {K}], got {tuple(state_pool.shape)}")
+    B = cache_indices.shape[0]
+    if cu_seqlens.shape != (B + 1,):
+        raise ValueError("cu_seqlens must have batch + 1 entries")
+    if out is None:
+        out = torch.empty((T, HV, V), dtype=v.dtype, device=dev)
+    else:
+        _req(out, "out", v.dtype, dev)
+        if tuple(out.shape) != (T, HV, V):
+            raise ValueError("out must be [T, HV, V]")
+    L = _lib.load()
+    need = int(L.gdn_workspace_size(T, B, H, HV, K, V, chunk_size))
+    if need == 0:
+        raise GdnError(2, f"unsupported sizes (K={K}, V={V}, chunk_size={chunk_size}, H={H}, HV={HV})")
+    if workspace is None:
+        ws = _workspace(dev, need)
+        ws_ptr, ws_bytes = _aligned_ptr(ws), ws.numel() - (_aligned_ptr(ws) - ws.data_ptr())
+    else:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dtype_code = _lib.GDN_BF16 if q.dtype == torch.bfloat16 else _lib.GDN_FP16
+    st = L.gdn_extend_chunkwise(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype_code,
+        a.data_ptr(), b.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr(),
+        state_pool.data_ptr(), state_pool.shape[0], cache_indices.data_ptr(), cu_seqlens.data_ptr(), B,
+        out.data_ptr(), T, H, HV, K, V, int(chunk_size), float(scale), ws_ptr, ws_bytes, sp)
+    _lib.check(st, "gdn_extend_chunkwise")
+    if check:
+        _lib.check(L.gdn_get_device_status(ws_ptr, sp), "gdn_extend_chunkwise (device)")
+    return out
+
+
+def gdn_get_device_status(device=None, stream=None) -> int:
+    """Status recorded by the last call on ``device`` that used the cached workspace."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    ws = _ws_cache.get((dev.index,))
+    if ws is None:
+        return 0
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return int(_lib.load().gdn_get_device_status(_aligned_ptr(ws), stream.cuda_stream))
+
+
+class KernelProfile:
+    """Per-kernel device time of the library's launches between start() and stop().
+
+    Each kernel is bracketed by CUDA events on the stream it is launched on.
+    """
+
+    def __init__(self, max_launches: int = 100000):
+        self.max_launches = max_launches
+        self.result = {}
+
+    def start(self):
+        _lib.check(_lib.load().gdn_profile_start(self.max_launches), "gdn_profile_start")
+        return self
+
+    def stop(self) -> dict:
+        import ctypes
+        L = _lib.load()
+        n = 16
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        k = L.gdn_profile_stop(ms, cnt, n)
+        if k < 0:
+            raise GdnError(6, "gdn_profile_stop failed")
+        self.result = {L.gdn_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(k)}
+        return self.result
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(_lib.load().gdn_launch_count())

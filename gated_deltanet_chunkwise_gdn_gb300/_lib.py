@@ -1,0 +1,80 @@
+"""ctypes loader for libgdn_gb300.so (the C ABI of include/gdn.h).
+
+There is no fallback: if the library cannot be loaded (or built), every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS_NAMES = {
+    0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_BAD_INDEX",
+    4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_CUDA", 7: "GDN_ERR_BAD_SEQLENS",
+}
+GDN_BF16, GDN_FP16 = 0, 1
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = True):
+    """Load the shared library (building it first if it is missing and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libgdn_gb300.so not found at {path}; run __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        i32, i64, f32, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        L.gdn_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+        L.gdn_workspace_size.restype = sz
+        L.gdn_extend_chunkwise.argtypes = [
+            vp, vp, vp, ctypes.c_int,      # q k v dtype
+            vp, vp, vp, vp,                # a b A_log dt_bias
+            vp, i64, vp, vp, i32,          # state_pool pool_size cache_indices cu_seqlens batch
+            vp, i64, i32, i32, i32, i32,   # out total_tokens H HV K V
+            i32, f32, vp, sz, vp]          # chunk_size scale workspace bytes stream
+        L.gdn_extend_chunkwise.restype = ctypes.c_int
+        L.gdn_get_device_status.argtypes = [vp, vp]
+        L.gdn_get_device_status.restype = ctypes.c_int
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_profile_start.argtypes = [i32]
+        L.gdn_profile_start.restype = ctypes.c_int
+        L.gdn_profile_stop.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64), i32]
+        L.gdn_profile_stop.restype = i32
+        L.gdn_kernel_name.argtypes = [i32]
+        L.gdn_kernel_name.restype = ctypes.c_char_p
+        L.gdn_launch_count.argtypes = []
+        L.gdn_launch_count.restype = i64
+        L.gdn_version.argtypes = []
+        L.gdn_version.restype = i32
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def check(status: int, what: str):
+    if status != 0:
+        raise GdnError(status, f"{what}: {status_string(status)}")

@@ -1,0 +1,217 @@
+// gdn_api.cu — host side of the C ABI declared in include/gdn.h: argument checks,
+// workspace carve-up and the launch sequence K0 (schedule) -> K2 (intra) -> K3 (scan).
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "gdn_common.cuh"
+
+namespace {
+
+// ---------------------------------------------------------------- instrumentation
+enum KernelId { kKernSchedule = 0, kKernIntra = 1, kKernScan = 2, kKernCount = 3 };
+const char* const kKernelNames[kKernCount] = {"schedule", "intra", "scan"};
+
+std::atomic<int64_t> g_launches{0};
+
+struct ProfRecord {
+  int id;
+  cudaEvent_t start, stop;
+};
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  int capacity = 0;
+  std::vector<ProfRecord> recs;
+  std::vector<cudaEvent_t> pool;  // created at start, 2 per allowed launch
+} g_prof;
+
+// Records the start event of kernel `id` on stream s; returns the record index or -1.
+int prof_begin(int id, cudaStream_t s) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.on || (int)g_prof.recs.size() >= g_prof.capacity) return -1;
+  const int i = (int)g_prof.recs.size();
+  ProfRecord r{id, g_prof.pool[2 * i], g_prof.pool[2 * i + 1]};
+  if (cudaEventRecord(r.start, s) != cudaSuccess) return -1;
+  g_prof.recs.push_back(r);
+  return i;
+}
+void prof_end(int rec, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (rec < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  cudaEventRecord(g_prof.recs[rec].stop, s);
+}
+
+constexpr int kSmCountHint = 152;  // GB300: 2 dies x 76 SMs
+
+bool supported_shape(int K, int V, int C) {
+  if (K != V) return false;
+  return (K == 64 || K == 128) && C == 64;
+}
+
+// Value-dimension split of the scan: enough (sequence, head, block) CTAs to cover
+// the SMs twice, with blocks of at least 16 state rows.
+int choose_nvb(int B, int HV, int V) {
+  const int64_t chains = (int64_t)B * HV;
+  if (chains * (V / 32) >= 2 * kSmCountHint) return V / 32;
+  return V / 16;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K, int32_t V,
+                          int32_t chunk_size) {
+  if (total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || batch < 0 || H <= 0 || HV <= 0 || HV % H != 0)
+    return 0;
+  if (!supported_shape(K, V, chunk_size)) return 0;
+  return gdn::make_layout(total_tokens, batch, H, HV, K, V, chunk_size).total;
+}
+
+gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* a,
+                                const float* b, const float* A_log, const float* dt_bias, float* state_pool,
+                                int64_t pool_size, const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                int32_t batch, void* out, int64_t total_tokens, int32_t H, int32_t HV, int32_t K,
+                                int32_t V, int32_t chunk_size, float scale, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (batch < 0 || total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || H <= 0 || HV <= 0 || HV % H != 0 ||
+      K <= 0 || V <= 0 || chunk_size <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_BF16 && dtype != GDN_FP16) return GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !A_log || !dt_bias) return GDN_ERR_INVALID_ARG;
+  if (batch > 0 && (!state_pool || !cache_indices || pool_size <= 0)) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
+  if (!supported_shape(K, V, chunk_size) || dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, chunk_size);
+  if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return GDN_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  gdn::Params p{};
+  p.q = static_cast<const gdn::bf16*>(q);
+  p.k = static_cast<const gdn::bf16*>(k);
+  p.v = static_cast<const gdn::bf16*>(v);
+  p.a = a;
+  p.b = b;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.state_pool = state_pool;
+  p.cache_indices = cache_indices;
+  p.cu_seqlens = cu_seqlens;
+  p.out = static_cast<gdn::bf16*>(out);
+  p.T = total_tokens;
+  p.pool_size = pool_size;
+  p.B = batch;
+  p.H = H;
+  p.HV = HV;
+  p.nvb = choose_nvb(batch, HV, V);
+  p.scale = scale;
+  p.max_chunks = L.max_chunks;
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  p.seq_chunk_off = reinterpret_cast<int32_t*>(ws + L.seq_chunk_off);
+  p.order = reinterpret_cast<int32_t*>(ws + L.order);
+  p.chunk_tab = reinterpret_cast<int4*>(ws + L.chunk_tab);
+  p.g = reinterpret_cast<float*>(ws + L.g);
+  p.rq = reinterpret_cast<float*>(ws + L.rq);
+  p.rk = reinterpret_cast<float*>(ws + L.rk);
+  p.W = reinterpret_cast<gdn::bf16*>(ws + L.w);
+  p.U = reinterpret_cast<gdn::bf16*>(ws + L.u);
+  p.P = reinterpret_cast<gdn::bf16*>(ws + L.p);
+
+  int rec = prof_begin(kKernSchedule, s);
+  gdn::schedule_kernel<<<1, 512, 0, s>>>(p, chunk_size);
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
+  if (total_tokens == 0 || batch == 0) return GDN_OK;
+  rec = prof_begin(kKernIntra, s);
+  if (gdn::launch_intra(p, K, chunk_size, s) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
+  rec = prof_begin(kKernScan, s);
+  if (gdn::launch_scan(p, K, chunk_size, s) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
+  return GDN_OK;
+}
+
+gdn_status gdn_get_device_status(const void* workspace, void* stream) {
+  if (!workspace) return GDN_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t st = 0;
+  if (cudaMemcpyAsync(&st, workspace, sizeof st, cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (st < 0 || st > GDN_ERR_BAD_SEQLENS) return GDN_ERR_CUDA;
+  return static_cast<gdn_status>(st);
+}
+
+const char* gdn_status_string(gdn_status status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer, bad size or HV not a multiple of H";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: head size, chunk size or dtype not built";
+    case GDN_ERR_BAD_INDEX: return "GDN_ERR_BAD_INDEX: cache index out of range or repeated";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace null, too small or not 256-byte aligned";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
+    case GDN_ERR_BAD_SEQLENS: return "GDN_ERR_BAD_SEQLENS: cu_seqlens not 0..total_tokens non-decreasing";
+  }
+  return "GDN_ERR_UNKNOWN";
+}
+
+gdn_status gdn_profile_start(int32_t max_launches) {
+  if (max_launches <= 0) return GDN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  for (cudaEvent_t e : g_prof.pool) cudaEventDestroy(e);
+  g_prof.pool.clear();
+  g_prof.recs.clear();
+  g_prof.on = false;
+  for (int i = 0; i < 2 * max_launches; ++i) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (cudaEvent_t x : g_prof.pool) cudaEventDestroy(x);
+      g_prof.pool.clear();
+      return GDN_ERR_CUDA;
+    }
+    g_prof.pool.push_back(e);
+  }
+  g_prof.recs.reserve(max_launches);
+  g_prof.capacity = max_launches;
+  g_prof.on = true;
+  return GDN_OK;
+}
+
+int32_t gdn_profile_stop(double* total_ms, int64_t* launches, int32_t n_slots) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (!g_prof.on) return -1;
+  g_prof.on = false;
+  int ok = 1;
+  for (int i = 0; i < n_slots; ++i) {
+    if (total_ms) total_ms[i] = 0.0;
+    if (launches) launches[i] = 0;
+  }
+  for (const ProfRecord& r : g_prof.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+      ok = 0;
+      continue;
+    }
+    if (r.id < n_slots) {
+      if (total_ms) total_ms[r.id] += ms;
+      if (launches) launches[r.id] += 1;
+    }
+  }
+  for (cudaEvent_t e : g_prof.pool) cudaEventDestroy(e);
+  g_prof.pool.clear();
+  g_prof.recs.clear();
+  return ok ? kKernCount : -1;
+}
+
+const char* gdn_kernel_name(int32_t id) { return (id >= 0 && id < kKernCount) ? kKernelNames[id] : nullptr; }
+
+int64_t gdn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t gdn_version(void) { return 100; }
+
+}  // extern "C"

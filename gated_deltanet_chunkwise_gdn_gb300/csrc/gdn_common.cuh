@@ -1,0 +1,175 @@
+// gdn_common.cuh — shared definitions of the GB300 chunkwise GDN prefill kernels.
+//
+// Notation (per chunk of C tokens of one sequence, one value head):
+//   g_i      = sum_{j<=i in chunk} log alpha_j          (chunk-local log decay, <= 0)
+//   Gamma    = exp(g_mu - g_nu) for mu >= nu           ("Simple math to speed up GDN
+//                                                       prefill", section "Reminder")
+//   M        = I + tril(diag(beta) K^ K^^T, -1)
+//   A        = (Gamma . M^{-1}) diag(beta) = N^{-1} B   (section "Save one invert")
+//   W<-      = A diag(exp(g)) K^                       (C x K, decayed WY keys)
+//   U~       = A V                                     (C x V, decayed WY values)
+//   P        = Gamma . tril(Q^ K^^T)                   (C x C, causal intra-chunk scores)
+// and the chunk step on the state S (V x K):
+//   U   = U~ - W<- S^T
+//   O   = diag(exp(g)) Q^ S^T + P U
+//   S  <- exp(g_C) S + U^T diag(exp(g_C - g)) K^
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+using bf16 = __nv_bfloat16;
+
+constexpr float kNormEps = 1e-6f;  // q^ = q / sqrt(|q|^2 + eps)
+
+// ----------------------------------------------------------------------------- workspace
+
+// Offsets (bytes) of the workspace regions for one call. Every region starts on a
+// 256-byte boundary.
+struct WsLayout {
+  size_t status;         // int32[64]: [0] status code, [1] number of chunks
+  size_t seq_chunk_off;  // int32[B+1]: first chunk of each sequence
+  size_t order;          // int32[B]: sequences, longest first
+  size_t chunk_tab;      // int4[max_chunks]: (seq, first token, length, chunk index in seq)
+  size_t g;              // fp32[max_chunks][HV][C]: chunk-local cumulative log decay
+  size_t rq;             // fp32[max_chunks][H][C]: 1/|q| per row (0 on padded rows)
+  size_t rk;             // fp32[max_chunks][H][C]: 1/|k| per row (0 on padded rows)
+  size_t w;              // bf16[max_chunks][HV][C][K]: W<-
+  size_t u;              // bf16[max_chunks][HV][C][V]: U~
+  size_t p;              // bf16[max_chunks][HV][C][C]: P
+  size_t total;
+  int64_t max_chunks;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C) {
+  WsLayout L{};
+  const int64_t mc = T / C + B + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  L.max_chunks = mc;
+  L.status = take(64 * sizeof(int32_t));
+  L.seq_chunk_off = take((size_t)(B + 1) * sizeof(int32_t));
+  L.order = take((size_t)(B > 0 ? B : 1) * sizeof(int32_t));
+  L.chunk_tab = take((size_t)mc * sizeof(int4));
+  L.g = take((size_t)mc * HV * C * sizeof(float));
+  L.rq = take((size_t)mc * H * C * sizeof(float));
+  L.rk = take((size_t)mc * H * C * sizeof(float));
+  L.w = take((size_t)mc * HV * C * K * sizeof(bf16));
+  L.u = take((size_t)mc * HV * C * V * sizeof(bf16));
+  L.p = take((size_t)mc * HV * C * C * sizeof(bf16));
+  L.total = off;
+  return L;
+}
+
+// ----------------------------------------------------------------------------- launch params
+
+struct Params {
+  const bf16* q;
+  const bf16* k;
+  const bf16* v;
+  const float* a;
+  const float* b;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  const int64_t* cache_indices;
+  const int64_t* cu_seqlens;
+  bf16* out;
+  int64_t T;
+  int64_t pool_size;
+  int B, H, HV;
+  int nvb;  // value-dimension blocks per (sequence, value head) chain in the scan
+  float scale;
+  int64_t max_chunks;
+  // workspace regions
+  int32_t* status;
+  int32_t* seq_chunk_off;
+  int32_t* order;
+  int4* chunk_tab;
+  float* g;
+  float* rq;
+  float* rk;
+  bf16* W;
+  bf16* U;
+  bf16* P;
+};
+
+// ----------------------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async_16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Status word: the first error recorded wins.
+__device__ __forceinline__ void set_status(int32_t* status, int code) {
+  atomicCAS(reinterpret_cast<int*>(status), 0, code);
+}
+
+// ----------------------------------------------------------------------------- kernels
+
+// K0: validates cu_seqlens / cache_indices, builds the chunk table and the
+// longest-first sequence order. One block.
+__global__ void schedule_kernel(Params p, int C);
+
+// Host-side launchers (one per translation unit, templated on head size).
+cudaError_t launch_intra(const Params& p, int D, int C, cudaStream_t s);
+cudaError_t launch_scan(const Params& p, int D, int C, cudaStream_t s);
+
+}  // namespace gdn

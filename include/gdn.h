@@ -1,0 +1,155 @@
+/*
+ * gdn.h — C ABI of the GB300 chunkwise Gated DeltaNet prefill library (libgdn_gb300.so).
+ *
+ * The operation
+ * -------------
+ * gdn_extend_chunkwise runs the Gated DeltaNet recurrence over a packed batch of
+ * prompts ("extend" / prefill), reading and writing each prompt's recurrent state
+ * in a pooled state buffer. It follows the interface documented for
+ * gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices,
+ * cu_seqlens, chunk_size=64) on the pymllm page "pymllm.layers.attention.gdn_chunkwise"
+ * (section "Module Contents", Parameters and Returns), and computes, for every
+ * sequence b and value head hv (q/k head h = hv / (HV/H)), token by token:
+ *
+ *   S  = state_pool[cache_indices[b], hv]                            (V x K, fp32)
+ *   q^ = q[t,h] / sqrt(|q[t,h]|^2 + 1e-6),   k^ likewise
+ *   alpha = exp(-exp(A_log[hv]) * softplus(a[t,hv] + dt_bias[hv]))
+ *   beta  = sigmoid(b[t,hv])
+ *   S  = S (alpha (I - beta k^ k^T)) + beta v[t,hv] k^T
+ *   out[t,hv] = scale * S q^
+ *
+ * The state transition is the one in "Simple math to speed up GDN prefill"
+ * (section "Reminder"); a token reads the state after its own write
+ * ("nrm-training-kernels", section "General implementation", item 4). The
+ * library evaluates it chunkwise in WY form with one triangular inverse per chunk,
+ * the decayed factor taken from N^{-1} = G M^{-1} G^{-1} ("Simple math to speed up
+ * GDN prefill", section "Save one invert"). Results equal the recurrence up to
+ * rounding; chunk_size does not change them beyond rounding.
+ *
+ * Memory, layout, ownership
+ * -------------------------
+ * Every array pointer is a DEVICE pointer, dense and row-major with the last
+ * index fastest. The caller owns every buffer; the library allocates nothing
+ * per call and keeps no pointer after the call returns.
+ *
+ * Execution
+ * ---------
+ * The call validates its host-side arguments, then enqueues its kernels on
+ * `stream` (a cudaStream_t; NULL means the legacy default stream) and returns
+ * without waiting. Errors that need device data (cu_seqlens, cache_indices) are
+ * detected by the first kernel, which records a status in the workspace; all
+ * later kernels of that call then do nothing, so state_pool is left untouched
+ * and `out` is left unwritten. Read that status with gdn_get_device_status.
+ * Calls on one stream are ordered; two calls that share a workspace must not
+ * run concurrently on different streams. No exception crosses this interface.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad size or HV % H != 0            */
+  GDN_ERR_UNSUPPORTED = 2,  /* (K, V, chunk_size, dtype) not built                */
+  GDN_ERR_BAD_INDEX = 3,    /* cache index outside [0, pool_size) or repeated     */
+  GDN_ERR_WORKSPACE = 4,    /* workspace null, too small or misaligned            */
+  GDN_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up                 */
+  GDN_ERR_CUDA = 6,         /* a CUDA runtime call failed                         */
+  GDN_ERR_BAD_SEQLENS = 7   /* cu_seqlens[0] != 0, decreasing, or last != total   */
+} gdn_status;
+
+typedef enum { GDN_BF16 = 0, GDN_FP16 = 1 } gdn_dtype;
+
+/*
+ * Bytes of device workspace one gdn_extend_chunkwise call needs for these sizes.
+ * Returns 0 if the sizes are invalid or not supported. The workspace must be
+ * 256-byte aligned. It holds the call's status word, the chunk schedule and the
+ * per-chunk WY factors; it needs no initialisation and may be reused by later
+ * calls on the same stream.
+ */
+GDN_API size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K,
+                          int32_t V, int32_t chunk_size);
+
+/*
+ * Chunkwise GDN prefill over a packed varlen batch.
+ *
+ *  q, k          [total_tokens, H, K]   bf16 or fp16 (dtype); q and k are NOT pre-normalised.
+ *  v             [total_tokens, HV, V]  same dtype.
+ *  a             [total_tokens, HV]     fp32, raw decay-gate input (before softplus/exp).
+ *  b             [total_tokens, HV]     fp32, raw update-gate input (before sigmoid).
+ *  A_log, dt_bias [HV]                  fp32.
+ *  state_pool    [pool_size, HV, V, K]  fp32, read and overwritten in place for the
+ *                                       slots named by cache_indices; other slots untouched.
+ *  cache_indices [batch]                int64, pool slot of each sequence; distinct, in range.
+ *  cu_seqlens    [batch + 1]            int64, cu_seqlens[0] = 0, non-decreasing,
+ *                                       cu_seqlens[batch] = total_tokens. Zero-length
+ *                                       sequences are allowed and leave their slot as is.
+ *  out           [total_tokens, HV, V]  same dtype as v, written (round to nearest even).
+ *  H, HV         q/k heads and value heads; HV must be a multiple of H.
+ *  K, V          head sizes (supported: K = V in {64, 128}, plus 256 with chunk_size 128).
+ *  chunk_size    WY block length (supported: 64; 128 for K = V = 256).
+ *  scale         multiplies every output (1.0 reads o_t = S_t q_t as written).
+ *  workspace     device buffer of at least gdn_workspace_size(...) bytes, 256-byte aligned.
+ *  stream        cudaStream_t to enqueue on.
+ *
+ * Returns GDN_OK once the work is enqueued, or an error detected on the host, in
+ * which case nothing was enqueued and no buffer was touched.
+ */
+GDN_API gdn_status gdn_extend_chunkwise(const void *q, const void *k, const void *v, gdn_dtype dtype,
+                                const float *a, const float *b, const float *A_log,
+                                const float *dt_bias, float *state_pool, int64_t pool_size,
+                                const int64_t *cache_indices, const int64_t *cu_seqlens,
+                                int32_t batch, void *out, int64_t total_tokens, int32_t H,
+                                int32_t HV, int32_t K, int32_t V, int32_t chunk_size, float scale,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then returns the status recorded on the device by the last
+ * gdn_extend_chunkwise call that used this workspace (GDN_OK, GDN_ERR_BAD_INDEX,
+ * GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the stream reported
+ * an error. Synchronises the host with the stream.
+ */
+GDN_API gdn_status gdn_get_device_status(const void *workspace, void *stream);
+
+/* Static, human-readable name of a status. Never NULL. */
+GDN_API const char *gdn_status_string(gdn_status status);
+
+/*
+ * Instrumentation. gdn_profile_start makes every later gdn_extend_chunkwise call
+ * record a pair of CUDA events around each kernel it launches, on the call's own
+ * stream, for up to max_launches kernel launches in total (the events are created
+ * here, on the current device). gdn_profile_stop waits for those events, adds the
+ * elapsed time of each kernel kind into total_ms[id] and its launch count into
+ * launches[id] for id < n_slots, frees the events and returns the number of kernel
+ * kinds (ids 0 .. n-1; see gdn_kernel_name). Returns -1 if profiling was not started
+ * or an event failed. Not meant to be used while another thread issues calls.
+ */
+GDN_API gdn_status gdn_profile_start(int32_t max_launches);
+GDN_API int32_t gdn_profile_stop(double *total_ms, int64_t *launches, int32_t n_slots);
+
+/* Name of kernel kind `id` (as used by gdn_profile_stop), or NULL if out of range. */
+GDN_API const char *gdn_kernel_name(int32_t id);
+
+/* Total number of kernels this library has launched in the process so far. */
+GDN_API int64_t gdn_launch_count(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+GDN_API int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

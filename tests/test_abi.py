@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads, and exports every symbol include/gdn.h declares.
+
+CPU only: the calls made here return from host-side validation before any CUDA
+call (null pointers, unsupported sizes, bad workspace).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_chunkwise_gdn_gb300 import _lib, build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    return re.findall(r"GDN_API\s+[\w\s\*]*?\b(gdn_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert {"gdn_extend_chunkwise", "gdn_workspace_size", "gdn_get_device_status",
+            "gdn_status_string", "gdn_version"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gdn.h but not exported"
+
+
+def test_only_the_abi_is_exported(lib):
+    import subprocess
+    r = subprocess.run(["nm", "-D", "--defined-only", gbuild.LIB_PATH], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("nm not available")
+    exported = {ln.split()[-1] for ln in r.stdout.splitlines() if " T " in ln}
+    assert exported == set(_declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        s = lib.gdn_status_string(code).decode()
+        assert s.startswith(name)
+    assert lib.gdn_status_string(99).decode() == "GDN_ERR_UNKNOWN"
+    assert lib.gdn_version() >= 100
+
+
+def test_workspace_size_rules(lib):
+    ws = lib.gdn_workspace_size
+    assert ws(65536, 1, 16, 16, 128, 128, 64) > 0
+    assert ws(0, 0, 1, 1, 64, 64, 64) > 0
+    assert ws(100, 2, 3, 4, 128, 128, 64) == 0     # HV not a multiple of H
+    assert ws(100, 2, 2, 4, 96, 96, 64) == 0       # head size not built
+    assert ws(100, 2, 2, 4, 128, 64, 64) == 0      # K != V
+    assert ws(100, 2, 2, 4, 128, 128, 32) == 0     # chunk size not built
+    assert ws(-1, 2, 2, 4, 128, 128, 64) == 0
+    # grows with tokens and value heads
+    assert ws(2000, 2, 2, 4, 128, 128, 64) > ws(1000, 2, 2, 4, 128, 128, 64)
+    assert ws(1000, 2, 2, 8, 128, 128, 64) > ws(1000, 2, 2, 4, 128, 128, 64)
+
+
+def _call(lib, **over):
+    args = dict(q=1, k=1, v=1, dtype=0, a=1, b=1, A_log=1, dt_bias=1, pool=1, pool_size=4, idx=1, cu=1,
+                batch=2, out=1, T=100, H=2, HV=4, K=128, V=128, C=64, scale=1.0, ws=256, ws_bytes=1 << 40,
+                stream=None)
+    args.update(over)
+    return lib.gdn_extend_chunkwise(*[args[k] for k in (
+        "q", "k", "v", "dtype", "a", "b", "A_log", "dt_bias", "pool", "pool_size", "idx", "cu", "batch",
+        "out", "T", "H", "HV", "K", "V", "C", "scale", "ws", "ws_bytes", "stream")])
+
+
+def test_host_side_errors_return_before_any_device_work(lib):
+    assert _call(lib, HV=3) == 1             # HV % H != 0
+    assert _call(lib, q=None) == 1           # null input
+    assert _call(lib, cu=None) == 1
+    assert _call(lib, batch=-1) == 1
+    assert _call(lib, dtype=7) == 1
+    assert _call(lib, K=96, V=96) == 2       # not built
+    assert _call(lib, C=32) == 2
+    assert _call(lib, dtype=1) == 2          # fp16 not built yet
+    assert _call(lib, ws=None) == 4          # workspace
+    assert _call(lib, ws=264) == 4           # misaligned
+    assert _call(lib, ws_bytes=16) == 4      # too small
+
+
+def test_product_path_has_no_fallback(monkeypatch):
+    """With the library missing, the binding raises instead of computing anything."""
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(gbuild, "LIB_PATH", "/nonexistent/libgdn_gb300.so")
+    with pytest.raises(RuntimeError):
+        _lib.load(build_if_missing=False)

@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA path through the C ABI vs the fp64 oracle, same seeded inputs.
+
+Bar: relative L2 <= 1e-2 on the bf16 outputs and <= 5e-3 on the final fp32 states,
+element by element over every compared chain; untouched pool slots bit-identical.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_chunkwise_gdn_gb300 import GdnError, gdn_extend_chunkwise, workloads as wl
+from gpu_helpers import (INPUT_KEYS, compare, oracle_for, rel_l2, run_gpu, to_device,
+                         untouched_slots_equal)
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # collected on CPU runs, skipped there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+# ----------------------------------------------------------------------------- the five configs
+
+def test_config_tiny_full():
+    d = wl.make_inputs(wl.CONFIGS[0])
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_config_varlen_full():
+    d = wl.make_inputs(wl.CONFIGS[1])
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
+def test_config_long_full():
+    """B=1, T=65536, H=HV=16, K=V=128: every chain, every token."""
+    d = wl.make_inputs(wl.CONFIGS[2])
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_config_throughput_sampled_chains():
+    """B=32 x 8192, H=HV=32: 24 sampled (sequence, head) chains, all their tokens."""
+    d = wl.make_inputs(wl.CONFIGS[3])
+    out, pool = run_gpu(d)
+    rng = np.random.default_rng(0)
+    chains = np.stack([rng.integers(0, 32, 24), rng.integers(0, 32, 24)], 1)
+    compare(d, out, pool, oracle_for(d, chains=chains))
+    untouched_slots_equal(d, pool)
+
+
+# ----------------------------------------------------------------------------- shapes and edge cases
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_lengths_and_gqa(D):
+    """Lengths around the chunk size (1, C-1, C, C+1, 0, several chunks + tail), GQA 1:2."""
+    w = wl.custom("ragged", [1, 63, 64, 65, 0, 200, 130], H=2, HV=4, K=D, V=D, chunk_size=64, seed=21)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+    # the zero-length sequence left its slot exactly as it was
+    s_empty = int(d["cache_indices"][4])
+    assert torch.equal(pool[s_empty], d["state_pool"][s_empty])
+
+
+def test_gqa_ratio_four():
+    w = wl.custom("gqa4", [300, 77], H=1, HV=4, K=128, V=128, chunk_size=64, seed=22)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_many_short_sequences():
+    rng = np.random.default_rng(23)
+    lens = rng.integers(1, 40, 100).tolist()
+    w = wl.custom("short", lens, H=2, HV=2, K=64, V=64, chunk_size=64, seed=23, pool_size=128)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_strong_decay_stays_finite():
+    """a ~ N(4, 1): sum of log alpha per chunk far below -87 (1/gamma would overflow fp32)."""
+    w = wl.custom("strong", [500, 129], H=2, HV=2, K=128, V=128, chunk_size=64, seed=24, a_mean=4.0)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_weak_decay_long_memory():
+    """A_log very negative: alpha ~ 1, the state carries across many chunks."""
+    w = wl.custom("weak", [700], H=1, HV=2, K=64, V=64, chunk_size=64, seed=25)
+    d = wl.make_inputs(w)
+    d["A_log"] = torch.full_like(d["A_log"], -8.0)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_scale_argument():
+    w = wl.custom("scale", [100], H=1, HV=1, K=64, V=64, chunk_size=64, seed=26)
+    d = wl.make_inputs(w)
+    s = 64 ** -0.5
+    out, pool = run_gpu(d, scale=s)
+    compare(d, out, pool, oracle_for(d, scale=s))
+
+
+def test_split_call_continuation():
+    """extend(T1) then extend(T - T1) on the same slot equals extend(T)."""
+    w = wl.custom("split", [333], H=2, HV=2, K=128, V=128, chunk_size=64, seed=27)
+    d = wl.make_inputs(w)
+    out_all, pool_all = run_gpu(d)
+    T1 = 130
+    d1 = dict(d, **{k: d[k][:T1] for k in ("q", "k", "v", "a", "b")}, cu_seqlens=torch.tensor([0, T1]))
+    out1, pool1 = run_gpu(d1)
+    d2 = dict(d, **{k: d[k][T1:] for k in ("q", "k", "v", "a", "b")}, cu_seqlens=torch.tensor([0, 333 - T1]),
+              state_pool=pool1)
+    out2, pool2 = run_gpu(d2)
+    res = oracle_for(d)
+    compare(d, out_all, pool_all, res)
+    compare(d, torch.cat([out1, out2]), pool2, res)   # the split calls meet the same bar
+
+
+def test_deterministic():
+    w = wl.custom("det", [257, 31], H=2, HV=4, K=128, V=128, chunk_size=64, seed=28)
+    d = wl.make_inputs(w)
+    o1, p1 = run_gpu(d)
+    o2, p2 = run_gpu(d)
+    assert torch.equal(o1, o2) and torch.equal(p1, p2)
+
+
+# ----------------------------------------------------------------------------- error paths
+
+def _sentinel_call(d, **over):
+    g = to_device(dict(d, **over))
+    out = torch.full((d["q"].shape[0], d["v"].shape[1], d["v"].shape[2]), 7.0, dtype=torch.bfloat16,
+                     device="cuda")
+    pool = g["state_pool"]
+    with pytest.raises(GdnError) as ei:
+        gdn_extend_chunkwise(*[g[k] for k in INPUT_KEYS[:7]], pool, g["cache_indices"], g["cu_seqlens"],
+                             chunk_size=64, out=out, check=True)
+    torch.cuda.synchronize()
+    assert torch.equal(pool.cpu(), d["state_pool"]), "state_pool modified by a rejected call"
+    assert bool((out == 7.0).all()), "out written by a rejected call"
+    return ei.value.status
+
+
+def test_bad_cache_indices_rejected_on_device():
+    w = wl.custom("bad", [40, 50], H=1, HV=2, K=64, V=64, chunk_size=64, seed=29, pool_size=4)
+    d = wl.make_inputs(w)
+    assert _sentinel_call(d, cache_indices=torch.tensor([1, 1])) == 3
+    assert _sentinel_call(d, cache_indices=torch.tensor([0, 4])) == 3
+    assert _sentinel_call(d, cache_indices=torch.tensor([-1, 2])) == 3
+
+
+def test_bad_cu_seqlens_rejected_on_device():
+    w = wl.custom("badcu", [40, 50], H=1, HV=2, K=64, V=64, chunk_size=64, seed=30, pool_size=4)
+    d = wl.make_inputs(w)
+    assert _sentinel_call(d, cu_seqlens=torch.tensor([0, 60, 50])) == 7   # last != total, decreasing
+    assert _sentinel_call(d, cu_seqlens=torch.tensor([1, 41, 90])) == 7   # does not start at 0
+    # and a good call afterwards works on the same workspace
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_host_errors_raise():
+    w = wl.custom("hosterr", [10], H=2, HV=2, K=64, V=64, chunk_size=64, seed=31)
+    d = to_device(wl.make_inputs(w))
+    with pytest.raises(GdnError):
+        gdn_extend_chunkwise(*[d[k] for k in INPUT_KEYS], chunk_size=48)
+    with pytest.raises(TypeError):
+        gdn_extend_chunkwise(d["q"].float(), *[d[k] for k in INPUT_KEYS[1:]])
