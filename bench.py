@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""GDN prefill benchmark on GB300: tokens/s and TFLOP/s through the C ABI.
+
+One step = one gdn_extend_chunkwise call over the whole workload (every chunk of
+every sequence and head: schedule, intra-chunk WY factors, inter-chunk scan with
+the output epilogue). Default workload: the long-prefill configuration
+(B=1, T=65536, H=HV=16, K=V=128, chunk_size=64, bf16, zero initial state), seeded
+synthetic inputs resident in HBM when the timed region starts.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle on
+the host cores instead (the reference arm of this benchmark).
+
+Multi-GPU (torchrun, N ranks): every rank runs its own replica of the workload on
+its own GPU (the path needs no exchange between GPUs); value = tokens of all
+ranks / the slowest rank's time ("weak" scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s and TFLOP/s (% of GB300 bf16 peak), 1 GPU"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indices", "cu_seqlens")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="long", help="workload name (tiny, varlen, long, throughput, wide)")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", device_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside:
+            after = [p for (t, p) in self.samples if t > t1]
+            inside = after[:1]
+            note = "timed region shorter than the sampling period: first sample after it"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def device_uuid(torch, dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ----------------------------------------------------------------------------- roofline
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_accounting(w, lengths):
+    """Algorithmic bytes and FLOPs per launch of each kernel."""
+    from gated_deltanet_chunkwise_gdn_gb300 import accounting as acc
+    T = sum(lengths)
+    H, HV, K, V, C = w.H, w.HV, w.K, w.V, w.chunk_size
+    B = len(lengths)
+    e = 2  # bf16
+    qk = T * H * K * e * 2
+    intra_bytes = qk + T * HV * V * e + T * HV * 8
+    scan_bytes = qk + T * HV * V * e + B * HV * V * K * 4 * 2
+    intra_flops = scan_flops = 0.0
+    for n in lengths:
+        for s in range(0, n, C):
+            L = min(C, n - s)
+            intra_flops += HV * ((H / HV) * (L * (L - 1) * K + L * (L + 1) * K) + L ** 3 / 3.0 + L * (L + 1) * (K + V))
+            scan_flops += HV * (6.0 * L * K * V + L * (L + 1) * V)
+    return {
+        "intra": {"bytes": intra_bytes, "flops": intra_flops},
+        "scan": {"bytes": scan_bytes, "flops": scan_flops},
+        "path": {"bytes": acc.min_hbm_bytes(lengths, H, HV, K, V), "flops": acc.flop_count(lengths, H, HV, K, V, C)},
+    }
+
+
+def kernel_source_hash(kernel: str) -> str:
+    files = {"intra": "gdn_intra.cu", "scan": "gdn_scan.cu", "schedule": "gdn_schedule.cu"}
+    csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (files.get(kernel, ""), "gdn_common.cuh"):
+        p = os.path.join(csrc, f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        tab = json.load(open(path))
+        ent = tab.get(workload, {}).get(kernel)
+        if ent and ent.get("source_hash") == kernel_source_hash(kernel):
+            return ent.get("dram_bytes_per_launch")
+    except (ValueError, OSError):
+        pass
+    return None
+
+
+def roofline_entry(name, acct, ms_avg, peaks, peak_kind, workload):
+    bw = float(peaks["hbm_gbs"])
+    tf = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    intensity = acct["flops"] / max(acct["bytes"], 1.0)
+    ridge = tf * 1e12 / (bw * 1e9)
+    if intensity < ridge:
+        achieved = acct["bytes"] / (ms_avg * 1e-3) / 1e9
+        ent = {"bound": "hbm", "achieved": round(achieved, 1), "peak": bw, "unit": "GB/s"}
+    else:
+        achieved = acct["flops"] / (ms_avg * 1e-3) / 1e12
+        ent = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tf, "unit": "TFLOP/s"}
+    ent["frac"] = round(ent["achieved"] / ent["peak"], 4)
+    ent["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback"
+    ent["kernel"] = name
+    ent["ms_per_launch"] = round(ms_avg, 4)
+    ent["algorithmic_bytes_per_launch"] = acct["bytes"]
+    ent["algorithmic_flops_per_launch"] = acct["flops"]
+    ent["traffic"] = measured_traffic(name, workload)
+    return ent
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(d: dict, w, target_s: float):
+    """Runs the oracle on the first S tokens of the first sequence (all value heads),
+    S sized so the run takes about target_s seconds. Returns (tokens, seconds, threads, S)."""
+    import oracle
+    import torch
+    cu = d["cu_seqlens"]
+    L0 = int(cu[1] - cu[0])
+
+    def run(S):
+        sub = dict(d)
+        for k in ("q", "k", "v", "a", "b"):
+            sub[k] = d[k][:S]
+        sub["cu_seqlens"] = torch.tensor([0, S], dtype=torch.int64)
+        sub["cache_indices"] = d["cache_indices"][:1]
+        t = time.perf_counter()
+        res = oracle.gdn_forward(*[sub[k] for k in KEYS])
+        return time.perf_counter() - t, res.threads
+
+    probe = min(L0, 512)
+    dt, _ = run(probe)
+    S = max(1, min(L0, int(probe * target_s / max(dt, 1e-6))))
+    dt, threads = run(S)
+    return S, dt, threads
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, dist):
+    """The reference arm: the fp64 CPU oracle timed on the host cores (rank 0 only)."""
+    if dist.rank != 0:
+        return
+    import oracle
+    from gated_deltanet_chunkwise_gdn_gb300 import workloads as wl
+    oracle.build()
+    w = wl.BY_NAME[args.config]
+    d = wl.make_inputs(w)
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    S, _, _ = oracle_sample(d, w, per_step)
+    import torch
+    sub = dict(d)
+    for k in ("q", "k", "v", "a", "b"):
+        sub[k] = d[k][:S]
+    sub["cu_seqlens"] = torch.tensor([0, S], dtype=torch.int64)
+    sub["cache_indices"] = d["cache_indices"][:1]
+    for _ in range(args.warmup):
+        oracle.gdn_forward(*[sub[k] for k in KEYS])
+    t = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        threads = oracle.gdn_forward(*[sub[k] for k in KEYS]).threads
+    el = time.perf_counter() - t
+    tok_s = S * args.steps / el
+    sample = f"first {S} tokens of sequence 0, all {w.HV} value heads, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.note}", "sample": sample},
+        "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, dist):
+    import torch
+    import gated_deltanet_chunkwise_gdn_gb300 as gdn
+    from gated_deltanet_chunkwise_gdn_gb300 import workloads as wl
+
+    dev = torch.device("cuda", dist.local_rank if dist.world > 1 else 0)
+    torch.cuda.set_device(dev)
+    w = wl.BY_NAME[args.config]
+    d = wl.make_inputs(w)
+    lengths = wl.sequence_lengths(w)
+    T = sum(lengths)
+    g = {k: d[k].to(dev) for k in KEYS}
+    out = torch.empty((T, w.HV, w.V), dtype=w.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.gdn_extend_chunkwise(*[g[k] for k in KEYS], chunk_size=w.chunk_size, out=out)
+
+    gdn.gdn_extend_chunkwise(*[g[k] for k in KEYS], chunk_size=w.chunk_size, out=out, check=True)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: kernels only, inputs resident in HBM
+    sampler = ClockSampler(device_uuid(torch, dev))
+    time.sleep(0.15)
+    prof = gdn.KernelProfile(max_launches=8 * args.steps + 64)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = gdn.launch_count()
+    prof.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    dist.barrier()
+    kernels = prof.stop()
+    launches = gdn.launch_count() - n0
+    time.sleep(0.1)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = dist.max(ms)
+    clocks = sampler.summary(t_host0, t_host1)
+
+    # ---- e2e: host buffers through the public API, copies inside the timed region
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+    host_in = {k: d[k].pin_memory() for k in ("q", "k", "v", "a", "b", "cache_indices", "cu_seqlens")}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, t in host_in.items():
+            g[k].copy_(t, non_blocking=True)
+        gdn.gdn_extend_chunkwise(*[g[k] for k in KEYS], chunk_size=w.chunk_size, out=out)
+        host_out.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist.max(f0.elapsed_time(f1))
+
+    if dist.rank != 0:
+        return
+    acct = kernel_accounting(w, lengths)
+    peaks, peak_kind = load_peaks()
+    per_kernel = {}
+    for name, (tot, n) in kernels.items():
+        if n:
+            per_kernel[name] = {"ms_per_launch": round(tot / n, 4), "launches": n,
+                                "share": round(tot / max(sum(v[0] for v in kernels.values()), 1e-9), 4)}
+    dominant = max((k for k in kernels if k in acct and kernels[k][1]), key=lambda k: kernels[k][0])
+    roof = roofline_entry(dominant, acct[dominant], kernels[dominant][0] / kernels[dominant][1], peaks, peak_kind,
+                          w.name)
+    step_ms = ms / args.steps
+    path = roofline_entry("path", acct["path"], step_ms, peaks, peak_kind, w.name)
+    path.pop("traffic", None)
+    tokens = T * args.steps * dist.world
+    value = tokens / (ms_max * 1e-3)
+    tflops = acct["path"]["flops"] * args.steps * dist.world / (ms_max * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.note}", "global_batch": len(lengths) * dist.world, "seq_len": max(lengths),
+                   "total_tokens_per_gpu": T, "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (q,k,v %.0f MB > 129 MB), no flush" % (
+                       3 * T * w.H * w.K * 2 / 1e6)},
+        "tflops": round(tflops, 2),
+        "frac_bf16_peak": round(tflops / float(peaks["bf16_tflops"]), 4),
+        "roofline": roof,
+        "path_roofline": path,
+        "kernels": per_kernel,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": {"value": round(T * e2e_steps * dist.world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms / e2e_steps, 4)},
+    }
+    if dist.world == 1 and not args.no_cpu_baseline:
+        S, dt, threads = oracle_sample(d, w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(S / dt, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {S} tokens of sequence 0, all {w.HV} value heads ({dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()
