@@ -53,6 +53,10 @@ def load(build_if_missing: bool = True):
             vp, i64, i32, i32, i32, i32,   # out total_tokens H HV K V
             i32, f32, vp, sz, vp]          # chunk_size scale workspace bytes stream
         L.gdn_extend_chunkwise.restype = ctypes.c_int
+        L.gdn_extend_chunkwise_noalloc.argtypes = [
+            vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp, i32,
+            vp, i64, i32, i32, i32, i32, i32, f32, vp, vp]
+        L.gdn_extend_chunkwise_noalloc.restype = ctypes.c_int
         L.gdn_get_device_status.argtypes = [vp, vp]
         L.gdn_get_device_status.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]

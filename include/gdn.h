@@ -116,6 +116,33 @@ GDN_API gdn_status gdn_extend_chunkwise(const void *q, const void *k, const void
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Same computation and arguments as gdn_extend_chunkwise, for callers that cannot
+ * allocate device memory (for example a plugin inside a host runtime that owns all
+ * device memory, or a serving loop that may not call cudaMalloc/cudaFree once running,
+ * since those can synchronise the device or fail under a fixed memory budget). The pages
+ * have no counterpart of this entry point: it is a deployment variant of the call above.
+ *
+ * Instead of a caller-provided workspace it uses a scratch array built into the library:
+ * 64 MiB, reserved on every GPU that loads the library until the process exits. Calls
+ * whose gdn_workspace_size(...) exceeds 64 MiB return GDN_ERR_WORKSPACE before touching
+ * anything. It calls no allocator. The first call on each device looks up the scratch
+ * address on that device (make it before capturing any stream). All calls share the
+ * scratch and it keeps the last call's contents; calls that overlap on the GPU (e.g. on
+ * two streams at once) race on it and must not be issued.
+ *
+ * device_status: optional DEVICE pointer to one int32. When not NULL, the status the
+ * call's first kernel records (GDN_OK, GDN_ERR_BAD_INDEX, GDN_ERR_BAD_SEQLENS) is copied
+ * there, in stream order, after the call's kernels.
+ */
+GDN_API gdn_status gdn_extend_chunkwise_noalloc(const void *q, const void *k, const void *v, gdn_dtype dtype,
+                                                const float *a, const float *b, const float *A_log,
+                                                const float *dt_bias, float *state_pool, int64_t pool_size,
+                                                const int64_t *cache_indices, const int64_t *cu_seqlens,
+                                                int32_t batch, void *out, int64_t total_tokens, int32_t H,
+                                                int32_t HV, int32_t K, int32_t V, int32_t chunk_size, float scale,
+                                                int32_t *device_status, void *stream);
+
+/*
  * Waits for `stream`, then returns the status recorded on the device by the last
  * gdn_extend_chunkwise call that used this workspace (GDN_OK, GDN_ERR_BAD_INDEX,
  * GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the stream reported
