@@ -15,6 +15,7 @@
 //   S  <- exp(g_C) S + U^T diag(exp(g_C - g)) K^
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -167,6 +168,12 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
 // K0: validates cu_seqlens / cache_indices, builds the chunk table and the
 // longest-first sequence order. One block.
 __global__ void schedule_kernel(Params p, int C);
+
+// Host-side tensor maps (gdn_tma.cu): token tiles of a [T, heads, D] bf16 array (128-byte
+// swizzled), and tiles of a row-major [rows, inner] bf16 array.
+bool make_token_tile_map(CUtensorMap* map, const void* base, int D, int heads, int64_t T, int box_rows);
+bool make_2d_tile_map(CUtensorMap* map, const void* base, int inner, int64_t rows, int box_inner, int box_rows,
+                      bool swizzle128);
 
 // Host-side launchers (one per translation unit, templated on head size).
 cudaError_t launch_intra(const Params& p, int D, int C, cudaStream_t s);

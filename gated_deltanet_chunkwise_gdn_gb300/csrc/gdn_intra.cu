@@ -1,63 +1,60 @@
-// gdn_intra.cu — K2: per-chunk gates, Gram products, the one triangular inverse and
-// the WY factors, for every chunk of every sequence in parallel.
+// gdn_intra.cu — K2: per-chunk gates, Gram products, the one triangular inverse and the
+// WY factors, for every chunk of every sequence in parallel, on the 5th-generation tensor
+// cores (tcgen05, fp32 accumulators in TMEM) with TMA tile loads.
 //
-// One CTA handles one (chunk, q/k head h) and loops over the HV/H value heads that
-// read head h, so K^K^^T and Q^K^^T are formed once per q/k head.
-//
-// Per value head it computes (see gdn_common.cuh for the notation):
-//   log alpha = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)   (pymllm page,
-//               Parameters: raw gate inputs before softplus/exp and sigmoid)
+// One CTA handles one (chunk, q/k head h) and loops over the HV/H value heads that read
+// head h, so K^K^^T and Q^K^^T are formed once per q/k head. Per value head it computes
+// (notation of gdn_common.cuh):
+//   log alpha = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)   (pymllm page
+//               "pymllm.layers.attention.gdn_chunkwise", Parameters: raw gate inputs)
 //   g        = chunk-local inclusive cumsum of log alpha
 //   M^{-1}   for M = I + tril(diag(beta) K^K^^T, -1)   (blocked forward substitution)
 //   A        = (Gamma . M^{-1}) diag(beta)             (N^{-1} B = G M^{-1} G^{-1} B,
 //                                                      "Simple math to speed up GDN
 //                                                      prefill", section "Save one invert")
 //   W<-      = A diag(exp(g)) K^,   U~ = A V,   P = Gamma . tril(Q^K^^T)
-// and stores g, 1/|q|, 1/|k|, W<-, U~ and P for the scan kernel.
+// and stores g, 1/|q|, 1/|k|, W<- [C][K], U~ [C][V] and P [C][C] for the scan.
 //
-// Normalisation and decay enter only as diagonal scalings of the fp32 Gram
-// accumulators or of the small C x C operand, so the raw bf16 q/k/v tiles feed the
-// tensor cores unchanged.
+// Tensor-core work (one elected thread issues, the accumulators live in TMEM):
+//   MMA1  D1[128 x 64]  = [K; Q] K^T            (M=128: rows 0-63 K K^T, rows 64-127 Q K^T)
+//   MMA2  DW[128 x D]   = [A'; A] K             (rows 0-63: W<- = A' K with A' = A diag(e^g/|k|))
+//   MMA3  DU[128 x D]   = [A'; A] V             (rows 64-127: U~ = A V)
+// Stacking A' and A keeps every MMA at M = 128 and puts W<- and U~ rows in TMEM lanes, so
+// each thread stores one contiguous output row. Normalisation and decay enter only as
+// diagonal scalings of fp32 accumulators or of the C x C operand; the raw bf16 q/k/v tiles
+// feed the tensor cores as TMA wrote them (128-byte swizzle, K-major for MMA1, the same
+// bytes read MN-major for MMA2/3).
 #include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int C = 64;
 constexpr int kThreads = 128;
+constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
 
 template <int D>
 struct IntraSmem {
-  static constexpr int LDT = D + 8;  // bf16 pitch of the q/k/v tiles
-  static constexpr int LDA = C + 8;  // bf16 pitch of A, A'
-  static constexpr int LDF = C + 1;  // fp32 pitch of L, X
-  static constexpr size_t tiles = 3ull * C * LDT * sizeof(bf16);
-  static constexpr size_t lx = 2ull * C * LDF * sizeof(float);
-  static constexpr size_t aa = 2ull * C * LDA * sizeof(bf16);
-  static constexpr size_t vec = 4ull * C * sizeof(float);
-  static constexpr size_t bytes = tiles + lx + aa + vec;
+  static constexpr int NB = D / 64;                     // 64-column blocks of a q/k/v row
+  static constexpr uint32_t KQ = 0;                     // NB x [K block 8 KB][Q block 8 KB]
+  static constexpr uint32_t V = KQ + NB * 16384;        // NB x V block 8 KB
+  static constexpr uint32_t AA = V + NB * 8192;         // [A' 8 KB][A 8 KB], 128-byte swizzled
+  static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x 65
+  static constexpr uint32_t XF = LF + 64 * 65 * 4;      // M^{-1}, fp32 64 x 65
+  static constexpr uint32_t VEC = XF + 64 * 65 * 4;     // g, beta, 1/|q|, 1/|k| (4 x 64 fp32)
+  static constexpr uint32_t BAR = VEC + 4 * 64 * 4;     // 3 mbarriers + TMEM address
+  static constexpr uint32_t bytes = BAR + 64;
+  static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
 };
+
+constexpr uint32_t kTmemCols = 256;  // D1 / DW at columns [0, 128), DU at [128, 256)
 
 __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
-// Loads `rows` valid rows of a C x D bf16 tile (global row stride `gstride` elements)
-// into smem with pitch LDT; rows >= rows are zero-filled.
-template <int D, int LDT>
-__device__ __forceinline__ void load_tile(bf16* s, const bf16* g, int64_t gstride, int rows) {
-  constexpr int SEG = D / 8;  // 16-byte segments per row
-  for (int e = threadIdx.x; e < C * SEG; e += kThreads) {
-    const int r = e / SEG, c = (e % SEG) * 8;
-    if (r < rows)
-      cp_async_16(s + r * LDT + c, g + r * gstride + c);
-    else
-      *reinterpret_cast<uint4*>(s + r * LDT + c) = make_uint4(0, 0, 0, 0);
-  }
-}
-
-// Inverts the unit lower-triangular 64x64 matrix I + L (L strictly lower, in Lf)
-// into Xf, by 16x16 blocks: the four diagonal blocks by forward substitution (one
-// warp each, one lane per column), then block rows I = 1..3 with
-//   X_IJ = -X_II * sum_{K=J}^{I-1} L_IK X_KJ.
+// Inverts the unit lower-triangular 64x64 matrix I + L (L strictly lower, in Lf) into Xf,
+// by 16x16 blocks: the four diagonal blocks by forward substitution (one warp each, one
+// lane per column), then block rows I = 1..3 with X_IJ = -X_II * sum_{K=J}^{I-1} L_IK X_KJ.
 template <int LDF>
 __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,7 +76,6 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   }
   __syncthreads();
   for (int I = 1; I < 4; ++I) {
-    // T_IJ = sum_{K=J}^{I-1} L_IK X_KJ, written into the X_IJ slots.
     float t[6];
     const int n_ent = I * 256;
 #pragma unroll
@@ -103,7 +99,6 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
       }
     }
     __syncthreads();
-    // X_IJ = -X_II T_IJ
 #pragma unroll
     for (int u = 0; u < 6; ++u) {
       const int e = threadIdx.x + u * kThreads;
@@ -129,46 +124,50 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   }
 }
 
-// Rows [16*warp, 16*warp+16) of Out(64 x D) = As(64 x 64) * Bs(64 x D), As row-major
-// (pitch LDA), Bs row-major [k][n] (pitch LDT); fp32 accumulators in acc.
-template <int D, int LDA, int LDT>
-__device__ __forceinline__ void mma_rows_AxB(const bf16* As, const bf16* Bs, float (&acc)[D / 8][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-  for (int nt = 0; nt < D / 8; ++nt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[nt][r] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < C / 16; ++kk) {
-    uint32_t a[4];
-    ldmatrix_x4(a, As + (16 * warp + (lane & 15)) * LDA + 16 * kk + (lane >> 4) * 8);
-#pragma unroll
-    for (int nt = 0; nt < D / 8; nt += 2) {
-      uint32_t b[4];
-      const int m = lane >> 3, r = lane & 7;
-      ldmatrix_x4_trans(b, Bs + (16 * kk + (m & 1) * 8 + r) * LDT + 8 * (nt + (m >> 1)));
-      mma_bf16_16816(acc[nt], a, b[0], b[1]);
-      mma_bf16_16816(acc[nt + 1], a, b[2], b[3]);
+// Gates of value head hv for the chunk's tokens: beta and the chunk-local cumulative log
+// decay g (inclusive prefix sum); padded rows get log alpha = 0 and beta = 0. All threads.
+__device__ __forceinline__ void chunk_gates(const Params& p, int hv, int64_t t0, int len, int64_t jh, float* s_g,
+                                            float* s_beta) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < C) {
+    float la = 0.f, beta = 0.f;
+    if (tid < len) {
+      const int64_t t = t0 + tid;
+      la = -expf(p.A_log[hv]) * softplus_f(p.a[t * p.HV + hv] + p.dt_bias[hv]);
+      beta = 1.f / (1.f + expf(-p.b[t * p.HV + hv]));
     }
+    float incl = la;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    s_g[tid] = incl;
+    s_beta[tid] = beta;
   }
+  __syncthreads();
+  if (tid >= 32 && tid < C) s_g[tid] += s_g[31];
+  __syncthreads();
+  if (tid < C) p.g[jh * C + tid] = s_g[tid];
+}
+
+// All threads: bounded wait; every thread leaves with the same verdict.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* status) {
+  const bool ok = tc::mbar_wait(bar, parity, kWaitBudget);
+  const bool all = __syncthreads_and(ok);
+  if (!all && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT);
+  return all;
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) intra_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                         const __grid_constant__ CUtensorMap tm_k,
+                                                         const __grid_constant__ CUtensorMap tm_v, Params p) {
   using SM = IntraSmem<D>;
-  constexpr int LDT = SM::LDT, LDA = SM::LDA, LDF = SM::LDF;
-  extern __shared__ __align__(16) unsigned char smem[];
-  bf16* Ks = reinterpret_cast<bf16*>(smem);
-  bf16* Qs = Ks + C * LDT;
-  bf16* Vs = Qs + C * LDT;
-  float* Lf = reinterpret_cast<float*>(Vs + C * LDT);
-  float* Xf = Lf + C * LDF;
-  bf16* As = reinterpret_cast<bf16*>(Xf + C * LDF);
-  bf16* Aw = As + C * LDA;
-  float* s_g = reinterpret_cast<float*>(Aw + C * LDA);
-  float* s_beta = s_g + C;
-  float* s_rq = s_beta + C;
-  float* s_rk = s_rq + C;
+  constexpr int NB = SM::NB;
+  constexpr int LDF = 65;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   if (p.status[0] != GDN_OK) return;
   const int j = blockIdx.x / p.H, h = blockIdx.x % p.H;
@@ -176,173 +175,226 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(Params p) {
   const int4 ct = p.chunk_tab[j];
   const int64_t t0 = ct.y;
   const int len = ct.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, t4 = lane & 3;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int r_heads = p.HV / p.H;
+  const int hv0 = h * r_heads;
 
-  // q/k tiles (group 0), then v of the first value head (group 1)
-  load_tile<D, LDT>(Ks, p.k + (t0 * p.H + h) * D, (int64_t)p.H * D, len);
-  load_tile<D, LDT>(Qs, p.q + (t0 * p.H + h) * D, (int64_t)p.H * D, len);
-  cp_async_commit();
-  load_tile<D, LDT>(Vs, p.v + (t0 * p.HV + h * r_heads) * D, (int64_t)p.HV * D, len);
-  cp_async_commit();
-  cp_async_wait<1>();
+  float* Lf = reinterpret_cast<float*>(smem + SM::LF);
+  float* Xf = reinterpret_cast<float*>(smem + SM::XF);
+  float* s_g = reinterpret_cast<float*>(smem + SM::VEC);
+  float* s_beta = s_g + C;
+  float* s_rq = s_beta + C;
+  float* s_rk = s_rq + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles, [1] v tile, [2] MMAs
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
+
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::mbar_init(&bar[2], 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar[0], NB * 16384);
+    for (int b = 0; b < NB; ++b) {
+      tc::tma_load_3d(smem + SM::KQ + b * 16384, &tm_k, 64 * b, h, (int)t0, &bar[0]);
+      tc::tma_load_3d(smem + SM::KQ + b * 16384 + 8192, &tm_q, 64 * b, h, (int)t0, &bar[0]);
+    }
+    tc::mbar_arrive_expect_tx(&bar[1], NB * 8192);
+    for (int b = 0; b < NB; ++b) tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, hv0, (int)t0, &bar[1]);
+  }
+  chunk_gates(p, hv0, t0, len, (int64_t)j * p.HV + hv0, s_g, s_beta);
+
+  bool ok = wait_all(&bar[0], 0, p.status);
+  if (ok && tid == 0) {
+    constexpr uint32_t idesc1 = tc::idesc_f16(128, 64, 1, false, false);
+    for (int b = 0; b < NB; ++b)
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t a = tc::saddr(smem + SM::KQ + b * 16384) + ks * 32;
+        const uint64_t d = tc::smem_desc(a, 16, 1024, tc::kSwizzle128B);
+        tc::mma_f16_ss(tmem, d, d, idesc1, (b | ks) != 0);
+      }
+    tc::mma_commit(&bar[2]);
+  }
+  if (ok) {
+    // inverse row norms from the swizzled tiles: threads 0-63 k rows, 64-127 q rows
+    const int row = tid & 63;
+    const unsigned char* base = smem + SM::KQ + (tid >= 64 ? 8192 : 0);
+    float ss = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(base + b * 16384 + tc::sw128_offset(row, c));
+        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v4);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __bfloat1622float2(e[u]);
+          ss += f.x * f.x + f.y * f.y;
+        }
+      }
+    const float r = row < len ? rsqrtf(ss + kNormEps) : 0.f;
+    const int64_t jq = (int64_t)j * p.H + h;
+    if (tid < 64) {
+      s_rk[row] = r;
+      p.rk[jq * C + row] = r;
+    } else {
+      s_rq[row] = r;
+      p.rq[jq * C + row] = r;
+    }
+  }
+  if (ok) ok = wait_all(&bar[2], 0, p.status);
+  float kq[C];  // this thread's row of K K^T (tid < 64) or Q K^T (tid >= 64), raw
+  if (ok) {
+    tc::fence_after_sync();
+#pragma unroll
+    for (int c = 0; c < C / 16; ++c) {
+      uint32_t r[16];
+      tc::tmem_ld16(tmem + lane_base + 16 * c, r);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) kq[16 * c + u] = __uint_as_float(r[u]);
+    }
+    tc::fence_before_sync();
+  }
   __syncthreads();
 
-  // inverse row norms (two threads per row)
-  {
-    const int row = tid >> 1, half = tid & 1;
-    float sk = 0.f, sq = 0.f;
-#pragma unroll 8
-    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 2) {
-      const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Ks + row * LDT + c));
-      const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Qs + row * LDT + c));
-      sk += kf.x * kf.x + kf.y * kf.y;
-      sq += qf.x * qf.x + qf.y * qf.y;
-    }
-    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    if (half == 0) {
-      const float rk = row < len ? rsqrtf(sk + kNormEps) : 0.f;
-      const float rq = row < len ? rsqrtf(sq + kNormEps) : 0.f;
-      s_rk[row] = rk;
-      s_rq[row] = rq;
-      p.rk[((int64_t)j * p.H + h) * C + row] = rk;
-      p.rq[((int64_t)j * p.H + h) * C + row] = rq;
-    }
-  }
-
-  // Gram products, rows [16*warp, +16): accK = K K^T, accQ = Q K^T (raw bf16 inputs)
-  float accK[C / 8][4], accQ[C / 8][4];
-#pragma unroll
-  for (int nt = 0; nt < C / 8; ++nt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) accK[nt][r] = accQ[nt][r] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    uint32_t ak[4], aq[4];
-    ldmatrix_x4(ak, Ks + (16 * warp + (lane & 15)) * LDT + 16 * kk + (lane >> 4) * 8);
-    ldmatrix_x4(aq, Qs + (16 * warp + (lane & 15)) * LDT + 16 * kk + (lane >> 4) * 8);
-#pragma unroll
-    for (int nt = 0; nt < C / 8; nt += 2) {
-      uint32_t b[4];
-      const int m = lane >> 3, r = lane & 7;
-      ldmatrix_x4(b, Ks + (8 * (nt + (m >> 1)) + r) * LDT + 16 * kk + (m & 1) * 8);
-      mma_bf16_16816(accK[nt], ak, b[0], b[1]);
-      mma_bf16_16816(accK[nt + 1], ak, b[2], b[3]);
-      mma_bf16_16816(accQ[nt], aq, b[0], b[1]);
-      mma_bf16_16816(accQ[nt + 1], aq, b[2], b[3]);
-    }
-  }
-
-  for (int ih = 0; ih < r_heads; ++ih) {
-    const int hv = h * r_heads + ih;
+  uint32_t mma_phase = 1, v_phase = 0;
+  for (int ih = 0; ok && ih < r_heads; ++ih) {
+    const int hv = hv0 + ih;
     const int64_t jh = (int64_t)j * p.HV + hv;
-    // gates and the chunk-local cumulative log decay (warps 0-1, one token per thread)
-    if (tid < C) {
-      float la = 0.f, beta = 0.f;
-      if (tid < len) {
-        const int64_t t = t0 + tid;
-        la = -expf(p.A_log[hv]) * softplus_f(p.a[t * p.HV + hv] + p.dt_bias[hv]);
-        beta = 1.f / (1.f + expf(-p.b[t * p.HV + hv]));
-      }
-      float incl = la;
+    if (ih > 0) chunk_gates(p, hv, t0, len, jh, s_g, s_beta);
+    if (tid < C) {  // L = tril(diag(beta) K^K^^T, -1), row i
+      const int i = tid;
+      const float bi = s_beta[i] * s_rk[i];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      s_g[tid] = incl;  // warp-local; warp 1 adds warp 0's total below
-      s_beta[tid] = beta;
-    }
-    __syncthreads();
-    if (tid >= 32 && tid < C) s_g[tid] += s_g[31];
-    __syncthreads();
-    if (tid < C) p.g[jh * C + tid] = s_g[tid];
-
-    // L = tril(diag(beta) K^K^^T, -1) into Lf; P = Gamma . tril(Q^K^^T) to global
-    bf16* Pg = p.P + jh * C * C;
+      for (int nu = 0; nu < C; ++nu) Lf[i * LDF + nu] = nu < i ? bi * s_rk[nu] * kq[nu] : 0.f;
+    } else {  // P = Gamma . tril(Q^K^^T), row r, straight to global
+      const int r = tid - C;
+      const float qr = s_rq[r], gr = s_g[r];
+      uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C);
 #pragma unroll
-    for (int nt = 0; nt < C / 8; ++nt) {
+      for (int c = 0; c < C / 8; ++c) {
+        uint32_t w[4];
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int i = 16 * warp + g4 + 8 * hr;
-        const int nu = 8 * nt + 2 * t4;
-        const float bi = s_beta[i] * s_rk[i];
-        const float l0 = nu < i ? bi * s_rk[nu] * accK[nt][2 * hr] : 0.f;
-        const float l1 = nu + 1 < i ? bi * s_rk[nu + 1] * accK[nt][2 * hr + 1] : 0.f;
-        Lf[i * LDF + nu] = l0;
-        Lf[i * LDF + nu + 1] = l1;
-        const float qi = s_rq[i], gi = s_g[i];
-        const float p0 = nu <= i ? expf(gi - s_g[nu]) * qi * s_rk[nu] * accQ[nt][2 * hr] : 0.f;
-        const float p1 = nu + 1 <= i ? expf(gi - s_g[nu + 1]) * qi * s_rk[nu + 1] * accQ[nt][2 * hr + 1] : 0.f;
-        *reinterpret_cast<uint32_t*>(Pg + i * C + nu) = pack_bf16(p0, p1);
+        for (int u = 0; u < 4; ++u) {
+          const int n0 = 8 * c + 2 * u, n1 = n0 + 1;
+          const float v0 = n0 <= r ? expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[n0] : 0.f;
+          const float v1 = n1 <= r ? expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[n1] : 0.f;
+          w[u] = pack_bf16(v0, v1);
+        }
+        prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     __syncthreads();
     invert_unit_lower_64<LDF>(Lf, Xf);
 
-    // A = (Gamma . X) diag(beta) and A' = A diag(exp(g) / |k|) (the W<- operand)
-    {
-      const int i = tid >> 1, c0 = (tid & 1) * 32;
+    {  // A' rows (threads 0-63) and A rows (threads 64-127), 128-byte swizzled K-major
+      const int i = tid & 63;
+      const bool is_a = tid >= 64;
       const float gi = s_g[i], egi = expf(gi);
-#pragma unroll 4
-      for (int c = c0; c < c0 + 32; c += 2) {
-        float a0 = 0.f, a1 = 0.f, w0 = 0.f, w1 = 0.f;
-        if (c <= i) {
-          const float x = (c == i) ? 1.f : Xf[i * LDF + c];
-          a0 = expf(gi - s_g[c]) * x * s_beta[c];
-          w0 = egi * x * s_beta[c] * s_rk[c];
+      unsigned char* dst = smem + SM::AA + (is_a ? 8192 : 0);
+#pragma unroll
+      for (int c = 0; c < C / 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float v2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int nu = 8 * c + 2 * u + e;
+            float val = 0.f;
+            if (nu <= i) {
+              const float x = nu == i ? 1.f : Xf[i * LDF + nu];
+              val = is_a ? expf(gi - s_g[nu]) * x * s_beta[nu] : egi * x * s_beta[nu] * s_rk[nu];
+            }
+            v2[e] = val;
+          }
+          w[u] = pack_bf16(v2[0], v2[1]);
         }
-        if (c + 1 <= i) {
-          const float x = (c + 1 == i) ? 1.f : Xf[i * LDF + c + 1];
-          a1 = expf(gi - s_g[c + 1]) * x * s_beta[c + 1];
-          w1 = egi * x * s_beta[c + 1] * s_rk[c + 1];
-        }
-        *reinterpret_cast<uint32_t*>(As + i * LDA + c) = pack_bf16(a0, a1);
-        *reinterpret_cast<uint32_t*>(Aw + i * LDA + c) = pack_bf16(w0, w1);
+        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(i, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    cp_async_wait<0>();
+    tc::fence_async_smem();
     __syncthreads();
+    ok = wait_all(&bar[1], v_phase, p.status);
+    v_phase ^= 1;
+    if (!ok) break;
+    if (tid == 0) {
+      tc::fence_after_sync();
+      constexpr uint32_t idesc2 = tc::idesc_f16(128, D, 1, false, true);
+      for (int ks = 0; ks < C / 16; ++ks) {
+        const uint64_t a = tc::smem_desc(tc::saddr(smem + SM::AA) + ks * 32, 16, 1024, tc::kSwizzle128B);
+        const uint64_t bk = tc::smem_desc(tc::saddr(smem + SM::KQ) + ks * 2048, 16384, 1024, tc::kSwizzle128B);
+        tc::mma_f16_ss(tmem, a, bk, idesc2, ks > 0);
+      }
+      for (int ks = 0; ks < C / 16; ++ks) {
+        const uint64_t a = tc::smem_desc(tc::saddr(smem + SM::AA) + ks * 32, 16, 1024, tc::kSwizzle128B);
+        const uint64_t bv = tc::smem_desc(tc::saddr(smem + SM::V) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+        tc::mma_f16_ss(tmem + 128, a, bv, idesc2, ks > 0);
+      }
+      tc::mma_commit(&bar[2]);
+    }
+    ok = wait_all(&bar[2], mma_phase & 1, p.status);
+    ++mma_phase;
+    if (!ok) break;
+    tc::fence_after_sync();
+    if (tid == 0 && ih + 1 < r_heads) {  // the v tile is free: fetch the next value head's
+      tc::mbar_arrive_expect_tx(&bar[1], NB * 8192);
+      for (int b = 0; b < NB; ++b)
+        tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, hv + 1, (int)t0, &bar[1]);
+    }
+    {  // rows 0-63 of DW are W<-, rows 64-127 of DU are U~: one output row per thread
+      const bool is_u = tid >= 64;
+      const int mu = tid & 63;
+      bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D;
+      const uint32_t col0 = is_u ? 128u : 0u;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + lane_base + col0 + 16 * c, r);
+        tc::tmem_wait_ld();
+        uint32_t w[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) w[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
+        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+  }
 
-    // W<- = A' K and U~ = A V, rows [16*warp, +16)
-    {
-      float acc[D / 8][4];
-      mma_rows_AxB<D, LDA, LDT>(Aw, Ks, acc);
-      bf16* Wg = p.W + jh * C * D;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int i = 16 * warp + g4 + 8 * hr;
-          *reinterpret_cast<uint32_t*>(Wg + i * D + 8 * nt + 2 * t4) = pack_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-        }
-      mma_rows_AxB<D, LDA, LDT>(As, Vs, acc);
-      bf16* Ug = p.U + jh * C * D;
-#pragma unroll
-      for (int nt = 0; nt < D / 8; ++nt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int i = 16 * warp + g4 + 8 * hr;
-          *reinterpret_cast<uint32_t*>(Ug + i * D + 8 * nt + 2 * t4) = pack_bf16(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-        }
-    }
-    __syncthreads();
-    if (ih + 1 < r_heads) {
-      load_tile<D, LDT>(Vs, p.v + (t0 * p.HV + hv + 1) * D, (int64_t)p.HV * D, len);
-      cp_async_commit();
-    }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <int D>
 cudaError_t launch_intra_t(const Params& p, cudaStream_t s) {
-  const size_t smem = IntraSmem<D>::bytes;
+  CUtensorMap mq, mk, mv;
+  if (!make_token_tile_map(&mq, p.q, D, p.H, p.T, C) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C) ||
+      !make_token_tile_map(&mv, p.v, D, p.HV, p.T, C))
+    return cudaErrorInvalidValue;
+  const uint32_t smem = IntraSmem<D>::alloc;
   cudaError_t e = cudaFuncSetAttribute(intra_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t blocks = p.max_chunks * p.H;
-  intra_kernel<D><<<(unsigned)blocks, kThreads, smem, s>>>(p);
+  intra_kernel<D><<<(unsigned)blocks, kThreads, smem, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
