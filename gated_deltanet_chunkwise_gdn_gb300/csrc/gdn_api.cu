@@ -44,20 +44,13 @@ void prof_end(int rec, cudaStream_t s) {
   cudaEventRecord(g_prof.recs[rec].stop, s);
 }
 
-constexpr int kSmCountHint = 152;  // GB300: 2 dies x 76 SMs
-
 bool supported_shape(int K, int V, int C) {
   if (K != V) return false;
   return (K == 64 || K == 128) && C == 64;
 }
 
-// Value-dimension split of the scan: enough (sequence, head, block) CTAs to cover
-// the SMs twice, with blocks of at least 16 state rows.
-int choose_nvb(int B, int HV, int V) {
-  const int64_t chains = (int64_t)B * HV;
-  if (chains * (V / 32) >= 2 * kSmCountHint) return V / 32;
-  return V / 16;
-}
+// Value-dimension split of the scan: blocks of 64 state rows per CTA.
+int choose_nvb(int V) { return V / 64; }
 
 }  // namespace
 
@@ -108,7 +101,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.B = batch;
   p.H = H;
   p.HV = HV;
-  p.nvb = choose_nvb(batch, HV, V);
+  p.nvb = choose_nvb(V);
   p.scale = scale;
   p.max_chunks = L.max_chunks;
   p.status = reinterpret_cast<int32_t*>(ws + L.status);

@@ -31,7 +31,7 @@ namespace gdn {
 namespace {
 
 constexpr int C = 64;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps; warps w and w+4 share TMEM lanes 32(w%4)..+31
 constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
 
 template <int D>
@@ -58,7 +58,7 @@ __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + lo
 template <int LDF>
 __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  {
+  if (warp < 4) {
     const int b = warp * 16;
     const int c = lane & 15;
     float x[16];
@@ -76,10 +76,10 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   }
   __syncthreads();
   for (int I = 1; I < 4; ++I) {
-    float t[6];
+    float t[3];
     const int n_ent = I * 256;
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
+    for (int u = 0; u < 3; ++u) {
       const int e = threadIdx.x + u * kThreads;
       t[u] = 0.f;
       if (e < n_ent) {
@@ -91,7 +91,7 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
       }
     }
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
+    for (int u = 0; u < 3; ++u) {
       const int e = threadIdx.x + u * kThreads;
       if (e < n_ent) {
         const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
@@ -100,7 +100,7 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
+    for (int u = 0; u < 3; ++u) {
       const int e = threadIdx.x + u * kThreads;
       if (e < n_ent) {
         const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
@@ -113,7 +113,7 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
     }
     __syncthreads();
 #pragma unroll
-    for (int u = 0; u < 6; ++u) {
+    for (int u = 0; u < 3; ++u) {
       const int e = threadIdx.x + u * kThreads;
       if (e < n_ent) {
         const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
@@ -175,7 +175,10 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   const int4 ct = p.chunk_tab[j];
   const int64_t t0 = ct.y;
   const int len = ct.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sub = warp & 3;       // TMEM lane quarter of this warp
+  const int half = warp >> 2;     // which half of a row's columns this warp handles
+  const int row = 32 * sub + lane;  // TMEM lane / accumulator row of this thread
   const int r_heads = p.HV / p.H;
   const int hv0 = h * r_heads;
 
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   float* s_beta = s_g + C;
   float* s_rq = s_beta + C;
   float* s_rk = s_rq + C;
+  float* s_part = reinterpret_cast<float*>(smem + SM::XF);  // norm partial sums (before X is formed)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles, [1] v tile, [2] MMAs
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
 
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
 
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar[0], NB * 16384);
@@ -227,40 +231,46 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     tc::mma_commit(&bar[2]);
   }
   if (ok) {
-    // inverse row norms from the swizzled tiles: threads 0-63 k rows, 64-127 q rows
-    const int row = tid & 63;
-    const unsigned char* base = smem + SM::KQ + (tid >= 64 ? 8192 : 0);
+    // squared row norms from the swizzled tiles: rows 0-63 k, 64-127 q; each half of the
+    // threads sums half of the 16-byte chunks of the row
+    const int r64 = row & 63;
+    const unsigned char* base = smem + SM::KQ + (row >= 64 ? 8192 : 0);
     float ss = 0.f;
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
+    for (int q = 0; q < 4 * NB; ++q) {
+      const int cg = half * 4 * NB + q;  // chunk index over the whole row
+      const uint4 v4 = *reinterpret_cast<const uint4*>(base + (cg >> 3) * 16384 + tc::sw128_offset(r64, cg & 7));
+      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v4);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(base + b * 16384 + tc::sw128_offset(row, c));
-        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v4);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = __bfloat1622float2(e[u]);
-          ss += f.x * f.x + f.y * f.y;
-        }
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(e[u]);
+        ss += f.x * f.x + f.y * f.y;
       }
-    const float r = row < len ? rsqrtf(ss + kNormEps) : 0.f;
+    }
+    s_part[half * 128 + row] = ss;
+  }
+  __syncthreads();
+  if (ok && tid < 128) {
+    const int r64 = tid & 63;
+    const float ss = s_part[tid] + s_part[128 + tid];
+    const float r = r64 < len ? rsqrtf(ss + kNormEps) : 0.f;
     const int64_t jq = (int64_t)j * p.H + h;
     if (tid < 64) {
-      s_rk[row] = r;
-      p.rk[jq * C + row] = r;
+      s_rk[r64] = r;
+      p.rk[jq * C + r64] = r;
     } else {
-      s_rq[row] = r;
-      p.rq[jq * C + row] = r;
+      s_rq[r64] = r;
+      p.rq[jq * C + r64] = r;
     }
   }
   if (ok) ok = wait_all(&bar[2], 0, p.status);
-  float kq[C];  // this thread's row of K K^T (tid < 64) or Q K^T (tid >= 64), raw
+  float kq[32];  // columns [32*half, 32*half+32) of this row of K K^T (rows 0-63) or Q K^T (64-127)
   if (ok) {
     tc::fence_after_sync();
 #pragma unroll
-    for (int c = 0; c < C / 16; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t r[16];
-      tc::tmem_ld16(tmem + lane_base + 16 * c, r);
+      tc::tmem_ld16(tmem + lane_base + 32 * half + 16 * c, r);
       tc::tmem_wait_ld();
 #pragma unroll
       for (int u = 0; u < 16; ++u) kq[16 * c + u] = __uint_as_float(r[u]);
@@ -269,28 +279,32 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   }
   __syncthreads();
 
+  const int cbase = 32 * half;  // first column of this thread's half row
   uint32_t mma_phase = 1, v_phase = 0;
   for (int ih = 0; ok && ih < r_heads; ++ih) {
     const int hv = hv0 + ih;
     const int64_t jh = (int64_t)j * p.HV + hv;
     if (ih > 0) chunk_gates(p, hv, t0, len, jh, s_g, s_beta);
-    if (tid < C) {  // L = tril(diag(beta) K^K^^T, -1), row i
-      const int i = tid;
+    if (row < C) {  // L = tril(diag(beta) K^K^^T, -1), row i
+      const int i = row;
       const float bi = s_beta[i] * s_rk[i];
 #pragma unroll
-      for (int nu = 0; nu < C; ++nu) Lf[i * LDF + nu] = nu < i ? bi * s_rk[nu] * kq[nu] : 0.f;
+      for (int u = 0; u < 32; ++u) {
+        const int nu = cbase + u;
+        Lf[i * LDF + nu] = nu < i ? bi * s_rk[nu] * kq[u] : 0.f;
+      }
     } else {  // P = Gamma . tril(Q^K^^T), row r, straight to global
-      const int r = tid - C;
+      const int r = row - C;
       const float qr = s_rq[r], gr = s_g[r];
-      uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C);
+      uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C + cbase);
 #pragma unroll
-      for (int c = 0; c < C / 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int n0 = 8 * c + 2 * u, n1 = n0 + 1;
-          const float v0 = n0 <= r ? expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[n0] : 0.f;
-          const float v1 = n1 <= r ? expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[n1] : 0.f;
+          const int e0 = 8 * c + 2 * u, n0 = cbase + e0, n1 = n0 + 1;
+          const float v0 = n0 <= r ? __expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[e0] : 0.f;
+          const float v1 = n1 <= r ? __expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[e0 + 1] : 0.f;
           w[u] = pack_bf16(v0, v1);
         }
         prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -299,30 +313,30 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     __syncthreads();
     invert_unit_lower_64<LDF>(Lf, Xf);
 
-    {  // A' rows (threads 0-63) and A rows (threads 64-127), 128-byte swizzled K-major
-      const int i = tid & 63;
-      const bool is_a = tid >= 64;
+    {  // A' rows (rows 0-63) and A rows (rows 64-127), 128-byte swizzled K-major, half a row each
+      const int i = row & 63;
+      const bool is_a = row >= 64;
       const float gi = s_g[i], egi = expf(gi);
       unsigned char* dst = smem + SM::AA + (is_a ? 8192 : 0);
 #pragma unroll
-      for (int c = 0; c < C / 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float v2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int nu = 8 * c + 2 * u + e;
+            const int nu = cbase + 8 * c + 2 * u + e;
             float val = 0.f;
             if (nu <= i) {
               const float x = nu == i ? 1.f : Xf[i * LDF + nu];
-              val = is_a ? expf(gi - s_g[nu]) * x * s_beta[nu] : egi * x * s_beta[nu] * s_rk[nu];
+              val = is_a ? __expf(gi - s_g[nu]) * x * s_beta[nu] : egi * x * s_beta[nu] * s_rk[nu];
             }
             v2[e] = val;
           }
           w[u] = pack_bf16(v2[0], v2[1]);
         }
-        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(i, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(i, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     tc::fence_async_smem();
@@ -354,13 +368,13 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
       for (int b = 0; b < NB; ++b)
         tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, hv + 1, (int)t0, &bar[1]);
     }
-    {  // rows 0-63 of DW are W<-, rows 64-127 of DU are U~: one output row per thread
-      const bool is_u = tid >= 64;
-      const int mu = tid & 63;
-      bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D;
-      const uint32_t col0 = is_u ? 128u : 0u;
+    {  // rows 0-63 of DW are W<-, rows 64-127 of DU are U~: half an output row per thread
+      const bool is_u = row >= 64;
+      const int mu = row & 63;
+      bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D + half * (D / 2);
+      const uint32_t col0 = (is_u ? 128u : 0u) + half * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t r[16];
         tc::tmem_ld16(tmem + lane_base + col0 + 16 * c, r);
         tc::tmem_wait_ld();

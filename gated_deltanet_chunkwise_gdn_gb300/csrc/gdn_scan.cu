@@ -1,62 +1,71 @@
-// gdn_scan.cu — K3: the sequential inter-chunk scan with the output epilogue.
+// gdn_scan.cu — K3: the sequential inter-chunk scan with the output epilogue, on the
+// 5th-generation tensor cores (tcgen05, accumulators in TMEM) with TMA-fed chunk tiles.
 //
-// One CTA owns one (sequence, value head, block of VB state rows) chain. Rows of the
-// state S (V x K) evolve independently — the update contracts over the key dimension
-// only — so the value dimension is split across CTAs while the key dimension stays
-// whole ("nrm-training-kernels", section "Kernel": the grid splits batch, heads and
-// blocks of the value dimension, never the key dimension).
+// One CTA owns one (sequence, value head, block of VB = 64 state rows) chain. Rows of the
+// state S (V x K) evolve independently — the update contracts over the key dimension only
+// — so the value dimension is split across CTAs while the key dimension stays whole
+// ("nrm-training-kernels", section "Kernel": the grid splits batch, heads and blocks of
+// the value dimension, never the key dimension).
 //
 // For each chunk of the sequence, in order (pymllm page "pymllm.layers.attention.
-// gdn_chunkwise": the inter-chunk propagation stays sequential, ceil(T/C) steps), with
-// the state slice S (VB x K, fp32) held in registers for the whole chain:
+// gdn_chunkwise": the inter-chunk propagation stays sequential, ceil(T/C) steps):
 //   U  = U~ - W<- S^T                               (the chunk's new values)
 //   O  = diag(exp(g)/|q|) Q S^T + P U               (inter + masked intra part)
 //   S <- exp(g_C) S + (diag(exp(g_C - g)/|k|) U)^T K
-// which is "Simple math to speed up GDN prefill", section "Reminder": the chunk
-// transition S_[t+1] = S-> + (U~ - W<- S^T)^T K-> with S-> = gamma_C S and
-// K-> = diag(gamma_C / gamma) K^.
+// i.e. "Simple math to speed up GDN prefill", section "Reminder": the chunk transition
+// S_[t+1] = S-> + (U~ - W<- S^T)^T K-> with S-> = gamma_C S and K-> = diag(gamma_C/gamma) K^.
+//
+// Per chunk, three MMAs (M = 128, issued by one thread, fp32 accumulators in TMEM):
+//   MMA1  D1[128 x VB]  = [W<-; Q] S^T     rows 0-63: W<- S^T (-> U), rows 64-127: Q S^T
+//   MMA3  DS[K x VB]    = K^T Uk           the state increment, Uk = diag(exp(g_C-g)/|k|) U
+//   MMA2  D2[128 x VB]  = [*; P] U         rows 64-127: P U (rows 0-63 unused)
+// The fp32 state slice lives in registers as S^T (thread d holds key row d), its bf16
+// copy is the B operand of MMA1. U and Uk go through shared memory as the B operands of
+// MMA2/MMA3. A producer warp streams W<-, Q, K, P and the gate vectors of the next chunks
+// with TMA into a 3-stage ring (full/empty mbarriers, all waits bounded).
 //
 // The state is read from state_pool once at the start and written once at the end.
 #include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int C = 64;
-constexpr int kThreads = 128;
+constexpr int VB = 64;
+constexpr int kStages = 3;
+constexpr int kConsumers = 128;  // 4 warps: thread i <-> TMEM lane i
+constexpr int kThreads = kConsumers + 32;
+constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
+constexpr uint32_t kTmemCols = 256;           // D1 [0,64), DS [64,128), D2 [128,192)
 
-template <int D, int VB>
+template <int D>
 struct ScanSmem {
-  static constexpr int LDT = D + 8;   // bf16 pitch of W<-, q, k tiles and the bf16 state copy
-  static constexpr int LDP = C + 8;   // bf16 pitch of P
-  static constexpr int LDU = VB + 8;  // bf16 pitch of U~, U tiles
-  static constexpr size_t stage_bf16 = 3ull * C * LDT + 1ull * C * LDP + 1ull * C * LDU;
-  static constexpr size_t stage_bytes = stage_bf16 * sizeof(bf16) + 3ull * C * sizeof(float);
-  static constexpr size_t extra_bytes = (1ull * VB * LDT + 2ull * C * LDU) * sizeof(bf16);
-  static constexpr size_t bytes = 2 * stage_bytes + extra_bytes;
+  static constexpr int NB = D / 64;
+  // one stage (offsets from the stage base; every tile 128-byte swizzled, 1 KB aligned)
+  static constexpr uint32_t WQ = 0;                 // NB x [W<- block 8 KB][Q block 8 KB]
+  static constexpr uint32_t K = WQ + NB * 16384;    // NB x K block 8 KB
+  static constexpr uint32_t P = K + NB * 8192;      // P 8 KB (the 8 KB before it: A rows 0-63 of MMA2)
+  static constexpr uint32_t F = P + 8192;           // g, 1/|q|, 1/|k| (3 x 256 B)
+  static constexpr uint32_t STAGE = F + 1024;
+  static constexpr uint32_t SCOPY = kStages * STAGE;  // bf16 S^T: D rows x 128 B
+  static constexpr uint32_t VN = SCOPY + D * 128;     // U  [64 rows x 128 B]
+  static constexpr uint32_t VK = VN + 8192;           // Uk [64 rows x 128 B]
+  static constexpr uint32_t BAR = VK + 8192;          // full[3], empty[3], mma, TMEM address, flag
+  static constexpr uint32_t bytes = BAR + 128;
+  static constexpr uint32_t alloc = bytes + 1024;
+  static constexpr uint32_t stage_tx = NB * 16384 + NB * 8192 + 8192 + 3 * 256;
 };
 
-template <int W, int LD>
-__device__ __forceinline__ void load_rows(bf16* s, const bf16* g, int64_t gstride, int rows) {
-  constexpr int SEG = W / 8;
-  for (int e = threadIdx.x; e < C * SEG; e += kThreads) {
-    const int r = e / SEG, c = (e % SEG) * 8;
-    if (r < rows)
-      cp_async_16(s + r * LD + c, g + r * gstride + c);
-    else
-      *reinterpret_cast<uint4*>(s + r * LD + c) = make_uint4(0, 0, 0, 0);
-  }
-}
-
-template <int D, int VB>
-__global__ void __launch_bounds__(kThreads) scan_kernel(Params p) {
-  using SM = ScanSmem<D, VB>;
-  constexpr int LDT = SM::LDT, LDP = SM::LDP, LDU = SM::LDU;
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p) {
+  using SM = ScanSmem<D>;
+  constexpr int NB = SM::NB;
   constexpr int NVB = D / VB;
-  constexpr int MT = VB / 16;      // m-tiles of the state slice
-  constexpr int NTS = D / 32;      // n-tiles of the state slice per warp
-  constexpr int NTX = VB / 8;      // n-tiles of U / O
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   if (p.status[0] != GDN_OK) return;
   int bid = blockIdx.x;
@@ -69,240 +78,269 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(Params p) {
   const int n_c = p.seq_chunk_off[seq + 1] - c_beg;
   if (n_c == 0) return;  // empty sequence: the slot is left as it is
   const int64_t slot = p.cache_indices[seq];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, t4 = lane & 3;
-  const int lm = lane >> 3, lr = lane & 7;
+  const int tid = threadIdx.x, warp = tid >> 5;
 
-  auto stage_ptr = [&](int st) { return smem + st * SM::stage_bytes; };
-  auto Ws = [&](int st) { return reinterpret_cast<bf16*>(stage_ptr(st)); };
-  auto Qs = [&](int st) { return Ws(st) + C * LDT; };
-  auto Ks = [&](int st) { return Ws(st) + 2 * C * LDT; };
-  auto Ps = [&](int st) { return Ws(st) + 3 * C * LDT; };
-  auto Us = [&](int st) { return Ps(st) + C * LDP; };
-  auto Fs = [&](int st) { return reinterpret_cast<float*>(stage_ptr(st) + SM::stage_bf16 * sizeof(bf16)); };
-  bf16* Sbf = reinterpret_cast<bf16*>(smem + 2 * SM::stage_bytes);
-  bf16* Vn = Sbf + VB * LDT;
-  bf16* Vk = Vn + C * LDU;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::BAR);
+  uint64_t* empty = full + kStages;
+  uint64_t* mma_bar = empty + kStages;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
+  volatile int* s_fail = reinterpret_cast<volatile int*>(tslot + 1);
 
-  int st_t0[2], st_len[2];
-  auto issue = [&](int c, int st) {
-    const int j = c_beg + c;
-    const int4 ct = p.chunk_tab[j];
-    st_t0[st] = ct.y;
-    st_len[st] = ct.z;
-    const int64_t jh = (int64_t)j * p.HV + hv;
-    const int64_t t0 = ct.y;
-    load_rows<D, LDT>(Ws(st), p.W + jh * C * D, D, C);
-    load_rows<D, LDT>(Qs(st), p.q + (t0 * p.H + h) * D, (int64_t)p.H * D, ct.z);
-    load_rows<D, LDT>(Ks(st), p.k + (t0 * p.H + h) * D, (int64_t)p.H * D, ct.z);
-    load_rows<C, LDP>(Ps(st), p.P + jh * C * C, C, C);
-    load_rows<VB, LDU>(Us(st), p.U + jh * C * D + vblk * VB, D, C);
-    float* F = Fs(st);
-    const int64_t jq = (int64_t)j * p.H + h;
-    if (tid < 16) cp_async_16(F + tid * 4, p.g + jh * C + tid * 4);
-    else if (tid < 32) cp_async_16(F + C + (tid - 16) * 4, p.rq + jq * C + (tid - 16) * 4);
-    else if (tid < 48) cp_async_16(F + 2 * C + (tid - 32) * 4, p.rk + jq * C + (tid - 32) * 4);
-    cp_async_commit();
-  };
-
-  // state slice: warp w owns key columns [w*D/4, (w+1)*D/4)
-  float S[MT][NTS][4];
-  float* Sg = p.state_pool + ((slot * p.HV + hv) * (int64_t)D + vblk * VB) * D;
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NTS; ++nt)
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int row = 16 * mt + g4 + 8 * hr, col = warp * (D / 4) + 8 * nt + 2 * t4;
-        const float2 s2 = *reinterpret_cast<const float2*>(Sg + (int64_t)row * D + col);
-        S[mt][nt][2 * hr] = s2.x;
-        S[mt][nt][2 * hr + 1] = s2.y;
-        *reinterpret_cast<uint32_t*>(Sbf + row * LDT + col) = pack_bf16(s2.x, s2.y);
-      }
-
-  issue(0, 0);
-  for (int c = 0; c < n_c; ++c) {
-    const int st = c & 1;
-    if (c + 1 < n_c) {
-      issue(c + 1, st ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
     }
-    __syncthreads();
-    const float* F = Fs(st);
-    const float* gs = F;
-    const float* rqs = F + C;
-    const float* rks = F + 2 * C;
-    const float gC = gs[C - 1];
+    tc::mbar_init(mma_bar, 1);
+    *s_fail = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tslot;
 
-    // Step 1: X = [W<- ; Q] S^T, rows [32*warp, +32) of the 128-row stack
-    float X[2][NTX][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NTX; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) X[mt][nt][r] = 0.f;
-    const bf16* Abase = warp < 2 ? Ws(st) + 32 * warp * LDT : Qs(st) + 32 * (warp - 2) * LDT;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      uint32_t a0[4], a1[4];
-      ldmatrix_x4(a0, Abase + (lane & 15) * LDT + 16 * kk + (lane >> 4) * 8);
-      ldmatrix_x4(a1, Abase + (16 + (lane & 15)) * LDT + 16 * kk + (lane >> 4) * 8);
-#pragma unroll
-      for (int nt = 0; nt < NTX; nt += 2) {
-        uint32_t b[4];
-        ldmatrix_x4(b, Sbf + (8 * (nt + (lm >> 1)) + lr) * LDT + 16 * kk + (lm & 1) * 8);
-        mma_bf16_16816(X[0][nt], a0, b[0], b[1]);
-        mma_bf16_16816(X[0][nt + 1], a0, b[2], b[3]);
-        mma_bf16_16816(X[1][nt], a1, b[0], b[1]);
-        mma_bf16_16816(X[1][nt + 1], a1, b[2], b[3]);
+  if (warp == kConsumers / 32) {
+    // ------------------------------------------------------------------ producer warp
+    if ((tid & 31) == 0) {
+      for (int c = 0; c < n_c; ++c) {
+        const int s = c % kStages, use = c / kStages;
+        if (use > 0 && !tc::mbar_wait(&empty[s], (use - 1) & 1, kWaitBudget)) {
+          set_status(p.status, GDN_ERR_TIMEOUT);
+          *s_fail = 1;
+          break;
+        }
+        const int j = c_beg + c;
+        const int4 ct = p.chunk_tab[j];
+        const int t0 = ct.y;
+        const int64_t jh = (int64_t)j * p.HV + hv;
+        const int64_t jq = (int64_t)j * p.H + h;
+        unsigned char* st = smem + s * SM::STAGE;
+        reinterpret_cast<int*>(st + SM::F + 768)[0] = ct.y;  // first token and length of the chunk,
+        reinterpret_cast<int*>(st + SM::F + 768)[1] = ct.z;  // published by the barrier's release
+        tc::mbar_arrive_expect_tx(&full[s], SM::stage_tx);
+        for (int b = 0; b < NB; ++b) {
+          tc::tma_load_2d(st + SM::WQ + b * 16384, &tm_w, 64 * b, (int)(jh * C), &full[s]);
+          tc::tma_load_3d(st + SM::WQ + b * 16384 + 8192, &tm_q, 64 * b, h, t0, &full[s]);
+          tc::tma_load_3d(st + SM::K + b * 8192, &tm_k, 64 * b, h, t0, &full[s]);
+        }
+        tc::tma_load_2d(st + SM::P, &tm_p, 0, (int)(jh * C), &full[s]);
+        tc::bulk_load(st + SM::F, p.g + jh * C, 256, &full[s]);
+        tc::bulk_load(st + SM::F + 256, p.rq + jq * C, 256, &full[s]);
+        tc::bulk_load(st + SM::F + 512, p.rk + jq * C, 256, &full[s]);
       }
     }
-
-    // Step 2: U = U~ - W<- S^T (warps 0-1); row-scaled inter output (warps 2-3)
-    if (warp < 2) {
-      const bf16* Ut = Us(st);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ consumer warps
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const bool has_state = tid < D;      // thread d holds key row d of S^T
+    const bool u_row = tid < C;          // thread mu forms row mu of U
+    const bool o_row = tid >= 64;        // thread 64 + r forms output row r
+    float S[VB];
+    float* Sg = p.state_pool + ((slot * p.HV + hv) * (int64_t)D + vblk * VB) * D;  // S[v][d] = Sg[v*D + d]
+    if (has_state) {
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int v = 0; v < VB; ++v) S[v] = Sg[(int64_t)v * D + tid];
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int mu = 32 * warp + 16 * mt + g4 + 8 * hr;
-          const float sk = expf(gC - gs[mu]) * rks[mu];
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
 #pragma unroll
-          for (int nt = 0; nt < NTX; ++nt) {
-            const int col = 8 * nt + 2 * t4;
-            const float2 u2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Ut + mu * LDU + col));
-            const float n0 = u2.x - X[mt][nt][2 * hr], n1 = u2.y - X[mt][nt][2 * hr + 1];
-            *reinterpret_cast<uint32_t*>(Vn + mu * LDU + col) = pack_bf16(n0, n1);
-            *reinterpret_cast<uint32_t*>(Vk + mu * LDU + col) = pack_bf16(n0 * sk, n1 * sk);
-          }
-        }
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = 32 * (warp - 2) + 16 * mt + g4 + 8 * hr;
-          const float sq = expf(gs[r]) * rqs[r];
-#pragma unroll
-          for (int nt = 0; nt < NTX; ++nt) {
-            X[mt][nt][2 * hr] *= sq;
-            X[mt][nt][2 * hr + 1] *= sq;
-          }
-        }
+        for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S[8 * c + 2 * u], S[8 * c + 2 * u + 1]);
+        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
-    __syncthreads();
+    // U~ row of the first chunk (rows of later chunks are prefetched one chunk ahead)
+    uint4 ut[8];
+    if (u_row) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.U + ((int64_t)c_beg * p.HV + hv) * C * D + (int64_t)tid * D + vblk * VB);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ut[c] = src[c];
+    }
+    tc::fence_async_smem();
+    tc::named_sync(1, kConsumers);
 
-    // Step 3a: O = inter + P U, stored (warps 2-3)
-    if (warp >= 2) {
-      const bf16* Pb = Ps(st) + 32 * (warp - 2) * LDP;
+    constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
+    constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
+    uint32_t mma_phase = 0;
+    bool failed = false;
+    for (int c = 0; c < n_c; ++c) {
+      const int s = c % kStages;
+      unsigned char* st = smem + s * SM::STAGE;
+      bool bad = !tc::mbar_wait(&full[s], (c / kStages) & 1, kWaitBudget) || *s_fail != 0;
+      if (tc::named_sync_or(1, kConsumers, bad)) {  // the same verdict in every consumer thread
+        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+        failed = true;
+        break;
+      }
+      // MMA1: D1 = [W<-; Q] S^T
+      if (tid == 0) {
+        tc::fence_after_sync();
+        for (int b = 0; b < NB; ++b)
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::WQ + b * 16384) + ks * 32, 16, 1024, tc::kSwizzle128B);
+            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::SCOPY) + b * 8192 + ks * 2048, D * 128, 1024,
+                                              tc::kSwizzle128B);
+            tc::mma_f16_ss(tmem, a, bd, idesc_x, (b | ks) != 0);
+          }
+        tc::mma_commit(mma_bar);
+      }
+      const float* gs = reinterpret_cast<const float*>(st + SM::F);
+      const float* rqs = gs + C;
+      const float* rks = gs + 2 * C;
+      const float gC = gs[C - 1];
+      const int ct_t0 = reinterpret_cast<const int*>(st + SM::F + 768)[0];
+      const int ct_len = reinterpret_cast<const int*>(st + SM::F + 768)[1];
+      const float sk_row = u_row ? expf(gC - gs[tid]) * rks[tid] : 0.f;       // Uk row scale
+      const float sq_row = o_row ? expf(gs[tid - 64]) * rqs[tid - 64] * p.scale : 0.f;  // O row scale
+      if (!tc::mbar_wait(mma_bar, mma_phase & 1, kWaitBudget)) {
+        *s_fail = 1;
+        set_status(p.status, GDN_ERR_TIMEOUT);
+      }
+      ++mma_phase;
+      tc::fence_after_sync();
+      if (u_row) {  // U = U~ - W<- S^T and Uk, row mu = tid
+        const float sk = sk_row;
+        uint32_t rr[VB / 16][16];
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk) {
-        uint32_t a0[4], a1[4];
-        ldmatrix_x4(a0, Pb + (lane & 15) * LDP + 16 * kk + (lane >> 4) * 8);
-        ldmatrix_x4(a1, Pb + (16 + (lane & 15)) * LDP + 16 * kk + (lane >> 4) * 8);
+        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + 16 * cc, rr[cc]);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int nt = 0; nt < NTX; nt += 2) {
-          uint32_t b[4];
-          ldmatrix_x4_trans(b, Vn + (16 * kk + (lm & 1) * 8 + lr) * LDU + 8 * (nt + (lm >> 1)));
-          mma_bf16_16816(X[0][nt], a0, b[0], b[1]);
-          mma_bf16_16816(X[0][nt + 1], a0, b[2], b[3]);
-          mma_bf16_16816(X[1][nt], a1, b[0], b[1]);
-          mma_bf16_16816(X[1][nt + 1], a1, b[2], b[3]);
+        for (int cc = 0; cc < VB / 16; ++cc) {
+          const uint32_t* r = rr[cc];
+          uint32_t wn[8], wk[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat162 u2 = reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3];
+            const float2 uf = __bfloat1622float2(u2);
+            const float n0 = uf.x - __uint_as_float(r[2 * u]), n1 = uf.y - __uint_as_float(r[2 * u + 1]);
+            wn[u] = pack_bf16(n0, n1);
+            wk[u] = pack_bf16(n0 * sk, n1 * sk);
+          }
+          *reinterpret_cast<uint4*>(smem + SM::VN + tc::sw128_offset(tid, 2 * cc)) = make_uint4(wn[0], wn[1], wn[2], wn[3]);
+          *reinterpret_cast<uint4*>(smem + SM::VN + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(wn[4], wn[5], wn[6], wn[7]);
+          *reinterpret_cast<uint4*>(smem + SM::VK + tc::sw128_offset(tid, 2 * cc)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          *reinterpret_cast<uint4*>(smem + SM::VK + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(wk[4], wk[5], wk[6], wk[7]);
+        }
+        if (c + 1 < n_c) {  // prefetch the next chunk's U~ row
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.U + ((int64_t)(c_beg + c + 1) * p.HV + hv) * C * D + (int64_t)tid * D + vblk * VB);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) ut[q] = src[q];
         }
       }
-      const int64_t t0 = st_t0[st];
-      const int len = st_len[st];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = 32 * (warp - 2) + 16 * mt + g4 + 8 * hr;
-          if (r < len) {
-            bf16* orow = p.out + ((t0 + r) * p.HV + hv) * (int64_t)D + vblk * VB;
-#pragma unroll
-            for (int nt = 0; nt < NTX; ++nt)
-              *reinterpret_cast<uint32_t*>(orow + 8 * nt + 2 * t4) =
-                  pack_bf16(p.scale * X[mt][nt][2 * hr], p.scale * X[mt][nt][2 * hr + 1]);
-          }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, kConsumers);
+      // MMA3: DS = K^T Uk ; MMA2: D2 = [*; P] U
+      if (tid == 0) {
+        tc::fence_after_sync();
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::smem_desc(tc::saddr(st + SM::K) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+          const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VK) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16_ss(tmem + 64, a, bd, idesc_s, ks > 0);
         }
-    }
-
-    // Step 3b: S <- exp(g_C) S + Vk^T K (all warps, key columns of this warp)
-    {
-      const float eC = expf(gC);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = tc::smem_desc(tc::saddr(st + SM::P - 8192) + ks * 32, 16, 1024, tc::kSwizzle128B);
+          const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VN) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16_ss(tmem + 128, a, bd, idesc_x, ks > 0);
+        }
+        tc::mma_commit(mma_bar);
+      }
+      if (!tc::mbar_wait(mma_bar, mma_phase & 1, kWaitBudget)) {
+        *s_fail = 1;
+        set_status(p.status, GDN_ERR_TIMEOUT);
+      }
+      ++mma_phase;
+      tc::fence_after_sync();
+      if (tid == 0) tc::mbar_arrive(&empty[s]);  // the MMAs are done with stage s; scalars are in registers
+      if (has_state) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
+        const float eC = expf(gC);
+        uint32_t rr[VB / 16][16];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + 64 + 16 * cc, rr[cc]);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int nt = 0; nt < NTS; ++nt)
+        for (int cc = 0; cc < VB / 16; ++cc) {
+          const uint32_t* r = rr[cc];
+          uint32_t w[8];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) S[mt][nt][r] *= eC;
-      const bf16* Kt = Ks(st);
-      const int cb = warp * (D / 4);
+          for (int u = 0; u < 16; ++u) S[16 * cc + u] = fmaf(eC, S[16 * cc + u], __uint_as_float(r[u]));
 #pragma unroll
-      for (int kk = 0; kk < C / 16; ++kk) {
-        uint32_t a[MT][4];
+          for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S[16 * cc + 2 * u], S[16 * cc + 2 * u + 1]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+      if (o_row) {  // O row r = exp(g_r)/|q_r| (Q S^T)_r + (P U)_r
+        const int r = tid - 64;
+        const float sq = sq_row;
+        const bool store = r < ct_len;  // padded rows are computed but not stored
+        bf16* orow = p.out + (((int64_t)ct_t0 + r) * p.HV + hv) * (int64_t)D + vblk * VB;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          ldmatrix_x4_trans(a[mt], Vk + (16 * kk + (lm >> 1) * 8 + lr) * LDU + 16 * mt + (lm & 1) * 8);
+        for (int cc = 0; cc < VB / 16; ++cc) {
+          uint32_t a[16], b[16];  // tcgen05.ld is warp-collective: every lane loads
+          tc::tmem_ld16(tmem + lane_base + 16 * cc, a);
+          tc::tmem_ld16(tmem + lane_base + 128 + 16 * cc, b);
+          tc::tmem_wait_ld();
+          uint32_t w[8];
 #pragma unroll
-        for (int nt = 0; nt < NTS; nt += 2) {
-          uint32_t b[4];
-          ldmatrix_x4_trans(b, Kt + (16 * kk + (lm & 1) * 8 + lr) * LDT + cb + 8 * (nt + (lm >> 1)));
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            mma_bf16_16816(S[mt][nt], a[mt], b[0], b[1]);
-            mma_bf16_16816(S[mt][nt + 1], a[mt], b[2], b[3]);
+          for (int u = 0; u < 8; ++u)
+            w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
+                             sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
+          if (store) {
+            uint4* d4 = reinterpret_cast<uint4*>(orow + 16 * cc);
+            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
         }
       }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NTS; ++nt)
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const int row = 16 * mt + g4 + 8 * hr, col = cb + 8 * nt + 2 * t4;
-            *reinterpret_cast<uint32_t*>(Sbf + row * LDT + col) = pack_bf16(S[mt][nt][2 * hr], S[mt][nt][2 * hr + 1]);
-          }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, kConsumers);
     }
-    __syncthreads();
+    if (has_state && !failed) {
+#pragma unroll
+      for (int v = 0; v < VB; ++v) Sg[(int64_t)v * D + tid] = S[v];
+    }
   }
 
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NTS; ++nt)
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int row = 16 * mt + g4 + 8 * hr, col = warp * (D / 4) + 8 * nt + 2 * t4;
-        *reinterpret_cast<float2*>(Sg + (int64_t)row * D + col) = make_float2(S[mt][nt][2 * hr], S[mt][nt][2 * hr + 1]);
-      }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
-template <int D, int VB>
+template <int D>
 cudaError_t launch_scan_t(const Params& p, cudaStream_t s) {
-  const size_t smem = ScanSmem<D, VB>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(scan_kernel<D, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  using SM = ScanSmem<D>;
+  const int64_t rows = p.max_chunks * p.HV * C;
+  CUtensorMap mw, mp, mq, mk;
+  if (!make_2d_tile_map(&mw, p.W, D, rows, 64, C, true) || !make_2d_tile_map(&mp, p.P, C, rows, 64, C, true) ||
+      !make_token_tile_map(&mq, p.q, D, p.H, p.T, C) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(scan_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::alloc);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.B * p.HV * (D / VB);
-  scan_kernel<D, VB><<<(unsigned)blocks, kThreads, smem, s>>>(p);
+  scan_kernel<D><<<(unsigned)blocks, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
-  if (Cc != C) return cudaErrorInvalidValue;
-  const int vb = D / p.nvb;
-  if (D == 64 && vb == 16) return launch_scan_t<64, 16>(p, s);
-  if (D == 64 && vb == 32) return launch_scan_t<64, 32>(p, s);
-  if (D == 128 && vb == 16) return launch_scan_t<128, 16>(p, s);
-  if (D == 128 && vb == 32) return launch_scan_t<128, 32>(p, s);
-  return cudaErrorInvalidValue;
+  if (Cc != C || p.nvb != D / VB) return cudaErrorInvalidValue;
+  switch (D) {
+    case 64: return launch_scan_t<64>(p, s);
+    case 128: return launch_scan_t<128>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace gdn
