@@ -10,7 +10,7 @@
 namespace {
 
 // ---------------------------------------------------------------- instrumentation
-enum KernelId { kKernSchedule = 0, kKernIntra = 1, kKernScan = 2, kKernCount = 3 };
+enum KernelId { kKernSchedule = 0, kKernIntra = 1, kKernScan = 2, kKernCount = 3 };  // scan: every scan-stage launch
 const char* const kKernelNames[kKernCount] = {"schedule", "intra", "scan"};
 
 std::atomic<int64_t> g_launches{0};
@@ -37,8 +37,8 @@ int prof_begin(int id, cudaStream_t s) {
   g_prof.recs.push_back(r);
   return i;
 }
-void prof_end(int rec, cudaStream_t s) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+void prof_end(int rec, cudaStream_t s, int kernels = 1) {
+  g_launches.fetch_add(kernels, std::memory_order_relaxed);
   if (rec < 0) return;
   std::lock_guard<std::mutex> lk(g_prof.mu);
   cudaEventRecord(g_prof.recs[rec].stop, s);
@@ -114,6 +114,9 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.W = reinterpret_cast<gdn::bf16*>(ws + L.w);
   p.U = reinterpret_cast<gdn::bf16*>(ws + L.u);
   p.P = reinterpret_cast<gdn::bf16*>(ws + L.p);
+  p.seg_state = reinterpret_cast<float*>(ws + L.seg_state);
+  p.seg_map = reinterpret_cast<float*>(ws + L.seg_map);
+  p.nseg = L.nseg;
 
   int rec = prof_begin(kKernSchedule, s);
   gdn::schedule_kernel<<<1, 512, 0, s>>>(p, chunk_size);
@@ -125,7 +128,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   prof_end(rec, s);
   rec = prof_begin(kKernScan, s);
   if (gdn::launch_scan(p, K, chunk_size, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
+  prof_end(rec, s, p.nseg <= 1 ? 1 : (p.nseg == 2 ? 2 : 3));  // segmented: maps, combine, segments
   return GDN_OK;
 }
 

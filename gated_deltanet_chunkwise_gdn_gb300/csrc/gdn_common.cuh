@@ -44,9 +44,26 @@ struct WsLayout {
   size_t w;              // bf16[max_chunks][HV][C][K]: W<-
   size_t u;              // bf16[max_chunks][HV][C][V]: U~
   size_t p;              // bf16[max_chunks][HV][C][C]: P
+  size_t seg_state;      // fp32[B][HV][nseg][V][K]: start state of each segment (segmented scan)
+  size_t seg_map;        // fp32[B][HV][nseg][2][K][K]: affine map (B, T) of each segment
   size_t total;
   int64_t max_chunks;
+  int nseg;
 };
+
+// Segments per sequence for the scan: more than one only when there are too few
+// (sequence, head, 64-row block) chains to fill the GPU and the sequences may be long.
+// The first launch of a segmented scan runs ctas * (1 + 2 (nseg - 2)) CTAs, one per SM.
+inline int choose_nseg(int64_t T, int B, int HV, int V, int C) {
+  const int64_t ctas = (int64_t)B * HV * (V / 64);
+  const int64_t max_chunks = T / C;  // the longest sequence has at most this many chunks
+  int best = 1;
+  for (int n = 2; n <= 8; ++n) {
+    const int64_t grid1 = ctas * (1 + 2 * (n - 2));
+    if (grid1 <= 148 && max_chunks >= 32 * n) best = n;
+  }
+  return best;
+}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -70,6 +87,10 @@ inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C
   L.w = take((size_t)mc * HV * C * K * sizeof(bf16));
   L.u = take((size_t)mc * HV * C * V * sizeof(bf16));
   L.p = take((size_t)mc * HV * C * C * sizeof(bf16));
+  L.nseg = choose_nseg(T, B, HV, V, C);
+  const size_t per_head = (size_t)K * K * sizeof(float);
+  L.seg_state = take(L.nseg > 1 ? (size_t)B * HV * L.nseg * per_head : 0);
+  L.seg_map = take(L.nseg > 2 ? (size_t)B * HV * L.nseg * 2 * per_head : 0);
   L.total = off;
   return L;
 }
@@ -105,6 +126,9 @@ struct Params {
   bf16* W;
   bf16* U;
   bf16* P;
+  float* seg_state;
+  float* seg_map;
+  int nseg;  // segments per sequence in the scan (1: one pass over each whole sequence)
 };
 
 // ----------------------------------------------------------------------------- device helpers

@@ -40,7 +40,7 @@ struct IntraSmem {
   static constexpr uint32_t KQ = 0;                     // NB x [K block 8 KB][Q block 8 KB]
   static constexpr uint32_t V = KQ + NB * 16384;        // NB x V block 8 KB
   static constexpr uint32_t AA = V + NB * 8192;         // [A' 8 KB][A 8 KB], 128-byte swizzled
-  static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x 65
+  static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x 65; then the low parts of [A'; A]
   static constexpr uint32_t XF = LF + 64 * 65 * 4;      // M^{-1}, fp32 64 x 65
   static constexpr uint32_t VEC = XF + 64 * 65 * 4;     // g, beta, 1/|q|, 1/|k| (4 x 64 fp32)
   static constexpr uint32_t BAR = VEC + 4 * 64 * 4;     // 3 mbarriers + TMEM address
@@ -52,9 +52,52 @@ constexpr uint32_t kTmemCols = 256;  // D1 / DW at columns [0, 128), DU at [128,
 
 __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo with both parts representable in tf32 (3xTF32 products keep ~fp32 accuracy).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = to_tf32(x);
+  lo = to_tf32(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32_1688(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One warp: acc (16 x 16, two 16x8 accumulator tiles) += A (16 x 16) * B (16 x 16), both
+// fp32 row-major in shared memory with pitch LDF, as 3xTF32 tensor-core products.
+template <int LDF>
+__device__ __forceinline__ void mm16_acc(float (&acc)[2][4], const float* A, const float* B) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    uint32_t ah[4], al[4];
+    split_tf32(A[g * LDF + 8 * ks + t], ah[0], al[0]);
+    split_tf32(A[(g + 8) * LDF + 8 * ks + t], ah[1], al[1]);
+    split_tf32(A[g * LDF + 8 * ks + t + 4], ah[2], al[2]);
+    split_tf32(A[(g + 8) * LDF + 8 * ks + t + 4], ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(B[(8 * ks + t) * LDF + 8 * nt + g], bh0, bl0);
+      split_tf32(B[(8 * ks + t + 4) * LDF + 8 * nt + g], bh1, bl1);
+      mma_tf32_1688(acc[nt], ah, bh0, bh1);
+      mma_tf32_1688(acc[nt], ah, bl0, bl1);
+      mma_tf32_1688(acc[nt], al, bh0, bh1);
+    }
+  }
+}
+
 // Inverts the unit lower-triangular 64x64 matrix I + L (L strictly lower, in Lf) into Xf,
 // by 16x16 blocks: the four diagonal blocks by forward substitution (one warp each, one
-// lane per column), then block rows I = 1..3 with X_IJ = -X_II * sum_{K=J}^{I-1} L_IK X_KJ.
+// lane per column, in registers), then block rows I = 1..3, one warp per block, with
+//   X_IJ = -X_II * sum_{K=J}^{I-1} L_IK X_KJ
+// formed as 3xTF32 warp-level tensor-core products (fp32 accuracy up to rounding order).
 template <int LDF>
 __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,49 +118,30 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
     }
   }
   __syncthreads();
+  const int g = lane >> 2, t = lane & 3;
   for (int I = 1; I < 4; ++I) {
-    float t[3];
-    const int n_ent = I * 256;
+    if (warp < I) {
+      const int J = warp;
+      float acc[2][4] = {};
+      for (int K = J; K < I; ++K) mm16_acc<LDF>(acc, Lf + 16 * I * LDF + 16 * K, Xf + 16 * K * LDF + 16 * J);
+      float* xij = Xf + 16 * I * LDF + 16 * J;
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      t[u] = 0.f;
-      if (e < n_ent) {
-        const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
-        const float* lrow = Lf + (16 * I + a) * LDF;
-        float acc = 0.f;
-        for (int kk = 16 * J; kk < 16 * I; ++kk) acc += lrow[kk] * Xf[kk * LDF + 16 * J + bcol];
-        t[u] = acc;
+      for (int nt = 0; nt < 2; ++nt) {  // T_IJ into the X_IJ slot
+        xij[g * LDF + 8 * nt + 2 * t] = acc[nt][0];
+        xij[g * LDF + 8 * nt + 2 * t + 1] = acc[nt][1];
+        xij[(g + 8) * LDF + 8 * nt + 2 * t] = acc[nt][2];
+        xij[(g + 8) * LDF + 8 * nt + 2 * t + 1] = acc[nt][3];
       }
-    }
+      __syncwarp();
+      float acc2[2][4] = {};
+      mm16_acc<LDF>(acc2, Xf + 16 * I * LDF + 16 * I, xij);
+      __syncwarp();
 #pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      if (e < n_ent) {
-        const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
-        Xf[(16 * I + a) * LDF + 16 * J + bcol] = t[u];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      if (e < n_ent) {
-        const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
-        const float* drow = Xf + (16 * I + a) * LDF + 16 * I;
-        float acc = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) acc += drow[cc] * Xf[(16 * I + cc) * LDF + 16 * J + bcol];
-        t[u] = -acc;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 3; ++u) {
-      const int e = threadIdx.x + u * kThreads;
-      if (e < n_ent) {
-        const int J = e >> 8, a = (e >> 4) & 15, bcol = e & 15;
-        Xf[(16 * I + a) * LDF + 16 * J + bcol] = t[u];
+      for (int nt = 0; nt < 2; ++nt) {
+        xij[g * LDF + 8 * nt + 2 * t] = -acc2[nt][0];
+        xij[g * LDF + 8 * nt + 2 * t + 1] = -acc2[nt][1];
+        xij[(g + 8) * LDF + 8 * nt + 2 * t] = -acc2[nt][2];
+        xij[(g + 8) * LDF + 8 * nt + 2 * t + 1] = -acc2[nt][3];
       }
     }
     __syncthreads();
@@ -313,14 +337,16 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     __syncthreads();
     invert_unit_lower_64<LDF>(Lf, Xf);
 
-    {  // A' rows (rows 0-63) and A rows (rows 64-127), 128-byte swizzled K-major, half a row each
+    __syncthreads();  // L is dead from here on: its buffer takes the low bf16 parts of [A'; A]
+    {  // A' rows (rows 0-63) and A rows (rows 64-127) as bf16 hi + lo, 128-byte swizzled K-major
       const int i = row & 63;
       const bool is_a = row >= 64;
       const float gi = s_g[i], egi = expf(gi);
-      unsigned char* dst = smem + SM::AA + (is_a ? 8192 : 0);
+      unsigned char* dst_hi = smem + SM::AA + (is_a ? 8192 : 0);
+      unsigned char* dst_lo = smem + SM::LF + (is_a ? 8192 : 0);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t w[4];
+        uint32_t wh[4], wl[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float v2[2];
@@ -334,9 +360,13 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
             }
             v2[e] = val;
           }
-          w[u] = pack_bf16(v2[0], v2[1]);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(v2[0], v2[1]);
+          const float2 hf = __bfloat1622float2(hi);
+          wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
+          wl[u] = pack_bf16(v2[0] - hf.x, v2[1] - hf.y);
         }
-        *reinterpret_cast<uint4*>(dst + tc::sw128_offset(i, 4 * half + c)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst_hi + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(dst_lo + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
     }
     tc::fence_async_smem();
@@ -347,16 +377,18 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     if (tid == 0) {
       tc::fence_after_sync();
       constexpr uint32_t idesc2 = tc::idesc_f16(128, D, 1, false, true);
-      for (int ks = 0; ks < C / 16; ++ks) {
-        const uint64_t a = tc::smem_desc(tc::saddr(smem + SM::AA) + ks * 32, 16, 1024, tc::kSwizzle128B);
-        const uint64_t bk = tc::smem_desc(tc::saddr(smem + SM::KQ) + ks * 2048, 16384, 1024, tc::kSwizzle128B);
-        tc::mma_f16_ss(tmem, a, bk, idesc2, ks > 0);
-      }
-      for (int ks = 0; ks < C / 16; ++ks) {
-        const uint64_t a = tc::smem_desc(tc::saddr(smem + SM::AA) + ks * 32, 16, 1024, tc::kSwizzle128B);
-        const uint64_t bv = tc::smem_desc(tc::saddr(smem + SM::V) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-        tc::mma_f16_ss(tmem + 128, a, bv, idesc2, ks > 0);
-      }
+      for (int part = 0; part < 2; ++part)  // [A'; A] = hi + lo
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t a = tc::smem_desc(tc::saddr(smem + (part ? SM::LF : SM::AA)) + ks * 32, 16, 1024, tc::kSwizzle128B);
+          const uint64_t bk = tc::smem_desc(tc::saddr(smem + SM::KQ) + ks * 2048, 16384, 1024, tc::kSwizzle128B);
+          tc::mma_f16_ss(tmem, a, bk, idesc2, (part | ks) != 0);
+        }
+      for (int part = 0; part < 2; ++part)
+        for (int ks = 0; ks < C / 16; ++ks) {
+          const uint64_t a = tc::smem_desc(tc::saddr(smem + (part ? SM::LF : SM::AA)) + ks * 32, 16, 1024, tc::kSwizzle128B);
+          const uint64_t bv = tc::smem_desc(tc::saddr(smem + SM::V) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+          tc::mma_f16_ss(tmem + 128, a, bv, idesc2, (part | ks) != 0);
+        }
       tc::mma_commit(&bar[2]);
     }
     ok = wait_all(&bar[2], mma_phase & 1, p.status);

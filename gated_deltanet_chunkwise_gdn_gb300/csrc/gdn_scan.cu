@@ -1,30 +1,33 @@
 // gdn_scan.cu — K3: the sequential inter-chunk scan with the output epilogue, on the
 // 5th-generation tensor cores (tcgen05, accumulators in TMEM) with TMA-fed chunk tiles.
 //
-// One CTA owns one (sequence, value head, block of VB = 64 state rows) chain. Rows of the
-// state S (V x K) evolve independently — the update contracts over the key dimension only
-// — so the value dimension is split across CTAs while the key dimension stays whole
-// ("nrm-training-kernels", section "Kernel": the grid splits batch, heads and blocks of
-// the value dimension, never the key dimension).
+// One CTA owns one block of VB = 64 state rows of one (sequence, value head) chain, for a
+// range of chunks. Rows of the state S (V x K) evolve independently — the update contracts
+// over the key dimension only — so the value dimension is split across CTAs while the key
+// dimension stays whole ("nrm-training-kernels", section "Kernel": the grid splits batch,
+// heads and blocks of the value dimension, never the key dimension).
 //
-// For each chunk of the sequence, in order (pymllm page "pymllm.layers.attention.
-// gdn_chunkwise": the inter-chunk propagation stays sequential, ceil(T/C) steps):
+// For each chunk, in order (pymllm page "pymllm.layers.attention.gdn_chunkwise": the
+// inter-chunk propagation stays sequential):
 //   U  = U~ - W<- S^T                               (the chunk's new values)
 //   O  = diag(exp(g)/|q|) Q S^T + P U               (inter + masked intra part)
-//   S <- exp(g_C) S + (diag(exp(g_C - g)/|k|) U)^T K
+//   S <- exp(g_C) S + U^T K->,   K-> = diag(exp(g_C - g)/|k|) K
 // i.e. "Simple math to speed up GDN prefill", section "Reminder": the chunk transition
-// S_[t+1] = S-> + (U~ - W<- S^T)^T K-> with S-> = gamma_C S and K-> = diag(gamma_C/gamma) K^.
+// S_[t+1] = S-> + (U~ - W<- S^T)^T K-> with S-> = gamma_C S.
 //
-// Per chunk, three MMAs (M = 128, issued by one thread, fp32 accumulators in TMEM):
-//   MMA1  D1[128 x VB]  = [W<-; Q] S^T     rows 0-63: W<- S^T (-> U), rows 64-127: Q S^T
-//   MMA3  DS[K x VB]    = K^T Uk           the state increment, Uk = diag(exp(g_C-g)/|k|) U
-//   MMA2  D2[128 x VB]  = [*; P] U         rows 64-127: P U (rows 0-63 unused)
-// The fp32 state slice lives in registers as S^T (thread d holds key row d), its bf16
-// copy is the B operand of MMA1. U and Uk go through shared memory as the B operands of
-// MMA2/MMA3. A producer warp streams W<-, Q, K, P and the gate vectors of the next chunks
-// with TMA into a 3-stage ring (full/empty mbarriers, all waits bounded).
+// Critical path per chunk (the "chain" warps 0-3; thread i <-> TMEM lane i):
+//   MMA1  D1[128 x 64] = [Q; W<-] S^T          -> U = U~ - D1[64:128]; Uk = diag(exp(g_C-g)/|k|) U
+//   MMA3  DS[K x 64]   = K^T (Uk_hi + Uk_lo)   -> S = exp(g_C) S + DS, bf16 copy to smem
+// Uk is carried as two bf16 terms (hi + lo) against the exact bf16 K tile, so the state
+// increment keeps about 16 bits of precision. Off the critical path:
+//   MMA2  D2[128 x 64] = [P; *] U  and warps 4-5 form O from D1[0:64] and D2[0:64] one chunk
+//   behind (D1, D2 double-buffered in TMEM);
+//   warp 6 streams Q, W<-, K, P and the gate vectors with TMA (2-3 stage ring).
 //
-// The state is read from state_pool once at the start and written once at the end.
+// Segment-parallel use (few long chains): besides a full scan over a chunk range
+// (state from a buffer, outputs written), the same kernel computes the affine map of a
+// chunk range — S_end = S_start T + B — as two scans without outputs: B from S_start = 0,
+// and T (K x K) from the identity with U~ = 0. combine_kernel then chains the maps.
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 
@@ -33,66 +36,169 @@ namespace {
 
 constexpr int C = 64;
 constexpr int VB = 64;
-constexpr int kStages = 3;
-constexpr int kConsumers = 128;  // 4 warps: thread i <-> TMEM lane i
-constexpr int kThreads = kConsumers + 32;
 constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
-constexpr uint32_t kTmemCols = 256;           // D1 [0,64), DS [64,128), D2 [128,192)
+// warps 0-3 chain, warps 4-5 outputs (TMEM lanes 0-63), warp 6 producer
+constexpr int kChain = 128, kOut = 64;
+constexpr int kThreads = 224;
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: D1 buffers [0,64) [64,128); DS [128,192); D2 buffers [256,320) [320,384)
+constexpr uint32_t kColD1 = 0, kColDS = 128, kColD2 = 256;
+
+enum Mode : int { kFull = 0, kMapB = 1, kMapT = 2 };
 
 template <int D>
 struct ScanSmem {
   static constexpr int NB = D / 64;
-  // one stage (offsets from the stage base; every tile 128-byte swizzled, 1 KB aligned)
-  static constexpr uint32_t WQ = 0;                 // NB x [W<- block 8 KB][Q block 8 KB]
-  static constexpr uint32_t K = WQ + NB * 16384;    // NB x K block 8 KB
-  static constexpr uint32_t P = K + NB * 8192;      // P 8 KB (the 8 KB before it: A rows 0-63 of MMA2)
-  static constexpr uint32_t F = P + 8192;           // g, 1/|q|, 1/|k| (3 x 256 B)
+  static constexpr int STAGES = 3;
+  static constexpr uint32_t QW = 0;                 // NB x [Q block 8 KB][W<- block 8 KB]
+  static constexpr uint32_t P = QW + NB * 16384;    // P 8 KB (A rows 64-127 of MMA2 = the 8 KB after it)
+  static constexpr uint32_t K = P + 8192;           // NB x K block 8 KB (+ the 8 KB after: MMA3 rows K..127 if D = 64)
+  static constexpr uint32_t F = K + NB * 8192;      // g, 1/|q|, 1/|k| (3 x 256 B), chunk t0 / len
   static constexpr uint32_t STAGE = F + 1024;
-  static constexpr uint32_t SCOPY = kStages * STAGE;  // bf16 S^T: D rows x 128 B
-  static constexpr uint32_t VN = SCOPY + D * 128;     // U  [64 rows x 128 B]
-  static constexpr uint32_t VK = VN + 8192;           // Uk [64 rows x 128 B]
-  static constexpr uint32_t BAR = VK + 8192;          // full[3], empty[3], mma, TMEM address, flag
-  static constexpr uint32_t bytes = BAR + 128;
+  static constexpr uint32_t SCOPY = STAGES * STAGE; // bf16 S^T: D rows x 128 B
+  static constexpr uint32_t VN = SCOPY + D * 128;   // U      [64 rows x 128 B]
+  static constexpr uint32_t VKH = VN + 8192;        // Uk hi  [64 rows x 128 B]
+  static constexpr uint32_t VKL = VKH + 8192;       // Uk lo  [64 rows x 128 B]
+  static constexpr uint32_t BAR = VKL + 8192;
+  static constexpr uint32_t bytes = BAR + 256;
   static constexpr uint32_t alloc = bytes + 1024;
-  static constexpr uint32_t stage_tx = NB * 16384 + NB * 8192 + 8192 + 3 * 256;
+  static constexpr uint32_t tx_full = NB * 16384 + NB * 8192 + 8192 + 3 * 256;  // W, Q, K, P, F
+  static constexpr uint32_t tx_map = NB * 8192 + NB * 8192 + 3 * 256;           // W, K, F
 };
+
+struct ScanJob {
+  int mode;
+  int seq, hv, vblk;
+  int c0, c1;         // chunk range [c0, c1) within the sequence
+  const float* init;  // [rows][D] start state (kFull); zeros (kMapB) / identity (kMapT) otherwise
+  float* fin;         // [rows][D] where the final state goes, or nullptr
+};
+
+// Segment bookkeeping: a sequence of n chunks is split into ns = ceil(n / L) non-empty
+// segments of L = ceil(n / nseg) chunks (the last one possibly shorter).
+__device__ __forceinline__ void seg_bounds(int n, int nseg, int p, int& c0, int& c1, int& ns) {
+  const int L = (n + nseg - 1) / nseg;
+  ns = L > 0 ? (n + L - 1) / L : 0;
+  c0 = min(n, p * L);
+  c1 = min(n, (p + 1) * L);
+}
+
+// Decodes this CTA's job. kind 0: whole sequences; kind 1: segment 0 (full) and the maps of
+// segments 1 .. ns-2; kind 2: segments 1 .. ns-1 (full). Returns false if there is no job.
+template <int D>
+__device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
+  constexpr int NVB = D / VB;
+  const int B = p.B, HV = p.HV;
+  const int64_t per_head = (int64_t)D * D;  // floats per (slot, value head) state
+  int bid = blockIdx.x;
+  job.init = nullptr;
+  job.fin = nullptr;
+  if (kind == 0 || (kind == 1 && bid < B * HV * NVB)) {
+    job.vblk = bid % NVB;
+    bid /= NVB;
+    job.seq = p.order[bid / HV];
+    job.hv = bid % HV;
+    const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
+    float* pool = p.state_pool + (p.cache_indices[job.seq] * HV + job.hv) * per_head;
+    job.mode = kFull;
+    job.init = pool;
+    if (kind == 0) {
+      job.c0 = 0;
+      job.c1 = n;
+      job.fin = pool;
+    } else {
+      int ns;
+      seg_bounds(n, nseg, 0, job.c0, job.c1, ns);
+      job.fin = ns > 1 ? p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + 1) * per_head : pool;
+    }
+    return job.c1 > job.c0;
+  }
+  if (kind == 1) {  // maps of segments 1 .. nseg-2: (B rows | T rows) x NVB blocks each
+    bid -= B * HV * NVB;
+    const int per_chain = (nseg - 2) * 2 * NVB;
+    const int rest = bid / per_chain;
+    int idx = bid % per_chain;
+    job.seq = p.order[rest / HV];
+    job.hv = rest % HV;
+    job.vblk = idx % NVB;
+    idx /= NVB;
+    const int which = idx % 2, seg = 1 + idx / 2;
+    const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
+    int ns;
+    seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+    if (seg >= ns - 1) return false;
+    job.mode = which == 0 ? kMapB : kMapT;
+    job.fin = p.seg_map + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * 2 * per_head + (which == 0 ? 0 : per_head);
+    return job.c1 > job.c0;
+  }
+  // kind 2: segments 1 .. nseg-1, full
+  job.vblk = bid % NVB;
+  bid /= NVB;
+  const int seg = 1 + bid % (nseg - 1);
+  bid /= (nseg - 1);
+  job.seq = p.order[bid / HV];
+  job.hv = bid % HV;
+  const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
+  int ns;
+  seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+  if (seg >= ns) return false;
+  job.mode = kFull;
+  job.init = p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * per_head;
+  job.fin = seg == ns - 1 ? p.state_pool + (p.cache_indices[job.seq] * HV + job.hv) * per_head : nullptr;
+  return job.c1 > job.c0;
+}
+
+// Bounded mbarrier wait that also gives up as soon as another role reported a failure.
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (*fail || clock64() - t0 > kWaitBudget) return false;
+  }
+  return true;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
-                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p) {
+                const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p, int kind,
+                int nseg) {
   using SM = ScanSmem<D>;
-  constexpr int NB = SM::NB;
-  constexpr int NVB = D / VB;
+  constexpr int NB = SM::NB, S = SM::STAGES;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   if (p.status[0] != GDN_OK) return;
-  int bid = blockIdx.x;
-  const int vblk = bid % NVB;
-  bid /= NVB;
-  const int hv = bid % p.HV;
-  const int seq = p.order[bid / p.HV];
+  ScanJob job;
+  if (!decode_job<D>(p, kind, nseg, job)) return;  // uniform over the CTA
+  const int mode = job.mode, hv = job.hv, vblk = job.vblk;
   const int h = hv / (p.HV / p.H);
-  const int c_beg = p.seq_chunk_off[seq];
-  const int n_c = p.seq_chunk_off[seq + 1] - c_beg;
-  if (n_c == 0) return;  // empty sequence: the slot is left as it is
-  const int64_t slot = p.cache_indices[seq];
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int cb = p.seq_chunk_off[job.seq];
+  const int nc = job.c1 - job.c0;
+  const bool full_mode = mode == kFull;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::BAR);
-  uint64_t* empty = full + kStages;
-  uint64_t* mma_bar = empty + kStages;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mma_bar + 1);
-  volatile int* s_fail = reinterpret_cast<volatile int*>(tslot + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [S]
+  uint64_t* empty = full + S;                                    // [S]
+  uint64_t* mma1 = empty + S;                                    // D1 ready
+  uint64_t* mma3 = mma1 + 1;                                     // DS ready
+  uint64_t* mmao = mma3 + 1;                                     // [2] D2 ready (per buffer)
+  uint64_t* odone = mmao + 2;                                    // [2] O warps done with D1/D2 buffer
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(odone + 2);
+  volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&empty[s], full_mode ? 2 : 1);  // the chain (and the output warps) release a stage
     }
-    tc::mbar_init(mma_bar, 1);
-    *s_fail = 0;
+    tc::mbar_init(mma1, 1);
+    tc::mbar_init(mma3, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&mmao[b], 1);
+      tc::mbar_init(&odone[b], kOut);
+    }
+    *fail = 0;
     tc::mbar_fence_init();
   }
   if (warp == 0) {
@@ -103,209 +209,239 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tslot;
+  auto report = [&]() {
+    *fail = 1;
+    set_status(p.status, GDN_ERR_TIMEOUT);
+  };
 
-  if (warp == kConsumers / 32) {
-    // ------------------------------------------------------------------ producer warp
-    if ((tid & 31) == 0) {
-      for (int c = 0; c < n_c; ++c) {
-        const int s = c % kStages, use = c / kStages;
-        if (use > 0 && !tc::mbar_wait(&empty[s], (use - 1) & 1, kWaitBudget)) {
-          set_status(p.status, GDN_ERR_TIMEOUT);
-          *s_fail = 1;
+  if (warp == 6) {
+    // ------------------------------------------------------------------ producer: TMA
+    if (lane == 0) {
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % S, use = c / S;
+        if (use > 0 && !wait_or_fail(&empty[s], (use - 1) & 1, fail)) {
+          report();
           break;
         }
-        const int j = c_beg + c;
+        const int j = cb + job.c0 + c;
         const int4 ct = p.chunk_tab[j];
-        const int t0 = ct.y;
         const int64_t jh = (int64_t)j * p.HV + hv;
         const int64_t jq = (int64_t)j * p.H + h;
         unsigned char* st = smem + s * SM::STAGE;
-        reinterpret_cast<int*>(st + SM::F + 768)[0] = ct.y;  // first token and length of the chunk,
-        reinterpret_cast<int*>(st + SM::F + 768)[1] = ct.z;  // published by the barrier's release
-        tc::mbar_arrive_expect_tx(&full[s], SM::stage_tx);
+        reinterpret_cast<int*>(st + SM::F + 768)[0] = ct.y;
+        reinterpret_cast<int*>(st + SM::F + 768)[1] = ct.z;
+        tc::mbar_arrive_expect_tx(&full[s], full_mode ? SM::tx_full : SM::tx_map);
         for (int b = 0; b < NB; ++b) {
-          tc::tma_load_2d(st + SM::WQ + b * 16384, &tm_w, 64 * b, (int)(jh * C), &full[s]);
-          tc::tma_load_3d(st + SM::WQ + b * 16384 + 8192, &tm_q, 64 * b, h, t0, &full[s]);
-          tc::tma_load_3d(st + SM::K + b * 8192, &tm_k, 64 * b, h, t0, &full[s]);
+          if (full_mode) tc::tma_load_3d(st + SM::QW + b * 16384, &tm_q, 64 * b, h, ct.y, &full[s]);
+          tc::tma_load_2d(st + SM::QW + b * 16384 + 8192, &tm_w, 64 * b, (int)(jh * C), &full[s]);
+          tc::tma_load_3d(st + SM::K + b * 8192, &tm_k, 64 * b, h, ct.y, &full[s]);
         }
-        tc::tma_load_2d(st + SM::P, &tm_p, 0, (int)(jh * C), &full[s]);
+        if (full_mode) tc::tma_load_2d(st + SM::P, &tm_p, 0, (int)(jh * C), &full[s]);
         tc::bulk_load(st + SM::F, p.g + jh * C, 256, &full[s]);
         tc::bulk_load(st + SM::F + 256, p.rq + jq * C, 256, &full[s]);
         tc::bulk_load(st + SM::F + 512, p.rk + jq * C, 256, &full[s]);
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------------ consumer warps
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    const bool has_state = tid < D;      // thread d holds key row d of S^T
-    const bool u_row = tid < C;          // thread mu forms row mu of U
-    const bool o_row = tid >= 64;        // thread 64 + r forms output row r
-    float S[VB];
-    float* Sg = p.state_pool + ((slot * p.HV + hv) * (int64_t)D + vblk * VB) * D;  // S[v][d] = Sg[v*D + d]
-    if (has_state) {
-#pragma unroll
-      for (int v = 0; v < VB; ++v) S[v] = Sg[(int64_t)v * D + tid];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S[8 * c + 2 * u], S[8 * c + 2 * u + 1]);
-        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-    // U~ row of the first chunk (rows of later chunks are prefetched one chunk ahead)
-    uint4 ut[8];
-    if (u_row) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.U + ((int64_t)c_beg * p.HV + hv) * C * D + (int64_t)tid * D + vblk * VB);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) ut[c] = src[c];
-    }
-    tc::fence_async_smem();
-    tc::named_sync(1, kConsumers);
-
-    constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
-    constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
-    uint32_t mma_phase = 0;
-    bool failed = false;
-    for (int c = 0; c < n_c; ++c) {
-      const int s = c % kStages;
-      unsigned char* st = smem + s * SM::STAGE;
-      bool bad = !tc::mbar_wait(&full[s], (c / kStages) & 1, kWaitBudget) || *s_fail != 0;
-      if (tc::named_sync_or(1, kConsumers, bad)) {  // the same verdict in every consumer thread
-        if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
-        failed = true;
-        break;
-      }
-      // MMA1: D1 = [W<-; Q] S^T
-      if (tid == 0) {
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ outputs, one chunk behind
+    if (full_mode) {
+      const int r = tid - kChain;  // output row of the chunk (warps 4-5: TMEM lanes 0-63)
+      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % S, buf = c & 1;
+        if (!wait_or_fail(&mmao[buf], (c >> 1) & 1, fail)) {
+          report();
+          break;
+        }
         tc::fence_after_sync();
-        for (int b = 0; b < NB; ++b)
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::WQ + b * 16384) + ks * 32, 16, 1024, tc::kSwizzle128B);
-            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::SCOPY) + b * 8192 + ks * 2048, D * 128, 1024,
-                                              tc::kSwizzle128B);
-            tc::mma_f16_ss(tmem, a, bd, idesc_x, (b | ks) != 0);
-          }
-        tc::mma_commit(mma_bar);
-      }
-      const float* gs = reinterpret_cast<const float*>(st + SM::F);
-      const float* rqs = gs + C;
-      const float* rks = gs + 2 * C;
-      const float gC = gs[C - 1];
-      const int ct_t0 = reinterpret_cast<const int*>(st + SM::F + 768)[0];
-      const int ct_len = reinterpret_cast<const int*>(st + SM::F + 768)[1];
-      const float sk_row = u_row ? expf(gC - gs[tid]) * rks[tid] : 0.f;       // Uk row scale
-      const float sq_row = o_row ? expf(gs[tid - 64]) * rqs[tid - 64] * p.scale : 0.f;  // O row scale
-      if (!tc::mbar_wait(mma_bar, mma_phase & 1, kWaitBudget)) {
-        *s_fail = 1;
-        set_status(p.status, GDN_ERR_TIMEOUT);
-      }
-      ++mma_phase;
-      tc::fence_after_sync();
-      if (u_row) {  // U = U~ - W<- S^T and Uk, row mu = tid
-        const float sk = sk_row;
-        uint32_t rr[VB / 16][16];
-#pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + 16 * cc, rr[cc]);
-        tc::tmem_wait_ld();
+        const unsigned char* st = smem + s * SM::STAGE;
+        const float* gs = reinterpret_cast<const float*>(st + SM::F);
+        const float sq = expf(gs[r]) * gs[C + r] * p.scale;
+        const int t0 = reinterpret_cast<const int*>(st + SM::F + 768)[0];
+        const int len = reinterpret_cast<const int*>(st + SM::F + 768)[1];
+        tc::named_sync(3, kOut);
+        if (tid == kChain) tc::mbar_arrive(&empty[s]);  // P and the gates are no longer needed
+        bf16* orow = p.out + (((int64_t)t0 + r) * p.HV + hv) * (int64_t)D + vblk * VB;
 #pragma unroll
         for (int cc = 0; cc < VB / 16; ++cc) {
-          const uint32_t* r = rr[cc];
-          uint32_t wn[8], wk[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const __nv_bfloat162 u2 = reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3];
-            const float2 uf = __bfloat1622float2(u2);
-            const float n0 = uf.x - __uint_as_float(r[2 * u]), n1 = uf.y - __uint_as_float(r[2 * u + 1]);
-            wn[u] = pack_bf16(n0, n1);
-            wk[u] = pack_bf16(n0 * sk, n1 * sk);
-          }
-          *reinterpret_cast<uint4*>(smem + SM::VN + tc::sw128_offset(tid, 2 * cc)) = make_uint4(wn[0], wn[1], wn[2], wn[3]);
-          *reinterpret_cast<uint4*>(smem + SM::VN + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(wn[4], wn[5], wn[6], wn[7]);
-          *reinterpret_cast<uint4*>(smem + SM::VK + tc::sw128_offset(tid, 2 * cc)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-          *reinterpret_cast<uint4*>(smem + SM::VK + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(wk[4], wk[5], wk[6], wk[7]);
-        }
-        if (c + 1 < n_c) {  // prefetch the next chunk's U~ row
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.U + ((int64_t)(c_beg + c + 1) * p.HV + hv) * C * D + (int64_t)tid * D + vblk * VB);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) ut[q] = src[q];
-        }
-      }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      tc::named_sync(1, kConsumers);
-      // MMA3: DS = K^T Uk ; MMA2: D2 = [*; P] U
-      if (tid == 0) {
-        tc::fence_after_sync();
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::smem_desc(tc::saddr(st + SM::K) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-          const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VK) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-          tc::mma_f16_ss(tmem + 64, a, bd, idesc_s, ks > 0);
-        }
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t a = tc::smem_desc(tc::saddr(st + SM::P - 8192) + ks * 32, 16, 1024, tc::kSwizzle128B);
-          const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VN) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-          tc::mma_f16_ss(tmem + 128, a, bd, idesc_x, ks > 0);
-        }
-        tc::mma_commit(mma_bar);
-      }
-      if (!tc::mbar_wait(mma_bar, mma_phase & 1, kWaitBudget)) {
-        *s_fail = 1;
-        set_status(p.status, GDN_ERR_TIMEOUT);
-      }
-      ++mma_phase;
-      tc::fence_after_sync();
-      if (tid == 0) tc::mbar_arrive(&empty[s]);  // the MMAs are done with stage s; scalars are in registers
-      if (has_state) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
-        const float eC = expf(gC);
-        uint32_t rr[VB / 16][16];
-#pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + 64 + 16 * cc, rr[cc]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) {
-          const uint32_t* r = rr[cc];
-          uint32_t w[8];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) S[16 * cc + u] = fmaf(eC, S[16 * cc + u], __uint_as_float(r[u]));
-#pragma unroll
-          for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S[16 * cc + 2 * u], S[16 * cc + 2 * u + 1]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-        }
-      }
-      if (o_row) {  // O row r = exp(g_r)/|q_r| (Q S^T)_r + (P U)_r
-        const int r = tid - 64;
-        const float sq = sq_row;
-        const bool store = r < ct_len;  // padded rows are computed but not stored
-        bf16* orow = p.out + (((int64_t)ct_t0 + r) * p.HV + hv) * (int64_t)D + vblk * VB;
-#pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) {
-          uint32_t a[16], b[16];  // tcgen05.ld is warp-collective: every lane loads
-          tc::tmem_ld16(tmem + lane_base + 16 * cc, a);
-          tc::tmem_ld16(tmem + lane_base + 128 + 16 * cc, b);
+          uint32_t a[16], b[16];  // warp-collective TMEM loads: every lane loads
+          tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + 16 * cc, a);
+          tc::tmem_ld16(tmem + lane_base + kColD2 + 64 * buf + 16 * cc, b);
           tc::tmem_wait_ld();
-          uint32_t w[8];
+          if (r < len) {
+            uint32_t w[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
-                             sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
-          if (store) {
+            for (int u = 0; u < 8; ++u)
+              w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
+                               sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
             uint4* d4 = reinterpret_cast<uint4*>(orow + 16 * cc);
             d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
             d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
         }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&odone[buf]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ chain: U, state update
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const bool has_state = tid < D;  // thread d holds key row d of S^T
+    const bool u_row = tid >= 64;    // thread 64 + mu forms row mu of U (TMEM lanes 64-127)
+    const int mu = tid - 64;
+    float S_[VB];
+    const int64_t row0 = (int64_t)vblk * VB;  // first state row of this CTA
+    if (has_state) {
+      if (mode == kFull) {
+#pragma unroll
+        for (int v = 0; v < VB; ++v) S_[v] = job.init[(row0 + v) * D + tid];
+      } else if (mode == kMapT) {
+#pragma unroll
+        for (int v = 0; v < VB; ++v) S_[v] = (row0 + v == tid) ? 1.f : 0.f;
+      } else {
+#pragma unroll
+        for (int v = 0; v < VB; ++v) S_[v] = 0.f;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[8 * cc + 2 * u], S_[8 * cc + 2 * u + 1]);
+        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    const bool use_ut = mode != kMapT;
+    uint4 ut[8];
+    auto load_ut = [&](int c) {
+      const int64_t j = cb + job.c0 + c;
+      const uint4* src = reinterpret_cast<const uint4*>(p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + vblk * VB);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ut[q] = src[q];
+    };
+    if (u_row && use_ut) load_ut(0);
+    tc::fence_async_smem();
+    tc::named_sync(1, kChain);
+
+    constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
+    constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
+    bool failed = false;
+    for (int c = 0; c < nc; ++c) {
+      const int s = c % S, buf = c & 1;
+      unsigned char* st = smem + s * SM::STAGE;
+      bool bad = !wait_or_fail(&full[s], (c / S) & 1, fail);
+      if (tid == 0 && !bad && full_mode && c >= 2)  // O warps are done with D1[buf], D2[buf] of chunk c-2
+        bad = !wait_or_fail(&odone[buf], ((c - 2) >> 1) & 1, fail);
+      if (tc::named_sync_or(1, kChain, bad || *fail)) {
+        if (tid == 0) report();
+        failed = true;
+        break;
+      }
+      const float* gs = reinterpret_cast<const float*>(st + SM::F);
+      const float gC = gs[C - 1];
+      const float eC = expf(gC);
+      const float sk = u_row ? expf(gC - gs[mu]) * gs[2 * C + mu] : 0.f;  // exp(g_C - g_mu) / |k_mu|
+      // MMA1: D1[buf] = [Q; W<-] S^T
+      if (tid == 0) {
+        tc::fence_after_sync();
+        for (int b = 0; b < NB; ++b)
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::QW + b * 16384) + ks * 32, 16, 1024, tc::kSwizzle128B);
+            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::SCOPY) + b * 8192 + ks * 2048, D * 128, 1024,
+                                              tc::kSwizzle128B);
+            tc::mma_f16_ss(tmem + kColD1 + 64 * buf, a, bd, idesc_x, (b | ks) != 0);
+          }
+        tc::mma_commit(mma1);
+      }
+      bad = !wait_or_fail(mma1, c & 1, fail);
+      tc::fence_after_sync();
+      if (u_row && !bad) {  // U = U~ - W<- S^T (row mu); Uk = sk U as bf16 hi + lo
+        uint32_t rr[VB / 16][16];
+#pragma unroll
+        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + 16 * cc, rr[cc]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < VB / 16; ++cc) {
+          uint32_t wn[8], wh[8], wl[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            float2 uf = make_float2(0.f, 0.f);
+            if (use_ut) uf = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3]);
+            const float n0 = uf.x - __uint_as_float(rr[cc][2 * u]), n1 = uf.y - __uint_as_float(rr[cc][2 * u + 1]);
+            wn[u] = pack_bf16(n0, n1);
+            const float k0 = n0 * sk, k1 = n1 * sk;
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
+            const float2 hf = __bfloat1622float2(hi);
+            wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
+            wl[u] = pack_bf16(k0 - hf.x, k1 - hf.y);
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t o = tc::sw128_offset(mu, 2 * cc + hh);
+            *reinterpret_cast<uint4*>(smem + SM::VN + o) = make_uint4(wn[4 * hh], wn[4 * hh + 1], wn[4 * hh + 2], wn[4 * hh + 3]);
+            *reinterpret_cast<uint4*>(smem + SM::VKH + o) = make_uint4(wh[4 * hh], wh[4 * hh + 1], wh[4 * hh + 2], wh[4 * hh + 3]);
+            *reinterpret_cast<uint4*>(smem + SM::VKL + o) = make_uint4(wl[4 * hh], wl[4 * hh + 1], wl[4 * hh + 2], wl[4 * hh + 3]);
+          }
+        }
+        if (use_ut && c + 1 < nc) load_ut(c + 1);
       }
       tc::fence_async_smem();
       tc::fence_before_sync();
-      tc::named_sync(1, kConsumers);
-    }
-    if (has_state && !failed) {
+      if (tc::named_sync_or(1, kChain, bad)) {
+        if (tid == 0) report();
+        failed = true;
+        break;
+      }
+      // MMA3: DS = K^T (Uk_hi + Uk_lo) (the chain waits for this); MMA2: D2[buf] = [P; *] U (outputs)
+      if (tid == 0) {
+        tc::fence_after_sync();
+        for (int part = 0; part < 2; ++part)
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::K) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+            const uint64_t bd = tc::smem_desc(tc::saddr(smem + (part ? SM::VKL : SM::VKH)) + ks * 2048, 8192, 1024,
+                                              tc::kSwizzle128B);
+            tc::mma_f16_ss(tmem + kColDS, a, bd, idesc_s, (part | ks) != 0);
+          }
+        tc::mma_commit(mma3);
+        if (full_mode) {
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::P) + ks * 32, 16, 1024, tc::kSwizzle128B);
+            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VN) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
+            tc::mma_f16_ss(tmem + kColD2 + 64 * buf, a, bd, idesc_x, ks > 0);
+          }
+          tc::mma_commit(&mmao[buf]);
+        }
+      }
+      bad = !wait_or_fail(mma3, c & 1, fail);
+      tc::fence_after_sync();
+      if (tid == 0) tc::mbar_arrive(&empty[s]);  // MMA1 and MMA3 are done with Q, W<-, K; gates in registers
+      if (has_state && !bad) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
+        uint32_t rr[VB / 16][16];
 #pragma unroll
-      for (int v = 0; v < VB; ++v) Sg[(int64_t)v * D + tid] = S[v];
+        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + 16 * cc, rr[cc]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < VB / 16; ++cc) {
+          uint32_t w[8];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) S_[16 * cc + u] = fmaf(eC, S_[16 * cc + u], __uint_as_float(rr[cc][u]));
+#pragma unroll
+          for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S_[16 * cc + 2 * u], S_[16 * cc + 2 * u + 1]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      if (tc::named_sync_or(1, kChain, bad)) {
+        if (tid == 0) report();
+        failed = true;
+        break;
+      }
+    }
+    if (has_state && !failed && job.fin) {
+#pragma unroll
+      for (int v = 0; v < VB; ++v) job.fin[(row0 + v) * D + tid] = S_[v];
     }
   }
 
@@ -317,9 +453,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Chains the segment maps of one (sequence, value head): S_{p+1} = S_p T_p + B_p for
+// p = 1 .. ns-2, starting from S_1 (the end state of segment 0). One CTA per 16 state
+// rows; fp32 on CUDA cores with T_p staged in shared memory.
 template <int D>
-cudaError_t launch_scan_t(const Params& p, cudaStream_t s) {
+__global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
+  constexpr int R = 16;  // state rows per CTA
+  extern __shared__ float csm[];
+  float* T = csm;         // D x D
+  float* Sr = T + D * D;  // R x D
+  if (p.status[0] != GDN_OK) return;
+  int bid = blockIdx.x;
+  const int rb = bid % (D / R);
+  bid /= (D / R);
+  const int hv = bid % p.HV;
+  const int seq = p.order[bid / p.HV];
+  const int n = p.seq_chunk_off[seq + 1] - p.seq_chunk_off[seq];
+  const int L = (n + nseg - 1) / nseg;
+  const int ns = L > 0 ? (n + L - 1) / L : 0;
+  if (ns < 3) return;
+  const int64_t per_head = (int64_t)D * D;
+  const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < R * D; e += 256) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
+  for (int seg = 1; seg <= ns - 2; ++seg) {
+    const float* Tg = p.seg_map + (base + seg) * 2 * per_head + per_head;  // T_p (rows: key index)
+    const float* Bg = p.seg_map + (base + seg) * 2 * per_head;             // B_p (rows: value index)
+    __syncthreads();
+    for (int e = tid; e < D * D; e += 256) T[e] = Tg[e];
+    __syncthreads();
+    const int r = tid / 16, c0 = (tid % 16) * (D / 16);  // one row, D/16 columns per thread
+    float acc[D / 16];
+#pragma unroll
+    for (int u = 0; u < D / 16; ++u) acc[u] = Bg[((int64_t)rb * R + r) * D + c0 + u];
+    for (int k = 0; k < D; ++k) {
+      const float sk = Sr[r * D + k];
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) acc[u] = fmaf(sk, T[k * D + c0 + u], acc[u]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < D / 16; ++u) Sr[r * D + c0 + u] = acc[u];
+    __syncthreads();
+    for (int e = tid; e < R * D; e += 256)
+      p.seg_state[(base + seg + 1) * per_head + (int64_t)rb * R * D + e] = Sr[e];
+  }
+}
+
+template <int D>
+cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   using SM = ScanSmem<D>;
+  constexpr int NVB = D / VB;
   const int64_t rows = p.max_chunks * p.HV * C;
   CUtensorMap mw, mp, mq, mk;
   if (!make_2d_tile_map(&mw, p.W, D, rows, 64, C, true) || !make_2d_tile_map(&mp, p.P, C, rows, 64, C, true) ||
@@ -327,8 +511,23 @@ cudaError_t launch_scan_t(const Params& p, cudaStream_t s) {
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(scan_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::alloc);
   if (e != cudaSuccess) return e;
-  const int64_t blocks = (int64_t)p.B * p.HV * (D / VB);
-  scan_kernel<D><<<(unsigned)blocks, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p);
+  const int64_t chains = (int64_t)p.B * p.HV;
+  if (nseg <= 1) {
+    scan_kernel<D><<<(unsigned)(chains * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 0, 1);
+    return cudaGetLastError();
+  }
+  // segment 0 and the maps of segments 1 .. nseg-2, then the combine, then segments 1 .. nseg-1
+  const int64_t grid1 = chains * NVB + chains * (nseg - 2) * 2 * NVB;
+  scan_kernel<D><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (nseg > 2) {
+    const size_t csmem = (size_t)(D * D + 16 * D) * sizeof(float);
+    e = cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+    if (e != cudaSuccess) return e;
+    combine_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  scan_kernel<D><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
   return cudaGetLastError();
 }
 
@@ -337,8 +536,8 @@ cudaError_t launch_scan_t(const Params& p, cudaStream_t s) {
 cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
   if (Cc != C || p.nvb != D / VB) return cudaErrorInvalidValue;
   switch (D) {
-    case 64: return launch_scan_t<64>(p, s);
-    case 128: return launch_scan_t<128>(p, s);
+    case 64: return launch_scan_t<64>(p, p.nseg, s);
+    case 128: return launch_scan_t<128>(p, p.nseg, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -171,3 +171,32 @@ def test_host_errors_raise():
         gdn_extend_chunkwise(*[d[k] for k in INPUT_KEYS], chunk_size=48)
     with pytest.raises(TypeError):
         gdn_extend_chunkwise(d["q"].float(), *[d[k] for k in INPUT_KEYS[1:]])
+
+
+# ----------------------------------------------------------------------------- segment-parallel scan
+
+def test_segmented_scan_long_sequence():
+    """Few heads, one long sequence: the scan splits it into segments, computes the affine
+    map of the middle one, chains it, and re-runs the segments from their start states."""
+    w = wl.custom("seg", [6400], H=1, HV=2, K=128, V=128, chunk_size=64, seed=32)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_segmented_scan_weak_decay():
+    """alpha ~ 1: the segment transition maps are far from zero, so the chaining matters."""
+    w = wl.custom("segweak", [6400], H=1, HV=2, K=128, V=128, chunk_size=64, seed=33)
+    d = wl.make_inputs(w)
+    d["A_log"] = torch.full_like(d["A_log"], -7.0)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_segmented_scan_mixed_lengths():
+    w = wl.custom("segmix", [5000, 700, 1], H=1, HV=1, K=64, V=64, chunk_size=64, seed=34)
+    d = wl.make_inputs(w)
+    d["A_log"] = torch.full_like(d["A_log"], -6.0)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
