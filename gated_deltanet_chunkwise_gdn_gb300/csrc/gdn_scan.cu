@@ -15,14 +15,15 @@
 // i.e. "Simple math to speed up GDN prefill", section "Reminder": the chunk transition
 // S_[t+1] = S-> + (U~ - W<- S^T)^T K-> with S-> = gamma_C S.
 //
-// Critical path per chunk (the "chain" warps 0-3; thread i <-> TMEM lane i):
+// Critical path per chunk (the "chain" warps 0-7; warps w and w+4 serve TMEM lanes
+// 32(w%4)..+31, each taking half of the 64 columns):
 //   MMA1  D1[128 x 64] = [Q; W<-] S^T          -> U = U~ - D1[64:128]; Uk = diag(exp(g_C-g)/|k|) U
 //   MMA3  DS[K x 64]   = K^T (Uk_hi + Uk_lo)   -> S = exp(g_C) S + DS, bf16 copy to smem
 // Uk is carried as two bf16 terms (hi + lo) against the exact bf16 K tile, so the state
 // increment keeps about 16 bits of precision. Off the critical path:
-//   MMA2  D2[128 x 64] = [P; *] U  and warps 4-5 form O from D1[0:64] and D2[0:64] one chunk
+//   MMA2  D2[128 x 64] = [P; *] U  and warps 8-9 form O from D1[0:64] and D2[0:64] one chunk
 //   behind (D1, D2 double-buffered in TMEM);
-//   warp 6 streams Q, W<-, K, P and the gate vectors with TMA (2-3 stage ring).
+//   warp 10 streams Q, W<-, K, P and the gate vectors with TMA (2-3 stage ring).
 //
 // Segment-parallel use (few long chains): besides a full scan over a chunk range
 // (state from a buffer, outputs written), the same kernel computes the affine map of a
@@ -37,9 +38,11 @@ namespace {
 constexpr int C = 64;
 constexpr int VB = 64;
 constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
-// warps 0-3 chain, warps 4-5 outputs (TMEM lanes 0-63), warp 6 producer
-constexpr int kChain = 128, kOut = 64;
-constexpr int kThreads = 224;
+// warps 0-7 chain (warps w and w+4 share TMEM lanes 32(w%4)..+31 and split the columns),
+// warps 8-9 outputs (TMEM lanes 0-63), warp 10 producer
+constexpr int kChain = 256, kOut = 64;
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: D1 buffers [0,64) [64,128); DS [128,192); D2 buffers [256,320) [320,384)
 constexpr uint32_t kColD1 = 0, kColDS = 128, kColD2 = 256;
@@ -214,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     set_status(p.status, GDN_ERR_TIMEOUT);
   };
 
-  if (warp == 6) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer: TMA
     if (lane == 0) {
       for (int c = 0; c < nc; ++c) {
@@ -243,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= kChain / 32) {
     // ------------------------------------------------------------------ outputs, one chunk behind
     if (full_mode) {
       const int r = tid - kChain;  // output row of the chunk (warps 4-5: TMEM lanes 0-63)
@@ -286,38 +289,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ chain: U, state update
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    const bool has_state = tid < D;  // thread d holds key row d of S^T
-    const bool u_row = tid >= 64;    // thread 64 + mu forms row mu of U (TMEM lanes 64-127)
-    const int mu = tid - 64;
-    float S_[VB];
-    const int64_t row0 = (int64_t)vblk * VB;  // first state row of this CTA
+    const int sub = warp & 3, half = warp >> 2;
+    const int row = 32 * sub + lane;                        // TMEM lane of this thread
+    const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
+    const int cbase = 32 * half;                            // first of this thread's 32 columns
+    const bool has_state = row < D;  // thread (row, half) holds columns cbase.. of key row `row` of S^T
+    const bool u_row = row >= 64;    // thread (64 + mu, half) forms half of row mu of U (TMEM lanes 64-127)
+    const int mu = row - 64;
+    float S_[32];
+    const int64_t row0 = (int64_t)vblk * VB + cbase;  // first state row held by this thread
     if (has_state) {
       if (mode == kFull) {
 #pragma unroll
-        for (int v = 0; v < VB; ++v) S_[v] = job.init[(row0 + v) * D + tid];
+        for (int v = 0; v < 32; ++v) S_[v] = job.init[(row0 + v) * D + row];
       } else if (mode == kMapT) {
 #pragma unroll
-        for (int v = 0; v < VB; ++v) S_[v] = (row0 + v == tid) ? 1.f : 0.f;
+        for (int v = 0; v < 32; ++v) S_[v] = (row0 + v == row) ? 1.f : 0.f;
       } else {
 #pragma unroll
-        for (int v = 0; v < VB; ++v) S_[v] = 0.f;
+        for (int v = 0; v < 32; ++v) S_[v] = 0.f;
       }
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[8 * cc + 2 * u], S_[8 * cc + 2 * u + 1]);
-        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + cc)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
     const bool use_ut = mode != kMapT;
-    uint4 ut[8];
+    uint4 ut[4];
     auto load_ut = [&](int c) {
       const int64_t j = cb + job.c0 + c;
-      const uint4* src = reinterpret_cast<const uint4*>(p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + vblk * VB);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + vblk * VB + cbase);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) ut[q] = src[q];
+      for (int q = 0; q < 4; ++q) ut[q] = src[q];
     };
     if (u_row && use_ut) load_ut(0);
     tc::fence_async_smem();
@@ -325,9 +332,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
     constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
+    // Base descriptors; an operand at byte offset o from its base is base + (o >> 4) (the
+    // start-address field holds address >> 4 and shared addresses stay below 256 KB).
+    const uint64_t dA1 = tc::smem_desc(tc::saddr(smem + SM::QW), 16, 1024, tc::kSwizzle128B);
+    const uint64_t dB1 = tc::smem_desc(tc::saddr(smem + SM::SCOPY), D * 128, 1024, tc::kSwizzle128B);
+    const uint64_t dA3 = tc::smem_desc(tc::saddr(smem + SM::K), 8192, 1024, tc::kSwizzle128B);
+    const uint64_t dB3 = tc::smem_desc(tc::saddr(smem + SM::VKH), 8192, 1024, tc::kSwizzle128B);
+    const uint64_t dA2 = tc::smem_desc(tc::saddr(smem + SM::P), 16, 1024, tc::kSwizzle128B);
+    const uint64_t dB2 = tc::smem_desc(tc::saddr(smem + SM::VN), 8192, 1024, tc::kSwizzle128B);
+    static_assert(SM::VKL == SM::VKH + 8192, "Uk lo follows Uk hi");
     bool failed = false;
     for (int c = 0; c < nc; ++c) {
       const int s = c % S, buf = c & 1;
+      const uint32_t so = (uint32_t)(s * SM::STAGE) >> 4;  // stage offset in descriptor units
       unsigned char* st = smem + s * SM::STAGE;
       bool bad = !wait_or_fail(&full[s], (c / S) & 1, fail);
       if (tid == 0 && !bad && full_mode && c >= 2)  // O warps are done with D1[buf], D2[buf] of chunk c-2
@@ -337,31 +354,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         failed = true;
         break;
       }
+      // MMA1: D1[buf] = [Q; W<-] S^T
+      if (tid == 0) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16_ss(tmem + kColD1 + 64 * buf, dA1 + so + ((b * 16384 + ks * 32) >> 4),
+                           dB1 + ((b * 8192 + ks * 2048) >> 4), idesc_x, (b | ks) != 0);
+        tc::mma_commit(mma1);
+      }
       const float* gs = reinterpret_cast<const float*>(st + SM::F);
       const float gC = gs[C - 1];
       const float eC = expf(gC);
       const float sk = u_row ? expf(gC - gs[mu]) * gs[2 * C + mu] : 0.f;  // exp(g_C - g_mu) / |k_mu|
-      // MMA1: D1[buf] = [Q; W<-] S^T
-      if (tid == 0) {
-        tc::fence_after_sync();
-        for (int b = 0; b < NB; ++b)
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::QW + b * 16384) + ks * 32, 16, 1024, tc::kSwizzle128B);
-            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::SCOPY) + b * 8192 + ks * 2048, D * 128, 1024,
-                                              tc::kSwizzle128B);
-            tc::mma_f16_ss(tmem + kColD1 + 64 * buf, a, bd, idesc_x, (b | ks) != 0);
-          }
-        tc::mma_commit(mma1);
-      }
       bad = !wait_or_fail(mma1, c & 1, fail);
       tc::fence_after_sync();
-      if (u_row && !bad) {  // U = U~ - W<- S^T (row mu); Uk = sk U as bf16 hi + lo
-        uint32_t rr[VB / 16][16];
+      if (u_row && !bad) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as bf16 hi + lo
+        uint32_t rr[2][16];
 #pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + 16 * cc, rr[cc]);
+        for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + cbase + 16 * cc, rr[cc]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t wn[8], wh[8], wl[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -377,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t o = tc::sw128_offset(mu, 2 * cc + hh);
+            const uint32_t o = tc::sw128_offset(mu, 4 * half + 2 * cc + hh);
             *reinterpret_cast<uint4*>(smem + SM::VN + o) = make_uint4(wn[4 * hh], wn[4 * hh + 1], wn[4 * hh + 2], wn[4 * hh + 3]);
             *reinterpret_cast<uint4*>(smem + SM::VKH + o) = make_uint4(wh[4 * hh], wh[4 * hh + 1], wh[4 * hh + 2], wh[4 * hh + 3]);
             *reinterpret_cast<uint4*>(smem + SM::VKL + o) = make_uint4(wl[4 * hh], wl[4 * hh + 1], wl[4 * hh + 2], wl[4 * hh + 3]);
@@ -395,20 +411,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MMA3: DS = K^T (Uk_hi + Uk_lo) (the chain waits for this); MMA2: D2[buf] = [P; *] U (outputs)
       if (tid == 0) {
         tc::fence_after_sync();
+#pragma unroll
         for (int part = 0; part < 2; ++part)
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::K) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-            const uint64_t bd = tc::smem_desc(tc::saddr(smem + (part ? SM::VKL : SM::VKH)) + ks * 2048, 8192, 1024,
-                                              tc::kSwizzle128B);
-            tc::mma_f16_ss(tmem + kColDS, a, bd, idesc_s, (part | ks) != 0);
-          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16_ss(tmem + kColDS, dA3 + so + ((ks * 2048) >> 4), dB3 + ((part * 8192 + ks * 2048) >> 4), idesc_s,
+                           (part | ks) != 0);
         tc::mma_commit(mma3);
         if (full_mode) {
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t a = tc::smem_desc(tc::saddr(st + SM::P) + ks * 32, 16, 1024, tc::kSwizzle128B);
-            const uint64_t bd = tc::smem_desc(tc::saddr(smem + SM::VN) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-            tc::mma_f16_ss(tmem + kColD2 + 64 * buf, a, bd, idesc_x, ks > 0);
-          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16_ss(tmem + kColD2 + 64 * buf, dA2 + so + ((ks * 32) >> 4), dB2 + ((ks * 2048) >> 4), idesc_x, ks > 0);
           tc::mma_commit(&mmao[buf]);
         }
       }
@@ -416,19 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       if (tid == 0) tc::mbar_arrive(&empty[s]);  // MMA1 and MMA3 are done with Q, W<-, K; gates in registers
       if (has_state && !bad) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
-        uint32_t rr[VB / 16][16];
+        uint32_t rr[2][16];
 #pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + 16 * cc, rr[cc]);
+        for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + cbase + 16 * cc, rr[cc]);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t w[8];
 #pragma unroll
           for (int u = 0; u < 16; ++u) S_[16 * cc + u] = fmaf(eC, S_[16 * cc + u], __uint_as_float(rr[cc][u]));
 #pragma unroll
           for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S_[16 * cc + 2 * u], S_[16 * cc + 2 * u + 1]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(tid, 2 * cc + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + 2 * cc)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + 2 * cc + 1)) =
+              make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
       tc::fence_async_smem();
@@ -441,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (has_state && !failed && job.fin) {
 #pragma unroll
-      for (int v = 0; v < VB; ++v) job.fin[(row0 + v) * D + tid] = S_[v];
+      for (int v = 0; v < 32; ++v) job.fin[(row0 + v) * D + row] = S_[v];
     }
   }
 
