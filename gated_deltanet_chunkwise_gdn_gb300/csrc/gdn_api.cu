@@ -46,8 +46,13 @@ void prof_end(int rec, cudaStream_t s, int kernels = 1) {
 
 bool supported_shape(int K, int V, int C) {
   if (K != V) return false;
-  return (K == 64 || K == 128) && C == 64;
+  return (K == 64 || K == 128 || K == 256) && (C == 64 || C == 128);
 }
+
+// The kernels' WY block: 64 tokens. A 128-token chunk is processed as its two 64-token
+// halves, each with its own M^{-1}; in exact arithmetic the result does not depend on
+// the block length (the chunkwise form equals the token recurrence for any block length).
+constexpr int kWyBlock = 64;
 
 // Value-dimension split of the scan: blocks of 64 state rows per CTA.
 int choose_nvb(int V) { return V / 64; }
@@ -61,7 +66,7 @@ size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H, int32_
   if (total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || batch < 0 || H <= 0 || HV <= 0 || HV % H != 0)
     return 0;
   if (!supported_shape(K, V, chunk_size)) return 0;
-  return gdn::make_layout(total_tokens, batch, H, HV, K, V, chunk_size).total;
+  return gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock).total;
 }
 
 gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* a,
@@ -78,7 +83,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   if (batch > 0 && (!state_pool || !cache_indices || pool_size <= 0)) return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!q || !k || !v || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   if (!supported_shape(K, V, chunk_size) || dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
-  const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, chunk_size);
+  const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return GDN_ERR_WORKSPACE;
 
@@ -119,15 +124,15 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.nseg = L.nseg;
 
   int rec = prof_begin(kKernSchedule, s);
-  gdn::schedule_kernel<<<1, 512, 0, s>>>(p, chunk_size);
+  gdn::schedule_kernel<<<1, 512, 0, s>>>(p, kWyBlock);
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s);
   if (total_tokens == 0 || batch == 0) return GDN_OK;
   rec = prof_begin(kKernIntra, s);
-  if (gdn::launch_intra(p, K, chunk_size, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::launch_intra(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s);
   rec = prof_begin(kKernScan, s);
-  if (gdn::launch_scan(p, K, chunk_size, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (gdn::launch_scan(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s, p.nseg <= 1 ? 1 : (p.nseg == 2 ? 2 : 3));  // segmented: maps, combine, segments
   return GDN_OK;
 }

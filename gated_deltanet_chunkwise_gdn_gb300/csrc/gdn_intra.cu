@@ -48,7 +48,12 @@ struct IntraSmem {
   static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
 };
 
-constexpr uint32_t kTmemCols = 256;  // D1 / DW at columns [0, 128), DU at [128, 256)
+// TMEM columns: D1 and then DW from column 0, DU from column tmem_u<D>; D <= 128 takes 256
+// columns, D = 256 all 512.
+template <int D>
+__host__ __device__ constexpr uint32_t tmem_u() { return D < 128 ? 128u : (uint32_t)D; }
+template <int D>
+__host__ __device__ constexpr uint32_t tmem_cols() { return D < 256 ? 256u : 512u; }
 
 __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     tc::mbar_fence_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, kTmemCols);
+    tc::tmem_alloc(tslot, tmem_cols<D>());
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
         for (int ks = 0; ks < C / 16; ++ks) {
           const uint64_t a = tc::smem_desc(tc::saddr(smem + (part ? SM::LF : SM::AA)) + ks * 32, 16, 1024, tc::kSwizzle128B);
           const uint64_t bv = tc::smem_desc(tc::saddr(smem + SM::V) + ks * 2048, 8192, 1024, tc::kSwizzle128B);
-          tc::mma_f16_ss(tmem + 128, a, bv, idesc2, (part | ks) != 0);
+          tc::mma_f16_ss(tmem + tmem_u<D>(), a, bv, idesc2, (part | ks) != 0);
         }
       tc::mma_commit(&bar[2]);
     }
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
       const bool is_u = row >= 64;
       const int mu = row & 63;
       bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D + half * (D / 2);
-      const uint32_t col0 = (is_u ? 128u : 0u) + half * (D / 2);
+      const uint32_t col0 = (is_u ? tmem_u<D>() : 0u) + half * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[16];
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   __syncthreads();
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::tmem_dealloc(tmem, tmem_cols<D>());
   }
 }
 
@@ -451,6 +456,7 @@ cudaError_t launch_intra(const Params& p, int D, int Cc, cudaStream_t s) {
   switch (D) {
     case 64: return launch_intra_t<64>(p, s);
     case 128: return launch_intra_t<128>(p, s);
+    case 256: return launch_intra_t<256>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }

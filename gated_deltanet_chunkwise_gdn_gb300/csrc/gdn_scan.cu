@@ -44,7 +44,8 @@ constexpr int kChain = 256, kOut = 64;
 constexpr int kThreads = 352;
 constexpr int kProducerWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D1 buffers [0,64) [64,128); DS [128,192); D2 buffers [256,320) [320,384)
+// TMEM columns: D1 buffers [0,64) [64,128); DS [128,192) (keys 0-127) and, for K = 256,
+// [192,256) (keys 128-255); D2 buffers [256,320) [320,384)
 constexpr uint32_t kColD1 = 0, kColDS = 128, kColD2 = 256;
 
 enum Mode : int { kFull = 0, kMapB = 1, kMapT = 2 };
@@ -52,7 +53,7 @@ enum Mode : int { kFull = 0, kMapB = 1, kMapT = 2 };
 template <int D>
 struct ScanSmem {
   static constexpr int NB = D / 64;
-  static constexpr int STAGES = 3;
+  static constexpr int STAGES = D < 256 ? 3 : 1;  // a K = 256 stage is 105 KB
   static constexpr uint32_t QW = 0;                 // NB x [Q block 8 KB][W<- block 8 KB]
   static constexpr uint32_t P = QW + NB * 16384;    // P 8 KB (A rows 64-127 of MMA2 = the 8 KB after it)
   static constexpr uint32_t K = P + 8192;           // NB x K block 8 KB (+ the 8 KB after: MMA3 rows K..127 if D = 64)
@@ -293,28 +294,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * sub + lane;                        // TMEM lane of this thread
     const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
     const int cbase = 32 * half;                            // first of this thread's 32 columns
-    const bool has_state = row < D;  // thread (row, half) holds columns cbase.. of key row `row` of S^T
+    constexpr int NKR = D > 128 ? 2 : 1;  // key rows per thread: row and row + 128
+    const bool has_state = row < D;  // thread (row, half) holds columns cbase.. of key rows row (+128) of S^T
     const bool u_row = row >= 64;    // thread (64 + mu, half) forms half of row mu of U (TMEM lanes 64-127)
     const int mu = row - 64;
-    float S_[32];
+    float S_[NKR][32];
     const int64_t row0 = (int64_t)vblk * VB + cbase;  // first state row held by this thread
     if (has_state) {
-      if (mode == kFull) {
 #pragma unroll
-        for (int v = 0; v < 32; ++v) S_[v] = job.init[(row0 + v) * D + row];
-      } else if (mode == kMapT) {
+      for (int kr = 0; kr < NKR; ++kr) {
+        const int key = row + 128 * kr;
+        if (mode == kFull) {
 #pragma unroll
-        for (int v = 0; v < 32; ++v) S_[v] = (row0 + v == row) ? 1.f : 0.f;
-      } else {
+          for (int v = 0; v < 32; ++v) S_[kr][v] = job.init[(row0 + v) * D + key];
+        } else if (mode == kMapT) {
 #pragma unroll
-        for (int v = 0; v < 32; ++v) S_[v] = 0.f;
-      }
+          for (int v = 0; v < 32; ++v) S_[kr][v] = (row0 + v == key) ? 1.f : 0.f;
+        } else {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t w[4];
+          for (int v = 0; v < 32; ++v) S_[kr][v] = 0.f;
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[8 * cc + 2 * u], S_[8 * cc + 2 * u + 1]);
-        *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[kr][8 * cc + 2 * u], S_[kr][8 * cc + 2 * u + 1]);
+          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + cc)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
       }
     }
     const bool use_ut = mode != kMapT;
@@ -412,11 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) {
         tc::fence_after_sync();
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int kr = 0; kr < NKR; ++kr)  // keys 128 kr .. 128 kr + 127: K blocks 2 kr, 2 kr + 1
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16_ss(tmem + kColDS, dA3 + so + ((ks * 2048) >> 4), dB3 + ((part * 8192 + ks * 2048) >> 4), idesc_s,
-                           (part | ks) != 0);
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f16_ss(tmem + kColDS + 64 * kr, dA3 + so + ((kr * 16384 + ks * 2048) >> 4),
+                             dB3 + ((part * 8192 + ks * 2048) >> 4), idesc_s, (part | ks) != 0);
         tc::mma_commit(mma3);
         if (full_mode) {
 #pragma unroll
@@ -429,21 +438,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       if (tid == 0) tc::mbar_arrive(&empty[s]);  // MMA1 and MMA3 are done with Q, W<-, K; gates in registers
       if (has_state && !bad) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
-        uint32_t rr[2][16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + cbase + 16 * cc, rr[cc]);
-        tc::tmem_wait_ld();
+        for (int kr = 0; kr < NKR; ++kr) {
+          const int key = row + 128 * kr;
+          uint32_t rr[2][16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t w[8];
+          for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + 64 * kr + cbase + 16 * cc, rr[cc]);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 16; ++u) S_[16 * cc + u] = fmaf(eC, S_[16 * cc + u], __uint_as_float(rr[cc][u]));
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t w[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S_[16 * cc + 2 * u], S_[16 * cc + 2 * u + 1]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + 2 * cc)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(row, 4 * half + 2 * cc + 1)) =
-              make_uint4(w[4], w[5], w[6], w[7]);
+            for (int u = 0; u < 16; ++u)
+              S_[kr][16 * cc + u] = fmaf(eC, S_[kr][16 * cc + u], __uint_as_float(rr[cc][u]));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S_[kr][16 * cc + 2 * u], S_[kr][16 * cc + 2 * u + 1]);
+            *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + 2 * cc)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + 2 * cc + 1)) =
+                make_uint4(w[4], w[5], w[6], w[7]);
+          }
         }
       }
       tc::fence_async_smem();
@@ -456,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (has_state && !failed && job.fin) {
 #pragma unroll
-      for (int v = 0; v < 32; ++v) job.fin[(row0 + v) * D + row] = S_[v];
+      for (int kr = 0; kr < NKR; ++kr)
+#pragma unroll
+        for (int v = 0; v < 32; ++v) job.fin[(row0 + v) * D + row + 128 * kr] = S_[kr][v];
     }
   }
 
@@ -470,13 +486,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Chains the segment maps of one (sequence, value head): S_{p+1} = S_p T_p + B_p for
 // p = 1 .. ns-2, starting from S_1 (the end state of segment 0). One CTA per 16 state
-// rows; fp32 on CUDA cores with T_p staged in shared memory.
+// rows; fp32 on CUDA cores with T_p staged in shared memory 32 key rows at a time.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
-  constexpr int R = 16;  // state rows per CTA
+  constexpr int R = 16;   // state rows per CTA
+  constexpr int KB = 32;  // key rows of T_p per staging step
   extern __shared__ float csm[];
-  float* T = csm;         // D x D
-  float* Sr = T + D * D;  // R x D
+  float* Tb = csm;         // KB x D
+  float* Sr = Tb + KB * D;  // R x D
   if (p.status[0] != GDN_OK) return;
   int bid = blockIdx.x;
   const int rb = bid % (D / R);
@@ -491,20 +508,22 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
   const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
   const int tid = threadIdx.x;
   for (int e = tid; e < R * D; e += 256) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
+  const int r = tid / 16, c0 = (tid % 16) * (D / 16);  // one row, D/16 columns per thread
   for (int seg = 1; seg <= ns - 2; ++seg) {
     const float* Tg = p.seg_map + (base + seg) * 2 * per_head + per_head;  // T_p (rows: key index)
     const float* Bg = p.seg_map + (base + seg) * 2 * per_head;             // B_p (rows: value index)
-    __syncthreads();
-    for (int e = tid; e < D * D; e += 256) T[e] = Tg[e];
-    __syncthreads();
-    const int r = tid / 16, c0 = (tid % 16) * (D / 16);  // one row, D/16 columns per thread
     float acc[D / 16];
 #pragma unroll
     for (int u = 0; u < D / 16; ++u) acc[u] = Bg[((int64_t)rb * R + r) * D + c0 + u];
-    for (int k = 0; k < D; ++k) {
-      const float sk = Sr[r * D + k];
+    for (int k0 = 0; k0 < D; k0 += KB) {
+      __syncthreads();
+      for (int e = tid; e < KB * D; e += 256) Tb[e] = Tg[(int64_t)k0 * D + e];
+      __syncthreads();
+      for (int k = 0; k < KB; ++k) {
+        const float sk = Sr[r * D + k0 + k];
 #pragma unroll
-      for (int u = 0; u < D / 16; ++u) acc[u] = fmaf(sk, T[k * D + c0 + u], acc[u]);
+        for (int u = 0; u < D / 16; ++u) acc[u] = fmaf(sk, Tb[k * D + c0 + u], acc[u]);
+      }
     }
     __syncthreads();
 #pragma unroll
@@ -536,7 +555,7 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   scan_kernel<D><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nseg > 2) {
-    const size_t csmem = (size_t)(D * D + 16 * D) * sizeof(float);
+    const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
     e = cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
     if (e != cudaSuccess) return e;
     combine_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
@@ -553,6 +572,7 @@ cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
   switch (D) {
     case 64: return launch_scan_t<64>(p, p.nseg, s);
     case 128: return launch_scan_t<128>(p, p.nseg, s);
+    case 256: return launch_scan_t<256>(p, p.nseg, s);
     default: return cudaErrorInvalidValue;
   }
 }

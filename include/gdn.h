@@ -98,8 +98,11 @@ GDN_API size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H
  *                                       sequences are allowed and leave their slot as is.
  *  out           [total_tokens, HV, V]  same dtype as v, written (round to nearest even).
  *  H, HV         q/k heads and value heads; HV must be a multiple of H.
- *  K, V          head sizes (supported: K = V in {64, 128}, plus 256 with chunk_size 128).
- *  chunk_size    WY block length (supported: 64; 128 for K = V = 256).
+ *  K, V          head sizes (supported: K = V in {64, 128, 256}; otherwise
+ *                GDN_ERR_UNSUPPORTED).
+ *  chunk_size    64 or 128 (otherwise GDN_ERR_UNSUPPORTED). The kernels factor each chunk
+ *                in 64-token WY blocks: a 128-token chunk is computed as its two halves,
+ *                which gives the same result up to rounding.
  *  scale         multiplies every output (1.0 reads o_t = S_t q_t as written).
  *  workspace     device buffer of at least gdn_workspace_size(...) bytes, 256-byte aligned.
  *  stream        cudaStream_t to enqueue on.

@@ -62,6 +62,9 @@ def test_workspace_size_rules(lib):
     assert ws(100, 2, 2, 4, 128, 64, 64) == 0      # K != V
     assert ws(100, 2, 2, 4, 128, 128, 32) == 0     # chunk size not built
     assert ws(-1, 2, 2, 4, 128, 128, 64) == 0
+    assert ws(100, 2, 2, 4, 256, 256, 128) > 0     # wide heads, 128-token chunks
+    # a 128-token chunk runs as two 64-token WY blocks: the same workspace
+    assert ws(1000, 2, 2, 4, 128, 128, 128) == ws(1000, 2, 2, 4, 128, 128, 64)
     # grows with tokens and value heads
     assert ws(2000, 2, 2, 4, 128, 128, 64) > ws(1000, 2, 2, 4, 128, 128, 64)
     assert ws(1000, 2, 2, 8, 128, 128, 64) > ws(1000, 2, 2, 4, 128, 128, 64)

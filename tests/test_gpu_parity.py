@@ -50,9 +50,17 @@ def test_config_throughput_sampled_chains():
     untouched_slots_equal(d, pool)
 
 
+def test_config_wide_full():
+    """B=4 x 16384, H=HV=4, K=V=256, 128-token chunks, a shifted by -2: every chain, every token."""
+    d = wl.make_inputs(wl.CONFIGS[4])
+    assert d["chunk_size"] == 128 and d["q"].shape[-1] == 256
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
 # ----------------------------------------------------------------------------- shapes and edge cases
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_ragged_lengths_and_gqa(D):
     """Lengths around the chunk size (1, C-1, C, C+1, 0, several chunks + tail), GQA 1:2."""
     w = wl.custom("ragged", [1, 63, 64, 65, 0, 200, 130], H=2, HV=4, K=D, V=D, chunk_size=64, seed=21)
@@ -191,6 +199,26 @@ def test_segmented_scan_weak_decay():
     d["A_log"] = torch.full_like(d["A_log"], -7.0)
     out, pool = run_gpu(d)
     compare(d, out, pool, oracle_for(d))
+
+
+def test_segmented_scan_wide_heads():
+    """K = V = 256 with one long sequence: segment maps, the chaining over four middle
+    segments (state staged 32 key rows at a time) and the segment re-runs."""
+    w = wl.custom("segwide", [12800], H=1, HV=1, K=256, V=256, chunk_size=64, seed=35)
+    d = wl.make_inputs(w)
+    d["A_log"] = torch.full_like(d["A_log"], -6.0)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_chunk_size_128_matches_oracle():
+    """chunk_size=128 (two 64-token WY blocks per chunk) against the oracle, on ragged
+    lengths around both block lengths."""
+    w = wl.custom("c128", [1, 127, 128, 129, 300], H=2, HV=4, K=128, V=128, chunk_size=128, seed=36)
+    d = wl.make_inputs(w)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
 
 
 def test_segmented_scan_mixed_lengths():
