@@ -55,7 +55,7 @@ struct WsLayout {
 // (sequence, head, 64-row block) chains to fill the GPU and the sequences may be long.
 // The first launch of a segmented scan runs ctas * (1 + 2 (nseg - 2)) CTAs, one per SM.
 inline int choose_nseg(int64_t T, int B, int HV, int V, int C) {
-  const int64_t ctas = (int64_t)B * HV * (V / 64);
+  const int64_t ctas = (int64_t)B * HV * (V == 128 ? 1 : V / 64);  // K = V = 128: both value blocks in one CTA
   const int64_t max_chunks = T / C;  // the longest sequence has at most this many chunks
   int best = 1;
   for (int n = 2; n <= 8; ++n) {

@@ -38,41 +38,53 @@ namespace {
 constexpr int C = 64;
 constexpr int VB = 64;
 constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
-// warps 0-7 chain (warps w and w+4 share TMEM lanes 32(w%4)..+31 and split the columns),
-// warps 8-9 outputs (TMEM lanes 0-63), warp 10 producer
+// warps 0-7 chain workers (warps w and w+4 share TMEM lanes 32(w%4)..+31 and split the
+// columns), warps 8-9 outputs (TMEM lanes 0-63), warp 10 TMA producer, warp 11 MMA issuer
 constexpr int kChain = 256, kOut = 64;
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 10;
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 10, kMmaWarp = 11;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D1 buffers [0,64) [64,128); DS [128,192) (keys 0-127) and, for K = 256,
-// [192,256) (keys 128-255); D2 buffers [256,320) [320,384)
+// TMEM columns, per chain slot: D1 [64 slot, +64); DS [128 + 64 slot, +64) (and, for K = 256,
+// keys 128-255 at [192, 256)); D2 [256 + 64 slot, +64). One chain per CTA uses slots 0/1 as a
+// double buffer over chunks; two chains per CTA use slot = chain.
 constexpr uint32_t kColD1 = 0, kColDS = 128, kColD2 = 256;
 
 enum Mode : int { kFull = 0, kMapB = 1, kMapT = 2 };
 
+// Chains (blocks of VB state rows) per CTA: for K = V = 128 one CTA runs both value blocks of
+// a head, interleaved, so one block's tensor-core work overlaps the other's CUDA-core work
+// and the chunk tiles are fetched once for both.
+template <int D>
+__host__ __device__ constexpr int chains_per_cta() { return D == 128 ? 2 : 1; }
+
 template <int D>
 struct ScanSmem {
   static constexpr int NB = D / 64;
-  static constexpr int STAGES = D < 256 ? 3 : 1;  // a K = 256 stage is 105 KB
+  static constexpr int NCH = chains_per_cta<D>();
+  static constexpr int STAGES = D == 64 ? 3 : (D == 128 ? 2 : 1);  // a K = 256 stage is 105 KB
   static constexpr uint32_t QW = 0;                 // NB x [Q block 8 KB][W<- block 8 KB]
   static constexpr uint32_t P = QW + NB * 16384;    // P 8 KB (A rows 64-127 of MMA2 = the 8 KB after it)
   static constexpr uint32_t K = P + 8192;           // NB x K block 8 KB (+ the 8 KB after: MMA3 rows K..127 if D = 64)
   static constexpr uint32_t F = K + NB * 8192;      // g, 1/|q|, 1/|k| (3 x 256 B), chunk t0 / len
   static constexpr uint32_t STAGE = F + 1024;
-  static constexpr uint32_t SCOPY = STAGES * STAGE; // bf16 S^T: D rows x 128 B
-  static constexpr uint32_t VN = SCOPY + D * 128;   // U      [64 rows x 128 B]
-  static constexpr uint32_t VKH = VN + 8192;        // Uk hi  [64 rows x 128 B]
-  static constexpr uint32_t VKL = VKH + 8192;       // Uk lo  [64 rows x 128 B]
-  static constexpr uint32_t BAR = VKL + 8192;
+  // per chain ch at + ch * CH: bf16 S^T (D rows x 128 B), U, Uk hi, Uk lo, U~ (64 rows x 128 B each)
+  static constexpr uint32_t SCOPY = STAGES * STAGE;
+  static constexpr uint32_t VN = SCOPY + D * 128;
+  static constexpr uint32_t VKH = VN + 8192;
+  static constexpr uint32_t VKL = VKH + 8192;
+  static constexpr uint32_t UT = VKL + 8192;
+  static constexpr uint32_t CH = D * 128 + 4 * 8192;
+  static constexpr uint32_t BAR = SCOPY + NCH * CH;
   static constexpr uint32_t bytes = BAR + 256;
   static constexpr uint32_t alloc = bytes + 1024;
   static constexpr uint32_t tx_full = NB * 16384 + NB * 8192 + 8192 + 3 * 256;  // W, Q, K, P, F
   static constexpr uint32_t tx_map = NB * 8192 + NB * 8192 + 3 * 256;           // W, K, F
+  static_assert(alloc <= 232448, "shared memory per CTA");
 };
 
 struct ScanJob {
   int mode;
-  int seq, hv, vblk;
+  int seq, hv, vblk;  // vblk: the first of the CTA's value blocks
   int c0, c1;         // chunk range [c0, c1) within the sequence
   const float* init;  // [rows][D] start state (kFull); zeros (kMapB) / identity (kMapT) otherwise
   float* fin;         // [rows][D] where the final state goes, or nullptr
@@ -91,14 +103,14 @@ __device__ __forceinline__ void seg_bounds(int n, int nseg, int p, int& c0, int&
 // segments 1 .. ns-2; kind 2: segments 1 .. ns-1 (full). Returns false if there is no job.
 template <int D>
 __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
-  constexpr int NVB = D / VB;
+  constexpr int NVB = D / VB / chains_per_cta<D>();  // CTAs per state (VB x NCH rows each)
   const int B = p.B, HV = p.HV;
   const int64_t per_head = (int64_t)D * D;  // floats per (slot, value head) state
   int bid = blockIdx.x;
   job.init = nullptr;
   job.fin = nullptr;
   if (kind == 0 || (kind == 1 && bid < B * HV * NVB)) {
-    job.vblk = bid % NVB;
+    job.vblk = (bid % NVB) * chains_per_cta<D>();
     bid /= NVB;
     job.seq = p.order[bid / HV];
     job.hv = bid % HV;
@@ -124,7 +136,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
     int idx = bid % per_chain;
     job.seq = p.order[rest / HV];
     job.hv = rest % HV;
-    job.vblk = idx % NVB;
+    job.vblk = (idx % NVB) * chains_per_cta<D>();
     idx /= NVB;
     const int which = idx % 2, seg = 1 + idx / 2;
     const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
@@ -136,7 +148,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
     return job.c1 > job.c0;
   }
   // kind 2: segments 1 .. nseg-1, full
-  job.vblk = bid % NVB;
+  job.vblk = (bid % NVB) * chains_per_cta<D>();
   bid /= NVB;
   const int seg = 1 + bid % (nseg - 1);
   bid /= (nseg - 1);
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p, int kind,
                 int nseg) {
   using SM = ScanSmem<D>;
-  constexpr int NB = SM::NB, S = SM::STAGES;
+  constexpr int NB = SM::NB, S = SM::STAGES, NCH = SM::NCH;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -184,23 +196,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [S]
   uint64_t* empty = full + S;                                    // [S]
-  uint64_t* mma1 = empty + S;                                    // D1 ready
-  uint64_t* mma3 = mma1 + 1;                                     // DS ready
-  uint64_t* mmao = mma3 + 1;                                     // [2] D2 ready (per buffer)
-  uint64_t* odone = mmao + 2;                                    // [2] O warps done with D1/D2 buffer
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(odone + 2);
+  uint64_t* mma1 = empty + S;                                    // [2] D1 of chain ch ready
+  uint64_t* mma3 = mma1 + 2;                                     // [2] DS of chain ch ready
+  uint64_t* mmao = mma3 + 2;                                     // [2] D2 of slot ready
+  uint64_t* odone = mmao + 2;                                    // [2] O warps done with slot's D1/D2
+  uint64_t* uready = odone + 2;                                  // [2] chain ch: U, Uk written, gates read
+  uint64_t* sready = uready + 2;                                 // [2] chain ch: bf16 S^T written
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sready + 2);
   volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&empty[s], full_mode ? 2 : 1);  // the chain (and the output warps) release a stage
+      tc::mbar_init(&empty[s], full_mode ? 2 : 1);  // the MMAs (and the output warps) release a stage
     }
-    tc::mbar_init(mma1, 1);
-    tc::mbar_init(mma3, 1);
     for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&mma1[b], 1);
+      tc::mbar_init(&mma3[b], 1);
       tc::mbar_init(&mmao[b], 1);
       tc::mbar_init(&odone[b], kOut);
+      tc::mbar_init(&uready[b], kChain / 32);  // one arrival per chain warp
+      tc::mbar_init(&sready[b], kChain / 32);
     }
     *fail = 0;
     tc::mbar_fence_init();
@@ -247,49 +263,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= kChain / 32) {
-    // ------------------------------------------------------------------ outputs, one chunk behind
-    if (full_mode) {
-      const int r = tid - kChain;  // output row of the chunk (warps 4-5: TMEM lanes 0-63)
-      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-      for (int c = 0; c < nc; ++c) {
-        const int s = c % S, buf = c & 1;
-        if (!wait_or_fail(&mmao[buf], (c >> 1) & 1, fail)) {
-          report();
-          break;
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr int NKR = D > 128 ? 2 : 1;
+      constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
+      constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
+      // Base descriptors; an operand at byte offset o from its base is base + (o >> 4) (the
+      // start-address field holds address >> 4 and shared addresses stay below 256 KB).
+      const uint64_t dA1 = tc::smem_desc(tc::saddr(smem + SM::QW), 16, 1024, tc::kSwizzle128B);
+      const uint64_t dB1 = tc::smem_desc(tc::saddr(smem + SM::SCOPY), D * 128, 1024, tc::kSwizzle128B);
+      const uint64_t dA3 = tc::smem_desc(tc::saddr(smem + SM::K), 8192, 1024, tc::kSwizzle128B);
+      const uint64_t dB3 = tc::smem_desc(tc::saddr(smem + SM::VKH), 8192, 1024, tc::kSwizzle128B);
+      const uint64_t dA2 = tc::smem_desc(tc::saddr(smem + SM::P), 16, 1024, tc::kSwizzle128B);
+      const uint64_t dB2 = tc::smem_desc(tc::saddr(smem + SM::VN), 8192, 1024, tc::kSwizzle128B);
+      static_assert(SM::VKL == SM::VKH + 8192, "Uk lo follows Uk hi");
+      bool ok = true;
+      for (int c = 0; c < nc && ok; ++c) {
+        const int s = c % S;
+        const uint32_t so = (uint32_t)(s * SM::STAGE) >> 4;  // stage offset in descriptor units
+        ok = wait_or_fail(&full[s], (c / S) & 1, fail);
+        // MMA1: D1[slot] = [Q; W<-] S^T, once the chain's bf16 S^T of chunk c-1 is written and
+        // the output warps are done with the slot
+        for (int ch = 0; ch < NCH && ok; ++ch) {
+          const int slot = NCH == 1 ? (c & 1) : ch;
+          const int use = NCH == 1 ? (c >> 1) : c;
+          const uint32_t co = (uint32_t)(ch * SM::CH) >> 4;
+          ok = wait_or_fail(&sready[ch], c & 1, fail);
+          if (ok && full_mode && use >= 1) ok = wait_or_fail(&odone[slot], (use - 1) & 1, fail);
+          if (!ok) break;
+          tc::fence_after_sync();
+#pragma unroll
+          for (int b = 0; b < NB; ++b)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f16_ss(tmem + kColD1 + 64 * slot, dA1 + so + ((b * 16384 + ks * 32) >> 4),
+                             dB1 + co + ((b * 8192 + ks * 2048) >> 4), idesc_x, (b | ks) != 0);
+          tc::mma_commit(&mma1[ch]);
         }
-        tc::fence_after_sync();
-        const unsigned char* st = smem + s * SM::STAGE;
-        const float* gs = reinterpret_cast<const float*>(st + SM::F);
-        const float sq = expf(gs[r]) * gs[C + r] * p.scale;
-        const int t0 = reinterpret_cast<const int*>(st + SM::F + 768)[0];
-        const int len = reinterpret_cast<const int*>(st + SM::F + 768)[1];
-        tc::named_sync(3, kOut);
-        if (tid == kChain) tc::mbar_arrive(&empty[s]);  // P and the gates are no longer needed
-        bf16* orow = p.out + (((int64_t)t0 + r) * p.HV + hv) * (int64_t)D + vblk * VB;
+        // MMA3: DS[ch] = K^T (Uk_hi + Uk_lo) (the chain waits for this); MMA2: D2[slot] = [P; *] U
+        for (int ch = 0; ch < NCH && ok; ++ch) {
+          const int slot = NCH == 1 ? (c & 1) : ch;
+          const uint32_t co = (uint32_t)(ch * SM::CH) >> 4;
+          ok = wait_or_fail(&uready[ch], c & 1, fail);
+          if (!ok) break;
+          tc::fence_after_sync();
 #pragma unroll
-        for (int cc = 0; cc < VB / 16; ++cc) {
-          uint32_t a[16], b[16];  // warp-collective TMEM loads: every lane loads
-          tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + 16 * cc, a);
-          tc::tmem_ld16(tmem + lane_base + kColD2 + 64 * buf + 16 * cc, b);
-          tc::tmem_wait_ld();
-          if (r < len) {
-            uint32_t w[8];
+          for (int kr = 0; kr < NKR; ++kr)  // keys 128 kr .. 128 kr + 127: K blocks 2 kr, 2 kr + 1
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
-                               sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
-            uint4* d4 = reinterpret_cast<uint4*>(orow + 16 * cc);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16_ss(tmem + kColDS + 64 * (ch * NKR + kr), dA3 + so + ((kr * 16384 + ks * 2048) >> 4),
+                               dB3 + co + ((part * 8192 + ks * 2048) >> 4), idesc_s, (part | ks) != 0);
+          tc::mma_commit(&mma3[ch]);
+          if (full_mode) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              tc::mma_f16_ss(tmem + kColD2 + 64 * slot, dA2 + so + ((ks * 32) >> 4), dB2 + co + ((ks * 2048) >> 4),
+                             idesc_x, ks > 0);
+            tc::mma_commit(&mmao[slot]);
           }
         }
-        tc::fence_before_sync();
-        tc::mbar_arrive(&odone[buf]);
+        // the stage is free once every MMA of chunk c is done (no later chunk reuses the last S)
+        if (ok && c + S < nc) tc::mma_commit(&empty[s]);
+      }
+      if (!ok) report();
+    }
+    __syncwarp();
+  } else if (warp >= kChain / 32) {
+    // ------------------------------------------------------------------ outputs, one step behind
+    if (full_mode) {
+      const int r = tid - kChain;  // output row of the chunk (warps 8-9: TMEM lanes 0-63)
+      const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+      bool bad = false;
+      for (int c = 0; c < nc && !bad; ++c) {
+        const int s = c % S;
+        const unsigned char* st = smem + s * SM::STAGE;
+        float sq = 0.f;
+        int t0 = 0, len = 0;
+        for (int ch = 0; ch < NCH; ++ch) {
+          const int slot = NCH == 1 ? (c & 1) : ch;
+          const int use = NCH == 1 ? (c >> 1) : c;
+          if (!wait_or_fail(&mmao[slot], use & 1, fail)) {
+            report();
+            bad = true;
+            break;
+          }
+          tc::fence_after_sync();
+          if (ch == 0) {
+            const float* gs = reinterpret_cast<const float*>(st + SM::F);
+            sq = expf(gs[r]) * gs[C + r] * p.scale;
+            t0 = reinterpret_cast<const int*>(st + SM::F + 768)[0];
+            len = reinterpret_cast<const int*>(st + SM::F + 768)[1];
+          }
+          if (ch == NCH - 1) {  // every chain's P product is done and the gates are read
+            tc::named_sync(3, kOut);
+            if (tid == kChain) tc::mbar_arrive(&empty[s]);
+          }
+          bf16* orow = p.out + (((int64_t)t0 + r) * p.HV + hv) * (int64_t)D + (vblk + ch) * VB;
+#pragma unroll
+          for (int cc = 0; cc < VB / 16; ++cc) {
+            uint32_t a[16], b[16];  // warp-collective TMEM loads: every lane loads
+            tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * slot + 16 * cc, a);
+            tc::tmem_ld16(tmem + lane_base + kColD2 + 64 * slot + 16 * cc, b);
+            tc::tmem_wait_ld();
+            if (r < len) {
+              uint32_t w[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
+                                 sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
+              uint4* d4 = reinterpret_cast<uint4*>(orow + 16 * cc);
+              d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+          tc::fence_before_sync();
+          tc::mbar_arrive(&odone[slot]);
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------------ chain: U, state update
+    // ------------------------------------------------------------------ chain workers: U, state update
     const int sub = warp & 3, half = warp >> 2;
     const int row = 32 * sub + lane;                        // TMEM lane of this thread
     const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
@@ -297,182 +393,164 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NKR = D > 128 ? 2 : 1;  // key rows per thread: row and row + 128
     const bool has_state = row < D;  // thread (row, half) holds columns cbase.. of key rows row (+128) of S^T
     const bool u_row = row >= 64;    // thread (64 + mu, half) forms half of row mu of U (TMEM lanes 64-127)
-    const int mu = row - 64;
-    float S_[NKR][32];
-    const int64_t row0 = (int64_t)vblk * VB + cbase;  // first state row held by this thread
-    if (has_state) {
+    const int mu = row - 64;         // (both flags are uniform over a warp)
+    const bool use_ut = mode != kMapT;
+    float S_[NCH][NKR][32];
+    // bf16 copy of the state rows this thread holds, for the next MMA1 of chain ch
+    auto write_scopy = [&](int ch) {
+      unsigned char* scopy = smem + SM::SCOPY + ch * SM::CH;
 #pragma unroll
       for (int kr = 0; kr < NKR; ++kr) {
         const int key = row + 128 * kr;
-        if (mode == kFull) {
-#pragma unroll
-          for (int v = 0; v < 32; ++v) S_[kr][v] = job.init[(row0 + v) * D + key];
-        } else if (mode == kMapT) {
-#pragma unroll
-          for (int v = 0; v < 32; ++v) S_[kr][v] = (row0 + v == key) ? 1.f : 0.f;
-        } else {
-#pragma unroll
-          for (int v = 0; v < 32; ++v) S_[kr][v] = 0.f;
-        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t w[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[kr][8 * cc + 2 * u], S_[kr][8 * cc + 2 * u + 1]);
-          *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + cc)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+          for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[ch][kr][8 * cc + 2 * u], S_[ch][kr][8 * cc + 2 * u + 1]);
+          *reinterpret_cast<uint4*>(scopy + tc::sw128_offset(key, 4 * half + cc)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-    }
-    const bool use_ut = mode != kMapT;
-    uint4 ut[4];
-    auto load_ut = [&](int c) {
-      const int64_t j = cb + job.c0 + c;
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + vblk * VB + cbase);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) ut[q] = src[q];
     };
-    if (u_row && use_ut) load_ut(0);
-    tc::fence_async_smem();
-    tc::named_sync(1, kChain);
+    // a warp's shared-memory writes are complete and visible to the tensor cores: tell the issuer
+    auto signal = [&](uint64_t* bar) {
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar);
+    };
+    if (has_state) {
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int64_t row0 = (int64_t)(vblk + ch) * VB + cbase;  // first state row held by this thread
+#pragma unroll
+        for (int kr = 0; kr < NKR; ++kr) {
+          const int key = row + 128 * kr;
+          if (mode == kFull) {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) S_[ch][kr][v] = job.init[(row0 + v) * D + key];
+          } else if (mode == kMapT) {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) S_[ch][kr][v] = (row0 + v == key) ? 1.f : 0.f;
+          } else {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) S_[ch][kr][v] = 0.f;
+          }
+        }
+        write_scopy(ch);
+      }
+    }
+    // U~ rows of a chunk, fetched by the threads that use them (half a row each)
+    auto fetch_ut = [&](int c) {
+      const int64_t j = cb + job.c0 + c;
+#pragma unroll
+      for (int ch = 0; ch < NCH; ++ch) {
+        const bf16* src = p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + (vblk + ch) * VB + cbase;
+        unsigned char* dst = smem + SM::UT + ch * SM::CH;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cp_async_16(dst + tc::sw128_offset(mu, 4 * half + q), src + 8 * q);
+      }
+      cp_async_commit();
+    };
+    // bounded wait with one verdict per warp (the warp then stays converged)
+    auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
+      const bool ok = wait_or_fail(bar, parity, fail);
+      return __all_sync(0xffffffffu, ok);
+    };
+    if (u_row && use_ut) fetch_ut(0);
+    for (int ch = 0; ch < NCH; ++ch) signal(&sready[ch]);  // the start state is in place
 
-    constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
-    constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
-    // Base descriptors; an operand at byte offset o from its base is base + (o >> 4) (the
-    // start-address field holds address >> 4 and shared addresses stay below 256 KB).
-    const uint64_t dA1 = tc::smem_desc(tc::saddr(smem + SM::QW), 16, 1024, tc::kSwizzle128B);
-    const uint64_t dB1 = tc::smem_desc(tc::saddr(smem + SM::SCOPY), D * 128, 1024, tc::kSwizzle128B);
-    const uint64_t dA3 = tc::smem_desc(tc::saddr(smem + SM::K), 8192, 1024, tc::kSwizzle128B);
-    const uint64_t dB3 = tc::smem_desc(tc::saddr(smem + SM::VKH), 8192, 1024, tc::kSwizzle128B);
-    const uint64_t dA2 = tc::smem_desc(tc::saddr(smem + SM::P), 16, 1024, tc::kSwizzle128B);
-    const uint64_t dB2 = tc::smem_desc(tc::saddr(smem + SM::VN), 8192, 1024, tc::kSwizzle128B);
-    static_assert(SM::VKL == SM::VKH + 8192, "Uk lo follows Uk hi");
     bool failed = false;
     for (int c = 0; c < nc; ++c) {
-      const int s = c % S, buf = c & 1;
-      const uint32_t so = (uint32_t)(s * SM::STAGE) >> 4;  // stage offset in descriptor units
-      unsigned char* st = smem + s * SM::STAGE;
-      bool bad = !wait_or_fail(&full[s], (c / S) & 1, fail);
-      if (tid == 0 && !bad && full_mode && c >= 2)  // O warps are done with D1[buf], D2[buf] of chunk c-2
-        bad = !wait_or_fail(&odone[buf], ((c - 2) >> 1) & 1, fail);
-      if (tc::named_sync_or(1, kChain, bad || *fail)) {
-        if (tid == 0) report();
+      const int s = c % S;
+      const unsigned char* st = smem + s * SM::STAGE;
+      if (!wait_warp(&full[s], (c / S) & 1)) {
         failed = true;
         break;
-      }
-      // MMA1: D1[buf] = [Q; W<-] S^T
-      if (tid == 0) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int b = 0; b < NB; ++b)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16_ss(tmem + kColD1 + 64 * buf, dA1 + so + ((b * 16384 + ks * 32) >> 4),
-                           dB1 + ((b * 8192 + ks * 2048) >> 4), idesc_x, (b | ks) != 0);
-        tc::mma_commit(mma1);
       }
       const float* gs = reinterpret_cast<const float*>(st + SM::F);
       const float gC = gs[C - 1];
       const float eC = expf(gC);
       const float sk = u_row ? expf(gC - gs[mu]) * gs[2 * C + mu] : 0.f;  // exp(g_C - g_mu) / |k_mu|
-      bad = !wait_or_fail(mma1, c & 1, fail);
-      tc::fence_after_sync();
-      if (u_row && !bad) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as bf16 hi + lo
-        uint32_t rr[2][16];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * buf + cbase + 16 * cc, rr[cc]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t wn[8], wh[8], wl[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float2 uf = make_float2(0.f, 0.f);
-            if (use_ut) uf = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3]);
-            const float n0 = uf.x - __uint_as_float(rr[cc][2 * u]), n1 = uf.y - __uint_as_float(rr[cc][2 * u + 1]);
-            wn[u] = pack_bf16(n0, n1);
-            const float k0 = n0 * sk, k1 = n1 * sk;
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
-            const float2 hf = __bfloat1622float2(hi);
-            wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
-            wl[u] = pack_bf16(k0 - hf.x, k1 - hf.y);
+      if (u_row && use_ut) cp_async_wait<0>();  // this thread's U~ rows of chunk c
+      for (int ch = 0; ch < NCH && !failed; ++ch) {
+        if (u_row) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as bf16 hi + lo
+          if (!wait_warp(&mma1[ch], c & 1)) {
+            failed = true;
+            break;
           }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t o = tc::sw128_offset(mu, 4 * half + 2 * cc + hh);
-            *reinterpret_cast<uint4*>(smem + SM::VN + o) = make_uint4(wn[4 * hh], wn[4 * hh + 1], wn[4 * hh + 2], wn[4 * hh + 3]);
-            *reinterpret_cast<uint4*>(smem + SM::VKH + o) = make_uint4(wh[4 * hh], wh[4 * hh + 1], wh[4 * hh + 2], wh[4 * hh + 3]);
-            *reinterpret_cast<uint4*>(smem + SM::VKL + o) = make_uint4(wl[4 * hh], wl[4 * hh + 1], wl[4 * hh + 2], wl[4 * hh + 3]);
-          }
-        }
-        if (use_ut && c + 1 < nc) load_ut(c + 1);
-      }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      if (tc::named_sync_or(1, kChain, bad)) {
-        if (tid == 0) report();
-        failed = true;
-        break;
-      }
-      // MMA3: DS = K^T (Uk_hi + Uk_lo) (the chain waits for this); MMA2: D2[buf] = [P; *] U (outputs)
-      if (tid == 0) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int kr = 0; kr < NKR; ++kr)  // keys 128 kr .. 128 kr + 127: K blocks 2 kr, 2 kr + 1
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              tc::mma_f16_ss(tmem + kColDS + 64 * kr, dA3 + so + ((kr * 16384 + ks * 2048) >> 4),
-                             dB3 + ((part * 8192 + ks * 2048) >> 4), idesc_s, (part | ks) != 0);
-        tc::mma_commit(mma3);
-        if (full_mode) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16_ss(tmem + kColD2 + 64 * buf, dA2 + so + ((ks * 32) >> 4), dB2 + ((ks * 2048) >> 4), idesc_x, ks > 0);
-          tc::mma_commit(&mmao[buf]);
-        }
-      }
-      bad = !wait_or_fail(mma3, c & 1, fail);
-      tc::fence_after_sync();
-      if (tid == 0) tc::mbar_arrive(&empty[s]);  // MMA1 and MMA3 are done with Q, W<-, K; gates in registers
-      if (has_state && !bad) {  // S <- exp(g_C) S + DS, and the bf16 copy for the next MMA1
-#pragma unroll
-        for (int kr = 0; kr < NKR; ++kr) {
-          const int key = row + 128 * kr;
+          tc::fence_after_sync();
+          const int slot = NCH == 1 ? (c & 1) : ch;
+          unsigned char* cbuf = smem + ch * SM::CH;
           uint32_t rr[2][16];
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColDS + 64 * kr + cbase + 16 * cc, rr[cc]);
+          for (int cc = 0; cc < 2; ++cc) tc::tmem_ld16(tmem + lane_base + kColD1 + 64 * slot + cbase + 16 * cc, rr[cc]);
+          uint4 ut[4] = {};
+          if (use_ut) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ut[q] = *reinterpret_cast<const uint4*>(cbuf + SM::UT + tc::sw128_offset(mu, 4 * half + q));
+          }
           tc::tmem_wait_ld();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t w[8];
+            uint32_t wn[8], wh[8], wl[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-              S_[kr][16 * cc + u] = fmaf(eC, S_[kr][16 * cc + u], __uint_as_float(rr[cc][u]));
+            for (int u = 0; u < 8; ++u) {
+              const float2 uf = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3]);
+              const float n0 = uf.x - __uint_as_float(rr[cc][2 * u]), n1 = uf.y - __uint_as_float(rr[cc][2 * u + 1]);
+              wn[u] = pack_bf16(n0, n1);
+              const float k0 = n0 * sk, k1 = n1 * sk;
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
+              const float2 hf = __bfloat1622float2(hi);
+              wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
+              wl[u] = pack_bf16(k0 - hf.x, k1 - hf.y);
+            }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = pack_bf16(S_[kr][16 * cc + 2 * u], S_[kr][16 * cc + 2 * u + 1]);
-            *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + 2 * cc)) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(smem + SM::SCOPY + tc::sw128_offset(key, 4 * half + 2 * cc + 1)) =
-                make_uint4(w[4], w[5], w[6], w[7]);
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t o = tc::sw128_offset(mu, 4 * half + 2 * cc + hh);
+              *reinterpret_cast<uint4*>(cbuf + SM::VN + o) = make_uint4(wn[4 * hh], wn[4 * hh + 1], wn[4 * hh + 2], wn[4 * hh + 3]);
+              *reinterpret_cast<uint4*>(cbuf + SM::VKH + o) = make_uint4(wh[4 * hh], wh[4 * hh + 1], wh[4 * hh + 2], wh[4 * hh + 3]);
+              *reinterpret_cast<uint4*>(cbuf + SM::VKL + o) = make_uint4(wl[4 * hh], wl[4 * hh + 1], wl[4 * hh + 2], wl[4 * hh + 3]);
+            }
           }
         }
+        signal(&uready[ch]);  // also: this warp has read the chunk's gates
       }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      if (tc::named_sync_or(1, kChain, bad)) {
-        if (tid == 0) report();
-        failed = true;
-        break;
+      if (failed) break;
+      if (u_row && use_ut && c + 1 < nc) fetch_ut(c + 1);  // every chain has read its U~ rows of chunk c
+      for (int ch = 0; ch < NCH; ++ch) {
+        if (!wait_warp(&mma3[ch], c & 1)) {
+          failed = true;
+          break;
+        }
+        tc::fence_after_sync();
+        if (has_state) {  // S <- exp(g_C) S + DS
+#pragma unroll
+          for (int kr = 0; kr < NKR; ++kr) {
+            uint32_t rr[2][16];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+              tc::tmem_ld16(tmem + lane_base + kColDS + 64 * (ch * NKR + kr) + cbase + 16 * cc, rr[cc]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) S_[ch][kr][u] = fmaf(eC, S_[ch][kr][u], __uint_as_float(rr[u >> 4][u & 15]));
+          }
+          write_scopy(ch);
+        }
+        signal(&sready[ch]);
       }
+      if (failed) break;
     }
+    if (failed) report();
+    if (u_row && use_ut) cp_async_wait<0>();  // no copy outlives the CTA
     if (has_state && !failed && job.fin) {
 #pragma unroll
-      for (int kr = 0; kr < NKR; ++kr)
+      for (int ch = 0; ch < NCH; ++ch) {
+        const int64_t row0 = (int64_t)(vblk + ch) * VB + cbase;
 #pragma unroll
-        for (int v = 0; v < 32; ++v) job.fin[(row0 + v) * D + row + 128 * kr] = S_[kr][v];
+        for (int kr = 0; kr < NKR; ++kr)
+#pragma unroll
+          for (int v = 0; v < 32; ++v) job.fin[(row0 + v) * D + row + 128 * kr] = S_[ch][kr][v];
+      }
     }
   }
 
@@ -537,7 +615,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
 template <int D>
 cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   using SM = ScanSmem<D>;
-  constexpr int NVB = D / VB;
+  constexpr int NVB = D / VB / chains_per_cta<D>();  // CTAs per state
   const int64_t rows = p.max_chunks * p.HV * C;
   CUtensorMap mw, mp, mq, mk;
   if (!make_2d_tile_map(&mw, p.W, D, rows, 64, C, true) || !make_2d_tile_map(&mp, p.P, C, rows, 64, C, true) ||
