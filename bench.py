@@ -165,7 +165,8 @@ def kernel_accounting(w, lengths):
     B = len(lengths)
     e = 2  # bf16
     qk = T * H * K * e * 2
-    intra_bytes = qk + T * HV * V * e + T * HV * 8
+    intra_bytes = qk + T * HV * V * e
+    gates_bytes = T * HV * 8 * 2  # a, b read; g, beta written
     scan_bytes = qk + T * HV * V * e + B * HV * V * K * 4 * 2
     intra_flops = scan_flops = 0.0
     for n in lengths:
@@ -174,6 +175,7 @@ def kernel_accounting(w, lengths):
             intra_flops += HV * ((H / HV) * (L * (L - 1) * K + L * (L + 1) * K) + L ** 3 / 3.0 + L * (L + 1) * (K + V))
             scan_flops += HV * (6.0 * L * K * V + L * (L + 1) * V)
     return {
+        "gates": {"bytes": gates_bytes, "flops": 0.0},
         "intra": {"bytes": intra_bytes, "flops": intra_flops},
         "scan": {"bytes": scan_bytes, "flops": scan_flops},
         "path": {"bytes": acc.min_hbm_bytes(lengths, H, HV, K, V), "flops": acc.flop_count(lengths, H, HV, K, V, C)},
@@ -181,7 +183,7 @@ def kernel_accounting(w, lengths):
 
 
 def kernel_source_hash(kernel: str) -> str:
-    files = {"intra": "gdn_intra.cu", "scan": "gdn_scan.cu", "schedule": "gdn_schedule.cu"}
+    files = {"gates": "gdn_gates.cu", "intra": "gdn_intra.cu", "scan": "gdn_scan.cu", "schedule": "gdn_schedule.cu"}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
     h = hashlib.sha256()
     for f in (files.get(kernel, ""), "gdn_common.cuh"):

@@ -1,5 +1,5 @@
 // gdn_api.cu — host side of the C ABI declared in include/gdn.h: argument checks,
-// workspace carve-up and the launch sequence K0 (schedule) -> K2 (intra) -> K3 (scan).
+// workspace carve-up and the launch sequence K0 (schedule) -> K1 (gates) -> K2 (intra) -> K3 (scan).
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -10,8 +10,8 @@
 namespace {
 
 // ---------------------------------------------------------------- instrumentation
-enum KernelId { kKernSchedule = 0, kKernIntra = 1, kKernScan = 2, kKernCount = 3 };  // scan: every scan-stage launch
-const char* const kKernelNames[kKernCount] = {"schedule", "intra", "scan"};
+enum KernelId { kKernSchedule = 0, kKernGates = 1, kKernIntra = 2, kKernScan = 3, kKernCount = 4 };  // scan: every scan-stage launch
+const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "scan"};
 
 std::atomic<int64_t> g_launches{0};
 
@@ -114,6 +114,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.order = reinterpret_cast<int32_t*>(ws + L.order);
   p.chunk_tab = reinterpret_cast<int4*>(ws + L.chunk_tab);
   p.g = reinterpret_cast<float*>(ws + L.g);
+  p.beta = reinterpret_cast<float*>(ws + L.beta);
   p.rq = reinterpret_cast<float*>(ws + L.rq);
   p.rk = reinterpret_cast<float*>(ws + L.rk);
   p.W = reinterpret_cast<gdn::bf16*>(ws + L.w);
@@ -128,6 +129,9 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s);
   if (total_tokens == 0 || batch == 0) return GDN_OK;
+  rec = prof_begin(kKernGates, s);
+  if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
   rec = prof_begin(kKernIntra, s);
   if (gdn::launch_intra(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s);

@@ -39,6 +39,7 @@ struct WsLayout {
   size_t order;          // int32[B]: sequences, longest first
   size_t chunk_tab;      // int4[max_chunks]: (seq, first token, length, chunk index in seq)
   size_t g;              // fp32[max_chunks][HV][C]: chunk-local cumulative log decay
+  size_t beta;           // fp32[max_chunks][HV][C]: beta (0 on padded rows)
   size_t rq;             // fp32[max_chunks][H][C]: 1/|q| per row (0 on padded rows)
   size_t rk;             // fp32[max_chunks][H][C]: 1/|k| per row (0 on padded rows)
   size_t w;              // bf16[max_chunks][HV][C][K]: W<-
@@ -82,6 +83,7 @@ inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C
   L.order = take((size_t)(B > 0 ? B : 1) * sizeof(int32_t));
   L.chunk_tab = take((size_t)mc * sizeof(int4));
   L.g = take((size_t)mc * HV * C * sizeof(float));
+  L.beta = take((size_t)mc * HV * C * sizeof(float));
   L.rq = take((size_t)mc * H * C * sizeof(float));
   L.rk = take((size_t)mc * H * C * sizeof(float));
   L.w = take((size_t)mc * HV * C * K * sizeof(bf16));
@@ -121,6 +123,7 @@ struct Params {
   int32_t* order;
   int4* chunk_tab;
   float* g;
+  float* beta;
   float* rq;
   float* rk;
   bf16* W;
@@ -200,6 +203,7 @@ bool make_2d_tile_map(CUtensorMap* map, const void* base, int inner, int64_t row
                       bool swizzle128);
 
 // Host-side launchers (one per translation unit, templated on head size).
+cudaError_t launch_gates(const Params& p, int C, cudaStream_t s);
 cudaError_t launch_intra(const Params& p, int D, int C, cudaStream_t s);
 cudaError_t launch_scan(const Params& p, int D, int C, cudaStream_t s);
 

@@ -1,19 +1,16 @@
-// gdn_intra.cu — K2: per-chunk gates, Gram products, the one triangular inverse and the
-// WY factors, for every chunk of every sequence in parallel, on the 5th-generation tensor
+// gdn_intra.cu — K2: per-chunk Gram products, the one triangular inverse and the WY
+// factors, for every chunk of every sequence in parallel, on the 5th-generation tensor
 // cores (tcgen05, fp32 accumulators in TMEM) with TMA tile loads.
 //
 // One CTA handles one (chunk, q/k head h) and loops over the HV/H value heads that read
-// head h, so K^K^^T and Q^K^^T are formed once per q/k head. Per value head it computes
-// (notation of gdn_common.cuh):
-//   log alpha = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b)   (pymllm page
-//               "pymllm.layers.attention.gdn_chunkwise", Parameters: raw gate inputs)
-//   g        = chunk-local inclusive cumsum of log alpha
+// head h, so K^K^^T and Q^K^^T are formed once per q/k head. With the gates g and beta of
+// the gates kernel it computes, per value head (notation of gdn_common.cuh):
 //   M^{-1}   for M = I + tril(diag(beta) K^K^^T, -1)   (blocked forward substitution)
 //   A        = (Gamma . M^{-1}) diag(beta)             (N^{-1} B = G M^{-1} G^{-1} B,
 //                                                      "Simple math to speed up GDN
 //                                                      prefill", section "Save one invert")
 //   W<-      = A diag(exp(g)) K^,   U~ = A V,   P = Gamma . tril(Q^K^^T)
-// and stores g, 1/|q|, 1/|k|, W<- [C][K], U~ [C][V] and P [C][C] for the scan.
+// and stores 1/|q|, 1/|k|, W<- [C][K], U~ [C][V] and P [C][C] for the scan.
 //
 // Tensor-core work (one elected thread issues, the accumulators live in TMEM):
 //   MMA1  D1[128 x 64]  = [K; Q] K^T            (M=128: rows 0-63 K K^T, rows 64-127 Q K^T)
@@ -40,9 +37,10 @@ struct IntraSmem {
   static constexpr uint32_t KQ = 0;                     // NB x [K block 8 KB][Q block 8 KB]
   static constexpr uint32_t V = KQ + NB * 16384;        // NB x V block 8 KB
   static constexpr uint32_t AA = V + NB * 8192;         // [A' 8 KB][A 8 KB], 128-byte swizzled
-  static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x 65; then the low parts of [A'; A]
-  static constexpr uint32_t XF = LF + 64 * 65 * 4;      // M^{-1}, fp32 64 x 65
-  static constexpr uint32_t VEC = XF + 64 * 65 * 4;     // g, beta, 1/|q|, 1/|k| (4 x 64 fp32)
+  static constexpr int LDF = 68;                        // fp32 tile pitch: conflict-free fragment loads
+  static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x LDF; then the low parts of [A'; A]
+  static constexpr uint32_t XF = LF + 64 * LDF * 4;     // M^{-1}, fp32 64 x LDF
+  static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k| (4 x 64 fp32)
   static constexpr uint32_t BAR = VEC + 4 * 64 * 4;     // 3 mbarriers + TMEM address
   static constexpr uint32_t bytes = BAR + 64;
   static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
@@ -55,7 +53,6 @@ __host__ __device__ constexpr uint32_t tmem_u() { return D < 128 ? 128u : (uint3
 template <int D>
 __host__ __device__ constexpr uint32_t tmem_cols() { return D < 256 ? 256u : 512u; }
 
-__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
   uint32_t r;
@@ -103,10 +100,11 @@ __device__ __forceinline__ void mm16_acc(float (&acc)[2][4], const float* A, con
 // lane per column, in registers), then block rows I = 1..3, one warp per block, with
 //   X_IJ = -X_II * sum_{K=J}^{I-1} L_IK X_KJ
 // formed as 3xTF32 warp-level tensor-core products (fp32 accuracy up to rounding order).
+// Run by four warps (lw = 0..3 among them) that meet at named barrier 2.
 template <int LDF>
-__device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4) {
+__device__ void invert_unit_lower_64(const float* Lf, float* Xf, int lw) {
+  const int warp = lw, lane = threadIdx.x & 31;
+  {
     const int b = warp * 16;
     const int c = lane & 15;
     float x[16];
@@ -122,7 +120,7 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
       for (int i = 0; i < 16; ++i) Xf[(b + i) * LDF + b + c] = x[i];
     }
   }
-  __syncthreads();
+  tc::named_sync(2, 128);
   const int g = lane >> 2, t = lane & 3;
   for (int I = 1; I < 4; ++I) {
     if (warp < I) {
@@ -149,35 +147,18 @@ __device__ void invert_unit_lower_64(const float* Lf, float* Xf) {
         xij[(g + 8) * LDF + 8 * nt + 2 * t + 1] = -acc2[nt][3];
       }
     }
-    __syncthreads();
+    tc::named_sync(2, 128);
   }
 }
 
-// Gates of value head hv for the chunk's tokens: beta and the chunk-local cumulative log
-// decay g (inclusive prefix sum); padded rows get log alpha = 0 and beta = 0. All threads.
-__device__ __forceinline__ void chunk_gates(const Params& p, int hv, int64_t t0, int len, int64_t jh, float* s_g,
-                                            float* s_beta) {
-  const int tid = threadIdx.x, lane = tid & 31;
+// Gates of value head hv for the chunk (from the gates kernel). All threads.
+__device__ __forceinline__ void load_gates(const Params& p, int64_t jh, float* s_g, float* s_beta) {
+  const int tid = threadIdx.x;
   if (tid < C) {
-    float la = 0.f, beta = 0.f;
-    if (tid < len) {
-      const int64_t t = t0 + tid;
-      la = -expf(p.A_log[hv]) * softplus_f(p.a[t * p.HV + hv] + p.dt_bias[hv]);
-      beta = 1.f / (1.f + expf(-p.b[t * p.HV + hv]));
-    }
-    float incl = la;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    s_g[tid] = incl;
-    s_beta[tid] = beta;
+    s_g[tid] = p.g[jh * C + tid];
+    s_beta[tid] = p.beta[jh * C + tid];
   }
   __syncthreads();
-  if (tid >= 32 && tid < C) s_g[tid] += s_g[31];
-  __syncthreads();
-  if (tid < C) p.g[jh * C + tid] = s_g[tid];
 }
 
 // All threads: bounded wait; every thread leaves with the same verdict.
@@ -189,12 +170,12 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v, Params p) {
   using SM = IntraSmem<D>;
   constexpr int NB = SM::NB;
-  constexpr int LDF = 65;
+  constexpr int LDF = SM::LDF;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -238,7 +219,10 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   const uint32_t lane_base = (uint32_t)(32 * sub) << 16;
 
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bar[0], NB * 16384);
+    const int64_t jh0 = (int64_t)j * p.HV + hv0;
+    tc::mbar_arrive_expect_tx(&bar[0], NB * 16384 + 2 * C * 4);
+    tc::bulk_load(s_g, p.g + jh0 * C, C * 4, &bar[0]);
+    tc::bulk_load(s_beta, p.beta + jh0 * C, C * 4, &bar[0]);
     for (int b = 0; b < NB; ++b) {
       tc::tma_load_3d(smem + SM::KQ + b * 16384, &tm_k, 64 * b, h, (int)t0, &bar[0]);
       tc::tma_load_3d(smem + SM::KQ + b * 16384 + 8192, &tm_q, 64 * b, h, (int)t0, &bar[0]);
@@ -246,7 +230,6 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
     tc::mbar_arrive_expect_tx(&bar[1], NB * 8192);
     for (int b = 0; b < NB; ++b) tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, hv0, (int)t0, &bar[1]);
   }
-  chunk_gates(p, hv0, t0, len, (int64_t)j * p.HV + hv0, s_g, s_beta);
 
   bool ok = wait_all(&bar[0], 0, p.status);
   if (ok && tid == 0) {
@@ -313,16 +296,24 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
   for (int ih = 0; ok && ih < r_heads; ++ih) {
     const int hv = hv0 + ih;
     const int64_t jh = (int64_t)j * p.HV + hv;
-    if (ih > 0) chunk_gates(p, hv, t0, len, jh, s_g, s_beta);
-    if (row < C) {  // L = tril(diag(beta) K^K^^T, -1), row i
+    if (ih > 0) load_gates(p, jh, s_g, s_beta);
+    if (row < C) {  // warps 0, 1, 4, 5: L = tril(diag(beta) K^K^^T, -1), row i, then M^{-1}
       const int i = row;
       const float bi = s_beta[i] * s_rk[i];
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
+      for (int u = 0; u < 32; u += 4) {
+        const float4 rk4 = *reinterpret_cast<const float4*>(s_rk + cbase + u);
         const int nu = cbase + u;
-        Lf[i * LDF + nu] = nu < i ? bi * s_rk[nu] * kq[u] : 0.f;
+        float4 l4;
+        l4.x = nu < i ? bi * rk4.x * kq[u] : 0.f;
+        l4.y = nu + 1 < i ? bi * rk4.y * kq[u + 1] : 0.f;
+        l4.z = nu + 2 < i ? bi * rk4.z * kq[u + 2] : 0.f;
+        l4.w = nu + 3 < i ? bi * rk4.w * kq[u + 3] : 0.f;
+        *reinterpret_cast<float4*>(Lf + i * LDF + nu) = l4;
       }
-    } else {  // P = Gamma . tril(Q^K^^T), row r, straight to global
+      tc::named_sync(2, 128);
+      invert_unit_lower_64<LDF>(Lf, Xf, (warp & 1) | ((warp >> 2) << 1));
+    } else {  // warps 2, 3, 6, 7 meanwhile: P = Gamma . tril(Q^K^^T), row r, straight to global
       const int r = row - C;
       const float qr = s_rq[r], gr = s_g[r];
       uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C + cbase);
@@ -339,9 +330,6 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
         prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    __syncthreads();
-    invert_unit_lower_64<LDF>(Lf, Xf);
-
     __syncthreads();  // L is dead from here on: its buffer takes the low bf16 parts of [A'; A]
     {  // A' rows (rows 0-63) and A rows (rows 64-127) as bf16 hi + lo, 128-byte swizzled K-major
       const int i = row & 63;
@@ -351,19 +339,25 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
       unsigned char* dst_lo = smem + SM::LF + (is_a ? 8192 : 0);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        const int n0 = cbase + 8 * c;
+        float x8[8], g8[8], b8[8], k8[8];  // X row i, and g, beta, 1/|k| of columns n0 .. n0+7
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          *reinterpret_cast<float4*>(x8 + 4 * q) = *reinterpret_cast<const float4*>(Xf + i * LDF + n0 + 4 * q);
+          *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g + n0 + 4 * q);
+          *reinterpret_cast<float4*>(b8 + 4 * q) = *reinterpret_cast<const float4*>(s_beta + n0 + 4 * q);
+          *reinterpret_cast<float4*>(k8 + 4 * q) = *reinterpret_cast<const float4*>(s_rk + n0 + 4 * q);
+        }
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float v2[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int nu = cbase + 8 * c + 2 * u + e;
-            float val = 0.f;
-            if (nu <= i) {
-              const float x = nu == i ? 1.f : Xf[i * LDF + nu];
-              val = is_a ? __expf(gi - s_g[nu]) * x * s_beta[nu] : egi * x * s_beta[nu] * s_rk[nu];
-            }
-            v2[e] = val;
+            const int m = 2 * u + e, nu = n0 + m;
+            const float x = nu == i ? 1.f : x8[m];  // entries above the diagonal are never read
+            const float val = is_a ? __expf(gi - g8[m]) * x * b8[m] : egi * x * (b8[m] * k8[m]);
+            v2[e] = nu <= i ? val : 0.f;
           }
           const __nv_bfloat162 hi = __floats2bfloat162_rn(v2[0], v2[1]);
           const float2 hf = __bfloat1622float2(hi);
@@ -410,17 +404,22 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const __grid_constant__
       const int mu = row & 63;
       bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D + half * (D / 2);
       const uint32_t col0 = (is_u ? tmem_u<D>() : 0u) + half * (D / 2);
+      constexpr int NG = D / 32, GB = NG < 4 ? NG : 4;  // 16-column groups, loaded GB at a time
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + lane_base + col0 + 16 * c, r);
+      for (int g0 = 0; g0 < NG; g0 += GB) {
+        uint32_t r[GB][16];
+#pragma unroll
+        for (int c = 0; c < GB; ++c) tc::tmem_ld16(tmem + lane_base + col0 + 16 * (g0 + c), r[c]);
         tc::tmem_wait_ld();
-        uint32_t w[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
-        d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        for (int c = 0; c < GB; ++c) {
+          uint32_t w[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) w[u] = pack_bf16(__uint_as_float(r[c][2 * u]), __uint_as_float(r[c][2 * u + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * (g0 + c));
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
       }
     }
     tc::fence_before_sync();
