@@ -612,6 +612,78 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
   }
 }
 
+// The same chaining for K <= 128 with each T_p (K x K fp32, <= 64 KB) fetched whole by a bulk
+// copy one step ahead (two buffers), so the loads overlap the previous step's products.
+template <int D>
+__global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
+  constexpr int R = 16;  // state rows per CTA
+  extern __shared__ __align__(16) float cbm[];
+  float* Tb = cbm;                // 2 x D x D
+  float* Sr = Tb + 2 * D * D;     // R x D
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Sr + R * D);  // [2]
+  if (p.status[0] != GDN_OK) return;
+  int bid = blockIdx.x;
+  const int rb = bid % (D / R);
+  bid /= (D / R);
+  const int hv = bid % p.HV;
+  const int seq = p.order[bid / p.HV];
+  const int n = p.seq_chunk_off[seq + 1] - p.seq_chunk_off[seq];
+  const int L = (n + nseg - 1) / nseg;
+  const int ns = L > 0 ? (n + L - 1) / L : 0;
+  if (ns < 3) return;
+  const int64_t per_head = (int64_t)D * D;
+  const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
+  const int tid = threadIdx.x;
+  auto fetch = [&](int seg) {  // thread 0: T of segment seg into buffer (seg - 1) & 1
+    uint64_t* b = &bar[(seg - 1) & 1];
+    tc::mbar_arrive_expect_tx(b, D * D * 4);
+    tc::bulk_load(Tb + ((seg - 1) & 1) * D * D, p.seg_map + (base + seg) * 2 * per_head + per_head, D * D * 4, b);
+  };
+  if (tid == 0) {
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
+    tc::mbar_fence_init();
+    fetch(1);
+    if (ns - 2 >= 2) fetch(2);
+  }
+  for (int e = tid; e < R * D; e += 256) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
+  __syncthreads();
+  const int r = tid / 16, c0 = (tid % 16) * (D / 16);  // one row, D/16 columns per thread
+  for (int seg = 1; seg <= ns - 2; ++seg) {
+    const float* T = Tb + ((seg - 1) & 1) * D * D;
+    const float* Bg = p.seg_map + (base + seg) * 2 * per_head;  // B_p (rows: value index)
+    float acc[D / 16];
+#pragma unroll
+    for (int u = 0; u < D / 16; ++u) acc[u] = Bg[((int64_t)rb * R + r) * D + c0 + u];
+    if (!__syncthreads_and(tc::mbar_wait(&bar[(seg - 1) & 1], ((seg - 1) >> 1) & 1, 1ll << 31))) {
+      if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
+      return;
+    }
+#pragma unroll 4
+    for (int k = 0; k < D; ++k) {
+      const float sk = Sr[r * D + k];
+#pragma unroll
+      for (int u = 0; u < D / 16; u += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(T + k * D + c0 + u);
+        acc[u] = fmaf(sk, t4.x, acc[u]);
+        acc[u + 1] = fmaf(sk, t4.y, acc[u + 1]);
+        acc[u + 2] = fmaf(sk, t4.z, acc[u + 2]);
+        acc[u + 3] = fmaf(sk, t4.w, acc[u + 3]);
+      }
+    }
+    __syncthreads();  // every thread is done with S_p and this T buffer
+    if (tid == 0 && seg + 2 <= ns - 2) {
+      tc::fence_async_smem();
+      fetch(seg + 2);
+    }
+#pragma unroll
+    for (int u = 0; u < D / 16; ++u) Sr[r * D + c0 + u] = acc[u];
+    __syncthreads();
+    for (int e = tid; e < R * D; e += 256)
+      p.seg_state[(base + seg + 1) * per_head + (int64_t)rb * R * D + e] = Sr[e];
+  }
+}
+
 template <int D>
 cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   using SM = ScanSmem<D>;
@@ -633,10 +705,17 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   scan_kernel<D><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nseg > 2) {
-    const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
-    e = cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-    if (e != cudaSuccess) return e;
-    combine_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+    if constexpr (D <= 128) {
+      const size_t csmem = (size_t)(2 * D * D + 16 * D) * sizeof(float) + 16;
+      e = cudaFuncSetAttribute(combine_bulk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+      if (e != cudaSuccess) return e;
+      combine_bulk_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+    } else {
+      const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
+      e = cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+      if (e != cudaSuccess) return e;
+      combine_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+    }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   scan_kernel<D><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
