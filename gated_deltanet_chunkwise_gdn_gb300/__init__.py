@@ -65,7 +65,7 @@ def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indice
                          workspace: torch.Tensor = None, check: bool = False, stream=None) -> torch.Tensor:
     """Chunkwise GDN prefill; returns ``out [total_tokens, HV, V]`` in v's dtype.
 
-    q, k ``[T, H, K]``, v ``[T, HV, V]`` bf16 on one CUDA device; a, b ``[T, HV]``,
+    q, k ``[T, H, K]``, v ``[T, HV, V]`` bf16 or fp16 (one dtype) on one CUDA device; a, b ``[T, HV]``,
     A_log, dt_bias ``[HV]`` fp32; state_pool ``[pool, HV, V, K]`` fp32 (updated in
     place); cache_indices ``[B]`` and cu_seqlens ``[B+1]`` int64 on the same device.
     ``check=True`` waits for the device and raises on a device-detected error

@@ -82,7 +82,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   if (!cu_seqlens || !A_log || !dt_bias) return GDN_ERR_INVALID_ARG;
   if (batch > 0 && (!state_pool || !cache_indices || pool_size <= 0)) return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!q || !k || !v || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
-  if (!supported_shape(K, V, chunk_size) || dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+  if (!supported_shape(K, V, chunk_size)) return GDN_ERR_UNSUPPORTED;
   const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock);
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return GDN_ERR_WORKSPACE;
@@ -123,6 +123,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.seg_state = reinterpret_cast<float*>(ws + L.seg_state);
   p.seg_map = reinterpret_cast<float*>(ws + L.seg_map);
   p.nseg = L.nseg;
+  p.fp16 = dtype == GDN_FP16 ? 1 : 0;
 
   int rec = prof_begin(kKernSchedule, s);
   gdn::schedule_kernel<<<1, 512, 0, s>>>(p, kWyBlock);
@@ -155,7 +156,7 @@ const char* gdn_status_string(gdn_status status) {
   switch (status) {
     case GDN_OK: return "GDN_OK";
     case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer, bad size or HV not a multiple of H";
-    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: head size, chunk size or dtype not built";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: head size or chunk size not built";
     case GDN_ERR_BAD_INDEX: return "GDN_ERR_BAD_INDEX: cache index out of range or repeated";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace null, too small or not 256-byte aligned";
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a bounded device-side wait gave up";

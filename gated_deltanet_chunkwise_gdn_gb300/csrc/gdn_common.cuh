@@ -26,6 +26,7 @@
 namespace gdn {
 
 using bf16 = __nv_bfloat16;
+using f16 = __half;
 
 constexpr float kNormEps = 1e-6f;  // q^ = q / sqrt(|q|^2 + eps)
 
@@ -42,9 +43,9 @@ struct WsLayout {
   size_t beta;           // fp32[max_chunks][HV][C]: beta (0 on padded rows)
   size_t rq;             // fp32[max_chunks][H][C]: 1/|q| per row (0 on padded rows)
   size_t rk;             // fp32[max_chunks][H][C]: 1/|k| per row (0 on padded rows)
-  size_t w;              // bf16[max_chunks][HV][C][K]: W<-
-  size_t u;              // bf16[max_chunks][HV][C][V]: U~
-  size_t p;              // bf16[max_chunks][HV][C][C]: P
+  size_t w;              // E[max_chunks][HV][C][K]: W<-   (E: the call's 16-bit element type)
+  size_t u;              // E[max_chunks][HV][C][V]: U~
+  size_t p;              // E[max_chunks][HV][C][C]: P
   size_t seg_state;      // fp32[B][HV][nseg][V][K]: start state of each segment (segmented scan)
   size_t seg_map;        // fp32[B][HV][nseg][2][K][K]: affine map (B, T) of each segment
   size_t total;
@@ -100,7 +101,7 @@ inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C
 // ----------------------------------------------------------------------------- launch params
 
 struct Params {
-  const bf16* q;
+  const bf16* q;  // 16-bit elements of the call's type (bf16 or fp16, see fp16)
   const bf16* k;
   const bf16* v;
   const float* a;
@@ -132,6 +133,7 @@ struct Params {
   float* seg_state;
   float* seg_map;
   int nseg;  // segments per sequence in the scan (1: one pass over each whole sequence)
+  int fp16;  // q, k, v, out (and the workspace factors) hold fp16 elements, else bf16
 };
 
 // ----------------------------------------------------------------------------- device helpers
@@ -185,6 +187,35 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// The 16-bit element type of a call (q, k, v, out, and every tensor-core operand derived
+// from them: tcgen05 kind::f16 takes A and B of one type). fmt: the MMA operand format code.
+template <typename E>
+struct ElemT;
+template <>
+struct ElemT<bf16> {
+  static constexpr uint32_t fmt = 1;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16(lo, hi); }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  }
+};
+template <>
+struct ElemT<f16> {
+  static constexpr uint32_t fmt = 0;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t w) { return __half22float2(*reinterpret_cast<const __half2*>(&w)); }
+};
+// (a, b) = hi + lo with hi and lo both in E: the pair carries about twice E's precision.
+template <typename E>
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = ElemT<E>::pack(a, b);
+  const float2 h = ElemT<E>::unpack(hi);
+  lo = ElemT<E>::pack(a - h.x, b - h.y);
+}
+
 // Status word: the first error recorded wins.
 __device__ __forceinline__ void set_status(int32_t* status, int code) {
   atomicCAS(reinterpret_cast<int*>(status), 0, code);
@@ -196,11 +227,12 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
 // longest-first sequence order. One block.
 __global__ void schedule_kernel(Params p, int C);
 
-// Host-side tensor maps (gdn_tma.cu): token tiles of a [T, heads, D] bf16 array (128-byte
-// swizzled), and tiles of a row-major [rows, inner] bf16 array.
-bool make_token_tile_map(CUtensorMap* map, const void* base, int D, int heads, int64_t T, int box_rows);
+// Host-side tensor maps (gdn_tma.cu): token tiles of a [T, heads, D] array of 16-bit
+// elements (128-byte swizzled), and tiles of a row-major [rows, inner] array; fp16 selects
+// fp16 elements, else bf16.
+bool make_token_tile_map(CUtensorMap* map, const void* base, int D, int heads, int64_t T, int box_rows, bool fp16);
 bool make_2d_tile_map(CUtensorMap* map, const void* base, int inner, int64_t rows, int box_inner, int box_rows,
-                      bool swizzle128);
+                      bool swizzle128, bool fp16);
 
 // Host-side launchers (one per translation unit, templated on head size).
 cudaError_t launch_gates(const Params& p, int C, cudaStream_t s);

@@ -18,7 +18,7 @@
 //   MMA3  DU[128 x D]   = [A'; A] V             (rows 64-127: U~ = A V)
 // Stacking A' and A keeps every MMA at M = 128 and puts W<- and U~ rows in TMEM lanes, so
 // each thread stores one contiguous output row. Normalisation and decay enter only as
-// diagonal scalings of fp32 accumulators or of the C x C operand; the raw bf16 q/k/v tiles
+// diagonal scalings of fp32 accumulators or of the C x C operand; the raw 16-bit q/k/v tiles
 // feed the tensor cores as TMA wrote them (128-byte swizzle, K-major for MMA1, the same
 // bytes read MN-major for MMA2/3).
 #include "gdn_common.cuh"
@@ -168,7 +168,7 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
 // Persistent: CTA b handles items b, b + gridDim.x, ... (item = chunk * H + q/k head). The
 // next item's q/k/v tiles and gates are fetched by TMA while the current item's W<- and U~
 // rows are written out (for D <= 128 through shared memory and TMA stores).
-template <int D>
+template <int D, typename E>
 __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
                                                          const __grid_constant__ CUtensorMap tm_v,
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     const int len = ct.z;
     if (tid == 0) {  // MMA1: D1 = [K; Q] K^T
       tc::fence_after_sync();
-      constexpr uint32_t idesc1 = tc::idesc_f16(128, 64, 1, false, false);
+      constexpr uint32_t idesc1 = tc::idesc_f16(128, 64, ElemT<E>::fmt, false, false);
       const uint64_t d0 = tc::smem_desc(tc::saddr(smem + SM::KQ), 16, 1024, tc::kSwizzle128B);
 #pragma unroll
       for (int b = 0; b < NB; ++b)
@@ -271,10 +271,10 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       for (int q = 0; q < 4 * NB; ++q) {
         const int cg = half * 4 * NB + q;  // chunk index over the whole row
         const uint4 v4 = *reinterpret_cast<const uint4*>(base + (cg >> 3) * 16384 + tc::sw128_offset(r64, cg & 7));
-        const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&v4);
+        const uint32_t* e = reinterpret_cast<const uint32_t*>(&v4);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float2 f = __bfloat1622float2(e[u]);
+          const float2 f = ElemT<E>::unpack(e[u]);
           ss += f.x * f.x + f.y * f.y;
         }
       }
@@ -343,15 +343,15 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             const int e0 = 8 * c + 2 * u, n0 = cbase + e0, n1 = n0 + 1;
             const float v0 = n0 <= r ? __expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[e0] : 0.f;
             const float v1 = n1 <= r ? __expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[e0 + 1] : 0.f;
-            w[u] = pack_bf16(v0, v1);
+            w[u] = ElemT<E>::pack(v0, v1);
           }
           prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       __syncthreads();
       offdiag_blocks<LDF>(Lf, Xf, reinterpret_cast<float*>(smem + SM::AA));  // scratch: the [A'; A] tile, not yet written
-      // L is dead from here on: its buffer takes the low bf16 parts of [A'; A]
-      {  // A' rows (rows 0-63) and A rows (rows 64-127) as bf16 hi + lo, 128-byte swizzled K-major
+      // L is dead from here on: its buffer takes the low 16-bit parts of [A'; A]
+      {  // A' rows (rows 0-63) and A rows (rows 64-127) as 16-bit hi + lo, 128-byte swizzled K-major
         const int i = row & 63;
         const bool is_a = row >= 64;
         const float gi = s_g[i], egi = expf(gi);
@@ -379,10 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
               const float val = is_a ? __expf(gi - g8[m]) * x * b8[m] : egi * x * (b8[m] * k8[m]);
               v2[e] = nu <= i ? val : 0.f;
             }
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(v2[0], v2[1]);
-            const float2 hf = __bfloat1622float2(hi);
-            wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
-            wl[u] = pack_bf16(v2[0] - hf.x, v2[1] - hf.y);
+            split2<E>(v2[0], v2[1], wh[u], wl[u]);
           }
           *reinterpret_cast<uint4*>(dst_hi + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
           *reinterpret_cast<uint4*>(dst_lo + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
@@ -395,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       if (!ok) break;
       if (tid == 0) {  // DW = [A'; A] K (rows 0-63: W<-), DU = [A'; A] V (rows 64-127: U~), [A'; A] = hi + lo
         tc::fence_after_sync();
-        constexpr uint32_t idesc2 = tc::idesc_f16(128, D, 1, false, true);
+        constexpr uint32_t idesc2 = tc::idesc_f16(128, D, ElemT<E>::fmt, false, true);
         const uint64_t da = tc::smem_desc(tc::saddr(smem + SM::AA), 16, 1024, tc::kSwizzle128B);
         const uint64_t dk = tc::smem_desc(tc::saddr(smem + SM::KQ), 16384, 1024, tc::kSwizzle128B);
         const uint64_t dv = tc::smem_desc(tc::saddr(smem + SM::V), 8192, 1024, tc::kSwizzle128B);
@@ -430,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         const bool is_u = row >= 64;
         const int mu = row & 63;
         const uint32_t col0 = (is_u ? tmem_u<D>() : 0u) + half * (D / 2);
-        bf16* dst = (is_u ? p.U : p.W) + (jh * C + mu) * D + half * (D / 2);
+        E* dst = reinterpret_cast<E*>(is_u ? p.U : p.W) + (jh * C + mu) * D + half * (D / 2);
         // D <= 128: 64-column block `half` of the staged tile (128-byte swizzled, the TMA box)
         unsigned char* stage = smem + (is_u ? SM::LF : SM::AA) + (D == 128 ? half * 8192 : 0);
         constexpr int NG = D / 32, GB = NG < 4 ? NG : 4;  // 16-column groups, loaded GB at a time
@@ -444,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
           for (int c = 0; c < GB; ++c) {
             uint32_t w[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) w[u] = pack_bf16(__uint_as_float(r[c][2 * u]), __uint_as_float(r[c][2 * u + 1]));
+            for (int u = 0; u < 8; ++u) w[u] = ElemT<E>::pack(__uint_as_float(r[c][2 * u]), __uint_as_float(r[c][2 * u + 1]));
             if constexpr (kTmaStore) {
               const int ch = (D == 128 ? 0 : half * 4) + 2 * (g0 + c);  // 16-byte chunk within the 128-byte row
               *reinterpret_cast<uint4*>(stage + tc::sw128_offset(mu, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -481,16 +478,17 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   }
 }
 
-template <int D>
+template <int D, typename E>
 cudaError_t launch_intra_t(const Params& p, cudaStream_t s) {
+  const bool h = p.fp16 != 0;
   CUtensorMap mq, mk, mv, mw, mu;
   const int64_t rows = p.max_chunks * p.HV * C;  // rows of the W<- and U~ arrays
-  if (!make_token_tile_map(&mq, p.q, D, p.H, p.T, C) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C) ||
-      !make_token_tile_map(&mv, p.v, D, p.HV, p.T, C) || !make_2d_tile_map(&mw, p.W, D, rows, 64, C, true) ||
-      !make_2d_tile_map(&mu, p.U, D, rows, 64, C, true))
+  if (!make_token_tile_map(&mq, p.q, D, p.H, p.T, C, h) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C, h) ||
+      !make_token_tile_map(&mv, p.v, D, p.HV, p.T, C, h) || !make_2d_tile_map(&mw, p.W, D, rows, 64, C, true, h) ||
+      !make_2d_tile_map(&mu, p.U, D, rows, 64, C, true, h))
     return cudaErrorInvalidValue;
   const uint32_t smem = IntraSmem<D>::alloc;
-  cudaError_t e = cudaFuncSetAttribute(intra_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(intra_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -498,7 +496,7 @@ cudaError_t launch_intra_t(const Params& p, cudaStream_t s) {
   // persistent: two CTAs per SM (TMEM and shared memory allow two), never more than the items
   const int64_t items = p.max_chunks * p.H;
   const int64_t blocks = items < 2 * (int64_t)sms ? items : 2 * (int64_t)sms;
-  intra_kernel<D><<<(unsigned)blocks, kThreads, smem, s>>>(mq, mk, mv, mw, mu, p);
+  intra_kernel<D, E><<<(unsigned)blocks, kThreads, smem, s>>>(mq, mk, mv, mw, mu, p);
   return cudaGetLastError();
 }
 
@@ -507,9 +505,9 @@ cudaError_t launch_intra_t(const Params& p, cudaStream_t s) {
 cudaError_t launch_intra(const Params& p, int D, int Cc, cudaStream_t s) {
   if (Cc != C) return cudaErrorInvalidValue;
   switch (D) {
-    case 64: return launch_intra_t<64>(p, s);
-    case 128: return launch_intra_t<128>(p, s);
-    case 256: return launch_intra_t<256>(p, s);
+    case 64: return p.fp16 ? launch_intra_t<64, f16>(p, s) : launch_intra_t<64, bf16>(p, s);
+    case 128: return p.fp16 ? launch_intra_t<128, f16>(p, s) : launch_intra_t<128, bf16>(p, s);
+    case 256: return p.fp16 ? launch_intra_t<256, f16>(p, s) : launch_intra_t<256, bf16>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -18,8 +18,8 @@
 // Critical path per chunk (the "chain" warps 0-7; warps w and w+4 serve TMEM lanes
 // 32(w%4)..+31, each taking half of the 64 columns):
 //   MMA1  D1[128 x 64] = [Q; W<-] S^T          -> U = U~ - D1[64:128]; Uk = diag(exp(g_C-g)/|k|) U
-//   MMA3  DS[K x 64]   = K^T (Uk_hi + Uk_lo)   -> S = exp(g_C) S + DS, bf16 copy to smem
-// Uk is carried as two bf16 terms (hi + lo) against the exact bf16 K tile, so the state
+//   MMA3  DS[K x 64]   = K^T (Uk_hi + Uk_lo)   -> S = exp(g_C) S + DS, 16-bit copy to smem
+// Uk is carried as two 16-bit terms (hi + lo) against the exact K tile, so the state
 // increment keeps about 16 bits of precision. Off the critical path:
 //   MMA2  D2[128 x 64] = [P; *] U  and warps 8-9 form O from D1[0:64] and D2[0:64] one chunk
 //   behind (D1, D2 double-buffered in TMEM);
@@ -67,7 +67,7 @@ struct ScanSmem {
   static constexpr uint32_t K = P + 8192;           // NB x K block 8 KB (+ the 8 KB after: MMA3 rows K..127 if D = 64)
   static constexpr uint32_t F = K + NB * 8192;      // g, 1/|q|, 1/|k| (3 x 256 B), chunk t0 / len
   static constexpr uint32_t STAGE = F + 1024;
-  // per chain ch at + ch * CH: bf16 S^T (D rows x 128 B), U, Uk hi, Uk lo, U~ (64 rows x 128 B each)
+  // per chain ch at + ch * CH: 16-bit S^T (D rows x 128 B), U, Uk hi, Uk lo, U~ (64 rows x 128 B each)
   static constexpr uint32_t SCOPY = STAGES * STAGE;
   static constexpr uint32_t VN = SCOPY + D * 128;
   static constexpr uint32_t VKH = VN + 8192;
@@ -174,7 +174,7 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   return true;
 }
 
-template <int D>
+template <int D, typename E>
 __global__ void __launch_bounds__(kThreads, 1)
     scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
                 const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k, Params p, int kind,
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mmao = mma3 + 2;                                     // [2] D2 of slot ready
   uint64_t* odone = mmao + 2;                                    // [2] O warps done with slot's D1/D2
   uint64_t* uready = odone + 2;                                  // [2] chain ch: U, Uk written, gates read
-  uint64_t* sready = uready + 2;                                 // [2] chain ch: bf16 S^T written
+  uint64_t* sready = uready + 2;                                 // [2] chain ch: 16-bit S^T written
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sready + 2);
   volatile int* fail = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
       constexpr int NKR = D > 128 ? 2 : 1;
-      constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, 1, false, true);  // A K-major, B MN-major
-      constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, 1, true, true);   // both MN-major
+      constexpr uint32_t idesc_x = tc::idesc_f16(128, VB, ElemT<E>::fmt, false, true);  // A K-major, B MN-major
+      constexpr uint32_t idesc_s = tc::idesc_f16(128, VB, ElemT<E>::fmt, true, true);   // both MN-major
       // Base descriptors; an operand at byte offset o from its base is base + (o >> 4) (the
       // start-address field holds address >> 4 and shared addresses stay below 256 KB).
       const uint64_t dA1 = tc::smem_desc(tc::saddr(smem + SM::QW), 16, 1024, tc::kSwizzle128B);
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = c % S;
         const uint32_t so = (uint32_t)(s * SM::STAGE) >> 4;  // stage offset in descriptor units
         ok = wait_or_fail(&full[s], (c / S) & 1, fail);
-        // MMA1: D1[slot] = [Q; W<-] S^T, once the chain's bf16 S^T of chunk c-1 is written and
+        // MMA1: D1[slot] = [Q; W<-] S^T, once the chain's 16-bit S^T of chunk c-1 is written and
         // the output warps are done with the slot
         for (int ch = 0; ch < NCH && ok; ++ch) {
           const int slot = NCH == 1 ? (c & 1) : ch;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::named_sync(3, kOut);
             if (tid == kChain) tc::mbar_arrive(&empty[s]);
           }
-          bf16* orow = p.out + (((int64_t)t0 + r) * p.HV + hv) * (int64_t)D + (vblk + ch) * VB;
+          E* orow = reinterpret_cast<E*>(p.out) + (((int64_t)t0 + r) * p.HV + hv) * (int64_t)D + (vblk + ch) * VB;
 #pragma unroll
           for (int cc = 0; cc < VB / 16; ++cc) {
             uint32_t a[16], b[16];  // warp-collective TMEM loads: every lane loads
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t w[8];
 #pragma unroll
               for (int u = 0; u < 8; ++u)
-                w[u] = pack_bf16(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
+                w[u] = ElemT<E>::pack(sq * __uint_as_float(a[2 * u]) + p.scale * __uint_as_float(b[2 * u]),
                                  sq * __uint_as_float(a[2 * u + 1]) + p.scale * __uint_as_float(b[2 * u + 1]));
               uint4* d4 = reinterpret_cast<uint4*>(orow + 16 * cc);
               d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mu = row - 64;         // (both flags are uniform over a warp)
     const bool use_ut = mode != kMapT;
     float S_[NCH][NKR][32];
-    // bf16 copy of the state rows this thread holds, for the next MMA1 of chain ch
+    // 16-bit copy of the state rows this thread holds, for the next MMA1 of chain ch
     auto write_scopy = [&](int ch) {
       unsigned char* scopy = smem + SM::SCOPY + ch * SM::CH;
 #pragma unroll
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t w[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) w[u] = pack_bf16(S_[ch][kr][8 * cc + 2 * u], S_[ch][kr][8 * cc + 2 * u + 1]);
+          for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(S_[ch][kr][8 * cc + 2 * u], S_[ch][kr][8 * cc + 2 * u + 1]);
           *reinterpret_cast<uint4*>(scopy + tc::sw128_offset(key, 4 * half + cc)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t j = cb + job.c0 + c;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch) {
-        const bf16* src = p.U + (j * p.HV + hv) * C * D + (int64_t)mu * D + (vblk + ch) * VB + cbase;
+        const E* src = reinterpret_cast<const E*>(p.U) + (j * p.HV + hv) * C * D + (int64_t)mu * D + (vblk + ch) * VB + cbase;
         unsigned char* dst = smem + SM::UT + ch * SM::CH;
 #pragma unroll
         for (int q = 0; q < 4; ++q) cp_async_16(dst + tc::sw128_offset(mu, 4 * half + q), src + 8 * q);
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sk = u_row ? expf(gC - gs[mu]) * gs[2 * C + mu] : 0.f;  // exp(g_C - g_mu) / |k_mu|
       if (u_row && use_ut) cp_async_wait<0>();  // this thread's U~ rows of chunk c
       for (int ch = 0; ch < NCH && !failed; ++ch) {
-        if (u_row) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as bf16 hi + lo
+        if (u_row) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as 16-bit hi + lo
           if (!wait_warp(&mma1[ch], c & 1)) {
             failed = true;
             break;
@@ -495,14 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t wn[8], wh[8], wl[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const float2 uf = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(&ut[2 * cc + (u >> 2)])[u & 3]);
+              const float2 uf = ElemT<E>::unpack(reinterpret_cast<const uint32_t*>(&ut[2 * cc + (u >> 2)])[u & 3]);
               const float n0 = uf.x - __uint_as_float(rr[cc][2 * u]), n1 = uf.y - __uint_as_float(rr[cc][2 * u + 1]);
-              wn[u] = pack_bf16(n0, n1);
-              const float k0 = n0 * sk, k1 = n1 * sk;
-              const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
-              const float2 hf = __bfloat1622float2(hi);
-              wh[u] = *reinterpret_cast<const uint32_t*>(&hi);
-              wl[u] = pack_bf16(k0 - hf.x, k1 - hf.y);
+              wn[u] = ElemT<E>::pack(n0, n1);
+              split2<E>(n0 * sk, n1 * sk, wh[u], wl[u]);
             }
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -684,25 +680,26 @@ __global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
   }
 }
 
-template <int D>
+template <int D, typename E>
 cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
+  const bool h = p.fp16 != 0;
   using SM = ScanSmem<D>;
   constexpr int NVB = D / VB / chains_per_cta<D>();  // CTAs per state
   const int64_t rows = p.max_chunks * p.HV * C;
   CUtensorMap mw, mp, mq, mk;
-  if (!make_2d_tile_map(&mw, p.W, D, rows, 64, C, true) || !make_2d_tile_map(&mp, p.P, C, rows, 64, C, true) ||
-      !make_token_tile_map(&mq, p.q, D, p.H, p.T, C) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C))
+  if (!make_2d_tile_map(&mw, p.W, D, rows, 64, C, true, h) || !make_2d_tile_map(&mp, p.P, C, rows, 64, C, true, h) ||
+      !make_token_tile_map(&mq, p.q, D, p.H, p.T, C, h) || !make_token_tile_map(&mk, p.k, D, p.H, p.T, C, h))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(scan_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::alloc);
+  cudaError_t e = cudaFuncSetAttribute(scan_kernel<D, E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM::alloc);
   if (e != cudaSuccess) return e;
   const int64_t chains = (int64_t)p.B * p.HV;
   if (nseg <= 1) {
-    scan_kernel<D><<<(unsigned)(chains * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 0, 1);
+    scan_kernel<D, E><<<(unsigned)(chains * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 0, 1);
     return cudaGetLastError();
   }
   // segment 0 and the maps of segments 1 .. nseg-2, then the combine, then segments 1 .. nseg-1
   const int64_t grid1 = chains * NVB + chains * (nseg - 2) * 2 * NVB;
-  scan_kernel<D><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
+  scan_kernel<D, E><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nseg > 2) {
     if constexpr (D <= 128) {
@@ -718,7 +715,7 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  scan_kernel<D><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
+  scan_kernel<D, E><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
   return cudaGetLastError();
 }
 
@@ -727,9 +724,9 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
 cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
   if (Cc != C || p.nvb != D / VB) return cudaErrorInvalidValue;
   switch (D) {
-    case 64: return launch_scan_t<64>(p, p.nseg, s);
-    case 128: return launch_scan_t<128>(p, p.nseg, s);
-    case 256: return launch_scan_t<256>(p, p.nseg, s);
+    case 64: return p.fp16 ? launch_scan_t<64, f16>(p, p.nseg, s) : launch_scan_t<64, bf16>(p, p.nseg, s);
+    case 128: return p.fp16 ? launch_scan_t<128, f16>(p, p.nseg, s) : launch_scan_t<128, bf16>(p, p.nseg, s);
+    case 256: return p.fp16 ? launch_scan_t<256, f16>(p, p.nseg, s) : launch_scan_t<256, bf16>(p, p.nseg, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -62,7 +62,7 @@ extern "C" {
 typedef enum {
   GDN_OK = 0,
   GDN_ERR_INVALID_ARG = 1,  /* null pointer, bad size or HV % H != 0            */
-  GDN_ERR_UNSUPPORTED = 2,  /* (K, V, chunk_size, dtype) not built                */
+  GDN_ERR_UNSUPPORTED = 2,  /* (K, V, chunk_size) not built                       */
   GDN_ERR_BAD_INDEX = 3,    /* cache index outside [0, pool_size) or repeated     */
   GDN_ERR_WORKSPACE = 4,    /* workspace null, too small or misaligned            */
   GDN_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up                 */

@@ -88,7 +88,7 @@ def test_host_side_errors_return_before_any_device_work(lib):
     assert _call(lib, dtype=7) == 1
     assert _call(lib, K=96, V=96) == 2       # not built
     assert _call(lib, C=32) == 2
-    assert _call(lib, dtype=1) == 2          # fp16 not built yet
+    assert _call(lib, dtype=-1) == 1         # no such dtype
     assert _call(lib, ws=None) == 4          # workspace
     assert _call(lib, ws=264) == 4           # misaligned
     assert _call(lib, ws_bytes=16) == 4      # too small

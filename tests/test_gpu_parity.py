@@ -221,6 +221,46 @@ def test_chunk_size_128_matches_oracle():
     untouched_slots_equal(d, pool)
 
 
+# ----------------------------------------------------------------------------- fp16 inputs
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_fp16_ragged_lengths_and_gqa(D):
+    """fp16 q/k/v (and output): every tensor-core operand in fp16, lengths around the
+    chunk size, GQA 1:2."""
+    w = wl.custom("ragged16", [1, 63, 64, 65, 0, 200, 130], H=2, HV=4, K=D, V=D, chunk_size=64, seed=41,
+                  dtype=torch.float16)
+    d = wl.make_inputs(w)
+    assert d["q"].dtype == torch.float16
+    out, pool = run_gpu(d)
+    assert out.dtype == torch.float16
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
+def test_fp16_segmented_long_sequence_weak_decay():
+    """fp16 through the segment-parallel scan, with alpha ~ 1 so errors would accumulate."""
+    w = wl.custom("seg16", [6400], H=1, HV=2, K=128, V=128, chunk_size=64, seed=42, dtype=torch.float16)
+    d = wl.make_inputs(w)
+    d["A_log"] = torch.full_like(d["A_log"], -7.0)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_fp16_and_bf16_of_the_same_values():
+    """The bf16 inputs and their fp16 conversion (nearly all values exact in fp16), each
+    against the oracle on its own input bits; the two GPU outputs agree to 16-bit rounding."""
+    w = wl.custom("same", [300, 129], H=2, HV=2, K=128, V=128, chunk_size=64, seed=43)
+    d = wl.make_inputs(w)
+    d16 = dict(d)
+    for k in ("q", "k", "v"):
+        d16[k] = d[k].to(torch.float16)
+    out_b, pool_b = run_gpu(d)
+    out_h, pool_h = run_gpu(d16)
+    compare(d, out_b, pool_b, oracle_for(d))
+    compare(d16, out_h, pool_h, oracle_for(d16))
+    assert rel_l2(out_h.float().numpy(), out_b.float().numpy()) < 1e-2
+
+
 def test_segmented_scan_mixed_lengths():
     w = wl.custom("segmix", [5000, 700, 1], H=1, HV=1, K=64, V=64, chunk_size=64, seed=34)
     d = wl.make_inputs(w)
