@@ -117,6 +117,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.beta = reinterpret_cast<float*>(ws + L.beta);
   p.rq = reinterpret_cast<float*>(ws + L.rq);
   p.rk = reinterpret_cast<float*>(ws + L.rk);
+  p.ks = reinterpret_cast<float*>(ws + L.ks);
   p.W = reinterpret_cast<gdn::bf16*>(ws + L.w);
   p.U = reinterpret_cast<gdn::bf16*>(ws + L.u);
   p.P = reinterpret_cast<gdn::bf16*>(ws + L.p);

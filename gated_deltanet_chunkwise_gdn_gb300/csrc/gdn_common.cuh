@@ -43,6 +43,7 @@ struct WsLayout {
   size_t beta;           // fp32[max_chunks][HV][C]: beta (0 on padded rows)
   size_t rq;             // fp32[max_chunks][H][C]: 1/|q| per row (0 on padded rows)
   size_t rk;             // fp32[max_chunks][H][C]: 1/|k| per row (0 on padded rows)
+  size_t ks;             // fp32[max_chunks][HV][C]: power-of-two part of exp(g_C - g)/|k| (K = V = 128)
   size_t w;              // E[max_chunks][HV][C][K]: W<-   (E: the call's 16-bit element type)
   size_t u;              // E[max_chunks][HV][C][V]: U~
   size_t p;              // E[max_chunks][HV][C][C]: P
@@ -55,11 +56,18 @@ struct WsLayout {
 
 // Segments per sequence for the scan: more than one only when there are too few
 // (sequence, head, 64-row block) chains to fill the GPU and the sequences may be long.
-// The first launch of a segmented scan runs ctas * (1 + 2 (nseg - 2)) CTAs, one per SM.
-inline int choose_nseg(int64_t T, int B, int HV, int V, int C) {
-  const int64_t ctas = (int64_t)B * HV * (V == 128 ? 1 : V / 64);  // K = V = 128: both value blocks in one CTA
+// K = V = 128 (affine-transition scan): each pass runs ctas * (nseg - 1) CTAs, one per SM.
+// Otherwise the first launch runs ctas * (1 + 2 (nseg - 2)) CTAs.
+inline int choose_nseg(int64_t T, int B, int HV, int K, int V, int C) {
   const int64_t max_chunks = T / C;  // the longest sequence has at most this many chunks
   int best = 1;
+  if (K == 128 && V == 128) {
+    const int64_t ctas = (int64_t)B * HV;
+    for (int n = 2; n <= 16; ++n)
+      if (ctas * (n - 1) <= 148 && max_chunks >= 32 * n) best = n;
+    return best;
+  }
+  const int64_t ctas = (int64_t)B * HV * (V / 64);
   for (int n = 2; n <= 8; ++n) {
     const int64_t grid1 = ctas * (1 + 2 * (n - 2));
     if (grid1 <= 148 && max_chunks >= 32 * n) best = n;
@@ -87,10 +95,11 @@ inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C
   L.beta = take((size_t)mc * HV * C * sizeof(float));
   L.rq = take((size_t)mc * H * C * sizeof(float));
   L.rk = take((size_t)mc * H * C * sizeof(float));
+  L.ks = take(K == 128 && V == 128 ? (size_t)mc * HV * C * sizeof(float) : 0);
   L.w = take((size_t)mc * HV * C * K * sizeof(bf16));
   L.u = take((size_t)mc * HV * C * V * sizeof(bf16));
   L.p = take((size_t)mc * HV * C * C * sizeof(bf16));
-  L.nseg = choose_nseg(T, B, HV, V, C);
+  L.nseg = choose_nseg(T, B, HV, K, V, C);
   const size_t per_head = (size_t)K * K * sizeof(float);
   L.seg_state = take(L.nseg > 1 ? (size_t)B * HV * L.nseg * per_head : 0);
   L.seg_map = take(L.nseg > 2 ? (size_t)B * HV * L.nseg * 2 * per_head : 0);
@@ -127,6 +136,7 @@ struct Params {
   float* beta;
   float* rq;
   float* rk;
+  float* ks;  // K = V = 128 only: ks[t] = 2^e with exp(g_C - g_t)/|k_t| = m_t 2^e, m_t in [0.5, 1)
   bf16* W;
   bf16* U;
   bf16* P;

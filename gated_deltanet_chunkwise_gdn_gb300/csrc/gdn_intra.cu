@@ -12,6 +12,12 @@
 //   W<-      = A diag(exp(g)) K^,   U~ = A V,   P = Gamma . tril(Q^K^^T)
 // and stores 1/|q|, 1/|k|, W<- [C][K], U~ [C][V] and P [C][C] for the scan.
 //
+// For K = V = 128 the scan runs in affine-transition form and needs the per-row factor
+// sk_t = exp(g_C - g_t)/|k_t| applied to the chunk's keys. It is split exactly into a
+// mantissa and a power of two, sk_t = m_t 2^e_t with m_t in [0.5, 1): this kernel folds m_t
+// into the rows of W<- and U~ and 1/m_t into the columns of P (so P U stays unchanged), and
+// stores ks_t = 2^e_t, which the scan applies to the raw 16-bit keys without rounding.
+//
 // Tensor-core work (one elected thread issues, the accumulators live in TMEM):
 //   MMA1  D1[128 x 64]  = [K; Q] K^T            (M=128: rows 0-63 K K^T, rows 64-127 Q K^T)
 //   MMA2  DW[128 x D]   = [A'; A] K             (rows 0-63: W<- = A' K with A' = A diag(e^g/|k|))
@@ -40,8 +46,8 @@ struct IntraSmem {
   static constexpr int LDF = 68;                        // fp32 tile pitch: conflict-free fragment loads
   static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x LDF; then the low parts of [A'; A]
   static constexpr uint32_t XF = LF + 64 * LDF * 4;     // M^{-1}, fp32 64 x LDF
-  static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k| (4 x 64 fp32)
-  static constexpr uint32_t BAR = VEC + 4 * 64 * 4;     // 3 mbarriers + TMEM address
+  static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k|, m, 1/m (6 x 64 fp32)
+  static constexpr uint32_t BAR = VEC + 6 * 64 * 4;     // 3 mbarriers + TMEM address
   static constexpr uint32_t bytes = BAR + 64;
   static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
 };
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   constexpr int NB = SM::NB;
   constexpr int LDF = SM::LDF;
   constexpr bool kTmaStore = D <= 128;  // W<- and U~ tiles staged in the [A'; A] and L buffers
+  constexpr bool kAffine = D == 128;    // rows of W<-, U~ scaled by m_t, columns of P by 1/m_t
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -197,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   float* s_beta = s_g + C;
   float* s_rq = s_beta + C;
   float* s_rk = s_rq + C;
+  float* s_m = s_rk + C;   // K = V = 128: mantissa m_t of sk_t = exp(g_C - g_t)/|k_t| = m_t 2^e_t
+  float* s_im = s_m + C;   // 1/m_t
   float* s_part = reinterpret_cast<float*>(smem + SM::XF);  // norm partial sums (before X is formed)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles + gates, [1] v tile, [2] MMAs
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
@@ -315,6 +324,21 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       const int hv = hv0 + ih;
       const int64_t jh = (int64_t)j * p.HV + hv;
       if (ih > 0) load_gates(p, jh, s_g, s_beta);
+      if constexpr (kAffine) {  // sk_t = m_t 2^e_t, m_t in [0.5, 1); padded rows (1/|k| = 0): m = 1, ks = 0
+        if (tid < C) {
+          const float sk = expf(s_g[C - 1] - s_g[tid]) * s_rk[tid];
+          float m = 1.f, ks = 0.f;
+          if (sk > 0.f) {
+            int e;
+            m = frexpf(sk, &e);
+            ks = ldexpf(1.f, e);
+          }
+          s_m[tid] = m;
+          s_im[tid] = 1.f / m;
+          p.ks[jh * C + tid] = ks;
+        }
+        __syncthreads();
+      }
       if (row < C) {  // warps 0, 1, 4, 5: L = tril(diag(beta) K^K^^T, -1), row i; diagonal blocks of M^{-1}
         const int i = row;
         const float bi = s_beta[i] * s_rk[i];
@@ -341,8 +365,12 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int e0 = 8 * c + 2 * u, n0 = cbase + e0, n1 = n0 + 1;
-            const float v0 = n0 <= r ? __expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[e0] : 0.f;
-            const float v1 = n1 <= r ? __expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[e0 + 1] : 0.f;
+            float v0 = n0 <= r ? __expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[e0] : 0.f;
+            float v1 = n1 <= r ? __expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[e0 + 1] : 0.f;
+            if constexpr (kAffine) {
+              v0 *= s_im[n0];
+              v1 *= s_im[n1];
+            }
             w[u] = ElemT<E>::pack(v0, v1);
           }
           prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -355,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         const int i = row & 63;
         const bool is_a = row >= 64;
         const float gi = s_g[i], egi = expf(gi);
+        const float mi = kAffine ? s_m[i] : 1.f;  // row scale of W<- and U~
         unsigned char* dst_hi = smem + SM::AA + (is_a ? 8192 : 0);
         unsigned char* dst_lo = smem + SM::LF + (is_a ? 8192 : 0);
 #pragma unroll
@@ -376,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             for (int e = 0; e < 2; ++e) {
               const int m = 2 * u + e, nu = n0 + m;
               const float x = nu == i ? 1.f : x8[m];  // entries above the diagonal are never read
-              const float val = is_a ? __expf(gi - g8[m]) * x * b8[m] : egi * x * (b8[m] * k8[m]);
+              const float val = (is_a ? __expf(gi - g8[m]) * x * b8[m] : egi * x * (b8[m] * k8[m])) * mi;
               v2[e] = nu <= i ? val : 0.f;
             }
             split2<E>(v2[0], v2[1], wh[u], wl[u]);

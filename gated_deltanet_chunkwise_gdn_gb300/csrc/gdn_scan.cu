@@ -33,6 +33,9 @@
 #include "gdn_tc.cuh"
 
 namespace gdn {
+
+cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s);
+
 namespace {
 
 constexpr int C = 64;
@@ -701,31 +704,40 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
   const int64_t grid1 = chains * NVB + chains * (nseg - 2) * 2 * NVB;
   scan_kernel<D, E><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (nseg > 2) {
-    if constexpr (D <= 128) {
-      const size_t csmem = (size_t)(2 * D * D + 16 * D) * sizeof(float) + 16;
-      e = cudaFuncSetAttribute(combine_bulk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-      if (e != cudaSuccess) return e;
-      combine_bulk_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
-    } else {
-      const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
-      e = cudaFuncSetAttribute(combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
-      if (e != cudaSuccess) return e;
-      combine_kernel<D><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
-    }
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  if (nseg > 2 && (e = launch_combine(p, D, nseg, s)) != cudaSuccess) return e;
   scan_kernel<D, E><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+cudaError_t launch_affine_scan(const Params& p, cudaStream_t s);
+
+// Chains the segment maps (B, T) of every (sequence, value head): S_{p+1} = S_p T_p + B_p.
+cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s) {
+  const int64_t chains = (int64_t)p.B * p.HV;
+  cudaError_t e;
+  if (D <= 128) {
+    const size_t csmem = (size_t)(2 * D * D + 16 * D) * sizeof(float) + 16;
+    auto kern = D == 64 ? combine_bulk_kernel<64> : combine_bulk_kernel<128>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) != cudaSuccess) return e;
+    kern<<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+  } else {
+    const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
+    if ((e = cudaFuncSetAttribute(combine_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) !=
+        cudaSuccess)
+      return e;
+    combine_kernel<256><<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
-  if (Cc != C || p.nvb != D / VB) return cudaErrorInvalidValue;
+  if (Cc != C) return cudaErrorInvalidValue;
+  if (D == 128) return launch_affine_scan(p, s);  // K = V = 128: affine-transition form
+  if (p.nvb != D / VB) return cudaErrorInvalidValue;
   switch (D) {
     case 64: return p.fp16 ? launch_scan_t<64, f16>(p, p.nseg, s) : launch_scan_t<64, bf16>(p, p.nseg, s);
-    case 128: return p.fp16 ? launch_scan_t<128, f16>(p, p.nseg, s) : launch_scan_t<128, bf16>(p, p.nseg, s);
     case 256: return p.fp16 ? launch_scan_t<256, f16>(p, p.nseg, s) : launch_scan_t<256, bf16>(p, p.nseg, s);
     default: return cudaErrorInvalidValue;
   }
