@@ -77,6 +77,34 @@ inline int choose_nseg(int64_t T, int B, int HV, int K, int V, int C) {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Chunk range [c0, c1) of segment `part` when a sequence of n chunks is cut into at most
+// nseg segments for the segmented scan; ns = number of non-empty segments. Segment 0 is
+// r16/16 times as long as the others: its CTA runs in full mode (outputs) alongside the map
+// CTAs of the later segments, which do less work per chunk. The rest is split evenly.
+__host__ __device__ inline void seg_range(int n, int nseg, int r16, int part, int& c0, int& c1, int& ns) {
+  if (nseg <= 1 || n <= 0) {
+    ns = n > 0 ? 1 : 0;
+    c0 = part == 0 ? 0 : n;
+    c1 = n;
+    return;
+  }
+  const int den = (nseg - 1) * 16 + r16;
+  int L0 = (int)(((int64_t)n * r16 + den - 1) / den);
+  L0 = L0 < 1 ? 1 : (L0 > n ? n : L0);
+  const int rest = n - L0;
+  const int L1 = rest > 0 ? (rest + nseg - 2) / (nseg - 1) : 1;
+  ns = 1 + (rest + L1 - 1) / L1;
+  if (part == 0) {
+    c0 = 0;
+    c1 = L0;
+  } else {
+    c0 = L0 + (part - 1) * L1;
+    c1 = c0 + L1;
+    c0 = c0 < n ? c0 : n;
+    c1 = c1 < n ? c1 : n;
+  }
+}
+
 inline WsLayout make_layout(int64_t T, int B, int H, int HV, int K, int V, int C) {
   WsLayout L{};
   const int64_t mc = T / C + B + 1;
@@ -143,6 +171,7 @@ struct Params {
   float* seg_state;
   float* seg_map;
   int nseg;  // segments per sequence in the scan (1: one pass over each whole sequence)
+  int seg_r16;  // length of segment 0 relative to the others, in 16ths (see seg_range)
   int fp16;  // q, k, v, out (and the workspace factors) hold fp16 elements, else bf16
 };
 

@@ -93,15 +93,6 @@ struct ScanJob {
   float* fin;         // [rows][D] where the final state goes, or nullptr
 };
 
-// Segment bookkeeping: a sequence of n chunks is split into ns = ceil(n / L) non-empty
-// segments of L = ceil(n / nseg) chunks (the last one possibly shorter).
-__device__ __forceinline__ void seg_bounds(int n, int nseg, int p, int& c0, int& c1, int& ns) {
-  const int L = (n + nseg - 1) / nseg;
-  ns = L > 0 ? (n + L - 1) / L : 0;
-  c0 = min(n, p * L);
-  c1 = min(n, (p + 1) * L);
-}
-
 // Decodes this CTA's job. kind 0: whole sequences; kind 1: segment 0 (full) and the maps of
 // segments 1 .. ns-2; kind 2: segments 1 .. ns-1 (full). Returns false if there is no job.
 template <int D>
@@ -127,7 +118,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
       job.fin = pool;
     } else {
       int ns;
-      seg_bounds(n, nseg, 0, job.c0, job.c1, ns);
+      seg_range(n, nseg, p.seg_r16, 0, job.c0, job.c1, ns);
       job.fin = ns > 1 ? p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + 1) * per_head : pool;
     }
     return job.c1 > job.c0;
@@ -144,7 +135,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
     const int which = idx % 2, seg = 1 + idx / 2;
     const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
     int ns;
-    seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+    seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
     if (seg >= ns - 1) return false;
     job.mode = which == 0 ? kMapB : kMapT;
     job.fin = p.seg_map + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * 2 * per_head + (which == 0 ? 0 : per_head);
@@ -159,7 +150,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
   job.hv = bid % HV;
   const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
   int ns;
-  seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+  seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
   if (seg >= ns) return false;
   job.mode = kFull;
   job.init = p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * per_head;
@@ -578,8 +569,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
   const int hv = bid % p.HV;
   const int seq = p.order[bid / p.HV];
   const int n = p.seq_chunk_off[seq + 1] - p.seq_chunk_off[seq];
-  const int L = (n + nseg - 1) / nseg;
-  const int ns = L > 0 ? (n + L - 1) / L : 0;
+  int ns, c0_, c1_;
+  seg_range(n, nseg, p.seg_r16, 0, c0_, c1_, ns);
   if (ns < 3) return;
   const int64_t per_head = (int64_t)D * D;
   const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
@@ -611,14 +602,18 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
   }
 }
 
-// The same chaining for K <= 128 with each T_p (K x K fp32, <= 64 KB) fetched whole by a bulk
-// copy one step ahead (two buffers), so the loads overlap the previous step's products.
+// The same chaining for K <= 128: one CTA of 512 threads per 16 state rows; T_p (K x K fp32,
+// <= 64 KB) and the CTA's 16 rows of B_p are fetched by bulk copies one segment ahead (two
+// buffers), so the loads overlap the previous segment's products. Thread (row r, 32-lane
+// group) forms D/32 adjacent columns of row r.
 template <int D>
-__global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
-  constexpr int R = 16;  // state rows per CTA
+__global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
+  constexpr int R = 16;       // state rows per CTA
+  constexpr int NC = D / 32;  // columns per thread
   extern __shared__ __align__(16) float cbm[];
-  float* Tb = cbm;                // 2 x D x D
-  float* Sr = Tb + 2 * D * D;     // R x D
+  float* Tb = cbm;                 // 2 x D x D
+  float* Bb = Tb + 2 * D * D;      // 2 x R x D
+  float* Sr = Bb + 2 * R * D;      // R x D
   uint64_t* bar = reinterpret_cast<uint64_t*>(Sr + R * D);  // [2]
   if (p.status[0] != GDN_OK) return;
   int bid = blockIdx.x;
@@ -627,16 +622,18 @@ __global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
   const int hv = bid % p.HV;
   const int seq = p.order[bid / p.HV];
   const int n = p.seq_chunk_off[seq + 1] - p.seq_chunk_off[seq];
-  const int L = (n + nseg - 1) / nseg;
-  const int ns = L > 0 ? (n + L - 1) / L : 0;
+  int ns, c0_, c1_;
+  seg_range(n, nseg, p.seg_r16, 0, c0_, c1_, ns);
   if (ns < 3) return;
   const int64_t per_head = (int64_t)D * D;
   const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
   const int tid = threadIdx.x;
-  auto fetch = [&](int seg) {  // thread 0: T of segment seg into buffer (seg - 1) & 1
-    uint64_t* b = &bar[(seg - 1) & 1];
-    tc::mbar_arrive_expect_tx(b, D * D * 4);
-    tc::bulk_load(Tb + ((seg - 1) & 1) * D * D, p.seg_map + (base + seg) * 2 * per_head + per_head, D * D * 4, b);
+  auto fetch = [&](int seg) {  // thread 0: T and this CTA's rows of B of segment seg into buffer (seg - 1) & 1
+    const int b = (seg - 1) & 1;
+    const float* m = p.seg_map + (base + seg) * 2 * per_head;
+    tc::mbar_arrive_expect_tx(&bar[b], (D * D + R * D) * 4);
+    tc::bulk_load(Tb + b * D * D, m + per_head, D * D * 4, &bar[b]);
+    tc::bulk_load(Bb + b * R * D, m + (int64_t)rb * R * D, R * D * 4, &bar[b]);
   };
   if (tid == 0) {
     tc::mbar_init(&bar[0], 1);
@@ -645,41 +642,45 @@ __global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
     fetch(1);
     if (ns - 2 >= 2) fetch(2);
   }
-  for (int e = tid; e < R * D; e += 256) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
+  for (int e = tid; e < R * D; e += 512) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
   __syncthreads();
-  const int r = tid / 16, c0 = (tid % 16) * (D / 16);  // one row, D/16 columns per thread
+  const int r = tid >> 5, c0 = (tid & 31) * NC;
   for (int seg = 1; seg <= ns - 2; ++seg) {
-    const float* T = Tb + ((seg - 1) & 1) * D * D;
-    const float* Bg = p.seg_map + (base + seg) * 2 * per_head;  // B_p (rows: value index)
-    float acc[D / 16];
-#pragma unroll
-    for (int u = 0; u < D / 16; ++u) acc[u] = Bg[((int64_t)rb * R + r) * D + c0 + u];
-    if (!__syncthreads_and(tc::mbar_wait(&bar[(seg - 1) & 1], ((seg - 1) >> 1) & 1, 1ll << 31))) {
+    const int b = (seg - 1) & 1;
+    if (!__syncthreads_and(tc::mbar_wait(&bar[b], ((seg - 1) >> 1) & 1, 1ll << 31))) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
       return;
     }
-#pragma unroll 4
+    const float* T = Tb + b * D * D;
+    float acc[NC];
+#pragma unroll
+    for (int u = 0; u < NC; ++u) acc[u] = Bb[b * R * D + r * D + c0 + u];
+#pragma unroll 8
     for (int k = 0; k < D; ++k) {
       const float sk = Sr[r * D + k];
-#pragma unroll
-      for (int u = 0; u < D / 16; u += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(T + k * D + c0 + u);
-        acc[u] = fmaf(sk, t4.x, acc[u]);
-        acc[u + 1] = fmaf(sk, t4.y, acc[u + 1]);
-        acc[u + 2] = fmaf(sk, t4.z, acc[u + 2]);
-        acc[u + 3] = fmaf(sk, t4.w, acc[u + 3]);
+      if constexpr (NC == 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(T + k * D + c0);
+        acc[0] = fmaf(sk, t4.x, acc[0]);
+        acc[1] = fmaf(sk, t4.y, acc[1]);
+        acc[2] = fmaf(sk, t4.z, acc[2]);
+        acc[3] = fmaf(sk, t4.w, acc[3]);
+      } else {
+        const float2 t2 = *reinterpret_cast<const float2*>(T + k * D + c0);
+        acc[0] = fmaf(sk, t2.x, acc[0]);
+        acc[1] = fmaf(sk, t2.y, acc[1]);
       }
     }
-    __syncthreads();  // every thread is done with S_p and this T buffer
+    __syncthreads();  // every thread is done with S_p and buffer b
     if (tid == 0 && seg + 2 <= ns - 2) {
       tc::fence_async_smem();
       fetch(seg + 2);
     }
 #pragma unroll
-    for (int u = 0; u < D / 16; ++u) Sr[r * D + c0 + u] = acc[u];
+    for (int u = 0; u < NC; ++u) Sr[r * D + c0 + u] = acc[u];
+    float* dst = p.seg_state + (base + seg + 1) * per_head + ((int64_t)rb * R + r) * D + c0;
+#pragma unroll
+    for (int u = 0; u < NC; ++u) dst[u] = acc[u];
     __syncthreads();
-    for (int e = tid; e < R * D; e += 256)
-      p.seg_state[(base + seg + 1) * per_head + (int64_t)rb * R * D + e] = Sr[e];
   }
 }
 
@@ -718,10 +719,10 @@ cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s) {
   const int64_t chains = (int64_t)p.B * p.HV;
   cudaError_t e;
   if (D <= 128) {
-    const size_t csmem = (size_t)(2 * D * D + 16 * D) * sizeof(float) + 16;
+    const size_t csmem = (size_t)(2 * D * D + 3 * 16 * D) * sizeof(float) + 16;
     auto kern = D == 64 ? combine_bulk_kernel<64> : combine_bulk_kernel<128>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) != cudaSuccess) return e;
-    kern<<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
+    kern<<<(unsigned)(chains * (D / 16)), 512, csmem, s>>>(p, nseg);
   } else {
     const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
     if ((e = cudaFuncSetAttribute(combine_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) !=

@@ -113,15 +113,6 @@ struct Job {
   float* fin_t;       // [K][K] T of the map (map mode)
 };
 
-// A sequence of n chunks is split into ns = ceil(n / L) non-empty segments of
-// L = ceil(n / nseg) chunks (the last one possibly shorter).
-__device__ __forceinline__ void seg_bounds(int n, int nseg, int p, int& c0, int& c1, int& ns) {
-  const int L = (n + nseg - 1) / nseg;
-  ns = L > 0 ? (n + L - 1) / L : 0;
-  c0 = min(n, p * L);
-  c1 = min(n, (p + 1) * L);
-}
-
 // kind 0: whole sequences. kind 1: segment 0 (full) and the maps of segments 1 .. ns-2.
 // kind 2: segments 1 .. ns-1 (full). Returns false if this CTA has no work.
 __device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
@@ -144,7 +135,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
       job.c1 = n;
       job.fin = pool;
     } else {
-      seg_bounds(n, nseg, 0, job.c0, job.c1, ns);
+      seg_range(n, nseg, p.seg_r16, 0, job.c0, job.c1, ns);
       job.fin = ns > 1 ? p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + 1) * per_head : pool;
     }
     return job.c1 > job.c0;
@@ -157,7 +148,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
     job.seq = p.order[rest / HV];
     job.hv = rest % HV;
     const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
-    seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+    seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
     if (seg >= ns - 1) return false;
     job.mode = kMap;
     float* m = p.seg_map + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * 2 * per_head;
@@ -170,7 +161,7 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
   job.seq = p.order[bid / HV];
   job.hv = bid % HV;
   const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
-  seg_bounds(n, nseg, seg, job.c0, job.c1, ns);
+  seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
   if (seg >= ns) return false;
   job.mode = kFull;
   job.init = p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * per_head;
