@@ -20,15 +20,15 @@
 //   D_O[64:128] = W'' S^T  ->  U'' = U'' - D_O[64:128]   (= diag(m) U, in place)
 //   D_O[0:64]  += P'' U''                                (= P U)
 //   O = scale * D_O[0:64]
-// One CTA per (sequence, value head, chunk range), 576 threads:
-//   warps 0-7   chain: fp32 state rows in registers (TMEM lane quarter w%4, 64 key columns
+// One CTA per (sequence, value head, chunk range), 832 threads:
+//   warps 0-15  chain: fp32 state rows in registers (TMEM lane quarter w%4, 32 key columns
 //               each), S <- exp(g_C) S + D_S, 16-bit copy of S for the next products;
-//   warps 8-11  prep: K~ and Q~ in place in the chunk's tiles; M from TMEM to a 16-bit
+//   warps 16-19 prep: K~ and Q~ in place in the chunk's tiles; M from TMEM to a 16-bit
 //               B operand (negated);
-//   warps 12-15 full mode: output rows (warps 12-13, TMEM lanes 0-63) and U'' rows formed in
-//               place in the U'' tile (warps 14-15, lanes 64-127); map mode: the T chain;
-//   warp 16     TMA producer (2-stage ring of the chunk tiles and gate rows);
-//   warp 17     MMA issuer (one thread).
+//   warps 20-23 full mode: output rows (warps 20-21, TMEM lanes 0-63) and U'' rows formed in
+//               place in the U'' tile (warps 22-23, lanes 64-127); map mode: the T chain;
+//   warp 24     TMA producer (2-stage ring of the chunk tiles and gate rows);
+//   warp 25     MMA issuer (one thread).
 // Map mode (segment-parallel scan of few long sequences): for a chunk range the CTA runs,
 // with shared M, the B chain from S = 0 (chain warps) and the T chain T <- exp(g_C) T - T M
 // from T = I (warps 12-15, T kept in fp32 in TMEM), giving the range's affine map
@@ -47,8 +47,9 @@ namespace {
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
-constexpr int kThreads = 576;
-constexpr int kPrepWarp0 = 8, kXWarp0 = 12, kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kThreads = 832;
+constexpr int kChainWarps = 16;  // 4 per TMEM lane quarter, 32 state columns each
+constexpr int kPrepWarp0 = 16, kXWarp0 = 20, kProducerWarp = 24, kMmaWarp = 25;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns. M accumulator [0, 128) (lanes: k_in). Full mode: D_S buffers [128, 256) and
 // [256, 384) (lanes: state row), D_O [384, 512) (lanes: token rows 0-63 = outputs, 64-127 =
@@ -102,7 +103,8 @@ enum Bar : int {
   kOFree = 20,       // output rows read
   kNumBars = 21
 };
-constexpr int kEcRing = 4;  // exp(g_C) of the last chunks, written by the prep warps
+constexpr int kEcRing = 4;   // exp(g_C) of the last chunks, written by the prep warps
+constexpr int kL2Ahead = 3;  // chunks between an L2 prefetch and the load into shared memory
 
 struct Job {
   int mode;
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars[kMbFree], 1);
     tc::mbar_init(&bars[kChainTDone], 1);
     tc::mbar_init(&bars[kOutDone], 1);
-    tc::mbar_init(&bars[kSReady], 8);
+    tc::mbar_init(&bars[kSReady], kChainWarps);
     tc::mbar_init(&bars[kTReady], 4);
     tc::mbar_init(&bars[kUtReady], 2);
     tc::mbar_init(&bars[kPuDone], 1);
@@ -294,6 +296,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (full) tc::bulk_load(st + oF + Smem::FRQ, p.rq + jq * C, 256, fb);
         tc::bulk_load(st + oF + Smem::FKS, p.ks + jh * C, 256, fb);
         issued = c + 1;
+        if (c + kL2Ahead < nc) {  // warm L2 with a later chunk's tiles: its load then hits L2
+          const int j2 = j + kL2Ahead;
+          const int64_t jh2 = (int64_t)j2 * p.HV + hv;
+          const int t2 = p.chunk_tab[j2].y;
+          for (int b = 0; b < 2; ++b) {
+            tc::tma_prefetch_2d(&tm_w, 64 * b, (int)(jh2 * C));
+            tc::tma_prefetch_2d(&tm_u, 64 * b, (int)(jh2 * C));
+            tc::tma_prefetch_3d(&tm_k, 64 * b, h, t2);
+            if (full) tc::tma_prefetch_3d(&tm_q, 64 * b, h, t2);
+          }
+          if (full) tc::tma_prefetch_2d(&tm_p, 0, (int)(jh2 * C));
+        }
       }
       if (!ok) report();
       // no copy outlives the CTA: the last loads of each buffer have landed (bounded)
@@ -407,24 +421,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kPrepWarp0) {
     // ------------------------------------------------------------------ chain: S <- exp(g_C) S + D_S
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = 32 * quarter + lane;  // state row (TMEM lane)
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-    float S_[64];  // S[row][64 half .. 64 half + 63]
+    // this thread's 32 columns 32 part .. 32 part + 31: chunks 4 (part & 1) .. +3 of 64-column block part >> 1
+    unsigned char* sblk = smem + Smem::SB + (part >> 1) * 16384;
+    const int ch0 = 4 * (part & 1);
+    float S_[32];
     auto write_sb = [&]() {
-      unsigned char* blk = smem + Smem::SB + half * 16384;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t w[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(S_[8 * ch + 2 * u], S_[8 * ch + 2 * u + 1]);
-        *reinterpret_cast<uint4*>(blk + tc::sw128_offset(row, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(S_[8 * q + 2 * u], S_[8 * q + 2 * u + 1]);
+        *reinterpret_cast<uint4*>(sblk + tc::sw128_offset(row, ch0 + q)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     };
     if (full) {
-      const float4* src = reinterpret_cast<const float4*>(job.init + (int64_t)row * D + 64 * half);
+      const float4* src = reinterpret_cast<const float4*>(job.init + (int64_t)row * D + 32 * part);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const float4 x = src[u];
         S_[4 * u] = x.x;
         S_[4 * u + 1] = x.y;
@@ -433,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
 #pragma unroll
-      for (int u = 0; u < 64; ++u) S_[u] = 0.f;
+      for (int u = 0; u < 32; ++u) S_[u] = 0.f;
     }
     write_sb();
     signal(kSReady);
@@ -447,24 +463,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const float eC = ec[c % kEcRing];
-      const uint32_t dcol = (buf ? kColS1 : kColS0) + 64 * half;
+      const uint32_t dcol = (buf ? kColS1 : kColS0) + 32 * part;
 #pragma unroll
-      for (int g2 = 0; g2 < 2; ++g2) {
-        uint32_t rr[2][16];
-        tc::tmem_ld16(tmem + lane_base + dcol + 32 * g2, rr[0]);
-        tc::tmem_ld16(tmem + lane_base + dcol + 32 * g2 + 16, rr[1]);
+      for (int g = 0; g < 2; ++g) {
+        uint32_t rr[16];
+        tc::tmem_ld16(tmem + lane_base + dcol + 16 * g, rr);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) S_[32 * g2 + u] = fmaf(eC, S_[32 * g2 + u], __uint_as_float(rr[u >> 4][u & 15]));
+        for (int u = 0; u < 16; ++u) S_[16 * g + u] = fmaf(eC, S_[16 * g + u], __uint_as_float(rr[u]));
       }
       write_sb();
       signal(kSReady);
     }
     if (failed) report();
     if (!failed && job.fin) {
-      float4* dst = reinterpret_cast<float4*>(job.fin + (int64_t)row * D + 64 * half);
+      float4* dst = reinterpret_cast<float4*>(job.fin + (int64_t)row * D + 32 * part);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) dst[u] = make_float4(S_[4 * u], S_[4 * u + 1], S_[4 * u + 2], S_[4 * u + 3]);
+      for (int u = 0; u < 8; ++u) dst[u] = make_float4(S_[4 * u], S_[4 * u + 1], S_[4 * u + 2], S_[4 * u + 3]);
     }
   } else if (warp < kXWarp0) {
     // ------------------------------------------------------------------ prep: K~, Q~ in place; -M
@@ -505,23 +520,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      // -M (row kin, 128 columns) as the B operand [k_in][k_out]
-#pragma unroll
-      for (int g2 = 0; g2 < 4; ++g2) {
-        uint32_t rr[2][16];
-        tc::tmem_ld16(tmem + lane_base + kColM + 32 * g2, rr[0]);
-        tc::tmem_ld16(tmem + lane_base + kColM + 32 * g2 + 16, rr[1]);
+      // -M (row kin, 128 columns) as the B operand [k_in][k_out], 16 columns at a time
+#pragma unroll 2
+      for (int g = 0; g < 8; ++g) {
+        uint32_t rr[16];
+        tc::tmem_ld16(tmem + lane_base + kColM + 16 * g, rr);
         tc::tmem_wait_ld();
-        unsigned char* dst = smem + Smem::MB + (g2 >> 1) * 16384;
+        unsigned char* dst = smem + Smem::MB + (g >> 2) * 16384;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {  // 16-byte chunk (g2 & 1) * 4 + q4 of the 128-byte row
+        for (int q2 = 0; q2 < 2; ++q2) {  // 16-byte chunk 2 (g & 3) + q2 of the 128-byte row
           uint32_t w[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = 8 * q4 + 2 * u;
-            w[u] = ElemT<E>::pack(-__uint_as_float(rr[e >> 4][e & 15]), -__uint_as_float(rr[(e + 1) >> 4][(e + 1) & 15]));
-          }
-          *reinterpret_cast<uint4*>(dst + tc::sw128_offset(kin, (g2 & 1) * 4 + q4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int u = 0; u < 4; ++u)
+            w[u] = ElemT<E>::pack(-__uint_as_float(rr[8 * q2 + 2 * u]), -__uint_as_float(rr[8 * q2 + 2 * u + 1]));
+          *reinterpret_cast<uint4*>(dst + tc::sw128_offset(kin, 2 * (g & 3) + q2)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       signal(kMConv);
@@ -616,25 +628,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ---------------------------------------------------------------- T chain (map mode)
       const int v = lrow;  // key row of T
-      auto write_tb = [&](int g, const float* x) {  // 16 values of columns 16 g .. 16 g + 15
-        unsigned char* blk = smem + Smem::TB + (g >> 2) * 16384;
-        uint32_t w[8];
+      // 8 columns 8 g .. 8 g + 7 of the 16-bit T copy (one 16-byte chunk of row v)
+      auto tb_chunk = [&](int g) { return smem + Smem::TB + (g >> 3) * 16384 + tc::sw128_offset(v, g & 7); };
+#pragma unroll 4
+      for (int g = 0; g < 16; ++g) {  // T = I
+        uint32_t r[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) w[u] = ElemT<E>::pack(x[2 * u], x[2 * u + 1]);
-        *reinterpret_cast<uint4*>(blk + tc::sw128_offset(v, 2 * (g & 3))) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(blk + tc::sw128_offset(v, 2 * (g & 3) + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
-      };
+        for (int i = 0; i < 8; ++i) r[i] = __float_as_uint((8 * g + i == v) ? 1.f : 0.f);
+        tc::tmem_st8(tmem + lane_base + kColTS + 8 * g, r);
+        uint32_t w[4];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {  // T = I
-        uint32_t r[16];
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          x[i] = (16 * g + i == v) ? 1.f : 0.f;
-          r[i] = __float_as_uint(x[i]);
-        }
-        tc::tmem_st16(tmem + lane_base + kColTS + 16 * g, r);
-        write_tb(g, x);
+        for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+        *reinterpret_cast<uint4*>(tb_chunk(g)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       tc::tmem_wait_st();
       signal(kTReady);
@@ -645,35 +650,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_after_sync();
         const float eC = ec[c % kEcRing];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t a[16], b[16];
-          tc::tmem_ld16(tmem + lane_base + kColT + 16 * g, a);
-          tc::tmem_ld16(tmem + lane_base + kColTS + 16 * g, b);
+#pragma unroll 4
+        for (int g = 0; g < 16; ++g) {  // columns 8 g .. 8 g + 7
+          uint32_t a[8], b[8];
+          tc::tmem_ld8(tmem + lane_base + kColT + 8 * g, a);
+          tc::tmem_ld8(tmem + lane_base + kColTS + 8 * g, b);
           tc::tmem_wait_ld();
-          float x[16];
+          uint32_t w[4];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            x[i] = fmaf(eC, __uint_as_float(b[i]), __uint_as_float(a[i]));
-            b[i] = __float_as_uint(x[i]);
+          for (int u = 0; u < 4; ++u) {
+            const float x0 = fmaf(eC, __uint_as_float(b[2 * u]), __uint_as_float(a[2 * u]));
+            const float x1 = fmaf(eC, __uint_as_float(b[2 * u + 1]), __uint_as_float(a[2 * u + 1]));
+            b[2 * u] = __float_as_uint(x0);
+            b[2 * u + 1] = __float_as_uint(x1);
+            w[u] = ElemT<E>::pack(x0, x1);
           }
-          tc::tmem_st16(tmem + lane_base + kColTS + 16 * g, b);
-          write_tb(g, x);
+          tc::tmem_st8(tmem + lane_base + kColTS + 8 * g, b);
+          *reinterpret_cast<uint4*>(tb_chunk(g)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         tc::tmem_wait_st();
         signal(kTReady);
       }
       if (!failed && job.fin_t) {
         float4* dst = reinterpret_cast<float4*>(job.fin_t + (int64_t)v * D);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t b[16];
-          tc::tmem_ld16(tmem + lane_base + kColTS + 16 * g, b);
+#pragma unroll 4
+        for (int g = 0; g < 16; ++g) {
+          uint32_t b[8];
+          tc::tmem_ld8(tmem + lane_base + kColTS + 8 * g, b);
           tc::tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            dst[4 * g + u] = make_float4(__uint_as_float(b[4 * u]), __uint_as_float(b[4 * u + 1]),
-                                         __uint_as_float(b[4 * u + 2]), __uint_as_float(b[4 * u + 3]));
+          dst[2 * g] = make_float4(__uint_as_float(b[0]), __uint_as_float(b[1]), __uint_as_float(b[2]), __uint_as_float(b[3]));
+          dst[2 * g + 1] = make_float4(__uint_as_float(b[4]), __uint_as_float(b[5]), __uint_as_float(b[6]), __uint_as_float(b[7]));
         }
       }
     }
