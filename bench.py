@@ -183,10 +183,11 @@ def kernel_accounting(w, lengths):
 
 
 def kernel_source_hash(kernel: str) -> str:
-    files = {"gates": "gdn_gates.cu", "intra": "gdn_intra.cu", "scan": "gdn_scan.cu", "schedule": "gdn_schedule.cu"}
+    files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu"], "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
+             "schedule": ["gdn_schedule.cu"]}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (files.get(kernel, ""), "gdn_common.cuh"):
+    for f in files.get(kernel, []) + ["gdn_common.cuh", "gdn_tc.cuh"]:
         p = os.path.join(csrc, f)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
