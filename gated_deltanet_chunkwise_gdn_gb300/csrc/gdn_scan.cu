@@ -28,13 +28,17 @@
 // Segment-parallel use (few long chains): besides a full scan over a chunk range
 // (state from a buffer, outputs written), the same kernel computes the affine map of a
 // chunk range — S_end = S_start T + B — as two scans without outputs: B from S_start = 0,
-// and T (K x K) from the identity with U~ = 0. combine_kernel then chains the maps.
+// and T (K x K) from the identity with U~ = 0. combine_kernel then chains the maps. For
+// K = V = 128 the maps come from affine_scan_kernel (gdn_scan_affine.cu), and the factors are
+// stored m-scaled (W'' = diag(m) W<-, U'' = diag(m) U~, P'' = P diag(1/m), see gdn_intra.cu):
+// then U here is diag(m) U, P'' U'' = P U, and the key scale left to apply is ks = 2^e.
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 
 namespace gdn {
 
 cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s);
+cudaError_t launch_affine_map_pass(const Params& p, cudaStream_t s);
 
 namespace {
 
@@ -253,7 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (full_mode) tc::tma_load_2d(st + SM::P, &tm_p, 0, (int)(jh * C), &full[s]);
         tc::bulk_load(st + SM::F, p.g + jh * C, 256, &full[s]);
         tc::bulk_load(st + SM::F + 256, p.rq + jq * C, 256, &full[s]);
-        tc::bulk_load(st + SM::F + 512, p.rk + jq * C, 256, &full[s]);
+        // K = V = 128: the factors are stored m-scaled (see the intra kernel), the key scale is ks = 2^e
+        if (D == 128) tc::bulk_load(st + SM::F + 512, p.ks + jh * C, 256, &full[s]);
+        else tc::bulk_load(st + SM::F + 512, p.rk + jq * C, 256, &full[s]);
       }
     }
     __syncwarp();
@@ -464,7 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* gs = reinterpret_cast<const float*>(st + SM::F);
       const float gC = gs[C - 1];
       const float eC = expf(gC);
-      const float sk = u_row ? expf(gC - gs[mu]) * gs[2 * C + mu] : 0.f;  // exp(g_C - g_mu) / |k_mu|
+      // exp(g_C - g_mu) / |k_mu|; for K = V = 128 the rows of U~, W<- carry its mantissa m_mu (and P the
+      // inverse), so U here is diag(m) U and the remaining factor is ks_mu = 2^e_mu
+      const float sk = u_row ? (D == 128 ? gs[2 * C + mu] : expf(gC - gs[mu]) * gs[2 * C + mu]) : 0.f;
       if (u_row && use_ut) cp_async_wait<0>();  // this thread's U~ rows of chunk c
       for (int ch = 0; ch < NCH && !failed; ++ch) {
         if (u_row) {  // U = U~ - W<- S^T (half row mu); Uk = sk U as 16-bit hi + lo
@@ -701,18 +709,22 @@ cudaError_t launch_scan_t(const Params& p, int nseg, cudaStream_t s) {
     scan_kernel<D, E><<<(unsigned)(chains * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 0, 1);
     return cudaGetLastError();
   }
-  // segment 0 and the maps of segments 1 .. nseg-2, then the combine, then segments 1 .. nseg-1
-  const int64_t grid1 = chains * NVB + chains * (nseg - 2) * 2 * NVB;
-  scan_kernel<D, E><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // segment 0 and the maps of segments 1 .. nseg-2, then the combine, then segments 1 .. nseg-1.
+  // K = V = 128: the first pass runs in affine-transition form (one CTA per map builds B and T
+  // with a shared transition), the segment pass here.
+  if constexpr (D == 128) {
+    if ((e = launch_affine_map_pass(p, s)) != cudaSuccess) return e;
+  } else {
+    const int64_t grid1 = chains * NVB + chains * (nseg - 2) * 2 * NVB;
+    scan_kernel<D, E><<<(unsigned)grid1, kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 1, nseg);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (nseg > 2 && (e = launch_combine(p, D, nseg, s)) != cudaSuccess) return e;
   scan_kernel<D, E><<<(unsigned)(chains * (nseg - 1) * NVB), kThreads, SM::alloc, s>>>(mw, mp, mq, mk, p, 2, nseg);
   return cudaGetLastError();
 }
 
 }  // namespace
-
-cudaError_t launch_affine_scan(const Params& p, cudaStream_t s);
 
 // Chains the segment maps (B, T) of every (sequence, value head): S_{p+1} = S_p T_p + B_p.
 cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s) {
@@ -735,10 +747,10 @@ cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s) {
 
 cudaError_t launch_scan(const Params& p, int D, int Cc, cudaStream_t s) {
   if (Cc != C) return cudaErrorInvalidValue;
-  if (D == 128) return launch_affine_scan(p, s);  // K = V = 128: affine-transition form
   if (p.nvb != D / VB) return cudaErrorInvalidValue;
   switch (D) {
     case 64: return p.fp16 ? launch_scan_t<64, f16>(p, p.nseg, s) : launch_scan_t<64, bf16>(p, p.nseg, s);
+    case 128: return p.fp16 ? launch_scan_t<128, f16>(p, p.nseg, s) : launch_scan_t<128, bf16>(p, p.nseg, s);
     case 256: return p.fp16 ? launch_scan_t<256, f16>(p, p.nseg, s) : launch_scan_t<256, bf16>(p, p.nseg, s);
     default: return cudaErrorInvalidValue;
   }

@@ -1,26 +1,31 @@
-// gdn_scan_affine.cu — K3 for K = V = 128: the inter-chunk scan in affine-transition form,
-// with the output epilogue, on the 5th-generation tensor cores (tcgen05, accumulators in
-// TMEM) with TMA-fed chunk tiles.
+// gdn_scan_affine.cu — first pass of the segmented scan for K = V = 128, in affine-transition
+// form, on the 5th-generation tensor cores (tcgen05, accumulators in TMEM) with TMA-fed chunk tiles.
 //
 // The chunk step of "Simple math to speed up GDN prefill" (section "Reminder"),
 //   S_next = exp(g_C) S + (U~ - W<- S^T)^T diag(sk) K,   sk_t = exp(g_C - g_t)/|k_t|,
 // is affine in the state S (V x K):
 //   S_next = exp(g_C) S - S M + B,   M = W<-^T diag(sk) K  (K x K),   B = U~^T diag(sk) K  (V x K).
 // M and B do not depend on S, so each chunk's critical path is a single product S M
-// (one tcgen05 group of 8 MMAs) and one fp32 update, instead of two dependent products.
-// The factor sk is split exactly as sk_t = m_t 2^e_t (m_t in [0.5, 1)): the intra kernel
-// stored W'' = diag(m) W<-, U'' = diag(m) U~ and P'' = P diag(1/m), and this kernel scales
-// the raw keys by ks_t = 2^e_t (exact in 16 bits): K~ = diag(ks) K, so M = W''^T K~ and
-// B = U''^T K~ with no rounding beyond that of the stored factors.
+// (one tcgen05 group of 8 MMAs) and one fp32 update. A segment of chunks is the affine map
+// S_end = S_start T + B_seg, with T the product of the (exp(g_C) I - M) and B_seg the state reached
+// from S_start = 0: one CTA runs both chains with one shared M per chunk (the B chain in the chain
+// warps, the T chain T <- exp(g_C) T - T M from T = I in fp32 in TMEM). combine_kernel then chains
+// the maps and the second pass (scan_kernel) re-runs the segments from their start states.
+// Segment 0 of each sequence runs here in full mode (outputs, its end state to the segment-state
+// buffer), alongside the maps.
 //
-// The output of chunk c uses the state S entering the chunk ("nrm-training-kernels",
-// "General implementation": inter-chunk part from the carried state plus the masked
-// intra-chunk part):
+// The factor sk is split exactly as sk_t = m_t 2^e_t (m_t in [0.5, 1)): the intra kernel stored
+// W'' = diag(m) W<-, U'' = diag(m) U~ and P'' = P diag(1/m), and this kernel scales the raw keys by
+// ks_t = 2^e_t (exact in 16 bits): K~ = diag(ks) K, so M = W''^T K~ and B = U''^T K~ with no
+// rounding beyond that of the stored factors.
+//
+// Outputs (full mode) use the state S entering the chunk ("nrm-training-kernels", "General
+// implementation": inter-chunk part from the carried state plus the masked intra-chunk part):
 //   D_O[0:64]   = Q~ S^T,  Q~ = diag(exp(g)/|q|) Q       (rows: tokens)
 //   D_O[64:128] = W'' S^T  ->  U'' = U'' - D_O[64:128]   (= diag(m) U, in place)
 //   D_O[0:64]  += P'' U''                                (= P U)
 //   O = scale * D_O[0:64]
-// One CTA per (sequence, value head, chunk range), 832 threads:
+// One CTA per (sequence, value head, segment), 832 threads:
 //   warps 0-15  chain: fp32 state rows in registers (TMEM lane quarter w%4, 32 key columns
 //               each), S <- exp(g_C) S + D_S, 16-bit copy of S for the next products;
 //   warps 16-19 prep: K~ and Q~ in place in the chunk's tiles; M from TMEM to a 16-bit
@@ -29,12 +34,8 @@
 //               place in the U'' tile (warps 22-23, lanes 64-127); map mode: the T chain;
 //   warp 24     TMA producer (2-stage ring of the chunk tiles and gate rows);
 //   warp 25     MMA issuer (one thread).
-// Map mode (segment-parallel scan of few long sequences): for a chunk range the CTA runs,
-// with shared M, the B chain from S = 0 (chain warps) and the T chain T <- exp(g_C) T - T M
-// from T = I (warps 12-15, T kept in fp32 in TMEM), giving the range's affine map
-// S_end = S_start T + B; combine_kernel chains the maps and a second pass re-runs the
-// ranges from their start states with outputs. A map-mode stage is free as soon as M and B
-// of its chunk are formed, so the ring prefetches two chunks ahead.
+// A map-mode stage is free as soon as M and B of its chunk are formed, so the ring prefetches two
+// chunks ahead.
 #include "gdn_common.cuh"
 #include "gdn_tc.cuh"
 
@@ -115,9 +116,9 @@ struct Job {
   float* fin_t;       // [K][K] T of the map (map mode)
 };
 
-// kind 0: whole sequences. kind 1: segment 0 (full) and the maps of segments 1 .. ns-2.
-// kind 2: segments 1 .. ns-1 (full). Returns false if this CTA has no work.
-__device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
+// CTAs [0, B*HV): segment 0 of a chain in full mode; then one CTA per (chain, middle segment
+// 1 .. ns-2) builds that segment's map. Returns false if this CTA has no work.
+__device__ bool decode_job(const Params& p, int nseg, Job& job) {
   const int B = p.B, HV = p.HV;
   const int64_t per_head = (int64_t)D * D;
   int bid = blockIdx.x;
@@ -125,49 +126,30 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, Job& job) {
   job.fin = nullptr;
   job.fin_t = nullptr;
   int ns = 1;
-  if (kind == 0 || (kind == 1 && bid < B * HV)) {
+  if (bid < B * HV) {
     job.seq = p.order[bid / HV];
     job.hv = bid % HV;
     const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
     float* pool = p.state_pool + (p.cache_indices[job.seq] * HV + job.hv) * per_head;
     job.mode = kFull;
     job.init = pool;
-    if (kind == 0) {
-      job.c0 = 0;
-      job.c1 = n;
-      job.fin = pool;
-    } else {
-      seg_range(n, nseg, p.seg_r16, 0, job.c0, job.c1, ns);
-      job.fin = ns > 1 ? p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + 1) * per_head : pool;
-    }
+    seg_range(n, nseg, p.seg_r16, 0, job.c0, job.c1, ns);
+    job.fin = ns > 1 ? p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + 1) * per_head : pool;
     return job.c1 > job.c0;
   }
-  if (kind == 1) {
-    if (nseg < 3) return false;
-    bid -= B * HV;
-    const int seg = 1 + bid % (nseg - 2);
-    const int rest = bid / (nseg - 2);
-    job.seq = p.order[rest / HV];
-    job.hv = rest % HV;
-    const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
-    seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
-    if (seg >= ns - 1) return false;
-    job.mode = kMap;
-    float* m = p.seg_map + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * 2 * per_head;
-    job.fin = m;
-    job.fin_t = m + per_head;
-    return job.c1 > job.c0;
-  }
-  const int seg = 1 + bid % (nseg - 1);
-  bid /= (nseg - 1);
-  job.seq = p.order[bid / HV];
-  job.hv = bid % HV;
+  if (nseg < 3) return false;
+  bid -= B * HV;
+  const int seg = 1 + bid % (nseg - 2);
+  const int rest = bid / (nseg - 2);
+  job.seq = p.order[rest / HV];
+  job.hv = rest % HV;
   const int n = p.seq_chunk_off[job.seq + 1] - p.seq_chunk_off[job.seq];
   seg_range(n, nseg, p.seg_r16, seg, job.c0, job.c1, ns);
-  if (seg >= ns) return false;
-  job.mode = kFull;
-  job.init = p.seg_state + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * per_head;
-  job.fin = seg == ns - 1 ? p.state_pool + (p.cache_indices[job.seq] * HV + job.hv) * per_head : nullptr;
+  if (seg >= ns - 1) return false;
+  job.mode = kMap;
+  float* m = p.seg_map + (((int64_t)job.seq * HV + job.hv) * nseg + seg) * 2 * per_head;
+  job.fin = m;
+  job.fin_t = m + per_head;
   return job.c1 > job.c0;
 }
 
@@ -198,13 +180,13 @@ template <typename E>
 __global__ void __launch_bounds__(kThreads, 1)
     affine_scan_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k, Params p, int kind, int nseg) {
+                       const __grid_constant__ CUtensorMap tm_k, Params p, int nseg) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   if (p.status[0] != GDN_OK) return;
   Job job;
-  if (!decode_job(p, kind, nseg, job)) return;  // uniform over the CTA
+  if (!decode_job(p, nseg, job)) return;  // uniform over the CTA
   const bool full = job.mode == kFull;
   const int hv = job.hv;
   const int h = hv / (p.HV / p.H);
@@ -706,22 +688,16 @@ cudaError_t launch_t(const Params& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(affine_scan_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::alloc);
   if (e != cudaSuccess) return e;
   const int64_t chains = (int64_t)p.B * p.HV;
-  const int nseg = p.nseg;
-  if (nseg <= 1) {
-    affine_scan_kernel<E><<<(unsigned)chains, kThreads, Smem::alloc, s>>>(mw, mu, mp, mq, mk, p, 0, 1);
-    return cudaGetLastError();
-  }
-  // segment 0 and the maps of segments 1 .. nseg-2, then the combine, then segments 1 .. nseg-1
-  affine_scan_kernel<E><<<(unsigned)(chains * (nseg - 1)), kThreads, Smem::alloc, s>>>(mw, mu, mp, mq, mk, p, 1, nseg);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (nseg > 2 && (e = launch_combine(p, D, nseg, s)) != cudaSuccess) return e;
-  affine_scan_kernel<E><<<(unsigned)(chains * (nseg - 1)), kThreads, Smem::alloc, s>>>(mw, mu, mp, mq, mk, p, 2, nseg);
+  affine_scan_kernel<E><<<(unsigned)(chains * (p.nseg - 1)), kThreads, Smem::alloc, s>>>(mw, mu, mp, mq, mk, p, p.nseg);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_affine_scan(const Params& p, cudaStream_t s) {
+// First pass of a segmented scan for K = V = 128: segment 0 of every chain with outputs (its end
+// state to the segment-state buffer) and the affine map (B, T) of each middle segment.
+cudaError_t launch_affine_map_pass(const Params& p, cudaStream_t s) {
+  if (p.nseg < 2) return cudaErrorInvalidValue;
   return p.fp16 ? launch_t<f16>(p, s) : launch_t<bf16>(p, s);
 }
 
