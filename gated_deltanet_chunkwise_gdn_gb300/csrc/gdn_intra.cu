@@ -324,21 +324,6 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       const int hv = hv0 + ih;
       const int64_t jh = (int64_t)j * p.HV + hv;
       if (ih > 0) load_gates(p, jh, s_g, s_beta);
-      if constexpr (kAffine) {  // sk_t = m_t 2^e_t, m_t in [0.5, 1); padded rows (1/|k| = 0): m = 1, ks = 0
-        if (tid < C) {
-          const float sk = expf(s_g[C - 1] - s_g[tid]) * s_rk[tid];
-          float m = 1.f, ks = 0.f;
-          if (sk > 0.f) {
-            int e;
-            m = frexpf(sk, &e);
-            ks = ldexpf(1.f, e);
-          }
-          s_m[tid] = m;
-          s_im[tid] = 1.f / m;
-          p.ks[jh * C + tid] = ks;
-        }
-        __syncthreads();
-      }
       if (row < C) {  // warps 0, 1, 4, 5: L = tril(diag(beta) K^K^^T, -1), row i; diagonal blocks of M^{-1}
         const int i = row;
         const float bi = s_beta[i] * s_rk[i];
@@ -357,21 +342,45 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         if (warp < 2) diag_blocks<LDF>(Lf, Xf, warp);
       } else {  // warps 2, 3, 6, 7 meanwhile: P = Gamma . tril(Q^K^^T), row r, straight to global
         const int r = row - C;
+        if constexpr (kAffine) {  // sk_t = m_t 2^e_t, m_t in [0.5, 1); padded rows (1/|k| = 0): m = 1, ks = 0
+          if (half == 0) {
+            const float sk = expf(s_g[C - 1] - s_g[r]) * s_rk[r];
+            float m = 1.f, ks = 0.f;
+            if (sk > 0.f) {
+              int e;
+              m = frexpf(sk, &e);
+              ks = ldexpf(1.f, e);
+            }
+            s_m[r] = m;
+            s_im[r] = 1.f / m;
+            p.ks[jh * C + r] = ks;
+          }
+          tc::named_sync(3, 128);
+        }
         const float qr = s_rq[r], gr = s_g[r];
         uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C + cbase);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          const int n0 = cbase + 8 * c;
+          float g8[8], k8[8], m8[8];  // g, 1/|k| and 1/m of columns n0 .. n0+7
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g + n0 + 4 * q);
+            *reinterpret_cast<float4*>(k8 + 4 * q) = *reinterpret_cast<const float4*>(s_rk + n0 + 4 * q);
+            if constexpr (kAffine) *reinterpret_cast<float4*>(m8 + 4 * q) = *reinterpret_cast<const float4*>(s_im + n0 + 4 * q);
+          }
           uint32_t w[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int e0 = 8 * c + 2 * u, n0 = cbase + e0, n1 = n0 + 1;
-            float v0 = n0 <= r ? __expf(gr - s_g[n0]) * qr * s_rk[n0] * kq[e0] : 0.f;
-            float v1 = n1 <= r ? __expf(gr - s_g[n1]) * qr * s_rk[n1] * kq[e0 + 1] : 0.f;
-            if constexpr (kAffine) {
-              v0 *= s_im[n0];
-              v1 *= s_im[n1];
+            float v[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int m = 2 * u + e;
+              float x = __expf(gr - g8[m]) * qr * k8[m] * kq[8 * c + m];
+              if constexpr (kAffine) x *= m8[m];
+              v[e] = n0 + m <= r ? x : 0.f;
             }
-            w[u] = ElemT<E>::pack(v0, v1);
+            w[u] = ElemT<E>::pack(v[0], v[1]);
           }
           prow[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
