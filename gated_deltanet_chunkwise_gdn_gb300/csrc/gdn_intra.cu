@@ -128,13 +128,10 @@ __device__ void offdiag_blocks(const float* Lf, float* Xf, float* scratch) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     mm_piece<LDF, LDF>(acc, blk(Lf, I, I - 1), blk(Xf, I - 1, I - 1), r, c0);
     store_piece<LT1>(T1 + task * 16 * LT1, r, c0, acc, 1.f);
-  }
-  __syncthreads();
-  if (task < 2) {
-    const int I = 1 + 2 * task;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mm_piece<LDF, LT1>(acc, blk(Xf, I, I), T1 + task * 16 * LT1, r, c0);
-    store_piece<LDF>(blk(Xf, I, I - 1), r, c0, acc, -1.f);
+    tc::named_sync(4 + task, 64);  // the warp pair's partial product is complete
+    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    mm_piece<LDF, LT1>(acc2, blk(Xf, I, I), T1 + task * 16 * LT1, r, c0);
+    store_piece<LDF>(blk(Xf, I, I - 1), r, c0, acc2, -1.f);
   }
   __syncthreads();
   {  // stage 2: T_pq, p = task >> 1, q = task & 1
@@ -309,16 +306,19 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     if (!ok) break;
     float kq[32];  // columns [32*half, 32*half+32) of this row of K K^T (rows 0-63) or Q K^T (64-127)
     tc::fence_after_sync();
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      uint32_t r[16];
-      tc::tmem_ld16(tmem + lane_base + 32 * half + 16 * c, r);
+    {
+      uint32_t r0[16], r1[16];
+      tc::tmem_ld16(tmem + lane_base + 32 * half, r0);
+      tc::tmem_ld16(tmem + lane_base + 32 * half + 16, r1);
       tc::tmem_wait_ld();
 #pragma unroll
-      for (int u = 0; u < 16; ++u) kq[16 * c + u] = __uint_as_float(r[u]);
+      for (int u = 0; u < 16; ++u) {
+        kq[u] = __uint_as_float(r0[u]);
+        kq[16 + u] = __uint_as_float(r1[u]);
+      }
     }
+    // D1 is read: the later MMAs that overwrite its columns are issued after the barriers below
     tc::fence_before_sync();
-    __syncthreads();
 
     for (int ih = 0; ih < r_heads; ++ih) {
       const int hv = hv0 + ih;
@@ -424,8 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         }
       }
       tc::fence_async_smem();
-      __syncthreads();
-      ok = wait_all(&bar[1], ph1 & 1, p.status);
+      ok = wait_all(&bar[1], ph1 & 1, p.status);  // its barrier also publishes [A'; A] to the MMA issuer
       ++ph1;
       if (!ok) break;
       if (tid == 0) {  // DW = [A'; A] K (rows 0-63: W<-), DU = [A'; A] V (rows 64-127: U~), [A'; A] = hi + lo
