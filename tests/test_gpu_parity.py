@@ -201,6 +201,22 @@ def test_segmented_scan_weak_decay():
     compare(d, out, pool, oracle_for(d))
 
 
+@pytest.mark.parametrize("dtype,a_log", [(torch.bfloat16, None), (torch.bfloat16, -7.0), (torch.float16, -7.0)])
+def test_segmented_scan_many_segments_gqa(dtype, a_log):
+    """K = V = 128, GQA 1:2, nonzero start states, sequences of very different lengths: the
+    longest is cut into nine segments (a shorter segment 0 with outputs and seven affine
+    maps in the first pass, the chaining, the re-runs), a two-chunk sequence into two
+    segments (no map), a one-token sequence into one."""
+    w = wl.custom("segmany", [12000, 7000, 65, 1], H=1, HV=2, K=128, V=128, chunk_size=64, seed=37,
+                  dtype=dtype)
+    d = wl.make_inputs(w)
+    if a_log is not None:
+        d["A_log"] = torch.full_like(d["A_log"], a_log)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
 def test_segmented_scan_wide_heads():
     """K = V = 256 with one long sequence: segment maps, the chaining over four middle
     segments (state staged 32 key rows at a time) and the segment re-runs."""
