@@ -610,19 +610,21 @@ __global__ void __launch_bounds__(256) combine_kernel(Params p, int nseg) {
   }
 }
 
-// The same chaining for K <= 128: one CTA of 512 threads per 16 state rows; T_p (K x K fp32,
+// The same chaining for K <= 128: one CTA of 256 threads per 16 state rows; T_p (K x K fp32,
 // <= 64 KB) and the CTA's 16 rows of B_p are fetched by bulk copies one segment ahead (two
-// buffers), so the loads overlap the previous segment's products. Thread (row r, 32-lane
-// group) forms D/32 adjacent columns of row r.
+// buffers), so the loads overlap the previous segment's products. Thread (column c, row group)
+// forms column c of 16 * D / 256 rows, reading T_p[k][c] once per k for all of them; the CTA's
+// rows of S_p are kept transposed ([k][row], 16-byte groups XOR-swizzled by k) so that each k
+// brings them in with a few broadcast vector loads.
 template <int D>
-__global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
-  constexpr int R = 16;       // state rows per CTA
-  constexpr int NC = D / 32;  // columns per thread
+__global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
+  constexpr int R = 16;             // state rows per CTA
+  constexpr int RPT = R * D / 256;  // rows per thread (8 for D = 128, 4 for D = 64)
   extern __shared__ __align__(16) float cbm[];
   float* Tb = cbm;                 // 2 x D x D
   float* Bb = Tb + 2 * D * D;      // 2 x R x D
-  float* Sr = Bb + 2 * R * D;      // R x D
-  uint64_t* bar = reinterpret_cast<uint64_t*>(Sr + R * D);  // [2]
+  float* St = Bb + 2 * R * D;      // D x R: St[k][r] at k * R + swz(k, r)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(St + R * D);  // [2]
   if (p.status[0] != GDN_OK) return;
   int bid = blockIdx.x;
   const int rb = bid % (D / R);
@@ -636,6 +638,7 @@ __global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
   const int64_t per_head = (int64_t)D * D;
   const int64_t base = ((int64_t)seq * p.HV + hv) * nseg;
   const int tid = threadIdx.x;
+  auto swz = [](int k, int r) { return ((((r >> 2) ^ k) & (R / 4 - 1)) << 2) | (r & 3); };
   auto fetch = [&](int seg) {  // thread 0: T and this CTA's rows of B of segment seg into buffer (seg - 1) & 1
     const int b = (seg - 1) & 1;
     const float* m = p.seg_map + (base + seg) * 2 * per_head;
@@ -650,9 +653,13 @@ __global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
     fetch(1);
     if (ns - 2 >= 2) fetch(2);
   }
-  for (int e = tid; e < R * D; e += 512) Sr[e] = p.seg_state[(base + 1) * per_head + (int64_t)rb * R * D + e];
+  const float* S1 = p.seg_state + (base + 1) * per_head + (int64_t)rb * R * D;
+  for (int e = tid; e < R * D; e += 256) {
+    const int r = e / D, k = e % D;
+    St[k * R + swz(k, r)] = S1[e];
+  }
   __syncthreads();
-  const int r = tid >> 5, c0 = (tid & 31) * NC;
+  const int c = tid % D, r0 = (tid / D) * RPT;  // column and first row of this thread
   for (int seg = 1; seg <= ns - 2; ++seg) {
     const int b = (seg - 1) & 1;
     if (!__syncthreads_and(tc::mbar_wait(&bar[b], ((seg - 1) >> 1) & 1, 1ll << 31))) {
@@ -660,22 +667,19 @@ __global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
       return;
     }
     const float* T = Tb + b * D * D;
-    float acc[NC];
+    float acc[RPT];
 #pragma unroll
-    for (int u = 0; u < NC; ++u) acc[u] = Bb[b * R * D + r * D + c0 + u];
-#pragma unroll 8
+    for (int i = 0; i < RPT; ++i) acc[i] = Bb[b * R * D + (r0 + i) * D + c];
+#pragma unroll 4
     for (int k = 0; k < D; ++k) {
-      const float sk = Sr[r * D + k];
-      if constexpr (NC == 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(T + k * D + c0);
-        acc[0] = fmaf(sk, t4.x, acc[0]);
-        acc[1] = fmaf(sk, t4.y, acc[1]);
-        acc[2] = fmaf(sk, t4.z, acc[2]);
-        acc[3] = fmaf(sk, t4.w, acc[3]);
-      } else {
-        const float2 t2 = *reinterpret_cast<const float2*>(T + k * D + c0);
-        acc[0] = fmaf(sk, t2.x, acc[0]);
-        acc[1] = fmaf(sk, t2.y, acc[1]);
+      const float t = T[k * D + c];
+#pragma unroll
+      for (int q = 0; q < RPT / 4; ++q) {
+        const float4 s4 = *reinterpret_cast<const float4*>(St + k * R + swz(k, r0 + 4 * q));
+        acc[4 * q] = fmaf(s4.x, t, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(s4.y, t, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(s4.z, t, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(s4.w, t, acc[4 * q + 3]);
       }
     }
     __syncthreads();  // every thread is done with S_p and buffer b
@@ -683,11 +687,12 @@ __global__ void __launch_bounds__(512) combine_bulk_kernel(Params p, int nseg) {
       tc::fence_async_smem();
       fetch(seg + 2);
     }
+    float* dst = p.seg_state + (base + seg + 1) * per_head + (int64_t)rb * R * D;
 #pragma unroll
-    for (int u = 0; u < NC; ++u) Sr[r * D + c0 + u] = acc[u];
-    float* dst = p.seg_state + (base + seg + 1) * per_head + ((int64_t)rb * R + r) * D + c0;
-#pragma unroll
-    for (int u = 0; u < NC; ++u) dst[u] = acc[u];
+    for (int i = 0; i < RPT; ++i) {
+      St[c * R + swz(c, r0 + i)] = acc[i];
+      dst[(r0 + i) * D + c] = acc[i];
+    }
     __syncthreads();
   }
 }
@@ -734,7 +739,7 @@ cudaError_t launch_combine(const Params& p, int D, int nseg, cudaStream_t s) {
     const size_t csmem = (size_t)(2 * D * D + 3 * 16 * D) * sizeof(float) + 16;
     auto kern = D == 64 ? combine_bulk_kernel<64> : combine_bulk_kernel<128>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) != cudaSuccess) return e;
-    kern<<<(unsigned)(chains * (D / 16)), 512, csmem, s>>>(p, nseg);
+    kern<<<(unsigned)(chains * (D / 16)), 256, csmem, s>>>(p, nseg);
   } else {
     const size_t csmem = (size_t)(32 * D + 16 * D) * sizeof(float);
     if ((e = cudaFuncSetAttribute(combine_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem)) !=
