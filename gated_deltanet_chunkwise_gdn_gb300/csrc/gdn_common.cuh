@@ -35,7 +35,7 @@ constexpr float kNormEps = 1e-6f;  // q^ = q / sqrt(|q|^2 + eps)
 // Offsets (bytes) of the workspace regions for one call. Every region starts on a
 // 256-byte boundary.
 struct WsLayout {
-  size_t status;         // int32[64]: [0] status code, [1] number of chunks
+  size_t status;         // int32[64]: [0] status code, [1] number of chunks, [2] intra item counter
   size_t seq_chunk_off;  // int32[B+1]: first chunk of each sequence
   size_t order;          // int32[B]: sequences, longest first
   size_t chunk_tab;      // int4[max_chunks]: (seq, first token, length, chunk index in seq)

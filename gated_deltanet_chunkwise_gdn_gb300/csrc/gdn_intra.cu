@@ -48,7 +48,7 @@ struct IntraSmem {
   static constexpr uint32_t XF = LF + 64 * LDF * 4;     // M^{-1}, fp32 64 x LDF
   static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k|, m, 1/m (6 x 64 fp32)
   static constexpr uint32_t BAR = VEC + 6 * 64 * 4;     // 3 mbarriers + TMEM address
-  static constexpr uint32_t bytes = BAR + 64;
+  static constexpr uint32_t bytes = BAR + 96;
   static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
 };
 
@@ -207,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles + gates, [1] v tile, [2] MMAs
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
   int4* s_ct = reinterpret_cast<int4*>(bar + 4);                // chunk record of the item being fetched
+  int* s_next = reinterpret_cast<int*>(bar + 6);                 // this CTA's next item
+  int4* s_ct_next = reinterpret_cast<int4*>(bar + 8);            // its chunk record
 
   if (tid == 0) {
     tc::mbar_init(&bar[0], 1);
@@ -239,20 +241,32 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     tc::mbar_arrive_expect_tx(&bar[1], NB * 8192);
     for (int b = 0; b < NB; ++b) tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, h * r_heads, ct.y, &bar[1]);
   };
-  if (tid == 0) fetch_item(blockIdx.x, p.chunk_tab[blockIdx.x / p.H]);
+  // Items are handed out by a counter in the status words (zeroed by the schedule kernel), so a
+  // CTA that starts late simply takes fewer items.
+  if (tid == 0) {
+    const int first = atomicAdd(&p.status[2], 1);
+    *s_next = first;
+    if (first < n_items) fetch_item(first, p.chunk_tab[first / p.H]);
+  }
+  __syncthreads();
+  int item = *s_next;
 
   uint32_t ph0 = 0, ph1 = 0, ph2 = 0;  // completed phases of bar[0], bar[1], bar[2]
   bool ok = true;
-  for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+  while (ok && item < n_items) {
     const int j = item / p.H, h = item % p.H;
     const int hv0 = h * r_heads;
-    const int next = item + gridDim.x;
-    int4 ct_next = make_int4(0, 0, 0, 0);
-    if (tid == 0 && next < n_items) ct_next = p.chunk_tab[next / p.H];  // needed at the end of this item
 
     ok = wait_all(&bar[0], ph0 & 1, p.status);
     ++ph0;
     if (!ok) break;
+    // thread 32 claims the next item while thread 0 issues this one's MMAs (every thread has
+    // read the previous claim before this barrier; thread 0 reads this one after MMA2/3)
+    if (tid == 32) {
+      const int nx = atomicAdd(&p.status[2], 1);
+      *s_next = nx;
+      if (nx < n_items) *s_ct_next = p.chunk_tab[nx / p.H];
+    }
     const int4 ct = *s_ct;
     const int len = ct.z;
     if (tid == 0) {  // MMA1: D1 = [K; Q] K^T
@@ -456,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
           tc::mbar_arrive_expect_tx(&bar[1], NB * 8192);
           for (int b = 0; b < NB; ++b)
             tc::tma_load_3d(smem + SM::V + b * 8192, &tm_v, 64 * b, hv + 1, ct.y, &bar[1]);
-        } else if (next < n_items) {
-          fetch_item(next, ct_next);
+        } else if (*s_next < n_items) {
+          fetch_item(*s_next, *s_ct_next);
         }
       }
       {  // rows 0-63 of DW are W<-, rows 64-127 of DU are U~: half an output row per thread
@@ -504,6 +518,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         if (ih + 1 < r_heads) tc::bulk_wait_read();  // the next value head rebuilds [A'; A] in these buffers
       }
     }
+    item = *s_next;
   }
 
   if (kTmaStore && tid == 0) tc::bulk_wait_all();

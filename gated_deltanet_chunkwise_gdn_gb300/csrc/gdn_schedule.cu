@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Params p, int C) {
   }
   if (tid == 0) {
     p.status[1] = n_chunks;
+    p.status[2] = 0;  // item counter of the intra kernel
     p.status[0] = GDN_OK;
   }
 }
