@@ -182,7 +182,32 @@ def kernel_accounting(w, lengths):
     }
 
 
+def _code_only(src: str) -> str:
+    """C/CUDA source with comments and whitespace removed (string literals kept as they are)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        elif c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the code (not the comments) of a kernel's sources and the shared headers."""
     files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu"], "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
              "schedule": ["gdn_schedule.cu"]}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
@@ -190,7 +215,7 @@ def kernel_source_hash(kernel: str) -> str:
     for f in files.get(kernel, []) + ["gdn_common.cuh", "gdn_tc.cuh"]:
         p = os.path.join(csrc, f)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(_code_only(open(p, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -168,9 +168,9 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t
   return all;
 }
 
-// Persistent: CTA b handles items b, b + gridDim.x, ... (item = chunk * H + q/k head). The
-// next item's q/k/v tiles and gates are fetched by TMA while the current item's W<- and U~
-// rows are written out (for D <= 128 through shared memory and TMA stores).
+// Persistent: each CTA takes items (item = chunk * H + q/k head) from a global counter until
+// they run out. The next item's q/k/v tiles and gates are fetched by TMA while the current
+// item's W<- and U~ rows are written out (for D <= 128 through shared memory and TMA stores).
 template <int D, typename E>
 __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                          const __grid_constant__ CUtensorMap tm_k,
