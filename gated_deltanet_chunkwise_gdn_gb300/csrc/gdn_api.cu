@@ -124,7 +124,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.seg_state = reinterpret_cast<float*>(ws + L.seg_state);
   p.seg_map = reinterpret_cast<float*>(ws + L.seg_map);
   p.nseg = L.nseg;
-  p.seg_r16 = K == 128 ? 9 : 16;  // K = V = 128: a full-mode chunk costs about 1.8 map-mode chunks
+  p.seg_r16 = K == 128 ? 8 : 16;  // K = V = 128: a full-mode chunk costs about twice a map-mode chunk
   p.fp16 = dtype == GDN_FP16 ? 1 : 0;
 
   int rec = prof_begin(kKernSchedule, s);
