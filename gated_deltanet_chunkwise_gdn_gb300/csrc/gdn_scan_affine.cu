@@ -25,9 +25,13 @@
 //   D_O[64:128] = W'' S^T  ->  U'' = U'' - D_O[64:128]   (= diag(m) U, in place)
 //   D_O[0:64]  += P'' U''                                (= P U)
 //   O = scale * D_O[0:64]
+// Map mode keeps the 16-bit copies of S and T that feed the chain products in TMEM (the
+// products read their A operand from TMEM, so only -M streams from shared memory), and the T
+// chain accumulates in place: its TMEM state is pre-scaled by exp(g_C) and the MMA adds T (-M).
 // One CTA per (sequence, value head, segment), 832 threads:
 //   warps 0-15  chain: fp32 state rows in registers (TMEM lane quarter w%4, 32 key columns
-//               each), S <- exp(g_C) S + D_S, 16-bit copy of S for the next products;
+//               each), S <- exp(g_C) S + D_S, 16-bit copy of S for the next products (shared
+//               memory in full mode, TMEM in map mode);
 //   warps 16-19 prep: K~ and Q~ in place in the chunk's tiles; M from TMEM to a 16-bit
 //               B operand (negated);
 //   warps 20-23 full mode: output rows (warps 20-21, TMEM lanes 0-63) and U'' rows formed in
@@ -54,8 +58,10 @@ constexpr int kPrepWarp0 = 16, kXWarp0 = 20, kProducerWarp = 24, kMmaWarp = 25;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns. M accumulator [0, 128) (lanes: k_in). Full mode: D_S buffers [128, 256) and
 // [256, 384) (lanes: state row), D_O [384, 512) (lanes: token rows 0-63 = outputs, 64-127 =
-// W'' S^T). Map mode: D_B [128, 256), D_T [256, 384), T state (fp32) [384, 512) (lanes: key row).
-constexpr uint32_t kColM = 0, kColS0 = 128, kColS1 = 256, kColO = 384, kColT = 256, kColTS = 384;
+// W'' S^T). Map mode: D_B [128, 256); T state, fp32, also the accumulator of T (-M) [256, 384)
+// (lanes: key row); 16-bit S and T as MMA A operands [384, 448) and [448, 512) (lane = row,
+// two elements per column).
+constexpr uint32_t kColM = 0, kColS0 = 128, kColS1 = 256, kColO = 384, kColTS = 256, kColAS = 384, kColAT = 448;
 
 enum Mode : int { kFull = 0, kMap = 1 };
 
@@ -67,11 +73,11 @@ struct Smem {
   // (K~ in place), P'', gate rows
   static constexpr uint32_t fQ = 0, fW = 8192, fQW_BLK = 16384, fU = 32768, fK = 49152, fP = 65536, fF = 73728;
   static constexpr uint32_t fSTAGE = 74752;
-  // map-mode ring stage: W'', U'', K (K~ in place), gate rows; the 16-bit T copy follows the ring
+  // map-mode ring stage: W'', U'', K (K~ in place), gate rows
   static constexpr uint32_t mW = 0, mU = 16384, mK = 32768, mF = 49152;
   static constexpr uint32_t mSTAGE = 50176;
-  static constexpr uint32_t TB = 2 * mSTAGE;   // 16-bit T: [k_row][k], 2 column blocks of 16 KB
   static constexpr uint32_t MB = 151552;       // -M as B operand: [k_in][k_out], 2 column blocks of 16 KB
+  static constexpr uint32_t MB1 = 2 * mSTAGE;  // map mode: second -M buffer (odd chunks), after the ring
   static constexpr uint32_t SB = MB + 32768;   // 16-bit S (or B): [row][k], 2 column blocks of 16 KB
   static constexpr uint32_t BAR = SB + 32768;
   static constexpr uint32_t bytes = BAR + 256;
@@ -81,8 +87,8 @@ struct Smem {
   static constexpr uint32_t tx_full = 4 * 16384 + 8192 + 3 * 256;
   static constexpr uint32_t tx_map = 3 * 16384 + 2 * 256;
   static_assert(alloc <= 232448, "shared memory per CTA");
-  static_assert(2 * fSTAGE <= MB && TB + 32768 <= MB, "ring below the fixed tiles");
-  static_assert(fSTAGE % 1024 == 0 && mSTAGE % 1024 == 0 && TB % 1024 == 0 && MB % 1024 == 0, "1 KB aligned tiles");
+  static_assert(2 * fSTAGE <= MB && MB1 + 32768 <= MB, "ring below the fixed tiles");
+  static_assert(fSTAGE % 1024 == 0 && mSTAGE % 1024 == 0 && MB % 1024 == 0 && MB1 % 1024 == 0, "1 KB aligned tiles");
 };
 
 // Barrier indices (mbarriers at Smem::BAR).
@@ -93,7 +99,7 @@ enum Bar : int {
   kQReady0 = 6,      // [2] Q~ formed in the stage
   kMFull = 8,        // M accumulated
   kMConv = 10,       // -M written as B operand; M accumulator free
-  kMbFree = 11,      // chain products done with the -M operand
+  kMbFree = 11,      // chain products done with the -M operand (map mode: buffer 0)
   kChainDone0 = 12,  // [2] D_S buffer complete
   kChainTDone = 14,  // D_T complete (map mode)
   kOutDone = 15,     // [Q~; W''] S^T complete
@@ -102,7 +108,8 @@ enum Bar : int {
   kUtReady = 18,     // U'' formed in place
   kPuDone = 19,      // output rows complete
   kOFree = 20,       // output rows read
-  kNumBars = 21
+  kMbFree1 = 21,     // map mode: chain products done with -M buffer 1
+  kNumBars = 22
 };
 constexpr int kEcRing = 4;   // exp(g_C) of the last chunks, written by the prep warps
 constexpr int kL2Ahead = 3;  // chunks between an L2 prefetch and the load into shared memory
@@ -216,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(&bars[kMFull], 1);
     tc::mbar_init(&bars[kMConv], 4);
     tc::mbar_init(&bars[kMbFree], 1);
+    tc::mbar_init(&bars[kMbFree1], 1);
     tc::mbar_init(&bars[kChainTDone], 1);
     tc::mbar_init(&bars[kOutDone], 1);
     tc::mbar_init(&bars[kSReady], kChainWarps);
@@ -312,9 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK = tc::smem_desc(tc::saddr(smem + oK), 8192, 1024, tc::kSwizzle128B);
       const uint64_t dS = tc::smem_desc(tc::saddr(smem + Smem::SB), 16, 1024, tc::kSwizzle128B);
       const uint64_t dM = tc::smem_desc(tc::saddr(smem + Smem::MB), 16384, 1024, tc::kSwizzle128B);
+      const uint64_t dM1 = tc::smem_desc(tc::saddr(smem + Smem::MB1), 16384, 1024, tc::kSwizzle128B);
       const uint64_t dQW = tc::smem_desc(tc::saddr(smem + Smem::fQ), 16, 1024, tc::kSwizzle128B);
       const uint64_t dP = tc::smem_desc(tc::saddr(smem + Smem::fP), 16, 1024, tc::kSwizzle128B);
-      const uint64_t dT = tc::smem_desc(tc::saddr(smem + Smem::TB), 16, 1024, tc::kSwizzle128B);
       auto koff = [](int ks, uint32_t block) { return (uint32_t)(((ks >> 2) * block + (ks & 3) * 32) >> 4); };
       bool ok = true;
       auto W8 = [&](int b, uint32_t parity) {
@@ -347,25 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nc && ok; ++c) {
         const int s = c & 1;
         const int buf = c % nsb;
-        // chain product: D_S[buf] += S (-M); map mode also D_T = T (-M)
+        // chain product: D_S[buf] += S (-M); map mode also T += T (-M)
         W8(kMConv, c & 1);
         W8(kSReady, c & 1);
         if (!full) W8(kTReady, c & 1);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t dcol = buf ? kColS1 : kColS0;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_f16_ss(tmem + dcol, dS + koff(ks, 16384), dM + (ks * 2048 >> 4), id_ch, 1);
-        tc::mma_commit(&bars[kChainDone0 + buf]);
-        if (!full) {
+        if (full) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_f16_ss(tmem + kColT, dT + koff(ks, 16384), dM + (ks * 2048 >> 4), id_ch, ks > 0);
-          tc::mma_commit(&bars[kChainTDone]);
-        }
-        tc::mma_commit(&bars[kMbFree]);
-        if (full) {
+            tc::mma_f16_ss(tmem + dcol, dS + koff(ks, 16384), dM + (ks * 2048 >> 4), id_ch, 1);
+          tc::mma_commit(&bars[kChainDone0 + buf]);
+          tc::mma_commit(&bars[kMbFree]);
           // D_O = [Q~; W''] S^T
           W8(kQReady0 + s, (c >> 1) & 1);
           if (c >= 1) W8(kOFree, (c - 1) & 1);
@@ -375,16 +377,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             tc::mma_f16_ss(tmem + kColO, dQW + so(c) + koff(ks, Smem::fQW_BLK), dS + koff(ks, 16384), id_o, ks > 0);
           tc::mma_commit(&bars[kOutDone]);
-        }
-        if (c + 1 < nc) {  // the next chunk's M (its accumulator is free) and B
-          W8(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
-          W8(kKtReady0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_m(c + 1);
-          if (!full && !W8(kSReady, (c + 1) & 1)) break;  // single D_B buffer: the chain warps have read it
-          issue_b(c + 1);
-          if (!full) tc::mma_commit(&bars[kEmpty0 + ((c + 1) & 1)]);
+          if (c + 1 < nc) {  // the next chunk's M (its accumulator is free) and B
+            W8(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+            W8(kKtReady0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_m(c + 1);
+            issue_b(c + 1);
+          }
+        } else {
+          // A operands from TMEM (8 columns = 16 keys per MMA), -M from buffer c & 1. M of the next
+          // chunk goes between the two chain products, so that its conversion (into the other -M
+          // buffer) overlaps the T product.
+          const uint64_t dMc = (c & 1) ? dM1 : dM;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16_ts(tmem + dcol, tmem + kColAS + 8 * ks, dMc + (ks * 2048 >> 4), id_ch, 1);
+          tc::mma_commit(&bars[kChainDone0 + buf]);
+          if (c + 1 < nc) {
+            W8(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+            W8(kKtReady0 + ((c + 1) & 1), ((c + 1) >> 1) & 1);
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_m(c + 1);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // T state (pre-scaled by exp(g_C)) += T (-M)
+            tc::mma_f16_ts(tmem + kColTS, tmem + kColAT + 8 * ks, dMc + (ks * 2048 >> 4), id_ch, 1);
+          tc::mma_commit(&bars[kChainTDone]);
+          tc::mma_commit(&bars[(c & 1) ? kMbFree1 : kMbFree]);
+          if (c + 1 < nc) {
+            if (!W8(kSReady, (c + 1) & 1)) break;  // single D_B buffer: the chain warps have read it
+            issue_b(c + 1);
+            tc::mma_commit(&bars[kEmpty0 + ((c + 1) & 1)]);  // the stage is done once M, B are formed
+          }
         }
         if (full) {
           // D_O[0:64] += P'' U''
@@ -411,12 +437,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ch0 = 4 * (part & 1);
     float S_[32];
     auto write_sb = [&]() {
+      if (full) {  // shared memory (B operand of D_O, A operand of the chain product)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t w[4];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(S_[8 * q + 2 * u], S_[8 * q + 2 * u + 1]);
-        *reinterpret_cast<uint4*>(sblk + tc::sw128_offset(row, ch0 + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(S_[8 * q + 2 * u], S_[8 * q + 2 * u + 1]);
+          *reinterpret_cast<uint4*>(sblk + tc::sw128_offset(row, ch0 + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {  // TMEM A operand: keys 32 part .. 32 part + 31 in columns 16 part .. 16 part + 15
+        uint32_t w[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) w[u] = ElemT<E>::pack(S_[2 * u], S_[2 * u + 1]);
+        tc::tmem_st16(tmem + lane_base + kColAS + 16 * part, w);
+        tc::tmem_wait_st();
       }
     };
     if (full) {
@@ -470,13 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = pt & 63, blk = pt >> 6;  // tile row and 64-column block of this thread
     const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
     const int kin = 32 * quarter + lane;   // M accumulator row of this thread
-    auto form_kt = [&](int c) {  // K~ = diag(ks) K (exact: ks is a power of two, or 0 on padded rows)
+    auto form_kt = [&](int c) {  // K~ = diag(ks) K in place (exact: ks is a power of two, or 0 on padded rows)
       unsigned char* st = stage(c);
       const float* F = reinterpret_cast<const float*>(st + oF);
       const float f = F[Smem::FKS / 4 + r];
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) scale_chunk<E>(st + oK + blk * 8192 + tc::sw128_offset(r, ch), f);
-      if (pt == 0) ec[c % kEcRing] = expf(F[Smem::FG / 4 + C - 1]);
+    };
+    // exp(g_C) of chunk c into the gate ring; written before -M of chunk c - 1 is signalled, so
+    // that every role that waits for that signal may read it
+    auto put_ec = [&](int c) {
+      if (pt == 0) ec[c % kEcRing] = expf(reinterpret_cast<const float*>(stage(c) + oF)[Smem::FG / 4 + C - 1]);
     };
     auto form_qt = [&](int c) {  // Q~ = diag(exp(g)/|q|) Q
       unsigned char* st = stage(c);
@@ -489,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!wait_warp(kFull0, 0)) {
       failed = true;
     } else {
+      put_ec(0);
       form_kt(0);
       signal(kKtReady0);
       if (full) {
@@ -497,9 +536,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int c = 0; c < nc && !failed; ++c) {
-      if (!wait_warp(kMFull, c & 1) || (c >= 1 && !wait_warp(kMbFree, (c - 1) & 1))) {
+      // -M of chunk c goes to buffer MB (full mode: the only one; map mode: even chunks) or MB1,
+      // once the chain products of the buffer's previous chunk are done
+      const bool odd = !full && (c & 1);
+      const bool free_ok = full ? (c < 1 || wait_warp(kMbFree, (c - 1) & 1))
+                                : (c < 2 || wait_warp(odd ? kMbFree1 : kMbFree, ((c - 2) >> 1) & 1));
+      if (!wait_warp(kMFull, c & 1) || !free_ok) {
         failed = true;
         break;
+      }
+      // map mode: the T chain reads exp(g_C) of chunk c + 1 once -M of chunk c is signalled (its
+      // stage is loaded early, as map-mode stages are released once M and B are formed)
+      if (!full && c + 1 < nc) {
+        if (!wait_warp(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        put_ec(c + 1);
       }
       tc::fence_after_sync();
       // -M (row kin, 128 columns) as the B operand [k_in][k_out], 16 columns at a time
@@ -508,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[16];
         tc::tmem_ld16(tmem + lane_base + kColM + 16 * g, rr);
         tc::tmem_wait_ld();
-        unsigned char* dst = smem + Smem::MB + (g >> 2) * 16384;
+        unsigned char* dst = smem + (odd ? Smem::MB1 : Smem::MB) + (g >> 2) * 16384;
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {  // 16-byte chunk 2 (g & 3) + q2 of the 128-byte row
           uint32_t w[4];
@@ -520,9 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       signal(kMConv);
       if (c + 1 < nc) {
-        if (!wait_warp(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1)) {
-          failed = true;
-          break;
+        if (full) {  // full mode: the chains read it only after -M of chunk c + 1
+          if (!wait_warp(kFull0 + ((c + 1) & 1), ((c + 1) >> 1) & 1)) {
+            failed = true;
+            break;
+          }
+          put_ec(c + 1);
         }
         form_kt(c + 1);
         signal(kKtReady0 + ((c + 1) & 1));
@@ -609,59 +665,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ---------------------------------------------------------------- T chain (map mode)
+      // T (fp32, TMEM) holds exp(g_C) T before each chain product, which adds T (-M) in place; the
+      // 16-bit copy of T is the product's A operand (TMEM). T starts as the identity.
       const int v = lrow;  // key row of T
-      // 8 columns 8 g .. 8 g + 7 of the 16-bit T copy (one 16-byte chunk of row v)
-      auto tb_chunk = [&](int g) { return smem + Smem::TB + (g >> 3) * 16384 + tc::sw128_offset(v, g & 7); };
-#pragma unroll 4
-      for (int g = 0; g < 16; ++g) {  // T = I
-        uint32_t r[8];
+      auto put_row = [&](int g, const uint32_t (&x)[16], float f) {  // columns 16 g .. 16 g + 15
+        uint32_t w[8], y[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) r[i] = __float_as_uint((8 * g + i == v) ? 1.f : 0.f);
-        tc::tmem_st8(tmem + lane_base + kColTS + 8 * g, r);
-        uint32_t w[4];
+        for (int u = 0; u < 8; ++u) w[u] = ElemT<E>::pack(__uint_as_float(x[2 * u]), __uint_as_float(x[2 * u + 1]));
 #pragma unroll
-        for (int u = 0; u < 4; ++u) w[u] = ElemT<E>::pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
-        *reinterpret_cast<uint4*>(tb_chunk(g)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u = 0; u < 16; ++u) y[u] = __float_as_uint(f * __uint_as_float(x[u]));
+        tc::tmem_st8(tmem + lane_base + kColAT + 8 * g, w);
+        tc::tmem_st16(tmem + lane_base + kColTS + 16 * g, y);
+      };
+      // exp(g_C) of chunk 0 is in the gate ring once -M of chunk 0 is
+      if (!wait_warp(kMConv, 0)) failed = true;
+      if (!failed) {
+        const float e0 = ec[0];
+#pragma unroll 2
+        for (int g = 0; g < 8; ++g) {
+          uint32_t x[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) x[i] = __float_as_uint((16 * g + i == v) ? 1.f : 0.f);
+          put_row(g, x, e0);
+        }
+        tc::tmem_wait_st();
+        signal(kTReady);
       }
-      tc::tmem_wait_st();
-      signal(kTReady);
-      for (int c = 0; c < nc; ++c) {
+      for (int c = 0; c < nc && !failed; ++c) {
+        // kMConv(c) also orders the prep warps' exp(g_C) of chunk c + 1 before this read
         if (!wait_warp(kMConv, c & 1) || !wait_warp(kChainTDone, c & 1)) {
           failed = true;
           break;
         }
         tc::fence_after_sync();
-        const float eC = ec[c % kEcRing];
-#pragma unroll 4
-        for (int g = 0; g < 16; ++g) {  // columns 8 g .. 8 g + 7
-          uint32_t a[8], b[8];
-          tc::tmem_ld8(tmem + lane_base + kColT + 8 * g, a);
-          tc::tmem_ld8(tmem + lane_base + kColTS + 8 * g, b);
+        if (c + 1 == nc) break;  // the final T stays unscaled in TMEM
+        const float eN = ec[(c + 1) % kEcRing];
+#pragma unroll 2
+        for (int g = 0; g < 8; ++g) {
+          uint32_t x[16];
+          tc::tmem_ld16(tmem + lane_base + kColTS + 16 * g, x);
           tc::tmem_wait_ld();
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float x0 = fmaf(eC, __uint_as_float(b[2 * u]), __uint_as_float(a[2 * u]));
-            const float x1 = fmaf(eC, __uint_as_float(b[2 * u + 1]), __uint_as_float(a[2 * u + 1]));
-            b[2 * u] = __float_as_uint(x0);
-            b[2 * u + 1] = __float_as_uint(x1);
-            w[u] = ElemT<E>::pack(x0, x1);
-          }
-          tc::tmem_st8(tmem + lane_base + kColTS + 8 * g, b);
-          *reinterpret_cast<uint4*>(tb_chunk(g)) = make_uint4(w[0], w[1], w[2], w[3]);
+          put_row(g, x, eN);
         }
         tc::tmem_wait_st();
         signal(kTReady);
       }
       if (!failed && job.fin_t) {
         float4* dst = reinterpret_cast<float4*>(job.fin_t + (int64_t)v * D);
-#pragma unroll 4
-        for (int g = 0; g < 16; ++g) {
-          uint32_t b[8];
-          tc::tmem_ld8(tmem + lane_base + kColTS + 8 * g, b);
+#pragma unroll 2
+        for (int g = 0; g < 8; ++g) {
+          uint32_t b[16];
+          tc::tmem_ld16(tmem + lane_base + kColTS + 16 * g, b);
           tc::tmem_wait_ld();
-          dst[2 * g] = make_float4(__uint_as_float(b[0]), __uint_as_float(b[1]), __uint_as_float(b[2]), __uint_as_float(b[3]));
-          dst[2 * g + 1] = make_float4(__uint_as_float(b[4]), __uint_as_float(b[5]), __uint_as_float(b[6]), __uint_as_float(b[7]));
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[4 * g + q] = make_float4(__uint_as_float(b[4 * q]), __uint_as_float(b[4 * q + 1]),
+                                         __uint_as_float(b[4 * q + 2]), __uint_as_float(b[4 * q + 3]));
         }
       }
     }
