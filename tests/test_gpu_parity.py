@@ -217,6 +217,20 @@ def test_segmented_scan_many_segments_gqa(dtype, a_log):
     untouched_slots_equal(d, pool)
 
 
+@pytest.mark.parametrize("a_log", [None, -7.0])
+def test_segmented_scan_short_middle_segments(a_log):
+    """K = V = 128 with one long sequence next to sequences of 8, 9 and 11 chunks, cut into eight
+    segments each: the 8-chunk sequence's middle segments are one chunk long (the affine map pass runs
+    a single transition: no second -M buffer, no reuse), the others two chunks (one reuse of each)."""
+    w = wl.custom("segshort", [16000, 500, 576, 700], H=1, HV=2, K=128, V=128, chunk_size=64, seed=43)
+    d = wl.make_inputs(w)
+    if a_log is not None:
+        d["A_log"] = torch.full_like(d["A_log"], a_log)
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
 def test_segmented_scan_wide_heads():
     """K = V = 256 with one long sequence: segment maps, the chaining over four middle
     segments (state staged 32 key rows at a time) and the segment re-runs."""
