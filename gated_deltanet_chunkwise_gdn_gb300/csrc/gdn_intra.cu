@@ -402,16 +402,16 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       __syncthreads();
       offdiag_blocks<LDF>(Lf, Xf, reinterpret_cast<float*>(smem + SM::AA));  // scratch: the [A'; A] tile, not yet written
       // L is dead from here on: its buffer takes the low 16-bit parts of [A'; A]
-      {  // A' rows (rows 0-63) and A rows (rows 64-127) as 16-bit hi + lo, 128-byte swizzled K-major
+      {  // A' rows (rows 0-63) and A rows (rows 64-127) as 16-bit hi + lo, 128-byte swizzled K-major.
+         // Thread (i, qc) forms columns 16 qc .. 16 qc + 15 of row i of both A' and A, so each X element
+         // is loaded once and the exp of A's decay factor is spread over all eight warps.
         const int i = row & 63;
-        const bool is_a = row >= 64;
+        const int qc = 2 * half + (row >> 6);  // 16-column group of this thread
         const float gi = s_g[i], egi = expf(gi);
         const float mi = kAffine ? s_m[i] : 1.f;  // row scale of W<- and U~
-        unsigned char* dst_hi = smem + SM::AA + (is_a ? 8192 : 0);
-        unsigned char* dst_lo = smem + SM::LF + (is_a ? 8192 : 0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int n0 = cbase + 8 * c;
+        for (int c = 0; c < 2; ++c) {
+          const int n0 = 16 * qc + 8 * c;
           float x8[8], g8[8], b8[8], k8[8];  // X row i, and g, beta, 1/|k| of columns n0 .. n0+7
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -420,21 +420,26 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             *reinterpret_cast<float4*>(b8 + 4 * q) = *reinterpret_cast<const float4*>(s_beta + n0 + 4 * q);
             *reinterpret_cast<float4*>(k8 + 4 * q) = *reinterpret_cast<const float4*>(s_rk + n0 + 4 * q);
           }
-          uint32_t wh[4], wl[4];
+          uint32_t ah[4], al[4], bh[4], bl[4];  // A' and A, hi and lo
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            float v2[2];
+            float va[2], vb[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int m = 2 * u + e, nu = n0 + m;
               const float x = nu == i ? 1.f : x8[m];  // entries above the diagonal are never read
-              const float val = (is_a ? __expf(gi - g8[m]) * x * b8[m] : egi * x * (b8[m] * k8[m])) * mi;
-              v2[e] = nu <= i ? val : 0.f;
+              const float xb = x * b8[m] * mi;
+              va[e] = nu <= i ? egi * xb * k8[m] : 0.f;          // A'[i][nu] = e^{g_i} X beta_nu / |k_nu| m_i
+              vb[e] = nu <= i ? __expf(gi - g8[m]) * xb : 0.f;   // A[i][nu] = e^{g_i - g_nu} X beta_nu m_i
             }
-            split2<E>(v2[0], v2[1], wh[u], wl[u]);
+            split2<E>(va[0], va[1], ah[u], al[u]);
+            split2<E>(vb[0], vb[1], bh[u], bl[u]);
           }
-          *reinterpret_cast<uint4*>(dst_hi + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-          *reinterpret_cast<uint4*>(dst_lo + tc::sw128_offset(i, 4 * half + c)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          const uint32_t o = tc::sw128_offset(i, n0 >> 3);
+          *reinterpret_cast<uint4*>(smem + SM::AA + o) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
+          *reinterpret_cast<uint4*>(smem + SM::LF + o) = make_uint4(al[0], al[1], al[2], al[3]);
+          *reinterpret_cast<uint4*>(smem + SM::AA + 8192 + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+          *reinterpret_cast<uint4*>(smem + SM::LF + 8192 + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
         }
       }
       tc::fence_async_smem();
