@@ -260,13 +260,6 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     ok = wait_all(&bar[0], ph0 & 1, p.status);
     ++ph0;
     if (!ok) break;
-    // thread 32 claims the next item while thread 0 issues this one's MMAs (every thread has
-    // read the previous claim before this barrier; thread 0 reads this one after MMA2/3)
-    if (tid == 32) {
-      const int nx = atomicAdd(&p.status[2], 1);
-      *s_next = nx;
-      if (nx < n_items) *s_ct_next = p.chunk_tab[nx / p.H];
-    }
     const int4 ct = *s_ct;
     const int len = ct.z;
     if (tid == 0) {  // MMA1: D1 = [K; Q] K^T
@@ -446,6 +439,14 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       ok = wait_all(&bar[1], ph1 & 1, p.status);  // its barrier also publishes [A'; A] to the MMA issuer
       ++ph1;
       if (!ok) break;
+      // thread 32 claims the next item while the MMAs below run, so the atomic's round trip stays off
+      // the chain of barriers (every thread read the previous claim before this item's first barrier;
+      // thread 0 reads this one after the MMA barrier below, all threads at the end of the item)
+      if (ih == 0 && tid == 32) {
+        const int nx = atomicAdd(&p.status[2], 1);
+        *s_next = nx;
+        if (nx < n_items) *s_ct_next = p.chunk_tab[nx / p.H];
+      }
       if (tid == 0) {  // DW = [A'; A] K (rows 0-63: W<-), DU = [A'; A] V (rows 64-127: U~), [A'; A] = hi + lo
         tc::fence_after_sync();
         constexpr uint32_t idesc2 = tc::idesc_f16(128, D, ElemT<E>::fmt, false, true);
