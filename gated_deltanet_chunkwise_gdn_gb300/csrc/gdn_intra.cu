@@ -334,8 +334,10 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       if (row < C) {  // warps 0, 1, 4, 5: L = tril(diag(beta) K^K^^T, -1), row i; diagonal blocks of M^{-1}
         const int i = row;
         const float bi = s_beta[i] * s_rk[i];
+        // warp 4's part (rows 0-31, columns 32-63) is strictly upper: nothing reads it
 #pragma unroll
         for (int u = 0; u < 32; u += 4) {
+          if (warp == 4) break;
           const float4 rk4 = *reinterpret_cast<const float4*>(s_rk + cbase + u);
           const int nu = cbase + u;
           float4 l4;
@@ -345,8 +347,10 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
           l4.w = nu + 3 < i ? bi * rk4.w * kq[u + 3] : 0.f;
           *reinterpret_cast<float4*>(Lf + i * LDF + nu) = l4;
         }
-        tc::named_sync(2, 128);
-        if (warp < 2) diag_blocks<LDF>(Lf, Xf, warp);
+        // warp 0 holds the L rows of diagonal blocks 0, 1 (rows 0-31, columns 0-31) and warp 5 those of
+        // blocks 2, 3 (rows 32-63, columns 32-63): each sweeps its own two blocks
+        __syncwarp();
+        if (warp == 0 || warp == 5) diag_blocks<LDF>(Lf, Xf, warp == 0 ? 0 : 1);
       } else {  // warps 2, 3, 6, 7 meanwhile: P = Gamma . tril(Q^K^^T), row r, straight to global
         const int r = row - C;
         if constexpr (kAffine) {  // sk_t = m_t 2^e_t, m_t in [0.5, 1); padded rows (1/|k| = 0): m = 1, ks = 0
