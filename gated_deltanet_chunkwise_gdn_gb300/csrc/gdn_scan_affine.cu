@@ -95,7 +95,7 @@ struct Smem {
 enum Bar : int {
   kFull0 = 0,        // [2] ring stage loaded
   kEmpty0 = 2,       // [2] ring stage free (MMA commit)
-  kKtReady0 = 4,     // [2] K~ formed in the stage (and exp(g_C) in the gate ring)
+  kKtReady0 = 4,     // [2] K~ formed in the stage
   kQReady0 = 6,      // [2] Q~ formed in the stage
   kMFull = 8,        // M accumulated
   kMConv = 10,       // -M written as B operand; M accumulator free
