@@ -373,6 +373,10 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int n0 = cbase + 8 * c;
+          if (n0 > r) {  // strictly upper: zeros (a whole warp's columns for warp 6)
+            prow[c] = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+          }
           float g8[8], k8[8], m8[8];  // g, 1/|k| and 1/m of columns n0 .. n0+7
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -409,6 +413,15 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int n0 = 16 * qc + 8 * c;
+          const uint32_t o = tc::sw128_offset(i, n0 >> 3);
+          if (n0 > i) {  // strictly upper: zeros (every column of warps 4 and 6)
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(smem + SM::AA + o) = z;
+            *reinterpret_cast<uint4*>(smem + SM::LF + o) = z;
+            *reinterpret_cast<uint4*>(smem + SM::AA + 8192 + o) = z;
+            *reinterpret_cast<uint4*>(smem + SM::LF + 8192 + o) = z;
+            continue;
+          }
           float x8[8], g8[8], b8[8], k8[8];  // X row i, and g, beta, 1/|k| of columns n0 .. n0+7
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -432,7 +445,6 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             split2<E>(va[0], va[1], ah[u], al[u]);
             split2<E>(vb[0], vb[1], bh[u], bl[u]);
           }
-          const uint32_t o = tc::sw128_offset(i, n0 >> 3);
           *reinterpret_cast<uint4*>(smem + SM::AA + o) = make_uint4(ah[0], ah[1], ah[2], ah[3]);
           *reinterpret_cast<uint4*>(smem + SM::LF + o) = make_uint4(al[0], al[1], al[2], al[3]);
           *reinterpret_cast<uint4*>(smem + SM::AA + 8192 + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
