@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   float* s_rk = s_rq + C;
   float* s_m = s_rk + C;   // K = V = 128: mantissa m_t of sk_t = exp(g_C - g_t)/|k_t| = m_t 2^e_t
   float* s_im = s_m + C;   // 1/m_t
-  float* s_part = reinterpret_cast<float*>(smem + SM::XF);  // norm partial sums (before X is formed)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles + gates, [1] v tile, [2] MMAs
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
   int4* s_ct = reinterpret_cast<int4*>(bar + 4);                // chunk record of the item being fetched
@@ -262,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     if (!ok) break;
     const int4 ct = *s_ct;
     const int len = ct.z;
-    if (tid == 0) {  // MMA1: D1 = [K; Q] K^T
+    if (tid == 0) {  // MMA1: D1 = [K; Q] [K; Q]^T (columns 0-63: K K^T and Q K^T; the diagonal: |k|^2, |q|^2)
       tc::fence_after_sync();
-      constexpr uint32_t idesc1 = tc::idesc_f16(128, 64, ElemT<E>::fmt, false, false);
+      constexpr uint32_t idesc1 = tc::idesc_f16(128, 128, ElemT<E>::fmt, false, false);
       const uint64_t d0 = tc::smem_desc(tc::saddr(smem + SM::KQ), 16, 1024, tc::kSwizzle128B);
 #pragma unroll
       for (int b = 0; b < NB; ++b)
@@ -274,38 +273,6 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
           tc::mma_f16_ss(tmem, d, d, idesc1, (b | ks) != 0);
         }
       tc::mma_commit(&bar[2]);
-    }
-    {  // squared row norms from the swizzled tiles: rows 0-63 k, 64-127 q; each half of the
-       // threads sums half of the 16-byte chunks of the row
-      const int r64 = row & 63;
-      const unsigned char* base = smem + SM::KQ + (row >= 64 ? 8192 : 0);
-      float ss = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4 * NB; ++q) {
-        const int cg = half * 4 * NB + q;  // chunk index over the whole row
-        const uint4 v4 = *reinterpret_cast<const uint4*>(base + (cg >> 3) * 16384 + tc::sw128_offset(r64, cg & 7));
-        const uint32_t* e = reinterpret_cast<const uint32_t*>(&v4);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = ElemT<E>::unpack(e[u]);
-          ss += f.x * f.x + f.y * f.y;
-        }
-      }
-      s_part[half * 128 + row] = ss;
-    }
-    __syncthreads();
-    if (tid < 128) {
-      const int r64 = tid & 63;
-      const float ss = s_part[tid] + s_part[128 + tid];
-      const float r = r64 < len ? rsqrtf(ss + kNormEps) : 0.f;
-      const int64_t jq = (int64_t)j * p.H + h;
-      if (tid < 64) {
-        s_rk[r64] = r;
-        p.rk[jq * C + r64] = r;
-      } else {
-        s_rq[r64] = r;
-        p.rq[jq * C + r64] = r;
-      }
     }
     if (kTmaStore && tid == 0) tc::bulk_wait_read();  // the previous item's staged W<-, U~ have been read
     ok = wait_all(&bar[2], ph2 & 1, p.status);
@@ -324,8 +291,31 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         kq[16 + u] = __uint_as_float(r1[u]);
       }
     }
+    if (tid < 128) {  // 1/|k| (rows 0-63) and 1/|q| (rows 64-127), 0 on padded rows, from the diagonal of
+                      // D1: warp w's columns 32 w .. 32 w + 31 hold it for each lane's row (row = tid)
+      float ss = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t dd[16];
+        tc::tmem_ld16(tmem + lane_base + 32 * warp + 16 * hh, dd);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) ss = lane == 16 * hh + u ? __uint_as_float(dd[u]) : ss;
+      }
+      const int r64 = tid & 63;
+      const float r = r64 < len ? rsqrtf(ss + kNormEps) : 0.f;
+      const int64_t jq = (int64_t)j * p.H + h;
+      if (tid < 64) {
+        s_rk[r64] = r;
+        p.rk[jq * C + r64] = r;
+      } else {
+        s_rq[r64] = r;
+        p.rq[jq * C + r64] = r;
+      }
+    }
     // D1 is read: the later MMAs that overwrite its columns are issued after the barriers below
     tc::fence_before_sync();
+    __syncthreads();  // 1/|k|, 1/|q| of every row are in place
 
     for (int ih = 0; ih < r_heads; ++ih) {
       const int hv = hv0 + ih;
