@@ -19,7 +19,8 @@
 // stores ks_t = 2^e_t, which the scan applies to the raw 16-bit keys without rounding.
 //
 // Tensor-core work (one elected thread issues, the accumulators live in TMEM):
-//   MMA1  D1[128 x 64]  = [K; Q] K^T            (M=128: rows 0-63 K K^T, rows 64-127 Q K^T)
+//   MMA1  D1[128 x 128] = [K; Q] [K; Q]^T       (columns 0-63: K K^T in rows 0-63, Q K^T in rows 64-127;
+//                                                the diagonal: |k|^2 and |q|^2, so no pass over the tiles)
 //   MMA2  DW[128 x D]   = [A'; A] K             (rows 0-63: W<- = A' K with A' = A diag(e^g/|k|))
 //   MMA3  DU[128 x D]   = [A'; A] V             (rows 64-127: U~ = A V)
 // Stacking A' and A keeps every MMA at M = 128 and puts W<- and U~ rows in TMEM lanes, so
