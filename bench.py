@@ -32,6 +32,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s and TFLOP/s (% of GB300 bf16 peak), 1 GPU"
+METRIC_DECODE = "GDN single-token step (decode) tokens/s and state GB/s (% of GB300 HBM), 1 GPU"
+DEC_KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indices")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indices", "cu_seqlens")
 
@@ -42,7 +44,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="long", help="workload name (tiny, varlen, long, throughput, wide)")
+    ap.add_argument("--config", default="long",
+                    help="workload name (tiny, varlen, long, throughput, wide; decode: the single-token step)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
@@ -174,11 +177,14 @@ def kernel_accounting(w, lengths):
             L = min(C, n - s)
             intra_flops += HV * ((H / HV) * (L * (L - 1) * K + L * (L + 1) * K) + L ** 3 / 3.0 + L * (L + 1) * (K + V))
             scan_flops += HV * (6.0 * L * K * V + L * (L + 1) * V)
+    path = {"bytes": acc.min_hbm_bytes(lengths, H, HV, K, V), "flops": acc.flop_count(lengths, H, HV, K, V, C)}
+    if w.name == "decode":  # one kernel does the whole step
+        return {"decode": dict(path), "path": path}
     return {
         "gates": {"bytes": gates_bytes, "flops": 0.0},
         "intra": {"bytes": intra_bytes, "flops": intra_flops},
         "scan": {"bytes": scan_bytes, "flops": scan_flops},
-        "path": {"bytes": acc.min_hbm_bytes(lengths, H, HV, K, V), "flops": acc.flop_count(lengths, H, HV, K, V, C)},
+        "path": path,
     }
 
 
@@ -209,7 +215,7 @@ def _code_only(src: str) -> str:
 def kernel_source_hash(kernel: str) -> str:
     """Hash of the code (not the comments) of a kernel's sources and the shared headers."""
     files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu"], "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
-             "schedule": ["gdn_schedule.cu"]}
+             "schedule": ["gdn_schedule.cu"], "decode": ["gdn_decode.cu", "gdn_decode.cuh"]}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
     h = hashlib.sha256()
     for f in files.get(kernel, []) + ["gdn_common.cuh", "gdn_tc.cuh"]:
@@ -294,13 +300,18 @@ def run_reference(args, dist):
     w = wl.BY_NAME[args.config]
     d = wl.make_inputs(w)
     per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    S, _, _ = oracle_sample(d, w, per_step)
     import torch
-    sub = dict(d)
-    for k in ("q", "k", "v", "a", "b"):
-        sub[k] = d[k][:S]
-    sub["cu_seqlens"] = torch.tensor([0, S], dtype=torch.int64)
-    sub["cache_indices"] = d["cache_indices"][:1]
+    if w.name == "decode":  # the whole single-token batch is a small sample already
+        sub, S = d, int(d["cache_indices"].numel())
+        sample = f"the whole batch ({S} sequences x {w.HV} value heads), per step"
+    else:
+        S, _, _ = oracle_sample(d, w, per_step)
+        sub = dict(d)
+        for k in ("q", "k", "v", "a", "b"):
+            sub[k] = d[k][:S]
+        sub["cu_seqlens"] = torch.tensor([0, S], dtype=torch.int64)
+        sub["cache_indices"] = d["cache_indices"][:1]
+        sample = f"first {S} tokens of sequence 0, all {w.HV} value heads, per step"
     for _ in range(args.warmup):
         oracle.gdn_forward(*[sub[k] for k in KEYS])
     t = time.perf_counter()
@@ -309,9 +320,8 @@ def run_reference(args, dist):
         threads = oracle.gdn_forward(*[sub[k] for k in KEYS]).threads
     el = time.perf_counter() - t
     tok_s = S * args.steps / el
-    sample = f"first {S} tokens of sequence 0, all {w.HV} value heads, per step"
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_DECODE if w.name == "decode" else METRIC, "value": round(tok_s, 1), "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.note}", "sample": sample},
@@ -322,6 +332,21 @@ def run_reference(args, dist):
     print(json.dumps(line), flush=True)
 
 
+def oracle_sample_decode(d: dict, target_s: float):
+    """Runs the oracle on the whole single-token batch, repeated until about target_s seconds.
+    Returns (tokens, seconds, threads, repeats)."""
+    import oracle
+    t = time.perf_counter()
+    res = oracle.gdn_forward(*[d[k] for k in KEYS])
+    one = time.perf_counter() - t
+    reps = max(1, int(target_s / max(one, 1e-6)))
+    t = time.perf_counter()
+    for _ in range(reps):
+        res = oracle.gdn_forward(*[d[k] for k in KEYS])
+    dt = time.perf_counter() - t
+    return int(d["cache_indices"].numel()) * reps, dt, res.threads, reps
+
+
 def run_ours(args, dist):
     import torch
     import gated_deltanet_chunkwise_gdn_gb300 as gdn
@@ -330,6 +355,7 @@ def run_ours(args, dist):
     dev = torch.device("cuda", dist.local_rank if dist.world > 1 else 0)
     torch.cuda.set_device(dev)
     w = wl.BY_NAME[args.config]
+    decode = w.name == "decode"
     d = wl.make_inputs(w)
     lengths = wl.sequence_lengths(w)
     T = sum(lengths)
@@ -337,10 +363,16 @@ def run_ours(args, dist):
     out = torch.empty((T, w.HV, w.V), dtype=w.dtype, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        gdn.gdn_extend_chunkwise(*[g[k] for k in KEYS], chunk_size=w.chunk_size, out=out)
+    def call(bufs, o, check=False):
+        if decode:  # one token per sequence: q, k, v, a, b are [B, ...]
+            gdn.gdn_decode_step(*[bufs[k] for k in DEC_KEYS], out=o, check=check)
+        else:
+            gdn.gdn_extend_chunkwise(*[bufs[k] for k in KEYS], chunk_size=w.chunk_size, out=o, check=check)
 
-    gdn.gdn_extend_chunkwise(*[g[k] for k in KEYS], chunk_size=w.chunk_size, out=out, check=True)
+    def step():
+        call(g, out)
+
+    call(g, out, check=True)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
@@ -381,7 +413,7 @@ def run_ours(args, dist):
     # copies of neighbouring steps overlap the call (two device buffer sets, copy streams
     # ordered by events). The state pool is shared, so the calls stay in order on one stream.
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    in_keys = ("q", "k", "v", "a", "b", "cache_indices", "cu_seqlens")
+    in_keys = ("q", "k", "v", "a", "b", "cache_indices") + (() if decode else ("cu_seqlens",))
     host_in = {k: d[k].pin_memory() for k in in_keys}
     host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -410,7 +442,7 @@ def run_ours(args, dist):
             for e in ev_in[b]:
                 stream.wait_event(e)
             stream.wait_event(ev_out[b])  # the output buffer of step i-2 has been read back
-            gdn.gdn_extend_chunkwise(*[bufs[b][k] for k in KEYS], chunk_size=w.chunk_size, out=outs[b])
+            call(bufs[b], outs[b])
             ev_done[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[b])
@@ -450,14 +482,18 @@ def run_ours(args, dist):
     tokens = T * args.steps * dist.world
     value = tokens / (ms_max * 1e-3)
     tflops = acct["path"]["flops"] * args.steps * dist.world / (ms_max * 1e-3) / 1e12
+    if decode:
+        l2 = "inputs larger than L2 (state slots %.0f MB read and written > 129 MB), no flush" % (
+            len(lengths) * w.HV * w.V * w.K * 4 / 1e6)
+    else:
+        l2 = "inputs larger than L2 (q,k,v %.0f MB > 129 MB), no flush" % (3 * T * w.H * w.K * 2 / 1e6)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
+        "metric": METRIC_DECODE if decode else METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.note}", "global_batch": len(lengths) * dist.world, "seq_len": max(lengths),
                    "total_tokens_per_gpu": T, "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (q,k,v %.0f MB > 129 MB), no flush" % (
-                       3 * T * w.H * w.K * 2 / 1e6)},
+                   "l2": l2},
         "tflops": round(tflops, 2),
         "frac_bf16_peak": round(tflops / float(peaks["bf16_tflops"]), 4),
         "roofline": roof,
@@ -469,7 +505,12 @@ def run_ours(args, dist):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "ms_per_step": round(e2e_ms / e2e_steps, 4)},
     }
-    if dist.world == 1 and not args.no_cpu_baseline:
+    if dist.world == 1 and not args.no_cpu_baseline and decode:
+        n, dt, threads, reps = oracle_sample_decode(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(n / dt, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"the whole batch ({len(lengths)} sequences x {w.HV} value heads), "
+                                          f"{reps} times ({dt:.1f} s)"}
+    elif dist.world == 1 and not args.no_cpu_baseline:
         S, dt, threads = oracle_sample(d, w, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(S / dt, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {S} tokens of sequence 0, all {w.HV} value heads ({dt:.1f} s)"}

@@ -8,6 +8,7 @@ The entry point mirrors ``gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias,
 state_pool, cache_indices, cu_seqlens, chunk_size=64)`` of the pymllm page
 "pymllm.layers.attention.gdn_chunkwise" (Module Contents): same arguments, same
 shapes, state_pool updated in place, output returned in v's dtype.
+``gdn_decode_step`` advances the same pooled states by one token per sequence.
 """
 
 from __future__ import annotations
@@ -17,10 +18,11 @@ import torch
 from . import _lib
 from ._lib import GdnError
 
-__all__ = ["gdn_extend_chunkwise", "gdn_workspace_size", "gdn_get_device_status", "GdnError",
-           "library_path", "version"]
+__all__ = ["gdn_extend_chunkwise", "gdn_decode_step", "gdn_workspace_size", "gdn_get_device_status",
+           "GdnError", "library_path", "version"]
 
 _ws_cache: dict = {}
+_status_cache: dict = {}
 
 
 def library_path() -> str:
@@ -120,6 +122,60 @@ def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indice
     _lib.check(st, "gdn_extend_chunkwise")
     if check:
         _lib.check(L.gdn_get_device_status(ws_ptr, sp), "gdn_extend_chunkwise (device)")
+    return out
+
+
+def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *, scale: float = 1.0,
+                    out: torch.Tensor = None, check: bool = False, stream=None) -> torch.Tensor:
+    """One token per sequence against the state pool; returns ``out [B, HV, V]`` in v's dtype.
+
+    The one-token case of :func:`gdn_extend_chunkwise` (``cu_seqlens = 0, 1, ..., B``), run by a
+    dedicated kernel: q, k ``[B, H, K]``, v ``[B, HV, V]`` bf16 or fp16; a, b ``[B, HV]``, A_log,
+    dt_bias ``[HV]`` fp32; state_pool ``[pool, HV, V, K]`` fp32 (updated in place); cache_indices
+    ``[B]`` int64. ``check=True`` waits and raises on a bad or repeated cache index.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_decode_step runs on a CUDA device; move the inputs there first")
+    _req(q, "q", (torch.bfloat16, torch.float16), dev)
+    _req(k, "k", q.dtype, dev)
+    _req(v, "v", q.dtype, dev)
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias), ("state_pool", state_pool)):
+        _req(t, name, torch.float32, dev)
+    _req(cache_indices, "cache_indices", torch.int64, dev)
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
+        raise ValueError(f"bad q/k/v shapes {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    B, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    if a.shape != (B, HV) or b.shape != (B, HV) or A_log.shape != (HV,) or dt_bias.shape != (HV,):
+        raise ValueError("a, b must be [B, HV] and A_log, dt_bias [HV]")
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, V, K):
+        raise ValueError(f"state_pool must be [pool, {HV}, {V}, {K}], got {tuple(state_pool.shape)}")
+    if cache_indices.shape != (B,):
+        raise ValueError("cache_indices must have one entry per sequence")
+    if out is None:
+        out = torch.empty((B, HV, V), dtype=v.dtype, device=dev)
+    else:
+        _req(out, "out", v.dtype, dev)
+        if tuple(out.shape) != (B, HV, V):
+            raise ValueError("out must be [B, HV, V]")
+    status = _status_cache.get(dev.index)
+    if status is None:
+        status = torch.zeros(64, dtype=torch.int32, device=dev)
+        _status_cache[dev.index] = status
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    L = _lib.load()
+    dtype_code = _lib.GDN_BF16 if q.dtype == torch.bfloat16 else _lib.GDN_FP16
+    st = L.gdn_decode_step(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype_code,
+        a.data_ptr(), b.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr(),
+        state_pool.data_ptr(), state_pool.shape[0], cache_indices.data_ptr(), B, out.data_ptr(),
+        H, HV, K, V, float(scale), status.data_ptr(), sp)
+    _lib.check(st, "gdn_decode_step")
+    if check:
+        _lib.check(L.gdn_get_device_status(status.data_ptr(), sp), "gdn_decode_step (device)")
     return out
 
 

@@ -57,6 +57,13 @@ def load(build_if_missing: bool = True):
             vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp, i32,
             vp, i64, i32, i32, i32, i32, i32, f32, vp, vp]
         L.gdn_extend_chunkwise_noalloc.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [
+            vp, vp, vp, ctypes.c_int,      # q k v dtype
+            vp, vp, vp, vp,                # a b A_log dt_bias
+            vp, i64, vp, i32, vp,          # state_pool pool_size cache_indices batch out
+            i32, i32, i32, i32, f32,       # H HV K V scale
+            vp, vp]                        # device_status stream
+        L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_get_device_status.argtypes = [vp, vp]
         L.gdn_get_device_status.restype = ctypes.c_int
         L.gdn_status_string.argtypes = [ctypes.c_int]

@@ -1,17 +1,22 @@
 // gdn_api.cu — host side of the C ABI declared in include/gdn.h: argument checks,
-// workspace carve-up and the launch sequence K0 (schedule) -> K1 (gates) -> K2 (intra) -> K3 (scan).
+// workspace carve-up and the launch sequence K0 (schedule) -> K1 (gates) -> K2 (intra) -> K3 (scan)
+// of the prefill call, and the single-token step (slot check -> state update).
 #include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "gdn_common.cuh"
+#include "gdn_decode.cuh"
 
 namespace {
 
 // ---------------------------------------------------------------- instrumentation
-enum KernelId { kKernSchedule = 0, kKernGates = 1, kKernIntra = 2, kKernScan = 3, kKernCount = 4 };  // scan: every scan-stage launch
-const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "scan"};
+enum KernelId {  // scan: every scan-stage launch
+  kKernSchedule = 0, kKernGates = 1, kKernIntra = 2, kKernScan = 3, kKernDecodeCheck = 4, kKernDecode = 5,
+  kKernCount = 6
+};
+const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "scan", "decode_check", "decode"};
 
 std::atomic<int64_t> g_launches{0};
 
@@ -56,6 +61,10 @@ constexpr int kWyBlock = 64;
 
 // Value-dimension split of the scan: blocks of 64 state rows per CTA.
 int choose_nvb(int V) { return V / 64; }
+
+// Largest batch of one single-token step (the slot check runs one block per pair of
+// 256-index tiles, and the grid must stay within 2^31 - 1 blocks).
+constexpr int32_t kMaxDecodeBatch = 1 << 24;
 
 }  // namespace
 
@@ -144,6 +153,54 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   return GDN_OK;
 }
 
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* a,
+                           const float* b, const float* A_log, const float* dt_bias, float* state_pool,
+                           int64_t pool_size, const int64_t* cache_indices, int32_t batch, void* out, int32_t H,
+                           int32_t HV, int32_t K, int32_t V, float scale, int32_t* device_status, void* stream) {
+  if (batch < 0 || batch > kMaxDecodeBatch || H <= 0 || HV <= 0 || HV % H != 0 || K <= 0 || V <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if ((int64_t)batch * HV > (int64_t)INT32_MAX) return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_BF16 && dtype != GDN_FP16) return GDN_ERR_INVALID_ARG;
+  if (!device_status || (reinterpret_cast<uintptr_t>(device_status) & 3u) != 0 || !A_log || !dt_bias)
+    return GDN_ERR_INVALID_ARG;
+  if (batch > 0 && (!q || !k || !v || !a || !b || !out || !state_pool || !cache_indices || pool_size <= 0))
+    return GDN_ERR_INVALID_ARG;
+  if (K != V || (K != 64 && K != 128 && K != 256)) return GDN_ERR_UNSUPPORTED;
+  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; };
+  if (batch > 0 && !(al16(q) && al16(k) && al16(v) && al16(out) && al16(state_pool))) return GDN_ERR_INVALID_ARG;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  gdn::DecodeParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.a = a;
+  p.b = b;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.state_pool = state_pool;
+  p.cache_indices = cache_indices;
+  p.out = out;
+  p.pool_size = pool_size;
+  p.B = batch;
+  p.H = H;
+  p.HV = HV;
+  p.scale = scale;
+  p.status = device_status;
+  p.fp16 = dtype == GDN_FP16 ? 1 : 0;
+  if (batch == 0 || gdn::decode_check_needs_zeroed_status(batch)) {
+    if (cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (batch == 0) return GDN_OK;
+  }
+  int rec = prof_begin(kKernDecodeCheck, s);
+  if (gdn::launch_decode_check(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
+  rec = prof_begin(kKernDecode, s);
+  if (gdn::launch_decode(p, K, s) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s);
+  return GDN_OK;
+}
+
 gdn_status gdn_get_device_status(const void* workspace, void* stream) {
   if (!workspace) return GDN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -220,6 +277,6 @@ const char* gdn_kernel_name(int32_t id) { return (id >= 0 && id < kKernCount) ? 
 
 int64_t gdn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int32_t gdn_version(void) { return 100; }
+int32_t gdn_version(void) { return 200; }
 
 }  // extern "C"

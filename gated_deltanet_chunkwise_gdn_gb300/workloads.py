@@ -65,7 +65,13 @@ CONFIGS: List[Workload] = [
              a_mean=-2.0, b_mean=1.0,
              note="B=4 x T=16384, H=HV=4, K=V=256, C=128, a ~ N(-2,1), b ~ N(1,1), zero state"),
 ]
-BY_NAME = {w.name: w for w in CONFIGS}
+# Single-token step (decode): one new token for each of 256 sequences against a 512-slot pool,
+# the head shape of the varlen configuration. Every sequence has length 1, so cu_seqlens is
+# 0, 1, ..., 256 and the same inputs serve the chunkwise call and the oracle.
+DECODE = Workload("decode", 5, [1] * 256, H=16, HV=32, K=128, V=128, chunk_size=64, pool_size=512,
+                  state_std=0.1, index_rule="perm_subset",
+                  note="B=256 sequences x 1 token, H=16, HV=32, K=V=128, 512-slot pool, states N(0, 0.1^2)")
+BY_NAME = {w.name: w for w in CONFIGS + [DECODE]}
 
 
 def _randn_into(out: torch.Tensor, gen: torch.Generator, mean: float = 0.0, std: float = 1.0):

@@ -5,7 +5,8 @@
  * -------------
  * gdn_extend_chunkwise runs the Gated DeltaNet recurrence over a packed batch of
  * prompts ("extend" / prefill), reading and writing each prompt's recurrent state
- * in a pooled state buffer. It follows the interface documented for
+ * in a pooled state buffer; gdn_decode_step advances the same states by one token
+ * each (see its declaration). It follows the interface documented for
  * gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices,
  * cu_seqlens, chunk_size=64) on the pymllm page "pymllm.layers.attention.gdn_chunkwise"
  * (section "Module Contents", Parameters and Returns), and computes, for every
@@ -146,10 +147,48 @@ GDN_API gdn_status gdn_extend_chunkwise_noalloc(const void *q, const void *k, co
                                                 int32_t *device_status, void *stream);
 
 /*
+ * Single-token step (decode): one new token for each of `batch` sequences, against the
+ * same state pool and index contract as gdn_extend_chunkwise. It is that call with
+ * cu_seqlens = 0, 1, ..., batch (the one-token case of the recurrence above: the
+ * transition of "Simple math to speed up GDN prefill", section "Reminder", and the
+ * output read after the write), computed directly without chunking:
+ *
+ *   S' = alpha S + beta (v - alpha S k^) k^^T,   out = scale S' q^
+ *
+ *  q, k          [batch, H, K]   bf16 or fp16 (dtype), not pre-normalised.
+ *  v             [batch, HV, V]  same dtype.
+ *  a, b          [batch, HV]     fp32 raw gate inputs; A_log, dt_bias [HV] fp32.
+ *  state_pool    [pool_size, HV, V, K] fp32, slots named by cache_indices read and
+ *                overwritten in place; other slots untouched.
+ *  cache_indices [batch] int64, distinct, in [0, pool_size).
+ *  out           [batch, HV, V] same dtype as v, written.
+ *  K, V          K = V in {64, 128, 256} (otherwise GDN_ERR_UNSUPPORTED).
+ *  device_status DEVICE pointer to one int32 (4-byte aligned), owned by the caller. In
+ *                stream order the step sets it to GDN_OK, or to GDN_ERR_BAD_INDEX if a slot
+ *                is out of range or repeated, in which case the update kernel touches
+ *                nothing. Read it with gdn_get_device_status(device_status, stream).
+ *  stream        cudaStream_t to enqueue on.
+ *
+ * q, k, v, out and state_pool must be 16-byte aligned; 0 <= batch <= 2^24 and
+ * batch * HV < 2^31. Host-detectable errors (null pointer, misalignment, bad sizes,
+ * HV % H != 0, dtype) return before anything is enqueued; batch = 0 only resets the
+ * status word. No workspace; the library allocates nothing. Launches two kernels (the
+ * second with programmatic dependent launch behind the first); batches above 1024 also
+ * zero the status word with one memset before them.
+ */
+GDN_API gdn_status gdn_decode_step(const void *q, const void *k, const void *v, gdn_dtype dtype,
+                                   const float *a, const float *b, const float *A_log,
+                                   const float *dt_bias, float *state_pool, int64_t pool_size,
+                                   const int64_t *cache_indices, int32_t batch, void *out, int32_t H,
+                                   int32_t HV, int32_t K, int32_t V, float scale,
+                                   int32_t *device_status, void *stream);
+
+/*
  * Waits for `stream`, then returns the status recorded on the device by the last
  * gdn_extend_chunkwise call that used this workspace (GDN_OK, GDN_ERR_BAD_INDEX,
  * GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the stream reported
- * an error. Synchronises the host with the stream.
+ * an error. Synchronises the host with the stream. Given the device_status word of
+ * gdn_decode_step instead of a workspace, it returns that step's status.
  */
 GDN_API gdn_status gdn_get_device_status(const void *workspace, void *stream);
 
@@ -157,7 +196,7 @@ GDN_API gdn_status gdn_get_device_status(const void *workspace, void *stream);
 GDN_API const char *gdn_status_string(gdn_status status);
 
 /*
- * Instrumentation. gdn_profile_start makes every later gdn_extend_chunkwise call
+ * Instrumentation. gdn_profile_start makes every later gdn_extend_chunkwise or gdn_decode_step call
  * record a pair of CUDA events around each kernel it launches, on the call's own
  * stream, for up to max_launches kernel launches in total (the events are created
  * here, on the current device). gdn_profile_stop waits for those events, adds the

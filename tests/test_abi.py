@@ -100,3 +100,28 @@ def test_product_path_has_no_fallback(monkeypatch):
     monkeypatch.setattr(gbuild, "LIB_PATH", "/nonexistent/libgdn_gb300.so")
     with pytest.raises(RuntimeError):
         _lib.load(build_if_missing=False)
+
+
+def _decode(lib, **over):
+    args = dict(q=16, k=16, v=16, dtype=0, a=16, b=16, A_log=16, dt_bias=16, pool=16, pool_size=4, idx=16,
+                batch=2, out=16, H=2, HV=4, K=128, V=128, scale=1.0, status=16, stream=None)
+    args.update(over)
+    return lib.gdn_decode_step(*[args[k] for k in (
+        "q", "k", "v", "dtype", "a", "b", "A_log", "dt_bias", "pool", "pool_size", "idx", "batch", "out",
+        "H", "HV", "K", "V", "scale", "status", "stream")])
+
+
+def test_decode_host_side_errors_return_before_any_device_work(lib):
+    assert _decode(lib, HV=3) == 1             # HV % H != 0
+    assert _decode(lib, q=None) == 1           # null input
+    assert _decode(lib, status=None) == 1      # no status word
+    assert _decode(lib, status=18) == 1        # misaligned status word
+    assert _decode(lib, pool=24) == 1          # state pool not 16-byte aligned
+    assert _decode(lib, out=8) == 1            # output not 16-byte aligned
+    assert _decode(lib, batch=-1) == 1
+    assert _decode(lib, batch=(1 << 24) + 1) == 1
+    assert _decode(lib, batch=1 << 24, HV=256, H=1) == 1   # grid would exceed 2^31 - 1 blocks
+    assert _decode(lib, dtype=5) == 1
+    assert _decode(lib, pool_size=0) == 1
+    assert _decode(lib, K=96, V=96) == 2       # not built
+    assert _decode(lib, K=128, V=64) == 2
