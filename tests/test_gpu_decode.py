@@ -145,3 +145,28 @@ def test_decode_equals_chunkwise_call_with_unit_lengths():
     res = oracle_for(d)
     compare(d, o2.cpu(), g["state_pool"].cpu(), res)
     assert rel_l2(o1.float().numpy().astype(np.float64), o2.float().cpu().numpy().astype(np.float64)) <= OUT_TOL
+
+
+def test_decode_batch_above_one_block_check():
+    """Above 1024 sequences the slot check runs as a grid of tile pairs after a memset."""
+    d = decode_inputs(1300, 1, 2, 64, seed=78, pool_size=2700)
+    out, pool = run_decode(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
+@pytest.mark.parametrize("pos", [(3, 1290), (1100, 1299), (1025, 1026)])
+def test_decode_batch_above_one_block_check_rejects_repeats(pos):
+    d = decode_inputs(1300, 1, 2, 64, seed=79, pool_size=2700)
+    idx = d["cache_indices"].clone()
+    idx[pos[1]] = idx[pos[0]]
+    d["cache_indices"] = idx
+    g = to_device(d)
+    with pytest.raises(GdnError) as e:
+        gdn_decode_step(*[g[k] for k in DEC_KEYS], check=True)
+    assert e.value.status == 3
+    assert torch.equal(g["state_pool"].cpu(), d["state_pool"]), "a rejected step changed the pool"
+    # the status word is reset by the next good step
+    d2 = decode_inputs(1300, 1, 2, 64, seed=80, pool_size=2700)
+    g2 = to_device(d2)
+    gdn_decode_step(*[g2[k] for k in DEC_KEYS], check=True)
