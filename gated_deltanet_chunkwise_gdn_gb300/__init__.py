@@ -126,13 +126,16 @@ def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indice
 
 
 def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *, scale: float = 1.0,
-                    out: torch.Tensor = None, check: bool = False, stream=None) -> torch.Tensor:
+                    out: torch.Tensor = None, check: bool = False, stream=None,
+                    status: torch.Tensor = None) -> torch.Tensor:
     """One token per sequence against the state pool; returns ``out [B, HV, V]`` in v's dtype.
 
     The one-token case of :func:`gdn_extend_chunkwise` (``cu_seqlens = 0, 1, ..., B``), run by a
     dedicated kernel: q, k ``[B, H, K]``, v ``[B, HV, V]`` bf16 or fp16; a, b ``[B, HV]``, A_log,
     dt_bias ``[HV]`` fp32; state_pool ``[pool, HV, V, K]`` fp32 (updated in place); cache_indices
     ``[B]`` int64. ``check=True`` waits and raises on a bad or repeated cache index.
+    ``status``: an int32 device tensor for the step's status word; by default one cached word
+    per device, which steps issued concurrently on different streams would share.
     """
     dev = q.device
     if dev.type != "cuda":
@@ -159,10 +162,15 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *,
         _req(out, "out", v.dtype, dev)
         if tuple(out.shape) != (B, HV, V):
             raise ValueError("out must be [B, HV, V]")
-    status = _status_cache.get(dev.index)
     if status is None:
-        status = torch.zeros(64, dtype=torch.int32, device=dev)
-        _status_cache[dev.index] = status
+        status = _status_cache.get(dev.index)
+        if status is None:
+            status = torch.zeros(64, dtype=torch.int32, device=dev)
+            _status_cache[dev.index] = status
+    else:
+        _req(status, "status", torch.int32, dev)
+        if status.numel() < 1:
+            raise ValueError("status must hold at least one int32")
     if stream is None:
         stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
