@@ -10,6 +10,8 @@ package never imports the GPU library: the two share no code.
 * :func:`delta_rule` — the same recurrence with alpha, beta and normalised q/k given
   directly (for the hand-chosen pins).
 * :mod:`oracle.chunkwise` — O2, numpy restatements of the chunkwise WY algebra.
+* :mod:`oracle.backward` — O3, gradients of the recurrence (chain rule, fp64), with the final
+  state's incoming gradient as an input.
 """
 
 from __future__ import annotations
