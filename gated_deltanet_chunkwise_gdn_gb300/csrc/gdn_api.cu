@@ -62,6 +62,12 @@ constexpr int kWyBlock = 64;
 // Value-dimension split of the scan: blocks of 64 state rows per CTA.
 int choose_nvb(int V) { return V / 64; }
 
+// The per-chunk factors W<-, U~ and P are tiles of [max_chunks * HV * 64, *] arrays that TMA
+// addresses with 32-bit signed row coordinates, so the row count must stay below 2^31.
+bool factor_rows_fit(const gdn::WsLayout& L, int HV) {
+  return L.max_chunks * (int64_t)HV * kWyBlock <= (int64_t)INT32_MAX;
+}
+
 // Largest batch of one single-token step (the slot check runs one block per pair of
 // 256-index tiles, and the grid must stay within 2^31 - 1 blocks).
 constexpr int32_t kMaxDecodeBatch = 1 << 24;
@@ -75,7 +81,8 @@ size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H, int32_
   if (total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || batch < 0 || H <= 0 || HV <= 0 || HV % H != 0)
     return 0;
   if (!supported_shape(K, V, chunk_size)) return 0;
-  return gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock).total;
+  const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock);
+  return factor_rows_fit(L, HV) ? L.total : 0;
 }
 
 gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* a,
@@ -93,6 +100,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   if (total_tokens > 0 && (!q || !k || !v || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   if (!supported_shape(K, V, chunk_size)) return GDN_ERR_UNSUPPORTED;
   const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock);
+  if (!factor_rows_fit(L, HV)) return GDN_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return GDN_ERR_WORKSPACE;
 

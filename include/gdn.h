@@ -104,6 +104,9 @@ GDN_API size_t gdn_workspace_size(int64_t total_tokens, int32_t batch, int32_t H
  *  chunk_size    64 or 128 (otherwise GDN_ERR_UNSUPPORTED). The kernels factor each chunk
  *                in 64-token WY blocks: a 128-token chunk is computed as its two halves,
  *                which gives the same result up to rounding.
+ *                Size limit: (total_tokens / 64 + batch + 1) * HV * 64 < 2^31 (the rows of
+ *                the per-chunk factors in the workspace); larger calls return
+ *                GDN_ERR_UNSUPPORTED and gdn_workspace_size returns 0 for them.
  *  scale         multiplies every output (1.0 reads o_t = S_t q_t as written).
  *  workspace     device buffer of at least gdn_workspace_size(...) bytes, 256-byte aligned.
  *  stream        cudaStream_t to enqueue on.

@@ -125,3 +125,12 @@ def test_decode_host_side_errors_return_before_any_device_work(lib):
     assert _decode(lib, pool_size=0) == 1
     assert _decode(lib, K=96, V=96) == 2       # not built
     assert _decode(lib, K=128, V=64) == 2
+
+
+def test_calls_beyond_the_factor_row_limit_are_refused(lib):
+    """(T/64 + B + 1) * HV * 64 rows of per-chunk factors must fit 32-bit TMA coordinates."""
+    ws = lib.gdn_workspace_size
+    assert ws(1 << 25, 1 << 25, 1, 1, 64, 64, 64) == 0          # 2^25 one-token sequences, one head
+    assert ws(1 << 20, 1 << 20, 1, 4, 64, 64, 64) > 0
+    assert ws(1 << 28, 1, 1, 8, 64, 64, 64) == 0                # 2^28 tokens x 8 value heads
+    assert _call(lib, T=1 << 25, batch=1 << 25, H=1, HV=1, K=64, V=64) == 2
