@@ -68,9 +68,9 @@ bool factor_rows_fit(const gdn::WsLayout& L, int HV) {
   return L.max_chunks * (int64_t)HV * kWyBlock <= (int64_t)INT32_MAX;
 }
 
-// Largest batch of one single-token step (the slot check runs one block per pair of
-// 256-index tiles, and the grid must stay within 2^31 - 1 blocks).
-constexpr int32_t kMaxDecodeBatch = 1 << 24;
+// Largest batch of one single-token step. Above 1024 sequences the slot check runs one block
+// per pair of 256-index tiles: 2^20 sequences take 8.4 M blocks, far inside the grid limit.
+constexpr int32_t kMaxDecodeBatch = 1 << 20;
 
 }  // namespace
 

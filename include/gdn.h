@@ -172,7 +172,7 @@ GDN_API gdn_status gdn_extend_chunkwise_noalloc(const void *q, const void *k, co
  *                nothing. Read it with gdn_get_device_status(device_status, stream).
  *  stream        cudaStream_t to enqueue on.
  *
- * q, k, v, out and state_pool must be 16-byte aligned; 0 <= batch <= 2^24 and
+ * q, k, v, out and state_pool must be 16-byte aligned; 0 <= batch <= 2^20 and
  * batch * HV < 2^31. Host-detectable errors (null pointer, misalignment, bad sizes,
  * HV % H != 0, dtype) return before anything is enqueued; batch = 0 only resets the
  * status word. No workspace; the library allocates nothing. Launches two kernels (the

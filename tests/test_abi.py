@@ -119,8 +119,8 @@ def test_decode_host_side_errors_return_before_any_device_work(lib):
     assert _decode(lib, pool=24) == 1          # state pool not 16-byte aligned
     assert _decode(lib, out=8) == 1            # output not 16-byte aligned
     assert _decode(lib, batch=-1) == 1
-    assert _decode(lib, batch=(1 << 24) + 1) == 1
-    assert _decode(lib, batch=1 << 24, HV=256, H=1) == 1   # grid would exceed 2^31 - 1 blocks
+    assert _decode(lib, batch=(1 << 20) + 1) == 1
+    assert _decode(lib, batch=1 << 20, HV=4096, H=1) == 1  # grid would exceed 2^31 - 1 blocks
     assert _decode(lib, dtype=5) == 1
     assert _decode(lib, pool_size=0) == 1
     assert _decode(lib, K=96, V=96) == 2       # not built
