@@ -161,7 +161,9 @@ def load_peaks():
 
 
 def kernel_accounting(w, lengths):
-    """Algorithmic bytes and FLOPs per launch of each kernel."""
+    """Algorithmic bytes and FLOPs per launch of each kernel: what the method must move (q, k, v, a, b
+    read once, o written once, each touched state read and written once) and compute (triangular
+    products at their true size), not what a kernel happens to execute."""
     from gated_deltanet_chunkwise_gdn_gb300 import accounting as acc
     T = sum(lengths)
     H, HV, K, V, C = w.H, w.HV, w.K, w.V, w.chunk_size

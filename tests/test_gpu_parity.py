@@ -21,13 +21,13 @@ if not torch.cuda.is_available():  # collected on CPU runs, skipped there
 # ----------------------------------------------------------------------------- the five configs
 
 def test_config_tiny_full():
-    d = wl.make_inputs(wl.CONFIGS[0])
+    d = wl.make_inputs(wl.BY_NAME["tiny"])
     out, pool = run_gpu(d)
     compare(d, out, pool, oracle_for(d))
 
 
 def test_config_varlen_full():
-    d = wl.make_inputs(wl.CONFIGS[1])
+    d = wl.make_inputs(wl.BY_NAME["varlen"])
     out, pool = run_gpu(d)
     compare(d, out, pool, oracle_for(d))
     untouched_slots_equal(d, pool)
@@ -35,14 +35,14 @@ def test_config_varlen_full():
 
 def test_config_long_full():
     """B=1, T=65536, H=HV=16, K=V=128: every chain, every token."""
-    d = wl.make_inputs(wl.CONFIGS[2])
+    d = wl.make_inputs(wl.BY_NAME["long"])
     out, pool = run_gpu(d)
     compare(d, out, pool, oracle_for(d))
 
 
 def test_config_throughput_sampled_chains():
     """B=32 x 8192, H=HV=32: 24 sampled (sequence, head) chains, all their tokens."""
-    d = wl.make_inputs(wl.CONFIGS[3])
+    d = wl.make_inputs(wl.BY_NAME["throughput"])
     out, pool = run_gpu(d)
     rng = np.random.default_rng(0)
     chains = np.stack([rng.integers(0, 32, 24), rng.integers(0, 32, 24)], 1)
@@ -52,7 +52,7 @@ def test_config_throughput_sampled_chains():
 
 def test_config_wide_full():
     """B=4 x 16384, H=HV=4, K=V=256, 128-token chunks, a shifted by -2: every chain, every token."""
-    d = wl.make_inputs(wl.CONFIGS[4])
+    d = wl.make_inputs(wl.BY_NAME["wide"])
     assert d["chunk_size"] == 128 and d["q"].shape[-1] == 256
     out, pool = run_gpu(d)
     compare(d, out, pool, oracle_for(d))
