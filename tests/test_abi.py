@@ -134,3 +134,9 @@ def test_calls_beyond_the_factor_row_limit_are_refused(lib):
     assert ws(1 << 20, 1 << 20, 1, 4, 64, 64, 64) > 0
     assert ws(1 << 28, 1, 1, 8, 64, 64, 64) == 0                # 2^28 tokens x 8 value heads
     assert _call(lib, T=1 << 25, batch=1 << 25, H=1, HV=1, K=64, V=64) == 2
+
+
+def test_kernel_kinds_named_for_the_profiler(lib):
+    names = [lib.gdn_kernel_name(i) for i in range(8)]
+    assert [n.decode() for n in names[:6]] == ["schedule", "gates", "intra", "scan", "decode_check", "decode"]
+    assert names[6] is None and lib.gdn_kernel_name(-1) is None
