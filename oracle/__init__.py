@@ -12,6 +12,8 @@ package never imports the GPU library: the two share no code.
 * :mod:`oracle.chunkwise` — O2, numpy restatements of the chunkwise WY algebra.
 * :mod:`oracle.backward` — O3, gradients of the recurrence (chain rule, fp64), with the final
   state's incoming gradient as an input.
+* :mod:`oracle.chunkwise_grad` — O4, the chunkwise WY forward in fp64 PyTorch differentiated by
+  autograd (a second route to O3's gradients, and per-chunk intermediate gradients).
 """
 
 from __future__ import annotations

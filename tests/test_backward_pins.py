@@ -7,6 +7,9 @@
   changes L by exactly <gradient, step>.
 * A closed form: with beta = 0 the state only decays.
 * Teeth: plausible mistakes planted in a copy of the backward fail the finite-difference pin.
+* A second route: autograd through the chunkwise WY form (O4, oracle/chunkwise_grad.py) gives the same
+  gradients as O3's chain rule through the token recurrence, and O4's kept gradients of the state entering
+  each chunk pass the exact-linearity check against O1.
 """
 
 import numpy as np
@@ -222,3 +225,47 @@ def test_pins_catch_planted_backward_mistakes(kind):
     assert_matches_fd(chain_grads(p, d_out, d_state, fn=_mutant_backward("none")), fd)  # the unplanted copy passes
     with pytest.raises(AssertionError):
         assert_matches_fd(chain_grads(p, d_out, d_state, fn=_mutant_backward(kind)), fd)
+
+
+# --------------------------------------------------------------------------- O4: autograd of the chunkwise form
+
+from oracle import chunkwise_grad as cg  # noqa: E402
+
+
+@pytest.mark.parametrize("C", [16, 64])
+@pytest.mark.parametrize("gates", [(0.0, 0.0), (3.0, -2.0), (-4.0, 3.0)])
+def test_autograd_of_chunkwise_form_equals_chain_rule_of_recurrence(C, gates):
+    """Two independent routes to the same gradients: O3 (hand chain rule, token recurrence) and O4
+    (autograd, chunkwise WY form with one inverse), over several chunks and a ragged tail."""
+    p, d_out, d_state = random_chain(60, T=150, K=6, V=5, a_mean=gates[0], b_mean=gates[1])
+    g3 = chain_grads(p, d_out, d_state, 0.8)
+    g4 = cg.chunkwise_backward(p["q"], p["k"], p["v"], p["a"], p["b"], float(p["A_log"]), float(p["dt_bias"]),
+                               p["S0"], d_out, d_state, C=C, scale=0.8)
+    for name in ("dq", "dk", "dv", "da", "db", "dS0"):
+        ref = np.asarray(g3[name])
+        assert np.max(np.abs(g4[name] - ref)) <= 1e-9 * (1.0 + np.max(np.abs(ref))), name
+    for name in ("dA_log", "ddt_bias"):
+        assert abs(g4[name] - g3[name]) <= 1e-9 * (1.0 + abs(g3[name])), name
+
+
+def test_chunk_boundary_state_gradients_by_exact_linearity():
+    """The gradient of the state entering chunk c, kept by O4, checked against O1: the tail of the
+    loss (tokens from c C on, and the final state) is affine in that state."""
+    C, T = 16, 70
+    p, d_out, d_state = random_chain(61, T=T, K=5, V=4)
+    g4 = cg.chunkwise_backward(p["q"], p["k"], p["v"], p["a"], p["b"], float(p["A_log"]), float(p["dt_bias"]),
+                               p["S0"], d_out, d_state, C=C, keep=True)
+    rng = np.random.default_rng(62)
+    for c in range(len(g4["dS_in"])):
+        t0 = c * C
+        head = dict(p, q=p["q"][:t0], k=p["k"][:t0], v=p["v"][:t0], a=p["a"][:t0], b=p["b"][:t0])
+        S_c = p["S0"] if t0 == 0 else o1_chain(head["q"], head["k"], head["v"], head["a"], head["b"],
+                                               float(p["A_log"]), float(p["dt_bias"]), p["S0"])[1]
+        tail = dict(p, q=p["q"][t0:], k=p["k"][t0:], v=p["v"][t0:], a=p["a"][t0:], b=p["b"][t0:])
+        step = rng.standard_normal(S_c.shape)
+        change = (o1_loss(dict(tail, S0=S_c + step), d_out[t0:], d_state)
+                  - o1_loss(dict(tail, S0=S_c), d_out[t0:], d_state))
+        assert abs(change - float(np.sum(g4["dS_in"][c] * step))) <= 1e-10 * (1.0 + abs(change)), c
+    # U = U~ - W<- S^T: the kept factor gradients follow from dU and the entering state
+    for c in range(len(g4["dU"])):
+        assert np.allclose(g4["dUt"][c], g4["dU"][c], rtol=0, atol=1e-13)
