@@ -269,3 +269,23 @@ def test_chunk_boundary_state_gradients_by_exact_linearity():
     # U = U~ - W<- S^T: the kept factor gradients follow from dU and the entering state
     for c in range(len(g4["dU"])):
         assert np.allclose(g4["dUt"][c], g4["dU"][c], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("C", [16, 64])
+@pytest.mark.parametrize("gates", [(0.0, 0.0), (3.0, -2.0), (-4.0, 3.0)])
+def test_explicit_chunkwise_backward_stage_by_stage(C, gates):
+    """The chunkwise backward written out (reverse sweep of the state gradient, then per-chunk local
+    gradients) equals autograd of the chunkwise form in every per-chunk intermediate and every input
+    gradient, and hence O3."""
+    p, d_out, d_state = random_chain(70, T=150, K=6, V=5, a_mean=gates[0], b_mean=gates[1])
+    args = (p["q"], p["k"], p["v"], p["a"], p["b"], float(p["A_log"]), float(p["dt_bias"]), p["S0"], d_out,
+            d_state)
+    g4 = cg.chunkwise_backward(*args, C=C, scale=0.8, keep=True)
+    gx = cg.chunkwise_backward_explicit(*args, C=C, scale=0.8)
+    for name in ("dW", "dUt", "dU", "dS_in"):
+        for c, (x, y) in enumerate(zip(gx[name], g4[name])):
+            assert np.max(np.abs(x - y)) <= 1e-11 * (1.0 + np.max(np.abs(y))), (name, c)
+    g3 = chain_grads(p, d_out, d_state, 0.8)
+    for name in ("dq", "dk", "dv", "da", "db", "dS0", "dA_log", "ddt_bias"):
+        ref = np.asarray(g3[name])
+        assert np.max(np.abs(np.asarray(gx[name]) - ref)) <= 1e-9 * (1.0 + np.max(np.abs(ref))), name
