@@ -1,6 +1,8 @@
 // gdn_api.cu — host side of the C ABI declared in include/gdn.h: argument checks,
 // workspace carve-up and the launch sequence K0 (schedule) -> K1 (gates) -> K2 (intra) -> K3 (scan)
 // of the prefill call, and the single-token step (slot check -> state update).
+#include <nvtx3/nvToolsExt.h>
+
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -12,6 +14,15 @@
 namespace {
 
 // ---------------------------------------------------------------- instrumentation
+
+// An NVTX range over one entry-point call (host side: argument checks and the enqueue of its
+// kernels), visible in Nsight timelines next to the kernels; a no-op unless a tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 enum KernelId {  // scan: every scan-stage launch
   kKernSchedule = 0, kKernGates = 1, kKernIntra = 2, kKernScan = 3, kKernDecodeCheck = 4, kKernDecode = 5,
   kKernCount = 6
@@ -91,6 +102,7 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
                                 int32_t batch, void* out, int64_t total_tokens, int32_t H, int32_t HV, int32_t K,
                                 int32_t V, int32_t chunk_size, float scale, void* workspace, size_t workspace_bytes,
                                 void* stream) {
+  NvtxRange range("gdn_extend_chunkwise");
   if (batch < 0 || total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || H <= 0 || HV <= 0 || HV % H != 0 ||
       K <= 0 || V <= 0 || chunk_size <= 0)
     return GDN_ERR_INVALID_ARG;
@@ -165,6 +177,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, gdn_dtyp
                            const float* b, const float* A_log, const float* dt_bias, float* state_pool,
                            int64_t pool_size, const int64_t* cache_indices, int32_t batch, void* out, int32_t H,
                            int32_t HV, int32_t K, int32_t V, float scale, int32_t* device_status, void* stream) {
+  NvtxRange range("gdn_decode_step");
   if (batch < 0 || batch > kMaxDecodeBatch || H <= 0 || HV <= 0 || HV % H != 0 || K <= 0 || V <= 0)
     return GDN_ERR_INVALID_ARG;
   if ((int64_t)batch * HV > (int64_t)INT32_MAX) return GDN_ERR_INVALID_ARG;
