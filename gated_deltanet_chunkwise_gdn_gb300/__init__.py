@@ -37,11 +37,19 @@ def gdn_workspace_size(total_tokens: int, batch: int, H: int, HV: int, K: int, V
     return int(_lib.load().gdn_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size))
 
 
-def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    key = (device.index,)
+def _workspace(device: torch.device, stream: torch.cuda.Stream, nbytes: int) -> torch.Tensor:
+    """The cached workspace of (device, stream).
+
+    One buffer per stream: calls on one stream are ordered, so they may share it, while calls
+    on two streams of a device run concurrently and must not. The buffer is allocated on the
+    call's stream, so when it is replaced by a larger one, the caching allocator reuses the old
+    memory only in that stream's order, after the calls already enqueued there.
+    """
+    key = (device.index, stream.cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
+        with torch.cuda.stream(stream):
+            buf = torch.empty(max(nbytes, 256) + 256, dtype=torch.uint8, device=device)
         _ws_cache[key] = buf
     return buf
 
@@ -105,14 +113,16 @@ def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indice
     need = int(L.gdn_workspace_size(T, B, H, HV, K, V, chunk_size))
     if need == 0:
         raise GdnError(2, f"unsupported sizes (K={K}, V={V}, chunk_size={chunk_size}, H={H}, HV={HV})")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    elif not hasattr(stream, "cuda_stream"):
+        stream = torch.cuda.ExternalStream(int(stream), device=dev)
+    sp = stream.cuda_stream
     if workspace is None:
-        ws = _workspace(dev, need)
+        ws = _workspace(dev, stream, need)
         ws_ptr, ws_bytes = _aligned_ptr(ws), ws.numel() - (_aligned_ptr(ws) - ws.data_ptr())
     else:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    if stream is None:
-        stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     dtype_code = _lib.GDN_BF16 if q.dtype == torch.bfloat16 else _lib.GDN_FP16
     st = L.gdn_extend_chunkwise(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype_code,
@@ -188,13 +198,13 @@ def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *,
 
 
 def gdn_get_device_status(device=None, stream=None) -> int:
-    """Status recorded by the last call on ``device`` that used the cached workspace."""
+    """Status recorded by the last call on (``device``, ``stream``) that used the cached workspace."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
-    ws = _ws_cache.get((dev.index,))
-    if ws is None:
-        return 0
     if stream is None:
         stream = torch.cuda.current_stream(dev)
+    ws = _ws_cache.get((dev.index, stream.cuda_stream))
+    if ws is None:
+        return 0
     return int(_lib.load().gdn_get_device_status(_aligned_ptr(ws), stream.cuda_stream))
 
 

@@ -157,9 +157,24 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.fp16 = dtype == GDN_FP16 ? 1 : 0;
 
   int rec = prof_begin(kKernSchedule, s);
-  gdn::schedule_kernel<<<1, 512, 0, s>>>(p, kWyBlock);
+  const bool pre_check = batch > gdn::kScheduleSortMax;
+  if (pre_check) {  // large batch: the multi-block slot check records errors in the zeroed status word
+    gdn::DecodeParams dp{};
+    dp.cache_indices = cache_indices;
+    dp.pool_size = pool_size;
+    dp.B = batch;
+    dp.status = p.status;
+    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_decode_check(dp, s) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  const size_t sched_smem = gdn::schedule_smem_bytes(batch);
+  if (sched_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(gdn::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sched_smem) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::schedule_kernel<<<1, 512, sched_smem, s>>>(p, kWyBlock, pre_check ? 1 : 0);
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
+  prof_end(rec, s, pre_check ? 2 : 1);
   if (total_tokens == 0 || batch == 0) return GDN_OK;
   rec = prof_begin(kKernGates, s);
   if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;

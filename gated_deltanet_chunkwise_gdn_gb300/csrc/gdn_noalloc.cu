@@ -11,7 +11,9 @@
 // reserves it (kNoAllocScratchBytes) for the life of the process. In host code its name is
 // only a host-side stand-in, so the device address is fetched with cudaGetSymbolAddress,
 // once per device, the first time the entry point runs on that device (with the device
-// current). Make that first call before capturing any stream.
+// current). Make that first call before capturing any stream. The address is kept for the
+// life of the process: after cudaDeviceReset (or anything else that destroys the device's
+// primary context) it is stale, so this entry point must not be used on that device again.
 //
 // All calls share the one array and it keeps whatever the last call left there: nothing in
 // it has to start at zero (the first kernel of a call writes every field it later reads).
@@ -55,6 +57,7 @@ gdn_status gdn_extend_chunkwise_noalloc(const void* q, const void* k, const void
                                         int32_t batch, void* out, int64_t total_tokens, int32_t H, int32_t HV,
                                         int32_t K, int32_t V, int32_t chunk_size, float scale, int32_t* device_status,
                                         void* stream) {
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u) != 0) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size);
   if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;  // larger than the built-in scratch
   void* scratch = nullptr;
@@ -64,7 +67,7 @@ gdn_status gdn_extend_chunkwise_noalloc(const void* q, const void* k, const void
       gdn_extend_chunkwise(q, k, v, dtype, a, b, A_log, dt_bias, state_pool, pool_size, cache_indices, cu_seqlens,
                            batch, out, total_tokens, H, HV, K, V, chunk_size, scale, scratch, kNoAllocScratchBytes,
                            stream);
-  if (r != GDN_OK || !device_status) return r;
+  if (r != GDN_OK || !device_status) return r;  // an error return enqueues nothing: *device_status keeps its value
   // The call's device-side status word is the first int32 of the workspace.
   if (cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
                       reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

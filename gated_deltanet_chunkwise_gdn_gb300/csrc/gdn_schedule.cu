@@ -10,29 +10,65 @@ namespace gdn {
 
 namespace {
 constexpr int kThreads = 512;
-constexpr int kOrderMaxBatch = 4096;  // above this, sequences keep their input order
+
+// Sorts the n (a power of two, <= kScheduleSortMax) keys in shared memory ascending; every thread
+// of the block takes part. Bitonic network: log2(n) (log2(n) + 1) / 2 passes of n / 2 exchanges.
+__device__ void bitonic_sort(uint64_t* a, int n) {
+  for (int k = 2; k <= n; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const uint64_t x = a[i], y = a[l];
+          if ((x > y) == ((i & k) == 0)) {
+            a[i] = y;
+            a[l] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
 }
 
-__global__ void __launch_bounds__(kThreads) schedule_kernel(Params p, int C) {
+__host__ __device__ inline int pow2_at_least(int n) {
+  int m = 1;
+  while (m < n) m <<= 1;
+  return m;
+}
+}  // namespace
+
+size_t schedule_smem_bytes(int B) {
+  return B <= kScheduleSortMax ? (size_t)pow2_at_least(B > 0 ? B : 1) * sizeof(uint64_t) : 0;
+}
+
+// pre_checked: the slots were already checked by the multi-block check (batches above
+// kScheduleSortMax), which left GDN_OK or GDN_ERR_BAD_INDEX in the status word.
+__global__ void __launch_bounds__(kThreads) schedule_kernel(Params p, int C, int pre_checked) {
+  extern __shared__ uint64_t s_key[];  // pow2_at_least(B) sort keys (B <= kScheduleSortMax)
   __shared__ int s_err;
   __shared__ int s_warp_sum[kThreads / 32];
   __shared__ int s_total;
   const int tid = threadIdx.x;
   const int B = p.B;
-  if (tid == 0) s_err = 0;
+  const bool sorted = B <= kScheduleSortMax;
+  const int n2 = sorted ? pow2_at_least(B > 0 ? B : 1) : 0;
+  if (tid == 0) s_err = pre_checked ? p.status[0] : 0;
   __syncthreads();
 
-  // 1. validation: monotone cu_seqlens from 0 to T; slots in range and distinct.
+  // 1. validation: monotone cu_seqlens from 0 to T; slots in range and distinct (distinct: the
+  //    sorted slots hold no two equal neighbours).
   if (tid == 0 && (p.cu_seqlens[0] != 0 || p.cu_seqlens[B] != p.T)) atomicCAS(&s_err, 0, GDN_ERR_BAD_SEQLENS);
   for (int i = tid; i < B; i += kThreads) {
     if (p.cu_seqlens[i + 1] < p.cu_seqlens[i]) atomicCAS(&s_err, 0, GDN_ERR_BAD_SEQLENS);
     const int64_t slot = p.cache_indices[i];
     if (slot < 0 || slot >= p.pool_size) atomicCAS(&s_err, 0, GDN_ERR_BAD_INDEX);
-    for (int j = 0; j < i; ++j)
-      if (p.cache_indices[j] == slot) {
-        atomicCAS(&s_err, 0, GDN_ERR_BAD_INDEX);
-        break;
-      }
+  }
+  if (sorted) {
+    for (int i = tid; i < n2; i += kThreads) s_key[i] = i < B ? (uint64_t)p.cache_indices[i] : ~0ull;
+    __syncthreads();
+    bitonic_sort(s_key, n2);
+    for (int i = tid + 1; i < B; i += kThreads)
+      if (s_key[i] == s_key[i - 1]) atomicCAS(&s_err, 0, GDN_ERR_BAD_INDEX);
   }
   __syncthreads();
   if (s_err != 0) {
@@ -95,20 +131,23 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(Params p, int C) {
     p.chunk_tab[j] = make_int4(lo, (int)t0, (int)len, c);
   }
 
-  // 4. longest-first order of sequences (ties by index): the scan's chains start
-  //    with the longest so the tail of the grid is short.
-  for (int i = tid; i < B; i += kThreads) {
-    if (B > kOrderMaxBatch) {
-      p.order[i] = i;
-      continue;
+  // 4. longest-first order of sequences (ties by index): the scan's chains start with the
+  //    longest so the tail of the grid is short. Key: (INT32_MAX - length, index), sorted.
+  if (sorted) {
+    __syncthreads();
+    for (int i = tid; i < n2; i += kThreads) {
+      uint64_t key = ~0ull;
+      if (i < B) {
+        const int64_t len = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
+        key = ((uint64_t)(INT32_MAX - len) << 32) | (uint32_t)i;
+      }
+      s_key[i] = key;
     }
-    const int64_t li = p.cu_seqlens[i + 1] - p.cu_seqlens[i];
-    int rank = 0;
-    for (int j = 0; j < B; ++j) {
-      const int64_t lj = p.cu_seqlens[j + 1] - p.cu_seqlens[j];
-      rank += (lj > li) || (lj == li && j < i);
-    }
-    p.order[rank] = i;
+    __syncthreads();
+    bitonic_sort(s_key, n2);
+    for (int r = tid; r < B; r += kThreads) p.order[r] = (int)(uint32_t)s_key[r];
+  } else {
+    for (int i = tid; i < B; i += kThreads) p.order[i] = i;
   }
   if (tid == 0) {
     p.status[1] = n_chunks;

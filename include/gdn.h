@@ -133,13 +133,17 @@ GDN_API gdn_status gdn_extend_chunkwise(const void *q, const void *k, const void
  * 64 MiB, reserved on every GPU that loads the library until the process exits. Calls
  * whose gdn_workspace_size(...) exceeds 64 MiB return GDN_ERR_WORKSPACE before touching
  * anything. It calls no allocator. The first call on each device looks up the scratch
- * address on that device (make it before capturing any stream). All calls share the
- * scratch and it keeps the last call's contents; calls that overlap on the GPU (e.g. on
- * two streams at once) race on it and must not be issued.
+ * address on that device (make it before capturing any stream); the address is kept until
+ * the process exits, so after cudaDeviceReset on a device this entry point must not be
+ * used there again. All calls share the scratch and it keeps the last call's contents;
+ * calls that overlap on the GPU (e.g. on two streams at once) race on it and must not be
+ * issued.
  *
- * device_status: optional DEVICE pointer to one int32. When not NULL, the status the
- * call's first kernel records (GDN_OK, GDN_ERR_BAD_INDEX, GDN_ERR_BAD_SEQLENS) is copied
- * there, in stream order, after the call's kernels.
+ * device_status: optional DEVICE pointer to one int32, 4-byte aligned (else
+ * GDN_ERR_INVALID_ARG). When not NULL and the call returns GDN_OK, the status the call's
+ * kernels record (GDN_OK, GDN_ERR_BAD_INDEX, GDN_ERR_BAD_SEQLENS, GDN_ERR_TIMEOUT) is
+ * copied there, in stream order, after the call's kernels. A call that returns an error
+ * enqueues nothing and leaves *device_status unwritten.
  */
 GDN_API gdn_status gdn_extend_chunkwise_noalloc(const void *q, const void *k, const void *v, gdn_dtype dtype,
                                                 const float *a, const float *b, const float *A_log,

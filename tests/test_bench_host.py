@@ -47,11 +47,16 @@ def test_source_hash_ignores_comments_and_whitespace():
     assert bench._code_only('char* s = "// kept";') == 'char*s="// kept";'
 
 
-def test_committed_traffic_matches_current_sources():
+def test_committed_traffic_is_reported_only_for_the_sources_it_was_taken_on():
+    """A committed DRAM figure is reported while its kernel's code hash matches, else null."""
     tab = json.load(open(os.path.join(ROOT, "profiles", "dram_traffic.json")))
     for workload, kernels in tab.items():
         for kernel, ent in kernels.items():
-            assert bench.measured_traffic(kernel, workload) == ent["dram_bytes_per_launch"], (workload, kernel)
+            got = bench.measured_traffic(kernel, workload)
+            if ent["source_hash"] == bench.kernel_source_hash(kernel):
+                assert got == ent["dram_bytes_per_launch"], (workload, kernel)
+            else:
+                assert got is None, (workload, kernel)
 
 
 @pytest.mark.timeout(300)
