@@ -78,8 +78,26 @@ def load(build_if_missing: bool = True):
         L.gdn_launch_count.restype = i64
         L.gdn_version.argtypes = []
         L.gdn_version.restype = i32
+        L.gdn_workspace_layout.argtypes = [i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(WorkspaceLayout)]
+        L.gdn_workspace_layout.restype = ctypes.c_int
+        L.gdn_test_set_stall.argtypes = [i32, i64]
+        L.gdn_test_set_stall.restype = ctypes.c_int
         _lib = L
         return L
+
+
+class WorkspaceLayout(ctypes.Structure):
+    """gdn_workspace_layout_t of include/gdn.h (byte offsets of the per-chunk intermediates)."""
+    _fields_ = [(n, ctypes.c_size_t) for n in ("status", "chunk_tab", "g", "beta", "rq", "rk", "ks", "w", "u", "p",
+                                                "total")] + [
+        ("max_chunks", ctypes.c_int64), ("block", ctypes.c_int32), ("affine_factors", ctypes.c_int32)]
+
+
+def workspace_layout(total_tokens: int, batch: int, H: int, HV: int, K: int, V: int, chunk_size: int):
+    lay = WorkspaceLayout()
+    check(load().gdn_workspace_layout(total_tokens, batch, H, HV, K, V, chunk_size, ctypes.byref(lay)),
+          "gdn_workspace_layout")
+    return lay
 
 
 def status_string(status: int) -> str:

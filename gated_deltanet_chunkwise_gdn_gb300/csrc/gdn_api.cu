@@ -31,6 +31,12 @@ const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "sca
 
 std::atomic<int64_t> g_launches{0};
 
+// Test hook (gdn_test_set_stall): the wait budget of every bounded device-side wait, and the
+// kernel that withholds its tile loads. Read by each prefill call when it builds its launch
+// arguments.
+std::atomic<long long> g_wait_budget{gdn::kDefaultWaitBudget};
+std::atomic<int> g_stall{gdn::kStallNone};
+
 struct ProfRecord {
   int id;
   cudaEvent_t start, stop;
@@ -155,6 +161,8 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.nseg = L.nseg;
   p.seg_r16 = K == 128 ? 8 : 16;  // K = V = 128: a full-mode chunk costs about twice a map-mode chunk
   p.fp16 = dtype == GDN_FP16 ? 1 : 0;
+  p.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
+  p.stall = g_stall.load(std::memory_order_relaxed);
 
   int rec = prof_begin(kKernSchedule, s);
   const bool pre_check = batch > gdn::kScheduleSortMax;
@@ -245,6 +253,37 @@ gdn_status gdn_get_device_status(const void* workspace, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   if (st < 0 || st > GDN_ERR_BAD_SEQLENS) return GDN_ERR_CUDA;
   return static_cast<gdn_status>(st);
+}
+
+gdn_status gdn_workspace_layout(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K, int32_t V,
+                                int32_t chunk_size, gdn_workspace_layout_t* out) {
+  if (!out) return GDN_ERR_INVALID_ARG;
+  if (gdn_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size) == 0) return GDN_ERR_UNSUPPORTED;
+  const gdn::WsLayout L = gdn::make_layout(total_tokens, batch, H, HV, K, V, kWyBlock);
+  out->status = L.status;
+  out->chunk_tab = L.chunk_tab;
+  out->g = L.g;
+  out->beta = L.beta;
+  out->rq = L.rq;
+  out->rk = L.rk;
+  out->ks = K == 128 ? L.ks : (size_t)-1;
+  out->w = L.w;
+  out->u = L.u;
+  out->p = L.p;
+  out->total = L.total;
+  out->max_chunks = L.max_chunks;
+  out->block = kWyBlock;
+  out->affine_factors = K == 128 ? 1 : 0;
+  return GDN_OK;
+}
+
+gdn_status gdn_test_set_stall(int32_t kernel, int64_t wait_budget_cycles) {
+  if (kernel < gdn::kStallNone || kernel > gdn::kStallAffineScan || wait_budget_cycles <= 0)
+    return GDN_ERR_INVALID_ARG;
+  g_wait_budget.store(kernel == gdn::kStallNone ? gdn::kDefaultWaitBudget : wait_budget_cycles,
+                      std::memory_order_relaxed);
+  g_stall.store(kernel, std::memory_order_relaxed);
+  return GDN_OK;
 }
 
 const char* gdn_status_string(gdn_status status) {

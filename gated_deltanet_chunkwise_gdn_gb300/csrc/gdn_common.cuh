@@ -173,7 +173,13 @@ struct Params {
   int nseg;  // segments per sequence in the scan (1: one pass over each whole sequence)
   int seg_r16;  // length of segment 0 relative to the others, in 16ths (see seg_range)
   int fp16;  // q, k, v, out (and the workspace factors) hold fp16 elements, else bf16
+  long long wait_budget;  // clock cycles before a bounded mbarrier wait gives up
+  int stall;  // test hook (gdn_test_set_stall): kernel whose CTAs withhold their tile loads, 0 = none
 };
+
+// Kernels a test can make stall (their producers issue no tile load, so every wait runs out).
+enum StallKernel : int { kStallNone = 0, kStallIntra = 1, kStallScan = 2, kStallAffineScan = 3 };
+constexpr long long kDefaultWaitBudget = 1ll << 31;  // about one second at the SM clock
 
 // ----------------------------------------------------------------------------- device helpers
 

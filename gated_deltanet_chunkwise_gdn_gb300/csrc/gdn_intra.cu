@@ -36,7 +36,6 @@ namespace {
 
 constexpr int C = 64;
 constexpr int kThreads = 256;  // 8 warps; warps w and w+4 share TMEM lanes 32(w%4)..+31
-constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
 
 template <int D>
 struct IntraSmem {
@@ -62,37 +61,89 @@ __host__ __device__ constexpr uint32_t tmem_cols() { return D < 256 ? 256u : 512
 
 
 // The one triangular inverse: X = (I + L)^{-1} for L strictly lower 64 x 64 (fp32, pitch LDF),
-// in 16 x 16 blocks, fp32 throughout ("Simple math to speed up GDN prefill", section "Save
-// one invert": M^{-1} by blocked forward substitution).
+// in 16 x 16 blocks ("Simple math to speed up GDN prefill", section "Save one invert": M^{-1}
+// by blocked forward substitution).
 //
-// Diagonal blocks: X_II = (I + L_II)^{-1} by a column sweep, one lane per column, two blocks
-// per warp (diag_blocks). Off-diagonal blocks by the 2 x 2 block rule on 32-row halves
-// [X_A 0; X_CA X_C] with X_CA = -X_C L_CA X_A:
-//   stage 1: X_10 = -X_11 (L_10 X_00),  X_32 = -X_33 (L_32 X_22)         (X_A and X_C)
-//   stage 2: T = L_CA X_A   (T_pq = sum_{K=q..1} L_{2+p,K} X_{K,q})
-//   stage 3: X_{2+p,q} = -sum_{m<=p} X_{2+p,2+m} T_{m,q}
-// Every product is split over a pair of warps by output rows (8 each); a lane forms 4
-// outputs of one row as plain fp32 FMAs, reading its A row and each B row as float4.
+// Diagonal blocks: X_II = (I + L_II)^{-1} by a column sweep in fp32, one lane per column, two
+// blocks per warp (diag_blocks). Off-diagonal blocks by the 2 x 2 block rule on 32-row halves
+// [X_A 0; X_CA X_C] with X_CA = -X_C L_CA X_A, every product on the tensor cores as warp-level
+// 16 x 8 x 16 MMAs (offdiag_blocks):
+//   stage 1 (warps 0, 1):    X_10 = -(X_11 L_10) X_00,   X_32 = -(X_33 L_32) X_22
+//   stage 2 (warps 0-3, p, q): Y_p = sum_{m<=p} X_{2+p,2+m} L_{2+m, 0..1}   (row block p of X_C L_CA)
+//                              X_{2+p,q} = -sum_{m>=q} Y_{p,m} X_{m,q}
+// The left factor of each second product is the first product's accumulator, which is already
+// laid out as an A operand, so the intermediates stay in registers. Each fp32 operand is split
+// into bf16 hi + lo and a product takes hi*hi + hi*lo + lo*hi (about 16 bits), so the blocks
+// come out with the accuracy of the fp32 substitution they replace.
 
-// acc (+)= A[r][0..15] . B[0..15][c0 .. c0+3]  (A, B: top-left of 16 x 16 fp32 blocks)
-template <int LDA, int LDB>
-__device__ __forceinline__ void mm_piece(float (&acc)[4], const float* A, const float* B, int r, int c0) {
-  float a[16];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) *reinterpret_cast<float4*>(a + 4 * q) = *reinterpret_cast<const float4*>(A + r * LDA + 4 * q);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float4 b = *reinterpret_cast<const float4*>(B + k * LDB + c0);
-    acc[0] = fmaf(a[k], b.x, acc[0]);
-    acc[1] = fmaf(a[k], b.y, acc[1]);
-    acc[2] = fmaf(a[k], b.z, acc[2]);
-    acc[3] = fmaf(a[k], b.w, acc[3]);
-  }
+// Warp-level D(16 x 8) += A(16 x 16) B(16 x 8), bf16 operands, fp32 accumulation.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// A 16 x 16 operand as bf16 hi + lo fragments (lane: rows lane/4 (+8), column pairs 2(lane%4) (+8)).
+struct AFrag {
+  uint32_t hi[4], lo[4];
+};
+// B operand (16 x 16: k rows, two 8-column n tiles) as bf16 hi + lo fragments.
+struct BFrag {
+  uint32_t hi[2][2], lo[2][2];
+};
+
 template <int LD>
-__device__ __forceinline__ void store_piece(float* dst, int r, int c0, const float (&acc)[4], float sign) {
-  *reinterpret_cast<float4*>(dst + r * LD + c0) = make_float4(sign * acc[0], sign * acc[1], sign * acc[2], sign * acc[3]);
+__device__ __forceinline__ AFrag load_a(const float* A) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, c = 2 * (lane & 3);
+  AFrag f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 x = *reinterpret_cast<const float2*>(A + (r + 8 * (u & 1)) * LD + c + 8 * (u >> 1));
+    split2<bf16>(x.x, x.y, f.hi[u], f.lo[u]);
+  }
+  return f;
+}
+template <int LD>
+__device__ __forceinline__ BFrag load_b(const float* B) {
+  const int lane = threadIdx.x & 31, n = lane >> 2, k = 2 * (lane & 3);
+  BFrag f;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const float* b = B + (k + 8 * u) * LD + 8 * nt + n;
+      split2<bf16>(b[0], b[LD], f.hi[nt][u], f.lo[nt][u]);
+    }
+  return f;
+}
+// The accumulator pair of a 16 x 16 product (n tiles 0 and 1) as the A operand of the next one.
+__device__ __forceinline__ AFrag acc_as_a(const float (&d)[2][4]) {
+  AFrag f;
+  split2<bf16>(d[0][0], d[0][1], f.hi[0], f.lo[0]);
+  split2<bf16>(d[0][2], d[0][3], f.hi[1], f.lo[1]);
+  split2<bf16>(d[1][0], d[1][1], f.hi[2], f.lo[2]);
+  split2<bf16>(d[1][2], d[1][3], f.hi[3], f.lo[3]);
+  return f;
+}
+// d (16 x 16, two n tiles) += a b with the three-term split.
+__device__ __forceinline__ void mma3(float (&d)[2][4], const AFrag& a, const BFrag& b) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    mma16816(d[nt], a.hi, b.hi[nt][0], b.hi[nt][1]);
+    mma16816(d[nt], a.hi, b.lo[nt][0], b.lo[nt][1]);
+    mma16816(d[nt], a.lo, b.hi[nt][0], b.hi[nt][1]);
+  }
+}
+template <int LD>
+__device__ __forceinline__ void store_neg(float* dst, const float (&d)[2][4]) {
+  const int lane = threadIdx.x & 31, r = lane >> 2, c = 2 * (lane & 3);
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2*>(dst + r * LD + 8 * nt + c) = make_float2(-d[nt][0], -d[nt][1]);
+    *reinterpret_cast<float2*>(dst + (r + 8) * LD + 8 * nt + c) = make_float2(-d[nt][2], -d[nt][3]);
+  }
 }
 
 // Diagonal blocks 2 w and 2 w + 1 (w = 0, 1): lanes 0-15 and 16-31 each solve one block.
@@ -112,41 +163,36 @@ __device__ __forceinline__ void diag_blocks(const float* Lf, float* Xf, int w) {
   for (int i = 0; i < 16; ++i) Xf[(b + i) * LDF + b + c] = x[i];
 }
 
-// Off-diagonal blocks, all 8 warps; the diagonal blocks are in Xf. scratch: 1152 + 640
-// floats, free shared memory. Ends with a block barrier.
+// Off-diagonal blocks (warps 0-3 work, the others pass straight to the closing barrier); the
+// diagonal blocks are in Xf. Ends with a block barrier.
 template <int LDF>
-__device__ void offdiag_blocks(const float* Lf, float* Xf, float* scratch) {
-  constexpr int LT2 = 36, LT1 = 20;  // pitches of the scratch products (16-byte rows)
-  float* T2 = scratch;               // 32 x LT2: T = L_CA X_A
-  float* T1 = scratch + 32 * LT2;    // 2 x (16 x LT1): stage-1 partial products
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int task = warp >> 1;
-  const int r = 8 * (warp & 1) + (lane >> 2), c0 = 4 * (lane & 3);
-  auto blk = [&](auto* M, int I, int J) { return M + 16 * I * LDF + 16 * J; };
-  // stage 1 (warps 0-3): task 0 -> X_10, task 1 -> X_32
-  if (task < 2) {
-    const int I = 1 + 2 * task;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    mm_piece<LDF, LDF>(acc, blk(Lf, I, I - 1), blk(Xf, I - 1, I - 1), r, c0);
-    store_piece<LT1>(T1 + task * 16 * LT1, r, c0, acc, 1.f);
-    tc::named_sync(4 + task, 64);  // the warp pair's partial product is complete
-    float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-    mm_piece<LDF, LT1>(acc2, blk(Xf, I, I), T1 + task * 16 * LT1, r, c0);
-    store_piece<LDF>(blk(Xf, I, I - 1), r, c0, acc2, -1.f);
+__device__ void offdiag_blocks(const float* Lf, float* Xf) {
+  const int warp = threadIdx.x >> 5;
+  auto blk = [&](const float* M, int I, int J) { return M + 16 * I * LDF + 16 * J; };
+  if (warp < 2) {  // stage 1: X_{I,I-1}, I = 1 + 2 warp
+    const int I = 1 + 2 * warp;
+    float t[2][4] = {}, x[2][4] = {};
+    mma3(t, load_a<LDF>(blk(Xf, I, I)), load_b<LDF>(blk(Lf, I, I - 1)));
+    mma3(x, acc_as_a(t), load_b<LDF>(blk(Xf, I - 1, I - 1)));
+    store_neg<LDF>(Xf + 16 * I * LDF + 16 * (I - 1), x);
   }
-  __syncthreads();
-  {  // stage 2: T_pq, p = task >> 1, q = task & 1
-    const int p = task >> 1, q = task & 1;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int K = q; K < 2; ++K) mm_piece<LDF, LDF>(acc, blk(Lf, 2 + p, K), blk(Xf, K, q), r, c0);
-    store_piece<LT2>(T2 + 16 * p * LT2 + 16 * q, r, c0, acc, 1.f);
-  }
-  __syncthreads();
-  {  // stage 3: X_{2+p,q}
-    const int p = task >> 1, q = task & 1;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int m = 0; m <= p; ++m) mm_piece<LDF, LT2>(acc, blk(Xf, 2 + p, 2 + m), T2 + 16 * m * LT2 + 16 * q, r, c0);
-    store_piece<LDF>(blk(Xf, 2 + p, q), r, c0, acc, -1.f);
+  if (warp < 4) {
+    tc::named_sync(4, 128);  // X_10 and X_32 are in place
+    const int p = warp >> 1, q = warp & 1;
+    // Y_{p,m} for m = q..1 (X_{2+p,q} needs Y_{p,q} and Y_{p,1})
+    float y[2][2][4] = {};
+#pragma unroll
+    for (int mm = 0; mm <= p; ++mm) {
+      const AFrag a = load_a<LDF>(blk(Xf, 2 + p, 2 + mm));
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+        if (m >= q) mma3(y[m], a, load_b<LDF>(blk(Lf, 2 + mm, m)));
+    }
+    float x[2][4] = {};
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+      if (m >= q) mma3(x, acc_as_a(y[m]), load_b<LDF>(blk(Xf, m, q)));
+    store_neg<LDF>(Xf + 16 * (2 + p) * LDF + 16 * q, x);
   }
   __syncthreads();
 }
@@ -162,8 +208,8 @@ __device__ __forceinline__ void load_gates(const Params& p, int64_t jh, float* s
 }
 
 // All threads: bounded wait; every thread leaves with the same verdict.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* status) {
-  const bool ok = tc::mbar_wait(bar, parity, kWaitBudget);
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* status, long long budget) {
+  const bool ok = tc::mbar_wait(bar, parity, budget);
   const bool all = __syncthreads_and(ok);
   if (!all && threadIdx.x == 0) set_status(status, GDN_ERR_TIMEOUT);
   return all;
@@ -246,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   if (tid == 0) {
     const int first = atomicAdd(&p.status[2], 1);
     *s_next = first;
-    if (first < n_items) fetch_item(first, p.chunk_tab[first / p.H]);
+    if (first < n_items && p.stall != kStallIntra) fetch_item(first, p.chunk_tab[first / p.H]);
   }
   __syncthreads();
   int item = *s_next;
@@ -257,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     const int j = item / p.H, h = item % p.H;
     const int hv0 = h * r_heads;
 
-    ok = wait_all(&bar[0], ph0 & 1, p.status);
+    ok = wait_all(&bar[0], ph0 & 1, p.status, p.wait_budget);
     ++ph0;
     if (!ok) break;
     const int4 ct = *s_ct;
@@ -276,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
       tc::mma_commit(&bar[2]);
     }
     if (kTmaStore && tid == 0) tc::bulk_wait_read();  // the previous item's staged W<-, U~ have been read
-    ok = wait_all(&bar[2], ph2 & 1, p.status);
+    ok = wait_all(&bar[2], ph2 & 1, p.status, p.wait_budget);
     ++ph2;
     if (!ok) break;
     float kq[32];  // columns [32*half, 32*half+32) of this row of K K^T (rows 0-63) or Q K^T (64-127)
@@ -392,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         }
       }
       __syncthreads();
-      offdiag_blocks<LDF>(Lf, Xf, reinterpret_cast<float*>(smem + SM::AA));  // scratch: the [A'; A] tile, not yet written
+      offdiag_blocks<LDF>(Lf, Xf);
       // L is dead from here on: its buffer takes the low 16-bit parts of [A'; A]
       {  // A' rows (rows 0-63) and A rows (rows 64-127) as 16-bit hi + lo, 128-byte swizzled K-major.
          // Thread (i, qc) forms columns 16 qc .. 16 qc + 15 of row i of both A' and A, so each X element
@@ -443,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         }
       }
       tc::fence_async_smem();
-      ok = wait_all(&bar[1], ph1 & 1, p.status);  // its barrier also publishes [A'; A] to the MMA issuer
+      ok = wait_all(&bar[1], ph1 & 1, p.status, p.wait_budget);  // its barrier also publishes [A'; A] to the MMA issuer
       ++ph1;
       if (!ok) break;
       // thread 32 claims the next item while the MMAs below run, so the atomic's round trip stays off
@@ -474,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
                            (part | ks) != 0);
         tc::mma_commit(&bar[2]);
       }
-      ok = wait_all(&bar[2], ph2 & 1, p.status);
+      ok = wait_all(&bar[2], ph2 & 1, p.status, p.wait_budget);
       ++ph2;
       if (!ok) break;
       tc::fence_after_sync();

@@ -44,7 +44,6 @@ namespace {
 
 constexpr int C = 64;
 constexpr int VB = 64;
-constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
 // warps 0-7 chain workers (warps w and w+4 share TMEM lanes 32(w%4)..+31 and split the
 // columns), warps 8-9 outputs (TMEM lanes 0-63), warp 10 TMA producer, warp 11 MMA issuer
 constexpr int kChain = 256, kOut = 64;
@@ -163,11 +162,11 @@ __device__ bool decode_job(const Params& p, int kind, int nseg, ScanJob& job) {
 }
 
 // Bounded mbarrier wait that also gives up as soon as another role reported a failure.
-__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail) {
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail, long long budget) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!tc::mbar_try_wait(bar, parity)) {
-    if (*fail || clock64() - t0 > kWaitBudget) return false;
+    if (*fail || clock64() - t0 > budget) return false;
   }
   return true;
 }
@@ -234,10 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer: TMA
-    if (lane == 0) {
+    if (lane == 0 && p.stall != kStallScan) {
       for (int c = 0; c < nc; ++c) {
         const int s = c % S, use = c / S;
-        if (use > 0 && !wait_or_fail(&empty[s], (use - 1) & 1, fail)) {
+        if (use > 0 && !wait_or_fail(&empty[s], (use - 1) & 1, fail, p.wait_budget)) {
           report();
           break;
         }
@@ -282,15 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nc && ok; ++c) {
         const int s = c % S;
         const uint32_t so = (uint32_t)(s * SM::STAGE) >> 4;  // stage offset in descriptor units
-        ok = wait_or_fail(&full[s], (c / S) & 1, fail);
+        ok = wait_or_fail(&full[s], (c / S) & 1, fail, p.wait_budget);
         // MMA1: D1[slot] = [Q; W<-] S^T, once the chain's 16-bit S^T of chunk c-1 is written and
         // the output warps are done with the slot
         for (int ch = 0; ch < NCH && ok; ++ch) {
           const int slot = NCH == 1 ? (c & 1) : ch;
           const int use = NCH == 1 ? (c >> 1) : c;
           const uint32_t co = (uint32_t)(ch * SM::CH) >> 4;
-          ok = wait_or_fail(&sready[ch], c & 1, fail);
-          if (ok && full_mode && use >= 1) ok = wait_or_fail(&odone[slot], (use - 1) & 1, fail);
+          ok = wait_or_fail(&sready[ch], c & 1, fail, p.wait_budget);
+          if (ok && full_mode && use >= 1) ok = wait_or_fail(&odone[slot], (use - 1) & 1, fail, p.wait_budget);
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
@@ -305,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < NCH && ok; ++ch) {
           const int slot = NCH == 1 ? (c & 1) : ch;
           const uint32_t co = (uint32_t)(ch * SM::CH) >> 4;
-          ok = wait_or_fail(&uready[ch], c & 1, fail);
+          ok = wait_or_fail(&uready[ch], c & 1, fail, p.wait_budget);
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
@@ -345,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ch = 0; ch < NCH; ++ch) {
           const int slot = NCH == 1 ? (c & 1) : ch;
           const int use = NCH == 1 ? (c >> 1) : c;
-          if (!wait_or_fail(&mmao[slot], use & 1, fail)) {
+          if (!wait_or_fail(&mmao[slot], use & 1, fail, p.wait_budget)) {
             report();
             bad = true;
             break;
@@ -453,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // bounded wait with one verdict per warp (the warp then stays converged)
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
-      const bool ok = wait_or_fail(bar, parity, fail);
+      const bool ok = wait_or_fail(bar, parity, fail, p.wait_budget);
       return __all_sync(0xffffffffu, ok);
     };
     if (u_row && use_ut) fetch_ut(0);
@@ -662,7 +661,7 @@ __global__ void __launch_bounds__(256) combine_bulk_kernel(Params p, int nseg) {
   const int c = tid % D, r0 = (tid / D) * RPT;  // column and first row of this thread
   for (int seg = 1; seg <= ns - 2; ++seg) {
     const int b = (seg - 1) & 1;
-    if (!__syncthreads_and(tc::mbar_wait(&bar[b], ((seg - 1) >> 1) & 1, 1ll << 31))) {
+    if (!__syncthreads_and(tc::mbar_wait(&bar[b], ((seg - 1) >> 1) & 1, p.wait_budget))) {
       if (tid == 0) set_status(p.status, GDN_ERR_TIMEOUT);
       return;
     }

@@ -51,7 +51,6 @@ namespace {
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr long long kWaitBudget = 1ll << 31;  // clock cycles before a wait gives up (~1 s)
 constexpr int kThreads = 832;
 constexpr int kChainWarps = 16;  // 4 per TMEM lane quarter, 32 state columns each
 constexpr int kPrepWarp0 = 16, kXWarp0 = 20, kProducerWarp = 24, kMmaWarp = 25;
@@ -161,11 +160,11 @@ __device__ bool decode_job(const Params& p, int nseg, Job& job) {
 }
 
 // Bounded mbarrier wait that also gives up as soon as another role reported a failure.
-__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail) {
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* fail, long long budget) {
   if (tc::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!tc::mbar_try_wait(bar, parity)) {
-    if (*fail || clock64() - t0 > kWaitBudget) return false;
+    if (*fail || clock64() - t0 > budget) return false;
   }
   return true;
 }
@@ -248,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // bounded wait with one verdict per warp (the warp then stays converged)
   auto wait_warp = [&](int b, uint32_t parity) {
-    const bool ok = wait_or_fail(&bars[b], parity, fail);
+    const bool ok = wait_or_fail(&bars[b], parity, fail, p.wait_budget);
     return __all_sync(0xffffffffu, ok);
   };
   // a warp's shared-memory writes (and TMEM reads) are complete: arrive on barrier b
@@ -265,9 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       bool ok = true;
       int issued = 0;
-      for (int c = 0; c < nc && ok; ++c) {
+      for (int c = 0; c < nc && ok && p.stall != kStallAffineScan; ++c) {
         const int s = c & 1;
-        if (c >= 2 && !(ok = wait_or_fail(&bars[kEmpty0 + s], ((c >> 1) - 1) & 1, fail))) break;
+        if (c >= 2 && !(ok = wait_or_fail(&bars[kEmpty0 + s], ((c >> 1) - 1) & 1, fail, p.wait_budget))) break;
         const int j = cb + job.c0 + c;
         const int4 ct = p.chunk_tab[j];
         const int64_t jh = (int64_t)j * p.HV + hv;
@@ -302,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) report();
       // no copy outlives the CTA: the last loads of each buffer have landed (bounded)
       for (int c = issued > 2 ? issued - 2 : 0; c < issued; ++c)
-        tc::mbar_wait(&bars[kFull0 + (c & 1)], (c >> 1) & 1, kWaitBudget);
+        tc::mbar_wait(&bars[kFull0 + (c & 1)], (c >> 1) & 1, p.wait_budget);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -326,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto koff = [](int ks, uint32_t block) { return (uint32_t)(((ks >> 2) * block + (ks & 3) * 32) >> 4); };
       bool ok = true;
       auto W8 = [&](int b, uint32_t parity) {
-        if (ok) ok = wait_or_fail(&bars[b], parity, fail);
+        if (ok) ok = wait_or_fail(&bars[b], parity, fail, p.wait_budget);
         return ok;
       };
       auto so = [&](int c) { return (uint32_t)((c & 1) * STG) >> 4; };

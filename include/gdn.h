@@ -199,6 +199,42 @@ GDN_API gdn_status gdn_decode_step(const void *q, const void *k, const void *v, 
  */
 GDN_API gdn_status gdn_get_device_status(const void *workspace, void *stream);
 
+/*
+ * Where one gdn_extend_chunkwise call keeps its per-chunk intermediates in the workspace
+ * (byte offsets from the workspace start), for inspection and tests; the layout belongs to
+ * this library version. For chunk j of the call's chunk table (int32[4] per chunk at
+ * chunk_tab: sequence, first token, length, chunk index in the sequence; chunks restart
+ * at each sequence and hold `block` tokens, the last one fewer), value head hv and q/k head h:
+ *   g    fp32 [.][HV][block]    chunk-local cumulative log decay at (j * HV + hv) * block
+ *   beta fp32 [.][HV][block]    beta, 0 on rows past the chunk's length
+ *   rq, rk fp32 [.][H][block]   1/|q|, 1/|k| at (j * H + h) * block, 0 past the length
+ *   w, u 16-bit [.][HV][block][K or V]  the WY factors W<- and U~ of the chunk
+ *   p    16-bit [.][HV][block][block]   the masked, decayed intra-chunk scores
+ * With affine_factors = 1 (K = V = 128) row t of w and u and column t of p carry the
+ * mantissa m_t of exp(g_last - g_t) / |k_t| = m_t * 2^e_t (rows times m_t, columns divided by
+ * it) and ks (fp32, like g) holds 2^e_t; otherwise ks is (size_t)-1 and the factors are
+ * unscaled. Returns GDN_ERR_UNSUPPORTED for sizes gdn_workspace_size rejects.
+ */
+typedef struct {
+  size_t status, chunk_tab, g, beta, rq, rk, ks, w, u, p, total;
+  int64_t max_chunks;
+  int32_t block;
+  int32_t affine_factors;
+} gdn_workspace_layout_t;
+GDN_API gdn_status gdn_workspace_layout(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K,
+                                        int32_t V, int32_t chunk_size, gdn_workspace_layout_t *out);
+
+/*
+ * Test hook for the failure path of the bounded device-side waits; never needed in use.
+ * kernel = 1 (the intra-chunk kernel), 2 (the chunk scan) or 3 (the first pass of the
+ * segmented scan for K = V = 128) makes that kernel's CTAs issue none of their tile loads in
+ * later gdn_extend_chunkwise calls, so every wait in them runs out after wait_budget_cycles
+ * SM clock cycles: the call then records GDN_ERR_TIMEOUT, leaves state_pool untouched and
+ * every kernel exits normally. kernel = 0 restores normal operation and the default budget
+ * (2^31 cycles, about a second). Process-wide; not to be changed while calls are in flight.
+ */
+GDN_API gdn_status gdn_test_set_stall(int32_t kernel, int64_t wait_budget_cycles);
+
 /* Static, human-readable name of a status. Never NULL. */
 GDN_API const char *gdn_status_string(gdn_status status);
 

@@ -76,6 +76,21 @@ def n_inverse_two_ways(kn: np.ndarray, log_alpha: np.ndarray, beta: np.ndarray):
     return np.linalg.inv(N), Gam * np.linalg.inv(M)
 
 
+def chunk_factors(qn, kn, v, log_alpha, beta):
+    """The per-chunk quantities of the page-4 form, for one chunk (rows = its tokens).
+
+    Returns a dict with g = cumsum(log alpha) (chunk-local), Minv = M^{-1},
+    A = N^{-1} B = (Gamma . M^{-1}) diag(beta) ("Save one invert"), W<- = A G K,
+    U~ = A V and P = Gamma . tril(Q K^T), the masked, decayed scores of the output
+    ("Reminder"): the same arithmetic as one iteration of :func:`chunkwise_forward`.
+    """
+    g = np.cumsum(log_alpha)
+    Gam = decay_matrix(g)
+    Minv = np.linalg.inv(gram_factors(kn, beta))
+    A = (Gam * Minv) * beta[None, :]
+    return dict(g=g, Minv=Minv, A=A, W=A @ (np.exp(g)[:, None] * kn), U=A @ v, P=Gam * (qn @ kn.T))
+
+
 def chunkwise_forward(qn, kn, v, log_alpha, beta, S0, C, scale=1.0, inverses=1):
     """Page-4 chunkwise WY form in log space.
 

@@ -41,28 +41,45 @@ def oracle_for(d: dict, chains=None, scale=1.0):
                               is_fp16=d["q"].dtype == torch.float16)
 
 
+# A single chain may be up to this many times its whole-tensor tolerance: one norm over a
+# whole call could otherwise hide a chain (or a segment of one) that is wrong.
+CHAIN_FACTOR = 2.0
+
+
 def compare(d: dict, out_gpu: torch.Tensor, pool_gpu: torch.Tensor, res, out_tol=OUT_TOL,
             state_tol=STATE_TOL) -> dict:
-    """Element-by-element comparison of the GPU result with the oracle's chains."""
+    """Element-by-element comparison of the GPU result with the oracle's chains: relative L2
+    over all compared elements, and the same per (sequence, value head) chain."""
     cu = d["cu_seqlens"].numpy()
     idx = d["cache_indices"].numpy()
     og, ro, sg, rs = [], [], [], []
     out_np = out_gpu.float().numpy()
     pool_np = pool_gpu.numpy()
+    worst_out = worst_state = 0.0
+    worst_chain = None
     for i, (s, hv) in enumerate(res.chains):
         t0, t1 = int(cu[s]), int(cu[s + 1])
         og.append(out_np[t0:t1, hv].astype(np.float64).reshape(-1))
         ro.append(res.chain_output(i).reshape(-1))
         sg.append(pool_np[idx[s], hv].astype(np.float64).reshape(-1))
         rs.append(res.states[i].reshape(-1))
+        eo = rel_l2(og[-1], ro[-1]) if t1 > t0 else 0.0
+        es = rel_l2(sg[-1], rs[-1])
+        if eo / out_tol + es / state_tol > worst_out / out_tol + worst_state / state_tol:
+            worst_chain = (int(s), int(hv))
+        worst_out, worst_state = max(worst_out, eo), max(worst_state, es)
     og, ro = np.concatenate(og), np.concatenate(ro)
     sg, rs = np.concatenate(sg), np.concatenate(rs)
     stats = dict(out_rel_l2=rel_l2(og, ro), state_rel_l2=rel_l2(sg, rs),
+                 chain_out_rel_l2=worst_out, chain_state_rel_l2=worst_state, worst_chain=worst_chain,
                  out_finite=bool(np.isfinite(og).all()), state_finite=bool(np.isfinite(sg).all()))
-    print(f"parity: out rel-L2 {stats['out_rel_l2']:.3e}  state rel-L2 {stats['state_rel_l2']:.3e}")
+    print(f"parity: out rel-L2 {stats['out_rel_l2']:.3e}  state rel-L2 {stats['state_rel_l2']:.3e}  "
+          f"worst chain {worst_chain}: out {worst_out:.3e} state {worst_state:.3e}")
     assert stats["out_finite"] and stats["state_finite"], stats
     assert stats["out_rel_l2"] <= out_tol, stats
     assert stats["state_rel_l2"] <= state_tol, stats
+    assert worst_out <= CHAIN_FACTOR * out_tol, stats
+    assert worst_state <= CHAIN_FACTOR * state_tol, stats
     return stats
 
 

@@ -40,6 +40,33 @@ def test_config_long_full():
     compare(d, out, pool, oracle_for(d))
 
 
+def test_config_long_weak_decay_full():
+    """The long prefill with A_log = -7 (log alpha about -6e-4 per token): the state carries
+    across hundreds of chunks, so every segment of the scan starts from a state that matters
+    (10 segments x 16 heads); every chain, every token."""
+    d = wl.make_inputs(wl.BY_NAME["long"])
+    d["A_log"].fill_(-7.0)
+    d["state_pool"].normal_(0.0, 0.1, generator=torch.Generator().manual_seed(99))
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+
+
+def test_exact_linearity_in_state_and_values():
+    """The recurrence is linear in (S0, v): doubling both doubles out and the final state. Every
+    scaling on the GPU path is by a power of two, so the results double bit for bit (the
+    segmented scan is included: 8192 tokens of one head run in segments)."""
+    w = wl.custom("linear", [8192, 300, 1], H=1, HV=2, K=128, V=128, chunk_size=64, seed=31)
+    d = wl.make_inputs(w)
+    out1, pool1 = run_gpu(d)
+    d2 = dict(d)
+    d2["v"] = (d["v"].float() * 2).to(d["v"].dtype)
+    d2["state_pool"] = d["state_pool"] * 2
+    assert torch.equal(d2["v"].float(), d["v"].float() * 2)
+    out2, pool2 = run_gpu(d2)
+    assert torch.equal(out2.float(), out1.float() * 2)
+    assert torch.equal(pool2, pool1 * 2)
+
+
 def test_config_throughput_sampled_chains():
     """B=32 x 8192, H=HV=32: 24 sampled (sequence, head) chains, all their tokens."""
     d = wl.make_inputs(wl.BY_NAME["throughput"])

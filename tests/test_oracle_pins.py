@@ -325,3 +325,33 @@ def test_pins_catch_planted_mistakes(kind, golden_dir):
                            np.array(g["alpha"]), np.array(g["beta"]), np.array(g["S0"]))
     assert (np.max(np.abs(out - np.array(g["out"]))) > 1e-3
             or np.max(np.abs(S - np.array(g["S_final"]))) > 1e-3)
+
+
+def test_chunk_factors_against_independent_routes():
+    """O2's per-chunk factors: W<- against the row recursion, U~ against the direct N^{-1},
+    P entry by entry, and the chunk step built from them against the token recurrence."""
+    rng = np.random.default_rng(7)
+    C, K, V = 12, 6, 5
+    kn = rng.standard_normal((C, K)); kn /= np.linalg.norm(kn, axis=1, keepdims=True)
+    qn = rng.standard_normal((C, K)); qn /= np.linalg.norm(qn, axis=1, keepdims=True)
+    v = rng.standard_normal((C, V))
+    la = -rng.uniform(0.05, 0.8, C)
+    be = rng.uniform(0.1, 0.9, C)
+    f = cw.chunk_factors(qn, kn, v, la, be)
+    g = np.cumsum(la)
+    np.testing.assert_allclose(f["g"], g, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(f["W"], np.exp(g)[:, None] * cw.wy_rows(kn, be), rtol=1e-12, atol=1e-13)
+    Ninv, _ = cw.n_inverse_two_ways(kn, la, be)
+    np.testing.assert_allclose(f["U"], Ninv @ (be[:, None] * v), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(f["Minv"] @ cw.gram_factors(kn, be), np.eye(C), atol=1e-13)
+    for i in range(C):
+        for j in range(C):
+            want = np.exp(g[i] - g[j]) * (qn[i] @ kn[j]) if j <= i else 0.0
+            assert abs(f["P"][i, j] - want) <= 1e-13
+    S0 = rng.standard_normal((V, K))
+    U = f["U"] - f["W"] @ S0.T
+    out = np.exp(g)[:, None] * (qn @ S0.T) + f["P"] @ U
+    S1 = np.exp(g[-1]) * S0 + U.T @ (np.exp(g[-1] - g)[:, None] * kn)
+    ref_out, ref_S = oracle.delta_rule(qn, kn, v, np.exp(la), be, S0)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(S1, ref_S, rtol=1e-11, atol=1e-12)
