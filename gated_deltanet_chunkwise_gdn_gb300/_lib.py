@@ -89,8 +89,9 @@ def load(build_if_missing: bool = True):
 class WorkspaceLayout(ctypes.Structure):
     """gdn_workspace_layout_t of include/gdn.h (byte offsets of the per-chunk intermediates)."""
     _fields_ = [(n, ctypes.c_size_t) for n in ("status", "chunk_tab", "g", "beta", "rq", "rk", "ks", "w", "u", "p",
-                                                "total")] + [
-        ("max_chunks", ctypes.c_int64), ("block", ctypes.c_int32), ("affine_factors", ctypes.c_int32)]
+                                                "seg_state", "seg_map", "total")] + [
+        ("max_chunks", ctypes.c_int64), ("block", ctypes.c_int32), ("affine_factors", ctypes.c_int32),
+        ("nseg", ctypes.c_int32)]
 
 
 def workspace_layout(total_tokens: int, batch: int, H: int, HV: int, K: int, V: int, chunk_size: int):

@@ -270,10 +270,13 @@ gdn_status gdn_workspace_layout(int64_t total_tokens, int32_t batch, int32_t H, 
   out->w = L.w;
   out->u = L.u;
   out->p = L.p;
+  out->seg_state = L.seg_state;
+  out->seg_map = L.seg_map;
   out->total = L.total;
   out->max_chunks = L.max_chunks;
   out->block = kWyBlock;
   out->affine_factors = K == 128 ? 1 : 0;
+  out->nseg = L.nseg;
   return GDN_OK;
 }
 

@@ -213,13 +213,18 @@ GDN_API gdn_status gdn_get_device_status(const void *workspace, void *stream);
  * With affine_factors = 1 (K = V = 128) row t of w and u and column t of p carry the
  * mantissa m_t of exp(g_last - g_t) / |k_t| = m_t * 2^e_t (rows times m_t, columns divided by
  * it) and ks (fp32, like g) holds 2^e_t; otherwise ks is (size_t)-1 and the factors are
- * unscaled. Returns GDN_ERR_UNSUPPORTED for sizes gdn_workspace_size rejects.
+ * unscaled. A scan cut into nseg > 1 segments per sequence keeps, per (sequence b, value
+ * head hv, segment s), the fp32 start state [V][K] at seg_state + ((b * HV + hv) * nseg + s) * V*K*4
+ * and, when nseg > 2, the segment's affine map S_end = S_start T + B0 at seg_map: B0 [V][K] then
+ * T [K][K] at ((b * HV + hv) * nseg + s) * 2 * K*K*4. Returns GDN_ERR_UNSUPPORTED for sizes
+ * gdn_workspace_size rejects.
  */
 typedef struct {
-  size_t status, chunk_tab, g, beta, rq, rk, ks, w, u, p, total;
+  size_t status, chunk_tab, g, beta, rq, rk, ks, w, u, p, seg_state, seg_map, total;
   int64_t max_chunks;
   int32_t block;
   int32_t affine_factors;
+  int32_t nseg;
 } gdn_workspace_layout_t;
 GDN_API gdn_status gdn_workspace_layout(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K,
                                         int32_t V, int32_t chunk_size, gdn_workspace_layout_t *out);

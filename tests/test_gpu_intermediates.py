@@ -116,3 +116,53 @@ def test_intra_factors_match_the_chunkwise_oracle(D):
     print(f"intermediates D={D}: worst per-tile rel-L2 W {worst['W']:.2e} U {worst['U']:.2e} P {worst['P']:.2e}")
     # 16-bit tiles (8-bit mantissa for bf16): about 2e-3 from the final rounding alone
     assert worst["W"] <= 1e-2 and worst["U"] <= 1e-2 and worst["P"] <= 1e-2, worst
+
+
+def _seg_range(n, nseg, r16, part):
+    """Chunk range of segment `part` when a sequence of n chunks is cut into nseg segments, segment 0
+    r16/16 as long as the others (the scan's cut; returns (c0, c1, number of non-empty segments))."""
+    if nseg <= 1 or n <= 0:
+        return (0 if part == 0 else n), n, (1 if n > 0 else 0)
+    den = (nseg - 1) * 16 + r16
+    L0 = min(max(-(-n * r16 // den), 1), n)
+    rest = n - L0
+    L1 = -(-rest // (nseg - 1)) if rest > 0 else 1
+    ns = 1 + -(-rest // L1)
+    if part == 0:
+        return 0, L0, ns
+    c0 = L0 + (part - 1) * L1
+    return min(c0, n), min(c0 + L1, n), ns
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_segment_start_states_match_the_recurrence(D):
+    """A long sequence of one head runs through the segmented scan (per-segment affine maps chained
+    into start states). With weak decay (A_log = -7) each start state carries the whole prefix; it
+    must equal the oracle's state after the prefix, to the state tolerance."""
+    T = 8192
+    w = wl.custom("segstates", [T], H=1, HV=1, K=D, V=D, chunk_size=64, seed=62)
+    d = wl.make_inputs(w)
+    d["A_log"].fill_(-7.0)
+    lay = _lib.workspace_layout(T, 1, 1, 1, D, D, 64)
+    assert lay.nseg > 2
+    ws = torch.zeros(lay.total + 256, dtype=torch.uint8, device="cuda")
+    g = {k: d[k].cuda() for k in INPUT_KEYS}
+    gdn_extend_chunkwise(*[g[k] for k in INPUT_KEYS], chunk_size=64, workspace=ws, check=True)
+    torch.cuda.synchronize()
+    ws = ws.cpu()
+    st = _region(ws, lay.seg_state, lay.nseg * D * D, torch.float32).view(lay.nseg, D, D).double().numpy()
+    n = T // 64
+    r16 = 8 if D == 128 else 16
+    _, _, ns = _seg_range(n, lay.nseg, r16, 0)
+    assert ns == lay.nseg
+    for s in range(1, ns):
+        c0, _, _ = _seg_range(n, lay.nseg, r16, s)
+        t = 64 * c0  # the state entering segment s is the state after the first t tokens
+        dp = dict(d)
+        for k in ("q", "k", "v", "a", "b"):
+            dp[k] = d[k][:t]
+        dp["cu_seqlens"] = torch.tensor([0, t], dtype=torch.int64)
+        ref = oracle.gdn_forward(*[dp[k] for k in INPUT_KEYS]).states[0]
+        err = rel_l2(st[s], ref)
+        print(f"segment {s} of {ns} (token {t}): start-state rel-L2 {err:.3e}")
+        assert err <= 5e-3, (s, err)
