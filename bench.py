@@ -41,7 +41,7 @@ KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indice
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="long",
@@ -109,6 +109,12 @@ class ClockSampler:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) >= 9:
                 self.samples.append((time.time(), parts))
+
+    def wait_first(self, timeout_s: float = 5.0):
+        """Waits until nvidia-smi has delivered a sample (it takes a moment to start)."""
+        t_end = time.time() + timeout_s
+        while self.proc and not self.samples and time.time() < t_end:
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc:
@@ -384,7 +390,9 @@ def run_ours(args, dist):
     # the previous one finishes), so the step time is taken without them; the per-kernel
     # durations come from a second pass over the same steps with the events on.
     sampler = ClockSampler(device_uuid(torch, dev))
-    time.sleep(0.15)
+    sampler.wait_first()
+    for _ in range(max(3, args.warmup)):  # the GPU is busy again when the timed region starts
+        step()
     dist.barrier()
     torch.cuda.synchronize(dev)
     n0 = gdn.launch_count()
