@@ -46,8 +46,8 @@ struct IntraSmem {
   static constexpr int LDF = 68;                        // fp32 tile pitch: conflict-free fragment loads
   static constexpr uint32_t LF = AA + 16384;            // L, fp32 64 x LDF; then the low parts of [A'; A]
   static constexpr uint32_t XF = LF + 64 * LDF * 4;     // M^{-1}, fp32 64 x LDF
-  static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k|, m, 1/m (6 x 64 fp32)
-  static constexpr uint32_t BAR = VEC + 6 * 64 * 4;     // 3 mbarriers + TMEM address
+  static constexpr uint32_t VEC = XF + 64 * LDF * 4;    // g, beta, 1/|q|, 1/|k|, m, 1/m, g log2(e), P's column factor (8 x 64 fp32)
+  static constexpr uint32_t BAR = VEC + 8 * 64 * 4;     // 3 mbarriers + TMEM address
   static constexpr uint32_t bytes = BAR + 96;
   static constexpr uint32_t alloc = bytes + 1024;      // slack to round the base up to 1 KB
 };
@@ -197,11 +197,22 @@ __device__ void offdiag_blocks(const float* Lf, float* Xf) {
   __syncthreads();
 }
 
-// Gates of value head hv for the chunk (from the gates kernel). All threads.
-__device__ __forceinline__ void load_gates(const Params& p, int64_t jh, float* s_g, float* s_beta) {
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the SFU's approximation (relative error about 2^-22); e^(a - b) is ex2(a log2(e) - b log2(e)).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Gates of value head hv for the chunk (from the gates kernel), and g log2(e). All threads.
+__device__ __forceinline__ void load_gates(const Params& p, int64_t jh, float* s_g, float* s_beta, float* s_g2) {
   const int tid = threadIdx.x;
   if (tid < C) {
-    s_g[tid] = p.g[jh * C + tid];
+    const float g = p.g[jh * C + tid];
+    s_g[tid] = g;
+    s_g2[tid] = g * kLog2e;
     s_beta[tid] = p.beta[jh * C + tid];
   }
   __syncthreads();
@@ -250,6 +261,8 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
   float* s_rk = s_rq + C;
   float* s_m = s_rk + C;   // K = V = 128: mantissa m_t of sk_t = exp(g_C - g_t)/|k_t| = m_t 2^e_t
   float* s_im = s_m + C;   // 1/m_t
+  float* s_g2 = s_im + C;  // g log2(e)
+  float* s_cf = s_g2 + C;  // column factor of P: 1/|k_t| (times 1/m_t for K = V = 128)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::BAR);  // [0] q/k tiles + gates, [1] v tile, [2] MMAs
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
   int4* s_ct = reinterpret_cast<int4*>(bar + 4);                // chunk record of the item being fetched
@@ -338,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
         kq[16 + u] = __uint_as_float(r1[u]);
       }
     }
+    if (tid >= 128 && tid < 128 + C) s_g2[tid - 128] = s_g[tid - 128] * kLog2e;
     if (tid < 128) {  // 1/|k| (rows 0-63) and 1/|q| (rows 64-127), 0 on padded rows, from the diagonal of
                       // D1: warp w's columns 32 w .. 32 w + 31 hold it for each lane's row (row = tid)
       float ss = 0.f;
@@ -367,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
     for (int ih = 0; ih < r_heads; ++ih) {
       const int hv = hv0 + ih;
       const int64_t jh = (int64_t)j * p.HV + hv;
-      if (ih > 0) load_gates(p, jh, s_g, s_beta);
+      if (ih > 0) load_gates(p, jh, s_g, s_beta, s_g2);
       if (row < C) {  // warps 0, 1, 4, 5: L = tril(diag(beta) K^K^^T, -1), row i; diagonal blocks of M^{-1}
         const int i = row;
         const float bi = s_beta[i] * s_rk[i];
@@ -401,11 +415,13 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             }
             s_m[r] = m;
             s_im[r] = 1.f / m;
+            s_cf[r] = s_rk[r] * (1.f / m);
             p.ks[jh * C + r] = ks;
           }
           tc::named_sync(3, 128);
         }
-        const float qr = s_rq[r], gr = s_g[r];
+        const float* cf = kAffine ? s_cf : s_rk;
+        const float qr = s_rq[r], gr2 = s_g2[r];
         uint4* prow = reinterpret_cast<uint4*>(p.P + (jh * C + r) * C + cbase);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -414,12 +430,11 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             prow[c] = make_uint4(0u, 0u, 0u, 0u);
             continue;
           }
-          float g8[8], k8[8], m8[8];  // g, 1/|k| and 1/m of columns n0 .. n0+7
+          float g8[8], c8[8];  // g log2(e) and the column factor of columns n0 .. n0+7
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g + n0 + 4 * q);
-            *reinterpret_cast<float4*>(k8 + 4 * q) = *reinterpret_cast<const float4*>(s_rk + n0 + 4 * q);
-            if constexpr (kAffine) *reinterpret_cast<float4*>(m8 + 4 * q) = *reinterpret_cast<const float4*>(s_im + n0 + 4 * q);
+            *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g2 + n0 + 4 * q);
+            *reinterpret_cast<float4*>(c8 + 4 * q) = *reinterpret_cast<const float4*>(cf + n0 + 4 * q);
           }
           uint32_t w[4];
 #pragma unroll
@@ -428,8 +443,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int m = 2 * u + e;
-              float x = __expf(gr - g8[m]) * qr * k8[m] * kq[8 * c + m];
-              if constexpr (kAffine) x *= m8[m];
+              const float x = ex2(gr2 - g8[m]) * (qr * kq[8 * c + m]) * c8[m];
               v[e] = n0 + m <= r ? x : 0.f;
             }
             w[u] = ElemT<E>::pack(v[0], v[1]);
@@ -445,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
          // is loaded once and the exp of A's decay factor is spread over all eight warps.
         const int i = row & 63;
         const int qc = 2 * half + (row >> 6);  // 16-column group of this thread
-        const float gi = s_g[i], egi = expf(gi);
+        const float gi = s_g[i], egi = expf(gi), gi2 = s_g2[i];
         const float mi = kAffine ? s_m[i] : 1.f;  // row scale of W<- and U~
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -459,11 +473,11 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
             *reinterpret_cast<uint4*>(smem + SM::LF + 8192 + o) = z;
             continue;
           }
-          float x8[8], g8[8], b8[8], k8[8];  // X row i, and g, beta, 1/|k| of columns n0 .. n0+7
+          float x8[8], g8[8], b8[8], k8[8];  // X row i, and g log2(e), beta, 1/|k| of columns n0 .. n0+7
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             *reinterpret_cast<float4*>(x8 + 4 * q) = *reinterpret_cast<const float4*>(Xf + i * LDF + n0 + 4 * q);
-            *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g + n0 + 4 * q);
+            *reinterpret_cast<float4*>(g8 + 4 * q) = *reinterpret_cast<const float4*>(s_g2 + n0 + 4 * q);
             *reinterpret_cast<float4*>(b8 + 4 * q) = *reinterpret_cast<const float4*>(s_beta + n0 + 4 * q);
             *reinterpret_cast<float4*>(k8 + 4 * q) = *reinterpret_cast<const float4*>(s_rk + n0 + 4 * q);
           }
@@ -477,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 2) intra_kernel(const __grid_constan
               const float x = nu == i ? 1.f : x8[m];  // entries above the diagonal are never read
               const float xb = x * b8[m] * mi;
               va[e] = nu <= i ? egi * xb * k8[m] : 0.f;          // A'[i][nu] = e^{g_i} X beta_nu / |k_nu| m_i
-              vb[e] = nu <= i ? __expf(gi - g8[m]) * xb : 0.f;   // A[i][nu] = e^{g_i - g_nu} X beta_nu m_i
+              vb[e] = nu <= i ? ex2(gi2 - g8[m]) * xb : 0.f;     // A[i][nu] = e^{g_i - g_nu} X beta_nu m_i
             }
             split2<E>(va[0], va[1], ah[u], al[u]);
             split2<E>(vb[0], vb[1], bh[u], bl[u]);

@@ -134,15 +134,20 @@ def _seg_range(n, nseg, r16, part):
     return min(c0, n), min(c0 + L1, n), ns
 
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_segment_start_states_match_the_recurrence(D):
+@pytest.mark.parametrize("D,decay", [(64, "weak"), (128, "weak"), (128, "strong"), (128, "switch")])
+def test_segment_start_states_match_the_recurrence(D, decay):
     """A long sequence of one head runs through the segmented scan (per-segment affine maps chained
-    into start states). With weak decay (A_log = -7) each start state carries the whole prefix; it
-    must equal the oracle's state after the prefix, to the state tolerance."""
+    into start states), and every segment's start state must equal the oracle's state after the
+    prefix before it, to the state tolerance. Weak decay (A_log = -7): each start state carries the
+    whole prefix. Strong: the default gates. Switch: weak decay for the first half of the sequence
+    and strong after it, so one chain mixes both."""
     T = 8192
     w = wl.custom("segstates", [T], H=1, HV=1, K=D, V=D, chunk_size=64, seed=62)
     d = wl.make_inputs(w)
-    d["A_log"].fill_(-7.0)
+    if decay == "weak":
+        d["A_log"].fill_(-7.0)
+    elif decay == "switch":
+        d["a"][: T // 2] = -12.0  # softplus(-12) ~ 6e-6: almost no decay in the first half
     lay = _lib.workspace_layout(T, 1, 1, 1, D, D, 64)
     assert lay.nseg > 2
     ws = torch.zeros(lay.total + 256, dtype=torch.uint8, device="cuda")

@@ -51,6 +51,18 @@ def test_config_long_weak_decay_full():
     compare(d, out, pool, oracle_for(d))
 
 
+def test_segmented_scan_with_mixed_decay_across_heads():
+    """Two value heads of one long sequence in one call (the segmented scan), one with weak decay
+    (A_log = -7: every segment's start state carries the whole prefix) and one with the default
+    gates; every token of both."""
+    w = wl.custom("mixed", [8192, 200], H=1, HV=2, K=128, V=128, chunk_size=64, seed=33)
+    d = wl.make_inputs(w)
+    d["A_log"][0] = -7.0
+    out, pool = run_gpu(d)
+    compare(d, out, pool, oracle_for(d))
+    untouched_slots_equal(d, pool)
+
+
 def test_exact_linearity_in_state_and_values():
     """The recurrence is linear in (S0, v): doubling both doubles out and the final state. Every
     scaling on the GPU path is by a power of two, so the results double bit for bit (the
