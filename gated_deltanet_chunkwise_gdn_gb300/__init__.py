@@ -13,13 +13,15 @@ shapes, state_pool updated in place, output returned in v's dtype.
 
 from __future__ import annotations
 
+from typing import NamedTuple
+
 import torch
 
 from . import _lib
 from ._lib import GdnError
 
-__all__ = ["gdn_extend_chunkwise", "gdn_decode_step", "gdn_workspace_size", "gdn_get_device_status",
-           "GdnError", "library_path", "version"]
+__all__ = ["gdn_extend_chunkwise", "gdn_decode_step", "gdn_chunkwise_backward", "GdnGrads", "gdn_workspace_size",
+           "gdn_backward_workspace_size", "gdn_get_device_status", "GdnError", "library_path", "version"]
 
 _ws_cache: dict = {}
 _status_cache: dict = {}
@@ -133,6 +135,104 @@ def gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indice
     if check:
         _lib.check(L.gdn_get_device_status(ws_ptr, sp), "gdn_extend_chunkwise (device)")
     return out
+
+
+class GdnGrads(NamedTuple):
+    """Gradients returned by :func:`gdn_chunkwise_backward` (all fp32)."""
+    dq: torch.Tensor            # [T, H, K]
+    dk: torch.Tensor            # [T, H, K]
+    dv: torch.Tensor            # [T, HV, V]
+    da: torch.Tensor            # [T, HV]
+    db: torch.Tensor            # [T, HV]
+    dA_log: torch.Tensor        # [HV]
+    ddt_bias: torch.Tensor      # [HV]
+    d_state_pool: torch.Tensor  # [pool, HV, V, K]: zero except at the batch's slots
+
+
+def gdn_backward_workspace_size(total_tokens: int, batch: int, H: int, HV: int, K: int, V: int,
+                                chunk_size: int) -> int:
+    return int(_lib.load().gdn_backward_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size))
+
+
+def gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, cu_seqlens, d_out,
+                           d_state=None, chunk_size: int = 64, *, scale: float = 1.0, check: bool = False,
+                           stream=None, workspace: torch.Tensor = None,
+                           d_state_pool: torch.Tensor = None) -> GdnGrads:
+    """Gradients of :func:`gdn_extend_chunkwise` for ``L = <d_out, out> + <d_state, final states>``.
+
+    Same inputs as the forward call, except that ``state_pool`` holds the INITIAL states (the pool
+    as the forward found it) and is only read. ``d_out [T, HV, V]`` has v's dtype; ``d_state``
+    (optional, fp32, shaped like the pool) is the gradient of the final states at the batch's
+    slots. Returns :class:`GdnGrads`. Its ``d_state_pool`` is a new zero tensor written at the
+    batch's slots, or the given ``d_state_pool``, written at those slots only; that may be
+    ``d_state`` itself, for a caller that carries the state gradient back through earlier calls.
+    ``check=True`` waits and raises on a device-detected error (bad cache index or cu_seqlens).
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("gdn_chunkwise_backward runs on a CUDA device; move the inputs there first")
+    _req(q, "q", (torch.bfloat16, torch.float16), dev)
+    _req(k, "k", q.dtype, dev)
+    _req(v, "v", q.dtype, dev)
+    _req(d_out, "d_out", q.dtype, dev)
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias), ("state_pool", state_pool)):
+        _req(t, name, torch.float32, dev)
+    _req(cache_indices, "cache_indices", torch.int64, dev)
+    _req(cu_seqlens, "cu_seqlens", torch.int64, dev)
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0] or d_out.shape != v.shape:
+        raise ValueError(f"bad q/k/v/d_out shapes {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)} "
+                         f"{tuple(d_out.shape)}")
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    if a.shape != (T, HV) or b.shape != (T, HV) or A_log.shape != (HV,) or dt_bias.shape != (HV,):
+        raise ValueError("a, b must be [T, HV] and A_log, dt_bias [HV]")
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, V, K):
+        raise ValueError(f"state_pool must be [pool, {HV}, {V}, {K}], got {tuple(state_pool.shape)}")
+    if d_state is not None:
+        _req(d_state, "d_state", torch.float32, dev)
+        if d_state.shape != state_pool.shape:
+            raise ValueError("d_state must have the shape of state_pool")
+    if d_state_pool is not None:
+        _req(d_state_pool, "d_state_pool", torch.float32, dev)
+        if d_state_pool.shape != state_pool.shape:
+            raise ValueError("d_state_pool must have the shape of state_pool")
+    B = cache_indices.shape[0]
+    if cu_seqlens.shape != (B + 1,):
+        raise ValueError("cu_seqlens must have batch + 1 entries")
+    L = _lib.load()
+    need = int(L.gdn_backward_workspace_size(T, B, H, HV, K, V, chunk_size))
+    if need == 0:
+        raise GdnError(2, f"unsupported sizes for the backward (K={K}, V={V}, chunk_size={chunk_size}, H={H}, HV={HV})")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    elif not hasattr(stream, "cuda_stream"):
+        stream = torch.cuda.ExternalStream(int(stream), device=dev)
+    sp = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        f32 = dict(dtype=torch.float32, device=dev)
+        g = GdnGrads(torch.empty((T, H, K), **f32), torch.empty((T, H, K), **f32), torch.empty((T, HV, V), **f32),
+                     torch.empty((T, HV), **f32), torch.empty((T, HV), **f32), torch.empty((HV,), **f32),
+                     torch.empty((HV,), **f32),
+                     d_state_pool if d_state_pool is not None else torch.zeros_like(state_pool))
+        if workspace is None:
+            ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+            ws_ptr = _aligned_ptr(ws)
+            ws_bytes = ws.numel() - (ws_ptr - ws.data_ptr())
+        else:
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    dtype_code = _lib.GDN_BF16 if q.dtype == torch.bfloat16 else _lib.GDN_FP16
+    st = L.gdn_chunkwise_backward(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), dtype_code,
+        a.data_ptr(), b.data_ptr(), A_log.data_ptr(), dt_bias.data_ptr(),
+        state_pool.data_ptr(), state_pool.shape[0], cache_indices.data_ptr(), cu_seqlens.data_ptr(), B,
+        d_out.data_ptr(), d_state.data_ptr() if d_state is not None else None,
+        g.dq.data_ptr(), g.dk.data_ptr(), g.dv.data_ptr(), g.da.data_ptr(), g.db.data_ptr(),
+        g.dA_log.data_ptr(), g.ddt_bias.data_ptr(), g.d_state_pool.data_ptr(),
+        T, H, HV, K, V, int(chunk_size), float(scale), ws_ptr, ws_bytes, sp)
+    _lib.check(st, "gdn_chunkwise_backward")
+    if check:
+        _lib.check(L.gdn_get_device_status(ws_ptr, sp), "gdn_chunkwise_backward (device)")
+    return g
 
 
 def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *, scale: float = 1.0,

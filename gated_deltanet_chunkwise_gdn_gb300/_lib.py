@@ -57,6 +57,17 @@ def load(build_if_missing: bool = True):
             vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i64, vp, vp, i32,
             vp, i64, i32, i32, i32, i32, i32, f32, vp, vp]
         L.gdn_extend_chunkwise_noalloc.restype = ctypes.c_int
+        L.gdn_backward_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32, i32]
+        L.gdn_backward_workspace_size.restype = sz
+        L.gdn_chunkwise_backward.argtypes = [
+            vp, vp, vp, ctypes.c_int,      # q k v dtype
+            vp, vp, vp, vp,                # a b A_log dt_bias
+            vp, i64, vp, vp, i32,          # state_pool pool_size cache_indices cu_seqlens batch
+            vp, vp,                        # d_out d_state
+            vp, vp, vp, vp, vp, vp, vp, vp,  # dq dk dv da db dA_log ddt_bias d_state_pool
+            i64, i32, i32, i32, i32,       # total_tokens H HV K V
+            i32, f32, vp, sz, vp]          # chunk_size scale workspace bytes stream
+        L.gdn_chunkwise_backward.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [
             vp, vp, vp, ctypes.c_int,      # q k v dtype
             vp, vp, vp, vp,                # a b A_log dt_bias

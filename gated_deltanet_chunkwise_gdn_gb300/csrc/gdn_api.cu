@@ -8,6 +8,7 @@
 #include <mutex>
 #include <vector>
 
+#include "gdn_backward.cuh"
 #include "gdn_common.cuh"
 #include "gdn_decode.cuh"
 
@@ -25,9 +26,10 @@ struct NvtxRange {
 };
 enum KernelId {  // scan: every scan-stage launch
   kKernSchedule = 0, kKernGates = 1, kKernIntra = 2, kKernScan = 3, kKernDecodeCheck = 4, kKernDecode = 5,
-  kKernCount = 6
+  kKernBackward = 6, kKernCount = 7
 };
-const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "scan", "decode_check", "decode"};
+const char* const kKernelNames[kKernCount] = {"schedule", "gates", "intra", "scan", "decode_check", "decode",
+                                              "backward"};
 
 std::atomic<int64_t> g_launches{0};
 
@@ -83,6 +85,11 @@ int choose_nvb(int V) { return V / 64; }
 // addresses with 32-bit signed row coordinates, so the row count must stay below 2^31.
 bool factor_rows_fit(const gdn::WsLayout& L, int HV) {
   return L.max_chunks * (int64_t)HV * kWyBlock <= (int64_t)INT32_MAX;
+}
+
+// The backward pass: K = V in {64, 128}; chunk_size 64 or 128 (64-token WY blocks either way).
+bool supported_backward_shape(int K, int V, int C) {
+  return K == V && (K == 64 || K == 128) && (C == 64 || C == 128);
 }
 
 // Largest batch of one single-token step. Above 1024 sequences the slot check runs one block
@@ -193,6 +200,150 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   rec = prof_begin(kKernScan, s);
   if (gdn::launch_scan(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
   prof_end(rec, s, p.nseg <= 1 ? 1 : (p.nseg == 2 ? 2 : 3));  // segmented: maps, combine, segments
+  return GDN_OK;
+}
+
+size_t gdn_backward_workspace_size(int64_t total_tokens, int32_t batch, int32_t H, int32_t HV, int32_t K,
+                                   int32_t V, int32_t chunk_size) {
+  if (total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || batch < 0 || H <= 0 || HV <= 0 || HV % H != 0 ||
+      HV > 65535)
+    return 0;
+  if (!supported_backward_shape(K, V, chunk_size)) return 0;
+  if ((int64_t)batch * HV * (K / 16) > (int64_t)INT32_MAX) return 0;
+  return gdn::make_bwd_layout(total_tokens, batch, H, HV, K).total;
+}
+
+gdn_status gdn_chunkwise_backward(const void* q, const void* k, const void* v, gdn_dtype dtype, const float* a,
+                                  const float* b, const float* A_log, const float* dt_bias, const float* state_pool,
+                                  int64_t pool_size, const int64_t* cache_indices, const int64_t* cu_seqlens,
+                                  int32_t batch, const void* d_out, const float* d_state, float* dq, float* dk,
+                                  float* dv, float* da, float* db, float* dA_log, float* ddt_bias,
+                                  float* d_state_pool, int64_t total_tokens, int32_t H, int32_t HV, int32_t K,
+                                  int32_t V, int32_t chunk_size, float scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  NvtxRange range("gdn_chunkwise_backward");
+  if (batch < 0 || total_tokens < 0 || total_tokens >= (int64_t)INT32_MAX || H <= 0 || HV <= 0 || HV % H != 0 ||
+      K <= 0 || V <= 0 || chunk_size <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (dtype != GDN_BF16 && dtype != GDN_FP16) return GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !A_log || !dt_bias || !dA_log || !ddt_bias) return GDN_ERR_INVALID_ARG;
+  if (batch > 0 && (!state_pool || !cache_indices || !d_state_pool || pool_size <= 0)) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!q || !k || !v || !a || !b || !d_out || !dq || !dk || !dv || !da || !db))
+    return GDN_ERR_INVALID_ARG;
+  auto al = [](const void* x, uintptr_t n) { return (reinterpret_cast<uintptr_t>(x) & (n - 1)) == 0; };
+  if (total_tokens > 0 && !(al(q, 16) && al(k, 16) && al(v, 16) && al(d_out, 16) && al(dv, 8)))
+    return GDN_ERR_INVALID_ARG;
+  if (batch > 0 && !(al(state_pool, 8) && al(d_state_pool, 8) && al(d_state, 8))) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_backward_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size);
+  if (need == 0) return GDN_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return GDN_ERR_WORKSPACE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const gdn::BwdLayout L = gdn::make_bwd_layout(total_tokens, batch, H, HV, K);
+  // The schedule and gates kernels of the forward, on the backward's workspace.
+  gdn::Params p{};
+  p.a = a;
+  p.b = b;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.cache_indices = cache_indices;
+  p.cu_seqlens = cu_seqlens;
+  p.T = total_tokens;
+  p.pool_size = pool_size;
+  p.B = batch;
+  p.H = H;
+  p.HV = HV;
+  p.max_chunks = L.max_chunks;
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  p.seq_chunk_off = reinterpret_cast<int32_t*>(ws + L.seq_chunk_off);
+  p.order = reinterpret_cast<int32_t*>(ws + L.order);
+  p.chunk_tab = reinterpret_cast<int4*>(ws + L.chunk_tab);
+  p.g = reinterpret_cast<float*>(ws + L.g);
+  p.beta = reinterpret_cast<float*>(ws + L.beta);
+  p.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
+
+  int rec = prof_begin(kKernSchedule, s);
+  const bool pre_check = batch > gdn::kScheduleSortMax;
+  if (pre_check) {
+    gdn::DecodeParams dp{};
+    dp.cache_indices = cache_indices;
+    dp.pool_size = pool_size;
+    dp.B = batch;
+    dp.status = p.status;
+    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_decode_check(dp, s) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  const size_t sched_smem = gdn::schedule_smem_bytes(batch);
+  if (sched_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(gdn::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sched_smem) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::schedule_kernel<<<1, 512, sched_smem, s>>>(p, kWyBlock, pre_check ? 1 : 0);
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s, pre_check ? 2 : 1);
+  if (batch == 0) return GDN_OK;
+  if (total_tokens > 0) {
+    rec = prof_begin(kKernGates, s);
+    if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
+    prof_end(rec, s);
+  }
+
+  gdn::BwdParams bp{};
+  bp.q = q;
+  bp.k = k;
+  bp.v = v;
+  bp.d_out = d_out;
+  bp.a = a;
+  bp.b = b;
+  bp.A_log = A_log;
+  bp.dt_bias = dt_bias;
+  bp.state_pool = state_pool;
+  bp.d_state = d_state;
+  bp.cache_indices = cache_indices;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.da = da;
+  bp.db = db;
+  bp.dA_log = dA_log;
+  bp.ddt_bias = ddt_bias;
+  bp.d_state_pool = d_state_pool;
+  bp.T = total_tokens;
+  bp.B = batch;
+  bp.H = H;
+  bp.HV = HV;
+  bp.scale = scale;
+  bp.max_chunks = L.max_chunks;
+  bp.status = p.status;
+  bp.seq_chunk_off = p.seq_chunk_off;
+  bp.order = p.order;
+  bp.chunk_tab = p.chunk_tab;
+  auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  bp.g = f(L.g);
+  bp.beta = f(L.beta);
+  bp.rq = f(L.rq);
+  bp.rk = f(L.rk);
+  bp.minv = f(L.minv);
+  bp.pm = f(L.pm);
+  bp.w = f(L.w);
+  bp.ut = f(L.ut);
+  bp.s_in = f(L.s_in);
+  bp.u = f(L.u);
+  bp.ds_out = f(L.ds_out);
+  bp.du = f(L.du);
+  bp.dqa = f(L.dqa);
+  bp.dw = f(L.dw);
+  bp.dkr = f(L.dkr);
+  bp.dgc = f(L.dgc);
+  bp.dqh = f(L.dqh);
+  bp.dkh = f(L.dkh);
+  bp.dlala = f(L.dlala);
+  rec = prof_begin(kKernBackward, s);
+  int kernels = 0;
+  if (gdn::launch_backward(bp, K, dtype == GDN_FP16, s, &kernels) != cudaSuccess) return GDN_ERR_CUDA;
+  prof_end(rec, s, kernels);
   return GDN_OK;
 }
 

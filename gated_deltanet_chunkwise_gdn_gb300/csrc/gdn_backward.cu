@@ -1,0 +1,1097 @@
+// gdn_backward.cu — the chunkwise backward pass of the GDN prefill.
+//
+// It differentiates the forward of gdn_extend_chunkwise,
+//   q^ = q / sqrt(|q|^2 + eps), k^ likewise, log alpha = -exp(A_log) softplus(a + dt_bias),
+//   beta = sigmoid(b), S_t = alpha_t S_{t-1} (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T,
+//   o_t = scale S_t q^_t
+// ("Simple math to speed up GDN prefill", section "Reminder"; pymllm page
+// "pymllm.layers.attention.gdn_chunkwise", Parameters), for the scalar
+//   L = sum_t <dO_t, o_t> + sum_chains <dS_final, S_final>,
+// so besides the output's gradient it takes the gradient arriving at each final state, the
+// incoming state gradient of the bottom-level backward in "nrm-training-kernels", section
+// "Kernel". The pages print no gradient formulas: what follows is the chain rule applied to
+// the chunkwise WY form of the forward (notation of gdn_common.cuh), chunk by chunk.
+//
+// Per chunk (rows = its C tokens), with S_in the state entering it and dS_out the gradient of
+// the state leaving it:
+//   forward:  U = U~ - W<- S_in^T,  O = scale (diag(e^g) Q^ S_in^T + P U),
+//             S_out = e^{g_C} S_in + U^T K->,  K-> = diag(e^{g_C - g}) K^
+//   reverse:  dU = scale P^T dO + K-> dS_out^T
+//             dS_in = e^{g_C} dS_out + scale dO^T diag(e^g) Q^ - dU^T W<-
+// and then, per chunk and independently of the others, the gradients through P, W<-, U~,
+// A = (Gamma . M^{-1}) diag(beta), the one inverse M^{-1} (dM = -M^{-T} dM^{-1} M^{-T},
+// kept strictly lower), the decays Gamma and e^g, the gates and the normalisation.
+//
+// Kernels, in launch order (after the forward's schedule and gates kernels):
+//   factor   per (chunk, value head): 1/|q|, 1/|k|, M^{-1}, P, W<-, U~     (parallel)
+//   state    per (chain, block of 16 state rows): S_in of every chunk, U    (sequential in chunks)
+//   dstate   per (chain, block of 16 state rows): dS_out of every chunk, dU, dS_0 (sequential, reversed)
+//   sgrad    per (chunk, value head): scale e^g (dO S_in), -dU S_in, U dS_out, e^{g_C} <dS_out, S_in>
+//   local    per (chunk, value head): dv, db, da, the gradients of q^ and k^ for this value head
+//   norm     per (token, q/k head): the value heads' gradients of q^, k^ summed, through the norm
+//   gate_sum per value head: dA_log and ddt_bias, summed over tokens in a fixed order
+// The state rows are independent in both sequential passes (the contractions run over the key
+// dimension and the chunk's tokens), so their CTAs split the value dimension. Every product
+// runs on the tensor cores as warp-level m16n8k16 MMAs (gdn_mma.cuh) with fp32 operands carried
+// as bf16 hi + lo pairs, so the backward keeps about fp32 accuracy; the intermediates between
+// kernels are fp32. Every sum is taken in a fixed order, so the results are deterministic.
+#include <type_traits>
+
+#include "gdn_backward.cuh"
+#include "gdn_mma.cuh"
+
+namespace gdn {
+
+BwdLayout make_bwd_layout(int64_t T, int B, int H, int HV, int D) {
+  (void)H;
+  constexpr int C = 64;
+  BwdLayout L{};
+  const int64_t mc = T / C + B + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t per = (size_t)mc * HV;  // (chunk, value head) items
+  L.max_chunks = mc;
+  L.status = take(64 * sizeof(int32_t));
+  L.seq_chunk_off = take((size_t)(B + 1) * sizeof(int32_t));
+  L.order = take((size_t)(B > 0 ? B : 1) * sizeof(int32_t));
+  L.chunk_tab = take((size_t)mc * sizeof(int4));
+  L.g = take(per * C * sizeof(float));
+  L.beta = take(per * C * sizeof(float));
+  L.rq = take(per * C * sizeof(float));
+  L.rk = take(per * C * sizeof(float));
+  L.minv = take(per * C * C * sizeof(float));
+  L.pm = take(per * C * C * sizeof(float));
+  L.w = take(per * C * D * sizeof(float));
+  L.ut = take(per * C * D * sizeof(float));
+  L.s_in = take(per * D * D * sizeof(float));
+  L.u = take(per * C * D * sizeof(float));
+  L.ds_out = take(per * D * D * sizeof(float));
+  L.du = take(per * C * D * sizeof(float));
+  L.dqa = take(per * C * D * sizeof(float));
+  L.dw = take(per * C * D * sizeof(float));
+  L.dkr = take(per * C * D * sizeof(float));
+  L.dgc = take(per * sizeof(float));
+  L.dqh = take((size_t)T * HV * D * sizeof(float));
+  L.dkh = take((size_t)T * HV * D * sizeof(float));
+  L.dlala = take((size_t)T * HV * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+namespace {
+
+constexpr int C = 64;   // WY block (tokens per chunk)
+constexpr int VB = 16;  // state rows per CTA of the sequential passes
+constexpr int CP = C + 4;   // pitch (floats) of C x C fp32 tiles
+constexpr int UP = VB + 4;  // pitch (floats) of C x VB fp32 tiles
+constexpr int DOP = VB + 8; // pitch (elements) of C x VB 16-bit tiles
+
+template <typename E>
+constexpr bool kSplitSrc = std::is_same<E, f16>::value;  // fp16 tiles enter the MMAs as bf16 pairs
+
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f(f16 x) { return __half2float(x); }
+
+__device__ __forceinline__ void cp_async_16z(void* smem, const void* gmem, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(valid ? 16 : 0));
+}
+
+// Token rows t0 .. t0 + C - 1 of a [T][heads][D] 16-bit array (head offset folded into src, row
+// stride ld elements) into smem rows of pitch DP elements; rows at or past len are zero-filled.
+template <int D, typename E>
+__device__ __forceinline__ void load_tokens(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid,
+                                            int nthr) {
+  constexpr int DP = D + 8, PER = D / 8;  // 16-byte pieces per row
+  for (int e = tid; e < C * PER; e += nthr) {
+    const int i = e / PER, q = e % PER;
+    const bool ok = i < len;
+    const E* s = src + (ok ? (t0 + i) * ld : t0 * ld) + q * 8;
+    cp_async_16z(dst + i * DP + q * 8, s, ok);
+  }
+}
+// Column block [c0, c0 + W) of the same rows (W a multiple of 8), pitch WP elements.
+template <int W, int WP, typename E>
+__device__ __forceinline__ void load_tokens_cols(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid,
+                                                 int nthr) {
+  constexpr int PER = W / 8;
+  for (int e = tid; e < C * PER; e += nthr) {
+    const int i = e / PER, q = e % PER;
+    const bool ok = i < len;
+    const E* s = src + (ok ? (t0 + i) * ld : t0 * ld) + q * 8;
+    cp_async_16z(dst + i * WP + q * 8, s, ok);
+  }
+}
+// rows x W fp32 (W a multiple of 4) from a row-major array of row stride ld floats, pitch LD.
+template <int W, int LD>
+__device__ __forceinline__ void load_f32(float* dst, const float* src, int64_t ld, int rows, int tid, int nthr) {
+  constexpr int PER = W / 4;
+  for (int e = tid; e < rows * PER; e += nthr) {
+    const int i = e / PER, q = e % PER;
+    cp_async_16(dst + i * LD + q * 4, src + i * ld + q * 4);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+// Sum over the four lanes of a fragment row (lanes 4 r .. 4 r + 3).
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+// Sum over the eight fragment rows of a lane column (lanes c/2, c/2 + 4, ..., c/2 + 28).
+__device__ __forceinline__ float col_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  x += __shfl_xor_sync(0xffffffffu, x, 16);
+  return x;
+}
+
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+
+// ----------------------------------------------------------------------------- factor
+
+template <int D>
+struct FacSmem {
+  static constexpr int DP = D + 8;
+  static constexpr uint32_t Q = 0;                    // 16-bit [C][DP] q, k, v tiles
+  static constexpr uint32_t K = Q + C * DP * 2;
+  static constexpr uint32_t V = K + C * DP * 2;
+  static constexpr uint32_t L = V + C * DP * 2;       // fp32 [C][CP]: beta_i k^_i . k^_j (j < i), then A
+  static constexpr uint32_t X = L + C * CP * 4;       // fp32 [C][CP]: M^{-1}
+  static constexpr uint32_t VEC = X + C * CP * 4;     // g, beta, 1/|q|, 1/|k|, e^g/|k|
+  static constexpr uint32_t bytes = VEC + 5 * C * 4;
+};
+
+template <int D, typename E>
+__global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
+  using S = FacSmem<D>;
+  constexpr int DP = S::DP;
+  constexpr bool XS = kSplitSrc<E>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const int j = blockIdx.x, hv = blockIdx.y;
+  if (j >= p.status[1]) return;
+  const int4 ct = p.chunk_tab[j];
+  const int64_t t0 = ct.y;
+  const int len = ct.z;
+  const int h = hv / (p.HV / p.H);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  E* sq = reinterpret_cast<E*>(smem + S::Q);
+  E* sk = reinterpret_cast<E*>(smem + S::K);
+  E* sv = reinterpret_cast<E*>(smem + S::V);
+  float* sL = reinterpret_cast<float*>(smem + S::L);
+  float* sX = reinterpret_cast<float*>(smem + S::X);
+  float* vg = reinterpret_cast<float*>(smem + S::VEC);
+  float* vb = vg + C;
+  float* vrq = vb + C;
+  float* vrk = vrq + C;
+  float* vek = vrk + C;
+
+  load_tokens<D>(sq, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(sk, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(sv, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  cp_async_commit();
+  const int64_t item = (int64_t)j * p.HV + hv;
+  if (tid < C) {
+    vg[tid] = p.g[item * C + tid];
+    vb[tid] = p.beta[item * C + tid];
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  for (int i = warp * 8; i < warp * 8 + 8; ++i) {  // row norms, one warp per 8 rows
+    float s2q = 0.f, s2k = 0.f;
+    for (int d = lane; d < D; d += 32) {
+      const float x = to_f(sq[i * DP + d]), y = to_f(sk[i * DP + d]);
+      s2q = fmaf(x, x, s2q);
+      s2k = fmaf(y, y, s2k);
+    }
+    s2q = warp_sum(s2q);
+    s2k = warp_sum(s2k);
+    if (lane == 0) {
+      vrq[i] = i < len ? 1.f / sqrtf(s2q + kNormEps) : 0.f;
+      vrk[i] = i < len ? 1.f / sqrtf(s2k + kNormEps) : 0.f;
+    }
+  }
+  __syncthreads();
+  if (tid < C) {
+    p.rq[item * C + tid] = vrq[tid];
+    p.rk[item * C + tid] = vrk[tid];
+    vek[tid] = expf(vg[tid]) * vrk[tid];
+  }
+
+  // K K^T and Q K^T (C x C): warp tile rows m0 .. m0 + 15, columns n0 .. n0 + 31
+  const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+  {
+    float kk[1][4][4], qk[1][4][4];
+    wm::zero(kk);
+    wm::zero(qk);
+    auto fk = [&](int m, int x) { return to_f(sk[m * DP + x]); };
+    auto fq = [&](int m, int x) { return to_f(sq[m * DP + x]); };
+    auto fkt = [&](int x, int n) { return to_f(sk[n * DP + x]); };
+    wm::gemm<1, 4, XS, XS>(kk, fk, fkt, m0, n0, 0, D);
+    wm::gemm<1, 4, XS, XS>(qk, fq, fkt, m0, n0, 0, D);
+    wm::for_each(kk, m0, n0, [&](int i, int c, float& x) {
+      sL[i * CP + c] = c < i ? vb[i] * vrk[i] * vrk[c] * x : 0.f;
+    });
+    float* P = p.pm + item * C * C;
+    wm::for_each_pair(qk, m0, n0, [&](int i, int c, float& x0, float& x1) {
+      const float y0 = c <= i ? expf(vg[i] - vg[c]) * vrq[i] * vrk[c] * x0 : 0.f;
+      const float y1 = c + 1 <= i ? expf(vg[i] - vg[c + 1]) * vrq[i] * vrk[c + 1] * x1 : 0.f;
+      *reinterpret_cast<float2*>(P + i * C + c) = make_float2(y0, y1);
+    });
+  }
+  __syncthreads();
+
+  // M^{-1} = (I + L)^{-1}: forward substitution, one column per thread
+  if (tid < C) {
+    const int c = tid;
+    for (int i = 0; i < c; ++i) sX[i * CP + c] = 0.f;
+    sX[c * CP + c] = 1.f;
+    for (int i = c + 1; i < C; ++i) {
+      float s = 0.f;
+      for (int x = c; x < i; ++x) s = fmaf(sL[i * CP + x], sX[x * CP + c], s);
+      sX[i * CP + c] = -s;
+    }
+  }
+  __syncthreads();
+  {
+    float* MI = p.minv + item * C * C;
+    for (int e = tid; e < C * C / 4; e += 256) {
+      const int i = e / (C / 4), c = (e % (C / 4)) * 4;
+      *reinterpret_cast<float4*>(MI + i * C + c) =
+          make_float4(sX[i * CP + c], sX[i * CP + c + 1], sX[i * CP + c + 2], sX[i * CP + c + 3]);
+    }
+    for (int e = tid; e < C * C; e += 256) {  // A = (Gamma . M^{-1}) diag(beta), lower triangular
+      const int i = e / C, c = e % C;
+      sL[i * CP + c] = c <= i ? expf(vg[i] - vg[c]) * sX[i * CP + c] * vb[c] : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // W<- = A diag(e^g / |k|) K and U~ = A V (C x D): rows m0.., columns nw .. nw + D/2; A is lower
+  // triangular, so rows m0 .. m0 + 15 need k < m0 + 16 only.
+  constexpr int NT = D / 16;
+  const int nw = (D / 2) * (warp >> 2);
+  auto fa_w = [&](int m, int x) { return sL[m * CP + x] * vek[x]; };
+  auto fa_u = [&](int m, int x) { return sL[m * CP + x]; };
+  auto fb_k = [&](int x, int n) { return to_f(sk[x * DP + n]); };
+  auto fb_v = [&](int x, int n) { return to_f(sv[x * DP + n]); };
+  {
+    float acc[1][NT][4];
+    wm::zero(acc);
+    wm::gemm<1, NT, true, XS>(acc, fa_w, fb_k, m0, nw, 0, m0 + 16);
+    float* Wg = p.w + item * C * D;
+    wm::for_each_pair(acc, m0, nw, [&](int i, int c, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(Wg + i * D + c) = make_float2(x0, x1);
+    });
+  }
+  {
+    float acc[1][NT][4];
+    wm::zero(acc);
+    wm::gemm<1, NT, true, XS>(acc, fa_u, fb_v, m0, nw, 0, m0 + 16);
+    float* Ug = p.ut + item * C * D;
+    wm::for_each_pair(acc, m0, nw, [&](int i, int c, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(Ug + i * D + c) = make_float2(x0, x1);
+    });
+  }
+}
+
+// ----------------------------------------------------------------------------- state (forward states)
+
+template <int D>
+struct StSmem {
+  static constexpr int DP = D + 8, WP = D + 4;
+  static constexpr uint32_t W = 0;                   // per stage: W<- fp32 [C][WP]
+  static constexpr uint32_t K = W + C * WP * 4;      //            k 16-bit [C][DP]
+  static constexpr uint32_t UT = K + C * DP * 2;     //            U~ columns fp32 [C][UP]
+  static constexpr uint32_t VEC = UT + C * UP * 4;   //            g, 1/|k|
+  static constexpr uint32_t STAGE = VEC + 2 * C * 4;
+  static constexpr uint32_t S = 2 * STAGE;           // state rows fp32 [VB][WP]
+  static constexpr uint32_t U = S + VB * WP * 4;     // U columns fp32 [C][UP]
+  static constexpr uint32_t SK = U + C * UP * 4;     // e^{g_C - g} / |k|
+  static constexpr uint32_t bytes = SK + C * 4;
+};
+
+// The CTA's chain: sequence (longest first), value head, first state row.
+struct ChainJob {
+  int seq, hv, h, vb, c0, c1;
+  int64_t slot;
+};
+template <int D>
+__device__ __forceinline__ ChainJob chain_job(const BwdParams& p) {
+  constexpr int NVB = D / VB;
+  ChainJob jb;
+  const int bid = blockIdx.x;
+  jb.vb = (bid % NVB) * VB;
+  const int chain = bid / NVB;
+  jb.seq = p.order[chain / p.HV];
+  jb.hv = chain % p.HV;
+  jb.h = jb.hv / (p.HV / p.H);
+  jb.c0 = p.seq_chunk_off[jb.seq];
+  jb.c1 = p.seq_chunk_off[jb.seq + 1];
+  jb.slot = p.cache_indices[jb.seq];
+  return jb;
+}
+
+template <int D, typename E>
+__global__ void __launch_bounds__(128) bwd_state_kernel(BwdParams p) {
+  using S = StSmem<D>;
+  constexpr int DP = S::DP, WP = S::WP;
+  constexpr bool XS = kSplitSrc<E>;
+  constexpr int NTS = D / 32;  // 8-column tiles per warp of the VB x D state
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const ChainJob jb = chain_job<D>(p);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  float* sS = reinterpret_cast<float*>(smem + S::S);
+  float* sU = reinterpret_cast<float*>(smem + S::U);
+  float* vsk = reinterpret_cast<float*>(smem + S::SK);
+  const E* kin = static_cast<const E*>(p.k) + (int64_t)jb.h * D;
+
+  auto issue = [&](int c, int st) {
+    unsigned char* base = smem + st * S::STAGE;
+    const int4 ct = p.chunk_tab[c];
+    const int64_t item = (int64_t)c * p.HV + jb.hv;
+    load_f32<D, WP>(reinterpret_cast<float*>(base + S::W), p.w + item * C * D, D, C, tid, 128);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
+    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, tid, 128);
+    float* vec = reinterpret_cast<float*>(base + S::VEC);
+    if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
+    else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rk + item * C + 4 * (tid - 16));
+  };
+
+  const float* S0 = p.state_pool + (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
+  const int ns0 = warp * (D / 4);  // the warp's state columns
+  float st[1][NTS][4];
+  wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { x = S0[i * D + c]; });
+  wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { sS[i * WP + c] = x; });
+  if (jb.c1 > jb.c0) issue(jb.c0, 0);
+  cp_async_commit();
+
+  for (int c = jb.c0; c < jb.c1; ++c) {
+    const int stg = (c - jb.c0) & 1;
+    cp_async_wait<0>();
+    __syncthreads();
+    if (c + 1 < jb.c1) issue(c + 1, stg ^ 1);
+    cp_async_commit();
+    const unsigned char* base = smem + stg * S::STAGE;
+    const float* sW = reinterpret_cast<const float*>(base + S::W);
+    const E* sK = reinterpret_cast<const E*>(base + S::K);
+    const float* sUT = reinterpret_cast<const float*>(base + S::UT);
+    const float* vg = reinterpret_cast<const float*>(base + S::VEC);
+    const float* vrk = vg + C;
+    const int64_t item = (int64_t)c * p.HV + jb.hv;
+
+    // the state entering this chunk
+    float* Sin = p.s_in + item * D * D + (int64_t)jb.vb * D;
+    wm::for_each_pair(st, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(Sin + i * D + cc) = make_float2(x0, x1);
+    });
+    // U = U~ - W<- S^T (C x VB): warp rows 16 warp
+    {
+      float ua[1][2][4];
+      wm::zero(ua);
+      auto fa = [&](int m, int x) { return sW[m * WP + x]; };
+      auto fb = [&](int x, int n) { return sS[n * WP + x]; };
+      wm::gemm<1, 2, true, true>(ua, fa, fb, 16 * warp, 0, 0, D);
+      float* Ug = p.u + item * C * D + jb.vb;
+      wm::for_each_pair(ua, 16 * warp, 0, [&](int i, int cc, float& x0, float& x1) {
+        const float u0 = sUT[i * UP + cc] - x0, u1 = sUT[i * UP + cc + 1] - x1;
+        sU[i * UP + cc] = u0;
+        sU[i * UP + cc + 1] = u1;
+        *reinterpret_cast<float2*>(Ug + i * D + cc) = make_float2(u0, u1);
+      });
+      if (tid < C) vsk[tid] = expf(vg[C - 1] - vg[tid]) * vrk[tid];
+    }
+    __syncthreads();
+    // S = e^{g_C} S + U^T diag(e^{g_C - g} / |k|) K
+    {
+      const float eC = expf(vg[C - 1]);
+      wm::for_each(st, 0, ns0, [&](int, int, float& x) { x *= eC; });
+      auto fa = [&](int m, int x) { return sU[x * UP + m] * vsk[x]; };
+      auto fb = [&](int x, int n) { return to_f(sK[x * DP + n]); };
+      wm::gemm<1, NTS, true, XS>(st, fa, fb, 0, ns0, 0, C);
+      wm::for_each(st, 0, ns0, [&](int i, int cc, float& x) { sS[i * WP + cc] = x; });
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- dstate (reverse)
+
+template <int D>
+struct DsSmem {
+  static constexpr int DP = D + 8, WP = D + 4;
+  static constexpr uint32_t P = 0;                   // per stage: P fp32 [C][CP]
+  static constexpr uint32_t DO = P + C * CP * 4;     //            dO columns 16-bit [C][DOP]
+  static constexpr uint32_t K = DO + C * DOP * 2;    //            k 16-bit [C][DP]
+  static constexpr uint32_t Q = K + C * DP * 2;      //            q 16-bit [C][DP]
+  static constexpr uint32_t W = Q + C * DP * 2;      //            W<- fp32 [C][WP]
+  static constexpr uint32_t VEC = W + C * WP * 4;    //            g, 1/|q|, 1/|k|
+  static constexpr uint32_t STAGE = VEC + 3 * C * 4;
+  static constexpr uint32_t DS = 2 * STAGE;          // gradient rows fp32 [VB][WP]
+  static constexpr uint32_t DU = DS + VB * WP * 4;   // dU columns fp32 [C][UP]
+  static constexpr uint32_t SK = DU + C * UP * 4;    // e^{g_C - g} / |k|, scale e^g / |q|
+  static constexpr uint32_t bytes = SK + 2 * C * 4;
+};
+
+template <int D, typename E>
+__global__ void __launch_bounds__(128) bwd_dstate_kernel(BwdParams p) {
+  using S = DsSmem<D>;
+  constexpr int DP = S::DP, WP = S::WP;
+  constexpr bool XS = kSplitSrc<E>;
+  constexpr int NTS = D / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const ChainJob jb = chain_job<D>(p);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  float* sdS = reinterpret_cast<float*>(smem + S::DS);
+  float* sdU = reinterpret_cast<float*>(smem + S::DU);
+  float* vsk = reinterpret_cast<float*>(smem + S::SK);
+  float* vsq = vsk + C;
+  const E* kin = static_cast<const E*>(p.k) + (int64_t)jb.h * D;
+  const E* qin = static_cast<const E*>(p.q) + (int64_t)jb.h * D;
+  const E* doin = static_cast<const E*>(p.d_out) + (int64_t)jb.hv * D + jb.vb;
+
+  auto issue = [&](int c, int st) {
+    unsigned char* base = smem + st * S::STAGE;
+    const int4 ct = p.chunk_tab[c];
+    const int64_t item = (int64_t)c * p.HV + jb.hv;
+    load_f32<C, CP>(reinterpret_cast<float*>(base + S::P), p.pm + item * C * C, C, C, tid, 128);
+    load_tokens_cols<VB, DOP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, tid, 128);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
+    load_f32<D, WP>(reinterpret_cast<float*>(base + S::W), p.w + item * C * D, D, C, tid, 128);
+    float* vec = reinterpret_cast<float*>(base + S::VEC);
+    if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
+    else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rq + item * C + 4 * (tid - 16));
+    else if (tid < 48) cp_async_16(vec + 2 * C + 4 * (tid - 32), p.rk + item * C + 4 * (tid - 32));
+  };
+
+  const int64_t srow = (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
+  const int ns0 = warp * (D / 4);
+  float ds[1][NTS][4];
+  wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { x = p.d_state ? p.d_state[srow + i * D + c] : 0.f; });
+  wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { sdS[i * WP + c] = x; });
+  if (jb.c1 > jb.c0) issue(jb.c1 - 1, 0);
+  cp_async_commit();
+
+  for (int c = jb.c1 - 1; c >= jb.c0; --c) {
+    const int stg = (jb.c1 - 1 - c) & 1;
+    cp_async_wait<0>();
+    __syncthreads();
+    if (c - 1 >= jb.c0) issue(c - 1, stg ^ 1);
+    cp_async_commit();
+    const unsigned char* base = smem + stg * S::STAGE;
+    const float* sP = reinterpret_cast<const float*>(base + S::P);
+    const E* sDO = reinterpret_cast<const E*>(base + S::DO);
+    const E* sK = reinterpret_cast<const E*>(base + S::K);
+    const E* sQ = reinterpret_cast<const E*>(base + S::Q);
+    const float* sW = reinterpret_cast<const float*>(base + S::W);
+    const float* vg = reinterpret_cast<const float*>(base + S::VEC);
+    const float* vrq = vg + C;
+    const float* vrk = vg + 2 * C;
+    const int64_t item = (int64_t)c * p.HV + jb.hv;
+
+    // the gradient of the state leaving this chunk
+    float* dSo = p.ds_out + item * D * D + (int64_t)jb.vb * D;
+    wm::for_each_pair(ds, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(dSo + i * D + cc) = make_float2(x0, x1);
+    });
+    if (tid < C) {
+      vsk[tid] = expf(vg[C - 1] - vg[tid]) * vrk[tid];
+      vsq[tid] = p.scale * expf(vg[tid]) * vrq[tid];
+    }
+    // dU = scale P^T dO + diag(e^{g_C - g} / |k|) (K dS^T)   (C x VB): warp rows 16 warp
+    {
+      const int m0 = 16 * warp;
+      float a1[1][2][4], a2[1][2][4];
+      wm::zero(a1);
+      wm::zero(a2);
+      auto fa1 = [&](int m, int x) { return sP[x * CP + m]; };  // P^T: zero for x < m
+      auto fb1 = [&](int x, int n) { return to_f(sDO[x * DOP + n]); };
+      auto fa2 = [&](int m, int x) { return to_f(sK[m * DP + x]); };
+      auto fb2 = [&](int x, int n) { return sdS[n * WP + x]; };
+      wm::gemm<1, 2, true, XS>(a1, fa1, fb1, m0, 0, m0, C);
+      wm::gemm<1, 2, XS, true>(a2, fa2, fb2, m0, 0, 0, D);
+      __syncthreads();  // vsk written
+      float* dUg = p.du + item * C * D + jb.vb;
+      const float sc = p.scale;
+      const int r = wm::lane_r(), cl = wm::lane_c();
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = m0 + r + 8 * hh, cc = 8 * jj + cl;
+          const float y0 = sc * a1[0][jj][2 * hh] + vsk[i] * a2[0][jj][2 * hh];
+          const float y1 = sc * a1[0][jj][2 * hh + 1] + vsk[i] * a2[0][jj][2 * hh + 1];
+          sdU[i * UP + cc] = y0;
+          sdU[i * UP + cc + 1] = y1;
+          *reinterpret_cast<float2*>(dUg + i * D + cc) = make_float2(y0, y1);
+        }
+    }
+    __syncthreads();
+    // dS = e^{g_C} dS + (scale diag(e^g / |q|) dO)^T Q - dU^T W<-   (VB x D)
+    {
+      const float eC = expf(vg[C - 1]);
+      wm::for_each(ds, 0, ns0, [&](int, int, float& x) { x *= eC; });
+      auto fa1 = [&](int m, int x) { return to_f(sDO[x * DOP + m]) * vsq[x]; };
+      auto fb1 = [&](int x, int n) { return to_f(sQ[x * DP + n]); };
+      auto fa2 = [&](int m, int x) { return -sdU[x * UP + m]; };
+      auto fb2 = [&](int x, int n) { return sW[x * WP + n]; };
+      wm::gemm<1, NTS, true, XS>(ds, fa1, fb1, 0, ns0, 0, C);
+      wm::gemm<1, NTS, true, true>(ds, fa2, fb2, 0, ns0, 0, C);
+      wm::for_each(ds, 0, ns0, [&](int i, int cc, float& x) { sdS[i * WP + cc] = x; });
+    }
+  }
+  float* dS0 = p.d_state_pool + srow;
+  wm::for_each_pair(ds, 0, ns0, [&](int i, int c, float& x0, float& x1) {
+    *reinterpret_cast<float2*>(dS0 + i * D + c) = make_float2(x0, x1);
+  });
+}
+
+// ----------------------------------------------------------------------------- sgrad
+
+template <int D>
+struct SgSmem {
+  static constexpr int DP = D + 8, WP = D + 4;
+  static constexpr uint32_t SB = 0;                  // fp32 [D][WP]: S_in, then dS_out
+  static constexpr uint32_t DO = SB + D * WP * 4;    // dO 16-bit [C][DP]
+  static constexpr uint32_t DU = DO + C * DP * 2;    // dU fp32 [C][WP]
+  static constexpr uint32_t U = DU + C * WP * 4;     // U fp32 [C][WP]
+  static constexpr uint32_t VEC = U + C * WP * 4;    // g; 8 warp partials
+  static constexpr uint32_t bytes = VEC + C * 4 + 8 * 4;
+};
+
+template <int D, typename E>
+__global__ void __launch_bounds__(256) bwd_sgrad_kernel(BwdParams p) {
+  using S = SgSmem<D>;
+  constexpr int DP = S::DP, WP = S::WP;
+  constexpr bool XS = kSplitSrc<E>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const int j = blockIdx.x, hv = blockIdx.y;
+  if (j >= p.status[1]) return;
+  const int4 ct = p.chunk_tab[j];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* sSB = reinterpret_cast<float*>(smem + S::SB);
+  E* sDO = reinterpret_cast<E*>(smem + S::DO);
+  float* sDU = reinterpret_cast<float*>(smem + S::DU);
+  float* sU = reinterpret_cast<float*>(smem + S::U);
+  float* vg = reinterpret_cast<float*>(smem + S::VEC);
+  float* vred = vg + C;
+  const int64_t item = (int64_t)j * p.HV + hv;
+
+  load_f32<D, WP>(sSB, p.s_in + item * D * D, D, D, tid, 256);
+  load_tokens<D>(sDO, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, ct.y, ct.z, tid, 256);
+  load_f32<D, WP>(sDU, p.du + item * C * D, D, C, tid, 256);
+  load_f32<D, WP>(sU, p.u + item * C * D, D, C, tid, 256);
+  if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // [dO; dU] S_in: warps 0-3 rows 16 w of dO, warps 4-7 rows 16 (w - 4) of dU; all D columns
+  {
+    constexpr int NT = D / 8;
+    const int m0 = 16 * (warp & 3);
+    float acc[1][NT][4];
+    wm::zero(acc);
+    auto fb = [&](int x, int n) { return sSB[x * WP + n]; };
+    if (warp < 4) {
+      auto fa = [&](int m, int x) { return to_f(sDO[m * DP + x]); };
+      wm::gemm<1, NT, XS, true>(acc, fa, fb, m0, 0, 0, D);
+      float* out = p.dqa + item * C * D;
+      const float sc = p.scale;
+      wm::for_each_pair(acc, m0, 0, [&](int i, int c, float& x0, float& x1) {
+        const float f = sc * expf(vg[i]);
+        *reinterpret_cast<float2*>(out + i * D + c) = make_float2(f * x0, f * x1);
+      });
+    } else {
+      auto fa = [&](int m, int x) { return sDU[m * WP + x]; };
+      wm::gemm<1, NT, true, true>(acc, fa, fb, m0, 0, 0, D);
+      float* out = p.dw + item * C * D;
+      wm::for_each_pair(acc, m0, 0, [&](int i, int c, float& x0, float& x1) {
+        *reinterpret_cast<float2*>(out + i * D + c) = make_float2(-x0, -x1);
+      });
+    }
+  }
+  __syncthreads();
+  // dS_out over S_in, with <dS_out, S_in>
+  {
+    const float* src = p.ds_out + item * D * D;
+    float part = 0.f;
+    for (int e = tid; e < D * D / 4; e += 256) {
+      const int i = e / (D / 4), c = (e % (D / 4)) * 4;
+      const float4 x = *reinterpret_cast<const float4*>(src + i * D + c);
+      float4* y = reinterpret_cast<float4*>(sSB + i * WP + c);
+      const float4 s = *y;
+      part = fmaf(x.x, s.x, part);
+      part = fmaf(x.y, s.y, part);
+      part = fmaf(x.z, s.z, part);
+      part = fmaf(x.w, s.w, part);
+      *y = x;
+    }
+    part = warp_sum(part);
+    if (lane == 0) vred[warp] = part;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += vred[w];
+    p.dgc[item] = expf(vg[C - 1]) * s;
+  }
+  // U dS_out (C x D): warp rows 16 (w & 3), columns (D/2) (w >> 2)
+  {
+    constexpr int NT = D / 16;
+    const int m0 = 16 * (warp & 3), n0 = (D / 2) * (warp >> 2);
+    float acc[1][NT][4];
+    wm::zero(acc);
+    auto fa = [&](int m, int x) { return sU[m * WP + x]; };
+    auto fb = [&](int x, int n) { return sSB[x * WP + n]; };
+    wm::gemm<1, NT, true, true>(acc, fa, fb, m0, n0, 0, D);
+    float* out = p.dkr + item * C * D;
+    wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(out + i * D + c) = make_float2(x0, x1);
+    });
+  }
+}
+
+// ----------------------------------------------------------------------------- local
+
+template <int D>
+struct LoSmem {
+  static constexpr int DP = D + 8, WP = D + 4;
+  static constexpr uint32_t TOK = C * DP * 2;        // one 16-bit token tile
+  static constexpr uint32_t CC = C * CP * 4;         // one fp32 C x C tile
+  static constexpr uint32_t RQ = 0;                  // q, k tiles (whole kernel)
+  static constexpr uint32_t RK = RQ + TOK;
+  static constexpr uint32_t RX = RK + TOK;           // v, dO tiles; after their last use: X1, X2 (C x C)
+  static constexpr uint32_t RXB = (2 * TOK > 2 * CC ? 2 * TOK : 2 * CC);
+  static constexpr uint32_t C1 = RX + RXB;           // M^{-1}, then A
+  static constexpr uint32_t C2 = C1 + CC;            // Q^K^^T, then dGamma
+  static constexpr uint32_t C3 = C2 + CC;            // K^K^^T
+  static constexpr uint32_t C4 = C3 + CC;            // dP
+  static constexpr uint32_t F1 = C4 + CC;            // U, then dW (fp32 [C][WP])
+  static constexpr uint32_t F2 = F1 + C * WP * 4;    // dU
+  static constexpr uint32_t VEC = F2 + C * WP * 4;   // 20 vectors of C
+  static constexpr uint32_t bytes = VEC + 20 * C * 4;
+  static_assert(bytes <= 232448, "shared memory per CTA");
+};
+
+template <int D, typename E>
+__global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
+  using S = LoSmem<D>;
+  constexpr int DP = S::DP, WP = S::WP;
+  constexpr bool XS = kSplitSrc<E>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const int j = blockIdx.x, hv = blockIdx.y;
+  if (j >= p.status[1]) return;
+  const int4 ct = p.chunk_tab[j];
+  const int64_t t0 = ct.y;
+  const int len = ct.z;
+  const int h = hv / (p.HV / p.H);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int64_t item = (int64_t)j * p.HV + hv;
+  E* rq_t = reinterpret_cast<E*>(smem + S::RQ);
+  E* rk_t = reinterpret_cast<E*>(smem + S::RK);
+  E* rv_t = reinterpret_cast<E*>(smem + S::RX);
+  E* rdo_t = reinterpret_cast<E*>(smem + S::RX + S::TOK);
+  float* X1 = reinterpret_cast<float*>(smem + S::RX);
+  float* X2 = reinterpret_cast<float*>(smem + S::RX + S::CC);
+  float* C1 = reinterpret_cast<float*>(smem + S::C1);
+  float* C2 = reinterpret_cast<float*>(smem + S::C2);
+  float* C3 = reinterpret_cast<float*>(smem + S::C3);
+  float* C4 = reinterpret_cast<float*>(smem + S::C4);
+  float* F1 = reinterpret_cast<float*>(smem + S::F1);
+  float* F2 = reinterpret_cast<float*>(smem + S::F2);
+  float* vg = reinterpret_cast<float*>(smem + S::VEC);
+  float* vbt = vg + C;
+  float* vrq = vbt + C;
+  float* vrk = vrq + C;
+  float* veg = vrk + C;      // e^g
+  float* vdec = veg + C;     // e^{g_C - g}
+  float* vdb = vdec + C;     // d beta
+  float* vdg = vdb + C;      // d g
+  float* vcolp = vdg + C;    // [4][C] column partials of dA . Z
+  float* vrow = vcolp + 4 * C;  // row sums of dGamma . Gamma
+  float* vcol = vrow + C;       // column sums of dGamma . Gamma
+  float* vpA = vcol + C;        // [2][C] eg <k^, A^T dW>
+  float* vpB = vpA + 2 * C;     // [2][C] dec <k^, dKr>
+  float* vpC = vpB + 2 * C;     // [2][C] <dQa, q^>
+
+  load_tokens<D>(rq_t, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(rk_t, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(rv_t, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_tokens<D>(rdo_t, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_f32<D, WP>(F1, p.u + item * C * D, D, C, tid, 256);
+  load_f32<D, WP>(F2, p.du + item * C * D, D, C, tid, 256);
+  load_f32<C, CP>(C1, p.minv + item * C * C, C, C, tid, 256);
+  if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
+  else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
+  else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
+  else if (tid < 64) cp_async_16(vrk + 4 * (tid - 48), p.rk + item * C + 4 * (tid - 48));
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < C) {
+    veg[tid] = expf(vg[tid]);
+    vdec[tid] = expf(vg[C - 1] - vg[tid]);
+  }
+
+  // C x C warp tiles: rows m0 .. m0 + 15, columns n0 .. n0 + 31
+  const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+  float da1[1][4][4];
+  {
+    float qk[1][4][4], kk[1][4][4], dp[1][4][4];
+    wm::zero(qk);
+    wm::zero(kk);
+    wm::zero(dp);
+    wm::zero(da1);
+    auto fq = [&](int m, int x) { return to_f(rq_t[m * DP + x]); };
+    auto fk = [&](int m, int x) { return to_f(rk_t[m * DP + x]); };
+    auto fkt = [&](int x, int n) { return to_f(rk_t[n * DP + x]); };
+    wm::gemm<1, 4, XS, XS>(qk, fq, fkt, m0, n0, 0, D);
+    wm::gemm<1, 4, XS, XS>(kk, fk, fkt, m0, n0, 0, D);
+    // dP = scale tril(dO U^T)
+    auto fdo = [&](int m, int x) { return to_f(rdo_t[m * DP + x]); };
+    auto fut = [&](int x, int n) { return F1[n * WP + x]; };
+    wm::gemm<1, 4, XS, true>(dp, fdo, fut, m0, n0, 0, D);
+    // dU V^T
+    auto fdu = [&](int m, int x) { return F2[m * WP + x]; };
+    auto fvt = [&](int x, int n) { return to_f(rv_t[n * DP + x]); };
+    wm::gemm<1, 4, true, XS>(da1, fdu, fvt, m0, n0, 0, D);
+    const float sc = p.scale;
+    wm::for_each(qk, m0, n0, [&](int i, int c, float& x) { C2[i * CP + c] = vrq[i] * vrk[c] * x; });
+    wm::for_each(kk, m0, n0, [&](int i, int c, float& x) { C3[i * CP + c] = vrk[i] * vrk[c] * x; });
+    wm::for_each(dp, m0, n0, [&](int i, int c, float& x) { C4[i * CP + c] = c <= i ? sc * x : 0.f; });
+  }
+  __syncthreads();  // U, v and dO tiles no longer read
+  load_f32<D, WP>(F1, p.dw + item * C * D, D, C, tid, 256);
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  {
+    // dA = dU V^T + dW (diag(e^g/|k|) K)^T on and below the diagonal; then dZ, d beta, dGamma, dM^{-1}
+    float da2[1][4][4];
+    wm::zero(da2);
+    auto fdw = [&](int m, int x) { return F1[m * WP + x]; };
+    auto fkt = [&](int x, int n) { return to_f(rk_t[n * DP + x]); };
+    wm::gemm<1, 4, true, XS>(da2, fdw, fkt, m0, n0, 0, D);
+    float colp[4][2];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) colp[jj][0] = colp[jj][1] = 0.f;
+    const int r = wm::lane_r(), cl = wm::lane_c();
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = m0 + r + 8 * (e >> 1), c = n0 + 8 * jj + cl + (e & 1);
+        float dA = da1[0][jj][e] + da2[0][jj][e] * veg[c] * vrk[c];
+        float gam = 0.f, mv = 0.f;
+        if (c <= i) {
+          gam = expf(vg[i] - vg[c]);
+          mv = C1[i * CP + c];
+        } else {
+          dA = 0.f;
+        }
+        colp[jj][e & 1] += dA * gam * mv;
+        const float dZ = dA * vbt[c];
+        C2[i * CP + c] = c <= i ? C4[i * CP + c] * C2[i * CP + c] + dZ * mv : 0.f;
+        X1[i * CP + c] = dZ * gam;
+      }
+    const int lane = tid & 31;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const float s = col_sum(colp[jj][h2]);
+        if (lane < 4) vcolp[(warp & 3) * C + n0 + 8 * jj + cl + h2] = s;
+      }
+  }
+  __syncthreads();
+  if (tid < C) vdb[tid] = vcolp[tid] + vcolp[C + tid] + vcolp[2 * C + tid] + vcolp[3 * C + tid];
+  {
+    // T1 = M^{-T} dM^{-1}  (M^{-T}[i][l] = M^{-1}[l][i], zero for l < i)
+    float t1[1][4][4];
+    wm::zero(t1);
+    auto fa = [&](int m, int x) { return C1[x * CP + m]; };
+    auto fb = [&](int x, int n) { return X1[x * CP + n]; };
+    wm::gemm<1, 4, true, true>(t1, fa, fb, m0, n0, m0, C);
+    wm::for_each(t1, m0, n0, [&](int i, int c, float& x) { X2[i * CP + c] = x; });
+  }
+  __syncthreads();
+  {
+    // X = -T1 M^{-T}, strictly lower  (M^{-T}[l][c] = M^{-1}[c][l], zero for l > c)
+    float xx[1][4][4];
+    wm::zero(xx);
+    auto fa = [&](int m, int x) { return X2[m * CP + x]; };
+    auto fb = [&](int x, int n) { return C1[n * CP + x]; };
+    wm::gemm<1, 4, true, true>(xx, fa, fb, m0, n0, 0, n0 + 32);
+    wm::for_each(xx, m0, n0, [&](int i, int c, float& x) { X1[i * CP + c] = c < i ? -x : 0.f; });
+  }
+  __syncthreads();
+  {
+    // d beta_i += sum_c X_ic (k^_i . k^_c); row and column sums of dGamma . Gamma
+    const int i = tid >> 2, q4 = tid & 3;
+    float sb = 0.f, sr = 0.f, scol = 0.f;
+    for (int c = 16 * q4; c < 16 * q4 + 16; ++c) {
+      sb = fmaf(X1[i * CP + c], C3[i * CP + c], sb);
+      if (c <= i) sr = fmaf(C2[i * CP + c], expf(vg[i] - vg[c]), sr);
+      if (i <= c) scol = fmaf(C2[c * CP + i], expf(vg[c] - vg[i]), scol);
+    }
+    sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+    sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+    sr += __shfl_xor_sync(0xffffffffu, sr, 1);
+    sr += __shfl_xor_sync(0xffffffffu, sr, 2);
+    scol += __shfl_xor_sync(0xffffffffu, scol, 1);
+    scol += __shfl_xor_sync(0xffffffffu, scol, 2);
+    if (q4 == 0) {
+      vdb[i] += sb;
+      vrow[i] = sr;
+      vcol[i] = scol;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < C * C; e += 256) {  // M^{-1} -> A = (Gamma . M^{-1}) diag(beta)
+    const int i = e / C, c = e % C;
+    C1[i * CP + c] = c <= i ? expf(vg[i] - vg[c]) * C1[i * CP + c] * vbt[c] : 0.f;
+  }
+  __syncthreads();
+
+  // C x D warp tiles: rows m0 .. m0 + 15, columns nd .. nd + D/2
+  constexpr int NT = D / 16;
+  const int nd = (D / 2) * (warp >> 2);
+  const int r = wm::lane_r();
+  const int lane = tid & 31;
+  auto fat = [&](int m, int x) { return C1[x * CP + m]; };  // A^T: zero for x < m
+  {
+    // dv = A^T dU
+    float acc[1][NT][4];
+    wm::zero(acc);
+    auto fb = [&](int x, int n) { return F2[x * WP + n]; };
+    wm::gemm<1, NT, true, true>(acc, fat, fb, m0, nd, m0, C);
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      if (i < len) *reinterpret_cast<float2*>(p.dv + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+    });
+  }
+  {
+    // dk^ = diag(e^g) A^T dW + diag(dec) dKr + (Gamma . dP)^T Q^ + diag(beta) X K^ + X^T diag(beta) K^
+    float acc[1][NT][4];
+    wm::zero(acc);
+    auto fb = [&](int x, int n) { return F1[x * WP + n]; };
+    wm::gemm<1, NT, true, true>(acc, fat, fb, m0, nd, m0, C);
+    const float* dkr = p.dkr + item * C * D;
+    float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      const bool lo8 = i - m0 < 8;
+      const float k0 = to_f(rk_t[i * DP + c]) * vrk[i], k1 = to_f(rk_t[i * DP + c + 1]) * vrk[i];
+      const float2 kr = *reinterpret_cast<const float2*>(dkr + i * D + c);
+      const float ya = fmaf(k0, x0, k1 * x1), yb = fmaf(k0, kr.x, k1 * kr.y);
+      if (lo8) {
+        pa[0] += ya;
+        pb[0] += yb;
+      } else {
+        pa[1] += ya;
+        pb[1] += yb;
+      }
+      x0 = veg[i] * x0 + vdec[i] * kr.x;
+      x1 = veg[i] * x1 + vdec[i] * kr.y;
+    });
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float a = quad_sum(pa[hh]), b2 = quad_sum(pb[hh]);
+      if ((lane & 3) == 0) {
+        const int i = m0 + r + 8 * hh;
+        vpA[(warp >> 2) * C + i] = veg[i] * a;
+        vpB[(warp >> 2) * C + i] = vdec[i] * b2;
+      }
+    }
+    auto fa1 = [&](int m, int x) { return x >= m ? expf(vg[x] - vg[m]) * C4[x * CP + m] * vrq[x] : 0.f; };
+    auto fbq = [&](int x, int n) { return to_f(rq_t[x * DP + n]); };
+    wm::gemm<1, NT, true, XS>(acc, fa1, fbq, m0, nd, m0, C);
+    auto fa2 = [&](int m, int x) { return vrk[x] * (vbt[m] * X1[m * CP + x] + vbt[x] * X1[x * CP + m]); };
+    auto fbk = [&](int x, int n) { return to_f(rk_t[x * DP + n]); };
+    wm::gemm<1, NT, true, XS>(acc, fa2, fbk, m0, nd, 0, C);
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      if (i < len) *reinterpret_cast<float2*>(p.dkh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+    });
+  }
+  {
+    // dq^ = dQa + (Gamma . dP) diag(1/|k|) K
+    float acc[1][NT][4];
+    const float* dqa = p.dqa + item * C * D;
+    float pc[2] = {0.f, 0.f};
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      const float2 a = *reinterpret_cast<const float2*>(dqa + i * D + c);
+      x0 = a.x;
+      x1 = a.y;
+      const float y = fmaf(to_f(rq_t[i * DP + c]), a.x, to_f(rq_t[i * DP + c + 1]) * a.y);
+      if (i - m0 < 8) pc[0] += y; else pc[1] += y;
+    });
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float s = quad_sum(pc[hh]);
+      if ((lane & 3) == 0) {
+        const int i = m0 + r + 8 * hh;
+        vpC[(warp >> 2) * C + i] = vrq[i] * s;
+      }
+    }
+    auto fa = [&](int m, int x) { return x <= m ? expf(vg[m] - vg[x]) * C4[m * CP + x] * vrk[x] : 0.f; };
+    auto fbk = [&](int x, int n) { return to_f(rk_t[x * DP + n]); };
+    wm::gemm<1, NT, true, XS>(acc, fa, fbk, m0, nd, 0, m0 + 16);
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      if (i < len) *reinterpret_cast<float2*>(p.dqh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+    });
+  }
+  __syncthreads();
+  if (tid < C) {
+    const int i = tid;
+    const float rb = vpB[i] + vpB[C + i];
+    vdg[i] = (vpC[i] + vpC[C + i]) - rb + (vpA[i] + vpA[C + i]) + vrow[i] - vcol[i];
+    vrow[i] = rb;  // r_i, for the chunk-end term
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float sr = 0.f;
+    for (int i = 0; i < C; ++i) sr += vrow[i];
+    vdg[C - 1] += sr + p.dgc[item];
+    float run = 0.f;  // d log alpha_i = sum_{i' >= i} dg_i'
+    for (int i = C - 1; i >= 0; --i) {
+      run += vdg[i];
+      vdg[i] = run;
+    }
+  }
+  __syncthreads();
+  if (tid < len) {
+    const int64_t t = t0 + tid;
+    const float dla = vdg[tid];
+    const float x = p.a[t * p.HV + hv] + p.dt_bias[hv];
+    const float eA = expf(p.A_log[hv]);
+    const float sig = 1.f / (1.f + expf(-x));
+    const float bt = vbt[tid];
+    p.da[t * p.HV + hv] = dla * (-eA) * sig;
+    p.db[t * p.HV + hv] = vdb[tid] * bt * (1.f - bt);
+    p.dlala[t * p.HV + hv] = dla * (-eA * softplus_f(x));
+  }
+}
+
+// ----------------------------------------------------------------------------- norm, gate sums
+
+template <int D, typename E>
+__global__ void __launch_bounds__(256) bwd_norm_kernel(BwdParams p) {
+  if (p.status[0] != GDN_OK) return;
+  const int64_t wid = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.T * p.H) return;
+  const int64_t t = wid / p.H;
+  const int h = (int)(wid % p.H), r = p.HV / p.H;
+  constexpr int U = D / 32;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const E* x = static_cast<const E*>(which == 0 ? p.q : p.k) + (t * p.H + h) * D;
+    const float* gh = (which == 0 ? p.dqh : p.dkh) + (t * p.HV + (int64_t)h * r) * D;
+    float* out = (which == 0 ? p.dq : p.dk) + (t * p.H + h) * D;
+    float xv[U], gv[U], n2 = 0.f, dot = 0.f;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int d = lane + 32 * u;
+      xv[u] = to_f(x[d]);
+      float s = 0.f;
+      for (int e = 0; e < r; ++e) s += gh[(int64_t)e * D + d];
+      gv[u] = s;
+      n2 = fmaf(xv[u], xv[u], n2);
+      dot = fmaf(xv[u], s, dot);
+    }
+    n2 = warp_sum(n2);
+    dot = warp_sum(dot);
+    const float n = sqrtf(n2 + kNormEps);
+    const float inv = 1.f / n, c3 = dot / (n * n * n);
+#pragma unroll
+    for (int u = 0; u < U; ++u) out[lane + 32 * u] = gv[u] * inv - xv[u] * c3;
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_gate_sum_kernel(BwdParams p) {
+  __shared__ float s1[256], s2[256];
+  if (p.status[0] != GDN_OK) return;
+  const int hv = blockIdx.x, tid = threadIdx.x;
+  float a1 = 0.f, a2 = 0.f;
+  for (int64_t t = tid; t < p.T; t += 256) {
+    a1 += p.dlala[t * p.HV + hv];
+    a2 += p.da[t * p.HV + hv];
+  }
+  s1[tid] = a1;
+  s2[tid] = a2;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if (tid < o) {
+      s1[tid] += s1[tid + o];
+      s2[tid] += s2[tid + o];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    p.dA_log[hv] = s1[0];
+    p.ddt_bias[hv] = s2[0];
+  }
+}
+
+template <typename Kern>
+cudaError_t set_smem(Kern k, uint32_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int D, typename E>
+cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
+  cudaError_t e;
+  int n = 0;
+  const dim3 items((unsigned)p.max_chunks, (unsigned)p.HV);
+  const unsigned chains = (unsigned)((int64_t)p.B * p.HV * (D / VB));
+  if ((e = set_smem(bwd_factor_kernel<D, E>, FacSmem<D>::bytes)) != cudaSuccess) return e;
+  bwd_factor_kernel<D, E><<<items, 256, FacSmem<D>::bytes, s>>>(p);
+  ++n;
+  if (chains > 0) {
+    if ((e = set_smem(bwd_state_kernel<D, E>, StSmem<D>::bytes)) != cudaSuccess) return e;
+    bwd_state_kernel<D, E><<<chains, 128, StSmem<D>::bytes, s>>>(p);
+    if ((e = set_smem(bwd_dstate_kernel<D, E>, DsSmem<D>::bytes)) != cudaSuccess) return e;
+    bwd_dstate_kernel<D, E><<<chains, 128, DsSmem<D>::bytes, s>>>(p);
+    n += 2;
+  }
+  if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D>::bytes)) != cudaSuccess) return e;
+  bwd_sgrad_kernel<D, E><<<items, 256, SgSmem<D>::bytes, s>>>(p);
+  if ((e = set_smem(bwd_local_kernel<D, E>, LoSmem<D>::bytes)) != cudaSuccess) return e;
+  bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
+  n += 2;
+  const int64_t rows = p.T * p.H;
+  if (rows > 0) {
+    bwd_norm_kernel<D, E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+    ++n;
+  }
+  bwd_gate_sum_kernel<<<(unsigned)p.HV, 256, 0, s>>>(p);
+  ++n;
+  *kernels = n;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdParams& p, int D, bool fp16, cudaStream_t s, int* kernels) {
+  *kernels = 0;
+  if (D == 64) return fp16 ? launch_all<64, f16>(p, s, kernels) : launch_all<64, bf16>(p, s, kernels);
+  if (D == 128) return fp16 ? launch_all<128, f16>(p, s, kernels) : launch_all<128, bf16>(p, s, kernels);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gdn

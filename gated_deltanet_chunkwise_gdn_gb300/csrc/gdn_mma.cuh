@@ -1,0 +1,123 @@
+// gdn_mma.cuh — warp-level tensor-core products for the backward kernels.
+//
+// One warp computes a (16 MT) x (8 NT) tile of D += A B with m16n8k16 bf16 MMAs and fp32
+// accumulation. Operands are read element by element through accessor functors
+// (fa(m, k), fb(k, n) -> float), so one routine serves row-major, transposed and scaled
+// views of shared-memory tiles. An fp32 operand is carried as a bf16 pair hi + lo
+// (about 16 significant bits) and a product takes hi*hi + hi*lo + lo*hi; an operand whose
+// values are bf16 already (the raw bf16 q, k, v, dO tiles) is carried as hi alone, and the
+// terms with its lo part drop out. fp16 inputs are carried as pairs too (an fp16 value is
+// exactly the sum of two bf16 values).
+//
+// Fragment layout (lane = 4 r + c/2, r in 0..7, c in {0, 2, 4, 6}):
+//   A (16 x 16): a[u] = (row r + 8 (u & 1), columns c + 8 (u >> 1) and +1)
+//   B (16 x 8):  b[u] = (rows c + 8 u and +1, column r)
+//   D (16 x 8):  d[e] = (row r + 8 (e >> 1), column c + (e & 1))
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace wm {
+
+__device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ int lane_r() { return (threadIdx.x & 31) >> 2; }
+__device__ __forceinline__ int lane_c() { return 2 * (threadIdx.x & 3); }
+
+// x, y -> hi (and lo when SPLIT) as packed bf16 pairs.
+template <bool SPLIT>
+__device__ __forceinline__ void pack(float x, float y, uint32_t& hi, uint32_t& lo) {
+  if (SPLIT) {
+    split2<bf16>(x, y, hi, lo);
+  } else {
+    hi = pack_bf16(x, y);
+    lo = 0u;
+  }
+}
+
+template <bool SPLIT, class FA>
+__device__ __forceinline__ void load_a(uint32_t (&hi)[4], uint32_t (&lo)[4], const FA& fa, int m0, int k0) {
+  const int r = lane_r(), c = lane_c();
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int m = m0 + r + 8 * (u & 1), k = k0 + c + 8 * (u >> 1);
+    pack<SPLIT>(fa(m, k), fa(m, k + 1), hi[u], lo[u]);
+  }
+}
+
+template <bool SPLIT, class FB>
+__device__ __forceinline__ void load_b(uint32_t (&hi)[2], uint32_t (&lo)[2], const FB& fb, int k0, int n0) {
+  const int r = lane_r(), c = lane_c();
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int k = k0 + c + 8 * u, n = n0 + r;
+    pack<SPLIT>(fb(k, n), fb(k + 1, n), hi[u], lo[u]);
+  }
+}
+
+// acc[i][j] (the 16 x 8 tile at rows m0 + 16 i, columns n0 + 8 j) += A B over k in [k_lo, k_hi)
+// (multiples of 16). AS / BS: the operand carries a lo part.
+template <int MT, int NT, bool AS, bool BS, class FA, class FB>
+__device__ __forceinline__ void gemm(float (&acc)[MT][NT][4], const FA& fa, const FB& fb, int m0, int n0, int k_lo,
+                                     int k_hi) {
+  for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
+    uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) load_a<AS>(ah[i], al[i], fa, m0 + 16 * i, k0);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      uint32_t bh[2], bl[2];
+      load_b<BS>(bh, bl, fb, k0, n0 + 8 * j);
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        mma(acc[i][j], ah[i], bh);
+        if (BS) mma(acc[i][j], ah[i], bl);
+        if (AS) mma(acc[i][j], al[i], bh);
+      }
+    }
+  }
+}
+
+template <int MT, int NT>
+__device__ __forceinline__ void zero(float (&acc)[MT][NT][4]) {
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+}
+
+// f(row, col, value&) for every accumulator element of the thread.
+template <int MT, int NT, class F>
+__device__ __forceinline__ void for_each(float (&acc)[MT][NT][4], int m0, int n0, const F& f) {
+  const int r = lane_r(), c = lane_c();
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f(m0 + 16 * i + r + 8 * (e >> 1), n0 + 8 * j + c + (e & 1), acc[i][j][e]);
+}
+
+// f(row, col, x0&, x1&) for the element pairs (row, col), (row, col + 1) of the thread.
+template <int MT, int NT, class F>
+__device__ __forceinline__ void for_each_pair(float (&acc)[MT][NT][4], int m0, int n0, const F& f) {
+  const int r = lane_r(), c = lane_c();
+#pragma unroll
+  for (int i = 0; i < MT; ++i)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) f(m0 + 16 * i + r + 8 * h, n0 + 8 * j + c, acc[i][j][2 * h], acc[i][j][2 * h + 1]);
+}
+
+}  // namespace wm
+}  // namespace gdn

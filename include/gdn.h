@@ -191,6 +191,70 @@ GDN_API gdn_status gdn_decode_step(const void *q, const void *k, const void *v, 
                                    int32_t *device_status, void *stream);
 
 /*
+ * Bytes of workspace that gdn_chunkwise_backward needs for these sizes, or 0 if the
+ * sizes are not supported (K != V, K not in {64, 128}, chunk_size not in {64, 128},
+ * HV % H != 0, HV > 65535, total_tokens >= 2^31). About 384 KB per (64-token chunk,
+ * value head) at K = V = 128 plus 1 KB per (token, value head): the per-chunk
+ * intermediates of the backward are kept in fp32.
+ */
+GDN_API size_t gdn_backward_workspace_size(int64_t total_tokens, int32_t batch, int32_t H,
+                                           int32_t HV, int32_t K, int32_t V, int32_t chunk_size);
+
+/*
+ * Backward pass of gdn_extend_chunkwise: the gradients of
+ *
+ *   L = sum_t <d_out_t, out_t> + sum over (sequence, value head) <d_state, S_final>
+ *
+ * with respect to every input of the forward call with the same arguments. The pages
+ * give no backward formulas; the bottom-level GDN backward of "nrm-training-kernels",
+ * section "Kernel", takes the gradient arriving at the final state besides the output's
+ * (d_state here). The kernels apply the chain rule to the chunkwise WY form of
+ * "Simple math to speed up GDN prefill" (sections "Reminder" and "Save one invert"):
+ * a forward pass over the chunks that recomputes the state entering each chunk, a
+ * reverse pass over the chunks for the state gradient, then per-chunk gradients through
+ * the one inverse, the decays, the gates and the q/k normalisation.
+ *
+ *  q, k, v, a, b, A_log, dt_bias, cache_indices, cu_seqlens, batch, total_tokens, H, HV,
+ *  K, V, chunk_size, scale, dtype: as for gdn_extend_chunkwise (DEVICE pointers).
+ *  state_pool    [pool_size, HV, V, K] fp32, READ ONLY: the initial states, i.e. the
+ *                pool as the forward call found it (the forward overwrites the slots it
+ *                uses, so a caller that needs the backward keeps a copy).
+ *  d_out         [total_tokens, HV, V] same dtype as v: gradient of out.
+ *  d_state       [pool_size, HV, V, K] fp32: gradient of the final state of each
+ *                sequence, read at the batch's slots; NULL means zero.
+ *  dq, dk        [total_tokens, H, K] fp32, written (value heads sharing a q/k head
+ *                contribute their sum).
+ *  dv            [total_tokens, HV, V] fp32, written.
+ *  da, db        [total_tokens, HV] fp32, written.
+ *  dA_log, ddt_bias  [HV] fp32, written (sums over all tokens, in a fixed order).
+ *  d_state_pool  [pool_size, HV, V, K] fp32: the gradient of the initial states is
+ *                written at the batch's slots; other slots are untouched. It may be the
+ *                same buffer as d_state (each slot is read before it is written).
+ *  workspace     DEVICE pointer, 256-byte aligned, >= gdn_backward_workspace_size bytes,
+ *                owned by the caller; no two calls in flight may share one.
+ *
+ * Supported: K = V in {64, 128}; chunk_size 64 or 128 (the kernels work on 64-token WY
+ * blocks; the gradients do not depend on the block length in exact arithmetic).
+ * q, k, v, d_out 16-byte aligned; dv, state_pool, d_state, d_state_pool 8-byte aligned.
+ * Host-detectable errors return before anything is enqueued. Device-detected errors
+ * (cu_seqlens, cache_indices: as for gdn_extend_chunkwise) are recorded in the
+ * workspace's status word, read by gdn_get_device_status(workspace, stream); the
+ * gradient outputs are then left unwritten. Every sum is taken in a fixed order, so
+ * repeated calls give bit-identical results.
+ */
+GDN_API gdn_status gdn_chunkwise_backward(const void *q, const void *k, const void *v,
+                                          gdn_dtype dtype, const float *a, const float *b,
+                                          const float *A_log, const float *dt_bias,
+                                          const float *state_pool, int64_t pool_size,
+                                          const int64_t *cache_indices, const int64_t *cu_seqlens,
+                                          int32_t batch, const void *d_out, const float *d_state,
+                                          float *dq, float *dk, float *dv, float *da, float *db,
+                                          float *dA_log, float *ddt_bias, float *d_state_pool,
+                                          int64_t total_tokens, int32_t H, int32_t HV, int32_t K,
+                                          int32_t V, int32_t chunk_size, float scale,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Waits for `stream`, then returns the status recorded on the device by the last
  * gdn_extend_chunkwise call that used this workspace (GDN_OK, GDN_ERR_BAD_INDEX,
  * GDN_ERR_BAD_SEQLENS or GDN_ERR_TIMEOUT), or GDN_ERR_CUDA if the stream reported

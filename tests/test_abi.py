@@ -138,5 +138,49 @@ def test_calls_beyond_the_factor_row_limit_are_refused(lib):
 
 def test_kernel_kinds_named_for_the_profiler(lib):
     names = [lib.gdn_kernel_name(i) for i in range(8)]
-    assert [n.decode() for n in names[:6]] == ["schedule", "gates", "intra", "scan", "decode_check", "decode"]
-    assert names[6] is None and lib.gdn_kernel_name(-1) is None
+    assert [n.decode() for n in names[:7]] == ["schedule", "gates", "intra", "scan", "decode_check", "decode",
+                                               "backward"]
+    assert names[7] is None and lib.gdn_kernel_name(-1) is None
+
+
+def test_backward_workspace_size_rules(lib):
+    ws = lib.gdn_backward_workspace_size
+    assert ws(65536, 1, 16, 16, 128, 128, 64) > 0
+    assert ws(0, 0, 1, 1, 64, 64, 64) > 0
+    assert ws(100, 2, 3, 4, 128, 128, 64) == 0     # HV not a multiple of H
+    assert ws(100, 2, 2, 4, 256, 256, 128) == 0    # wide heads: no backward
+    assert ws(100, 2, 2, 4, 128, 64, 64) == 0      # K != V
+    assert ws(100, 2, 2, 4, 128, 128, 32) == 0     # chunk size
+    assert ws(100, 2, 1, 1 << 16, 64, 64, 64) == 0  # HV above the grid's y limit
+    assert ws(1000, 2, 2, 4, 128, 128, 128) == ws(1000, 2, 2, 4, 128, 128, 64)
+    # fp32 intermediates: (C*C*2 + C*D*7 + D*D*2) floats per (chunk, value head) and 2*D + 1 per (token, value head)
+    per_item = (64 * 64 * 2 + 64 * 128 * 7 + 128 * 128 * 2) * 4
+    assert ws(65536, 1, 16, 16, 128, 128, 64) >= 1025 * 16 * per_item + 65536 * 16 * (2 * 128 + 1) * 4
+
+
+def _bwd(lib, **over):
+    args = dict(q=16, k=16, v=16, dtype=0, a=16, b=16, A_log=16, dt_bias=16, pool=16, pool_size=4, idx=16, cu=16,
+                batch=2, d_out=16, d_state=None, dq=16, dk=16, dv=16, da=16, db=16, dA_log=16, ddt_bias=16,
+                d_pool=16, T=100, H=2, HV=4, K=128, V=128, C=64, scale=1.0, ws=256, ws_bytes=1 << 40, stream=None)
+    args.update(over)
+    return lib.gdn_chunkwise_backward(*[args[k] for k in (
+        "q", "k", "v", "dtype", "a", "b", "A_log", "dt_bias", "pool", "pool_size", "idx", "cu", "batch",
+        "d_out", "d_state", "dq", "dk", "dv", "da", "db", "dA_log", "ddt_bias", "d_pool",
+        "T", "H", "HV", "K", "V", "C", "scale", "ws", "ws_bytes", "stream")])
+
+
+def test_backward_host_side_errors_return_before_any_device_work(lib):
+    assert _bwd(lib, HV=3) == 1              # HV % H != 0
+    assert _bwd(lib, q=None) == 1            # null input
+    assert _bwd(lib, d_out=None) == 1
+    assert _bwd(lib, dq=None) == 1           # null output
+    assert _bwd(lib, dA_log=None) == 1
+    assert _bwd(lib, d_pool=None) == 1
+    assert _bwd(lib, dtype=3) == 1
+    assert _bwd(lib, q=24) == 1              # tiles are copied in 16-byte pieces
+    assert _bwd(lib, dv=12) == 1             # 8-byte stores
+    assert _bwd(lib, K=256, V=256) == 2      # not built for the backward
+    assert _bwd(lib, C=32) == 2
+    assert _bwd(lib, ws=None) == 4
+    assert _bwd(lib, ws=264) == 4
+    assert _bwd(lib, ws_bytes=16) == 4
