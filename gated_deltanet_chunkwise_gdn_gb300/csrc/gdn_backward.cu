@@ -64,8 +64,8 @@ BwdLayout make_bwd_layout(int64_t T, int B, int H, int HV, int D) {
   L.rq = take(per * C * sizeof(float));
   L.rk = take(per * C * sizeof(float));
   L.minv = take(per * C * C * sizeof(float));
-  L.pm = take(per * C * C * sizeof(float));
-  L.w = take(per * C * D * sizeof(float));
+  L.pm = take(per * 2 * C * C * sizeof(bf16));
+  L.w = take(per * 2 * C * D * sizeof(bf16));
   L.ut = take(per * C * D * sizeof(float));
   L.s_in = take(per * D * D * sizeof(float));
   L.u = take(per * C * D * sizeof(float));
@@ -75,8 +75,11 @@ BwdLayout make_bwd_layout(int64_t T, int B, int H, int HV, int D) {
   L.dw = take(per * C * D * sizeof(float));
   L.dkr = take(per * C * D * sizeof(float));
   L.dgc = take(per * sizeof(float));
-  L.dqh = take((size_t)T * HV * D * sizeof(float));
-  L.dkh = take((size_t)T * HV * D * sizeof(float));
+  // gradients of q^, k^ per value head: only with grouped heads (otherwise the local kernel
+  // applies the normalisation's backward itself)
+  const size_t per_head_grads = HV != H ? (size_t)T * HV * D * sizeof(float) : 0;
+  L.dqh = take(per_head_grads);
+  L.dkh = take(per_head_grads);
   L.dlala = take((size_t)T * HV * sizeof(float));
   L.total = off;
   return L;
@@ -86,9 +89,9 @@ namespace {
 
 constexpr int C = 64;   // WY block (tokens per chunk)
 constexpr int VB = 16;  // state rows per CTA of the sequential passes
+constexpr int kSeqThreads = 256;  // 8 warps per CTA of the sequential passes
 constexpr int CP = C + 4;   // pitch (floats) of C x C fp32 tiles
 constexpr int UP = VB + 4;  // pitch (floats) of C x VB fp32 tiles
-constexpr int DOP = VB + 8; // pitch (elements) of C x VB 16-bit tiles
 
 template <typename E>
 constexpr bool kSplitSrc = std::is_same<E, f16>::value;  // fp16 tiles enter the MMAs as bf16 pairs
@@ -243,11 +246,11 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
     wm::for_each(kk, m0, n0, [&](int i, int c, float& x) {
       sL[i * CP + c] = c < i ? vb[i] * vrk[i] * vrk[c] * x : 0.f;
     });
-    float* P = p.pm + item * C * C;
+    bf16* P = reinterpret_cast<bf16*>(p.pm) + item * 2 * C * C;  // hi, lo planes
     wm::for_each_pair(qk, m0, n0, [&](int i, int c, float& x0, float& x1) {
       const float y0 = c <= i ? expf(vg[i] - vg[c]) * vrq[i] * vrk[c] * x0 : 0.f;
       const float y1 = c + 1 <= i ? expf(vg[i] - vg[c + 1]) * vrq[i] * vrk[c + 1] * x1 : 0.f;
-      *reinterpret_cast<float2*>(P + i * C + c) = make_float2(y0, y1);
+      wm::store_split2(P + i * C + c, P + C * C + i * C + c, y0, y1);
     });
   }
   __syncthreads();
@@ -290,9 +293,9 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
     float acc[1][NT][4];
     wm::zero(acc);
     wm::gemm<1, NT, true, XS>(acc, fa_w, fb_k, m0, nw, 0, m0 + 16);
-    float* Wg = p.w + item * C * D;
+    bf16* Wg = reinterpret_cast<bf16*>(p.w) + item * 2 * C * D;  // hi, lo planes
     wm::for_each_pair(acc, m0, nw, [&](int i, int c, float& x0, float& x1) {
-      *reinterpret_cast<float2*>(Wg + i * D + c) = make_float2(x0, x1);
+      wm::store_split2(Wg + i * D + c, Wg + C * D + i * D + c, x0, x1);
     });
   }
   {
@@ -307,19 +310,57 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
 }
 
 // ----------------------------------------------------------------------------- state (forward states)
+//
+// The two sequential passes take every MMA operand from bf16 planes in shared memory through
+// ldmatrix: an fp32 operand as two planes (hi, lo), a bf16 input tile as one. W<- and P arrive as
+// planes from the factor kernel; the state (or its gradient) and the chunk's small C x VB
+// operands are split into planes once per chunk. fp16 q/k/dO tiles are split into bf16 planes
+// after they land (an fp16 value is exactly hi + lo).
+
+// Splits an fp16 token tile (rows x W, pitch P) in place into bf16 planes: the hi plane
+// overwrites the tile, the lo plane goes to `lo` (same pitch).
+template <int W, int P>
+__device__ __forceinline__ void split_inplace(f16* tile, bf16* lo, int rows, int tid, int nthr) {
+  for (int e = tid; e < rows * W / 2; e += nthr) {
+    const int i = e / (W / 2), c = (e % (W / 2)) * 2;
+    const float x0 = __half2float(tile[i * P + c]), x1 = __half2float(tile[i * P + c + 1]);
+    wm::store_split2(reinterpret_cast<bf16*>(tile) + i * P + c, lo + i * P + c, x0, x1);
+  }
+}
+template <int W, int P>
+__device__ __forceinline__ void split_inplace(bf16*, bf16*, int, int, int) {}
+
+// MMA terms of one product: hi*hi, hi*lo (B has lo), lo*hi (A has lo).
+template <bool AL, bool BL>
+__device__ __forceinline__ void mma_terms(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                          const uint32_t* bh, const uint32_t* bl) {
+  const uint32_t b0[2] = {bh[0], bh[1]};
+  wm::mma(d, ah, b0);
+  if (BL) {
+    const uint32_t b1[2] = {bl[0], bl[1]};
+    wm::mma(d, ah, b1);
+  }
+  if (AL) wm::mma(d, al, b0);
+}
 
 template <int D>
 struct StSmem {
-  static constexpr int DP = D + 8, WP = D + 4;
-  static constexpr uint32_t W = 0;                   // per stage: W<- fp32 [C][WP]
-  static constexpr uint32_t K = W + C * WP * 4;      //            k 16-bit [C][DP]
-  static constexpr uint32_t UT = K + C * DP * 2;     //            U~ columns fp32 [C][UP]
+  static constexpr int DP = D + 8, HP = VB + 8;
+  static constexpr uint32_t TILE = C * DP * 2;       // one 16-bit C x D tile
+  static constexpr uint32_t WH = 0;                  // per stage: W<- hi, lo planes [C][DP]
+  static constexpr uint32_t WL = WH + TILE;
+  static constexpr uint32_t K = WL + TILE;           //            k [C][DP] (the input's type)
+  static constexpr uint32_t UT = K + TILE;           //            U~ columns fp32 [C][UP]
   static constexpr uint32_t VEC = UT + C * UP * 4;   //            g, 1/|k|
   static constexpr uint32_t STAGE = VEC + 2 * C * 4;
-  static constexpr uint32_t S = 2 * STAGE;           // state rows fp32 [VB][WP]
-  static constexpr uint32_t U = S + VB * WP * 4;     // U columns fp32 [C][UP]
-  static constexpr uint32_t SK = U + C * UP * 4;     // e^{g_C - g} / |k|
-  static constexpr uint32_t bytes = SK + C * 4;
+  static constexpr uint32_t SH = 2 * STAGE;          // state rows hi, lo planes [VB][DP]
+  static constexpr uint32_t SL = SH + VB * DP * 2;
+  static constexpr uint32_t UKH = SL + VB * DP * 2;  // diag(e^{g_C - g}/|k|) U, hi, lo planes [C][HP]
+  static constexpr uint32_t UKL = UKH + C * HP * 2;
+  static constexpr uint32_t KL = UKL + C * HP * 2;   // fp16 inputs: the lo plane of k (its hi plane
+                                                     // overwrites the stage's k tile)
+  static constexpr uint32_t bytes_bf16 = KL;
+  static constexpr uint32_t bytes_fp16 = KL + TILE;
 };
 
 // The CTA's chain: sequence (longest first), value head, first state row.
@@ -344,37 +385,47 @@ __device__ __forceinline__ ChainJob chain_job(const BwdParams& p) {
 }
 
 template <int D, typename E>
-__global__ void __launch_bounds__(128) bwd_state_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
   using S = StSmem<D>;
-  constexpr int DP = S::DP, WP = S::WP;
+  constexpr int DP = S::DP, HP = S::HP;
   constexpr bool XS = kSplitSrc<E>;
-  constexpr int NTS = D / 32;  // 8-column tiles per warp of the VB x D state
+  constexpr int NTS = D / 64;  // 8-column tiles per warp of the VB x D state (8 warps)
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
   const ChainJob jb = chain_job<D>(p);
   const int tid = threadIdx.x, warp = tid >> 5;
-  float* sS = reinterpret_cast<float*>(smem + S::S);
-  float* sU = reinterpret_cast<float*>(smem + S::U);
-  float* vsk = reinterpret_cast<float*>(smem + S::SK);
+  bf16* sSH = reinterpret_cast<bf16*>(smem + S::SH);
+  bf16* sSL = reinterpret_cast<bf16*>(smem + S::SL);
+  bf16* sUKH = reinterpret_cast<bf16*>(smem + S::UKH);
+  bf16* sUKL = reinterpret_cast<bf16*>(smem + S::UKL);
+  bf16* sKL = reinterpret_cast<bf16*>(smem + S::KL);
   const E* kin = static_cast<const E*>(p.k) + (int64_t)jb.h * D;
 
   auto issue = [&](int c, int st) {
     unsigned char* base = smem + st * S::STAGE;
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
-    load_f32<D, WP>(reinterpret_cast<float*>(base + S::W), p.w + item * C * D, D, C, tid, 128);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
-    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, tid, 128);
+    const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
+    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, tid, kSeqThreads);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
     if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
     else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rk + item * C + 4 * (tid - 16));
   };
 
   const float* S0 = p.state_pool + (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
-  const int ns0 = warp * (D / 4);  // the warp's state columns
+  const int ns0 = warp * (D / 8);                         // the warp's state columns
+  const int mu = 16 * (warp & 3), nu = 8 * (warp >> 2);  // the warp's 16 x 8 tile of U (C x VB)
   float st[1][NTS][4];
   wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { x = S0[i * D + c]; });
-  wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { sS[i * WP + c] = x; });
+  auto store_state = [&]() {
+    wm::for_each_pair(st, 0, ns0, [&](int i, int c, float& x0, float& x1) {
+      wm::store_split2(sSH + i * DP + c, sSL + i * DP + c, x0, x1);
+    });
+  };
+  store_state();
   if (jb.c1 > jb.c0) issue(jb.c0, 0);
   cp_async_commit();
 
@@ -385,79 +436,116 @@ __global__ void __launch_bounds__(128) bwd_state_kernel(BwdParams p) {
     if (c + 1 < jb.c1) issue(c + 1, stg ^ 1);
     cp_async_commit();
     const unsigned char* base = smem + stg * S::STAGE;
-    const float* sW = reinterpret_cast<const float*>(base + S::W);
-    const E* sK = reinterpret_cast<const E*>(base + S::K);
+    const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
+    const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
+    E* sK = reinterpret_cast<E*>(smem + stg * S::STAGE + S::K);
     const float* sUT = reinterpret_cast<const float*>(base + S::UT);
     const float* vg = reinterpret_cast<const float*>(base + S::VEC);
     const float* vrk = vg + C;
     const int64_t item = (int64_t)c * p.HV + jb.hv;
+    split_inplace<D, DP>(sK, sKL, XS ? C : 0, tid, kSeqThreads);
 
     // the state entering this chunk
     float* Sin = p.s_in + item * D * D + (int64_t)jb.vb * D;
     wm::for_each_pair(st, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
       *reinterpret_cast<float2*>(Sin + i * D + cc) = make_float2(x0, x1);
     });
-    // U = U~ - W<- S^T (C x VB): warp rows 16 warp
+    // U = U~ - W<- S^T (C x VB); then diag(e^{g_C - g}/|k|) U as planes for the state update
     {
-      float ua[1][2][4];
-      wm::zero(ua);
-      auto fa = [&](int m, int x) { return sW[m * WP + x]; };
-      auto fb = [&](int x, int n) { return sS[n * WP + x]; };
-      wm::gemm<1, 2, true, true>(ua, fa, fb, 16 * warp, 0, 0, D);
+      float ua[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k0 = 0; k0 < D; k0 += 16) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        wm::lda(ah, sWH, DP, mu, k0);
+        wm::lda(al, sWL, DP, mu, k0);
+        wm::ldb1(bh, sSH, DP, k0, nu);
+        wm::ldb1(bl, sSL, DP, k0, nu);
+        mma_terms<true, true>(ua, ah, al, bh, bl);
+      }
       float* Ug = p.u + item * C * D + jb.vb;
-      wm::for_each_pair(ua, 16 * warp, 0, [&](int i, int cc, float& x0, float& x1) {
-        const float u0 = sUT[i * UP + cc] - x0, u1 = sUT[i * UP + cc + 1] - x1;
-        sU[i * UP + cc] = u0;
-        sU[i * UP + cc + 1] = u1;
+      const float gC = vg[C - 1];
+      const int r = wm::lane_r(), cl = wm::lane_c();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = mu + r + 8 * hh, cc = nu + cl;
+        const float u0 = sUT[i * UP + cc] - ua[2 * hh], u1 = sUT[i * UP + cc + 1] - ua[2 * hh + 1];
         *reinterpret_cast<float2*>(Ug + i * D + cc) = make_float2(u0, u1);
-      });
-      if (tid < C) vsk[tid] = expf(vg[C - 1] - vg[tid]) * vrk[tid];
+        const float sk = expf(gC - vg[i]) * vrk[i];
+        wm::store_split2(sUKH + i * HP + cc, sUKL + i * HP + cc, sk * u0, sk * u1);
+      }
     }
     __syncthreads();
-    // S = e^{g_C} S + U^T diag(e^{g_C - g} / |k|) K
+    // S = e^{g_C} S + (diag(e^{g_C - g}/|k|) U)^T K
     {
       const float eC = expf(vg[C - 1]);
       wm::for_each(st, 0, ns0, [&](int, int, float& x) { x *= eC; });
-      auto fa = [&](int m, int x) { return sU[x * UP + m] * vsk[x]; };
-      auto fb = [&](int x, int n) { return to_f(sK[x * DP + n]); };
-      wm::gemm<1, NTS, true, XS>(st, fa, fb, 0, ns0, 0, C);
-      wm::for_each(st, 0, ns0, [&](int i, int cc, float& x) { sS[i * WP + cc] = x; });
+      const bf16* kh = reinterpret_cast<const bf16*>(sK);
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 16) {
+        uint32_t ah[4], al[4];
+        wm::lda_t(ah, sUKH, HP, 0, k0);
+        wm::lda_t(al, sUKL, HP, 0, k0);
+#pragma unroll
+        for (int j = 0; j < NTS; ++j) {
+          uint32_t bh[2], bl[2];
+          wm::ldb1_t(bh, kh, DP, k0, ns0 + 8 * j);
+          if (XS) wm::ldb1_t(bl, sKL, DP, k0, ns0 + 8 * j);
+          mma_terms<true, XS>(st[0][j], ah, al, bh, bl);
+        }
+      }
+      store_state();
     }
   }
 }
 
 // ----------------------------------------------------------------------------- dstate (reverse)
 
-template <int D>
+template <int D, bool XS>
 struct DsSmem {
-  static constexpr int DP = D + 8, WP = D + 4;
-  static constexpr uint32_t P = 0;                   // per stage: P fp32 [C][CP]
-  static constexpr uint32_t DO = P + C * CP * 4;     //            dO columns 16-bit [C][DOP]
-  static constexpr uint32_t K = DO + C * DOP * 2;    //            k 16-bit [C][DP]
-  static constexpr uint32_t Q = K + C * DP * 2;      //            q 16-bit [C][DP]
-  static constexpr uint32_t W = Q + C * DP * 2;      //            W<- fp32 [C][WP]
-  static constexpr uint32_t VEC = W + C * WP * 4;    //            g, 1/|q|, 1/|k|
+  static constexpr int DP = D + 8, HP = VB + 8, PP = C + 8;
+  static constexpr int NST = XS ? 1 : 2;              // fp16 inputs: one stage (room for the lo planes)
+  static constexpr uint32_t TILE = C * DP * 2;
+  static constexpr uint32_t PH = 0;                  // per stage: P hi, lo planes [C][PP]
+  static constexpr uint32_t PL = PH + C * PP * 2;
+  static constexpr uint32_t DO = PL + C * PP * 2;    //            dO columns [C][HP] (input type)
+  static constexpr uint32_t K = DO + C * HP * 2;     //            k [C][DP]
+  static constexpr uint32_t Q = K + TILE;            //            q [C][DP]
+  static constexpr uint32_t WH = Q + TILE;           //            W<- hi, lo planes [C][DP]
+  static constexpr uint32_t WL = WH + TILE;
+  static constexpr uint32_t VEC = WL + TILE;         //            g, 1/|q|, 1/|k|
   static constexpr uint32_t STAGE = VEC + 3 * C * 4;
-  static constexpr uint32_t DS = 2 * STAGE;          // gradient rows fp32 [VB][WP]
-  static constexpr uint32_t DU = DS + VB * WP * 4;   // dU columns fp32 [C][UP]
-  static constexpr uint32_t SK = DU + C * UP * 4;    // e^{g_C - g} / |k|, scale e^g / |q|
-  static constexpr uint32_t bytes = SK + 2 * C * 4;
+  static constexpr uint32_t GH = NST * STAGE;        // gradient rows hi, lo planes [VB][DP]
+  static constexpr uint32_t GL = GH + VB * DP * 2;
+  static constexpr uint32_t NUH = GL + VB * DP * 2;  // -dU hi, lo planes [C][HP]
+  static constexpr uint32_t NUL = NUH + C * HP * 2;
+  static constexpr uint32_t OSH = NUL + C * HP * 2;  // scale diag(e^g/|q|) dO hi, lo planes [C][HP]
+  static constexpr uint32_t OSL = OSH + C * HP * 2;
+  static constexpr uint32_t XQL = OSL + C * HP * 2;  // fp16 inputs: lo planes of q, k, dO (their hi
+  static constexpr uint32_t XKL = XQL + TILE;        // planes overwrite the stage's tiles)
+  static constexpr uint32_t XOL = XKL + TILE;
+  static constexpr uint32_t bytes = XS ? XOL + C * HP * 2 : XQL;
+  static_assert(bytes <= 232448, "shared memory per CTA");
 };
 
 template <int D, typename E>
-__global__ void __launch_bounds__(128) bwd_dstate_kernel(BwdParams p) {
-  using S = DsSmem<D>;
-  constexpr int DP = S::DP, WP = S::WP;
+__global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
   constexpr bool XS = kSplitSrc<E>;
-  constexpr int NTS = D / 32;
+  using S = DsSmem<D, XS>;
+  constexpr int DP = S::DP, HP = S::HP, PP = S::PP;
+  constexpr int NTS = D / 64;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
   const ChainJob jb = chain_job<D>(p);
   const int tid = threadIdx.x, warp = tid >> 5;
-  float* sdS = reinterpret_cast<float*>(smem + S::DS);
-  float* sdU = reinterpret_cast<float*>(smem + S::DU);
-  float* vsk = reinterpret_cast<float*>(smem + S::SK);
-  float* vsq = vsk + C;
+  bf16* sGH = reinterpret_cast<bf16*>(smem + S::GH);
+  bf16* sGL = reinterpret_cast<bf16*>(smem + S::GL);
+  bf16* sNUH = reinterpret_cast<bf16*>(smem + S::NUH);
+  bf16* sNUL = reinterpret_cast<bf16*>(smem + S::NUL);
+  bf16* sOSH = reinterpret_cast<bf16*>(smem + S::OSH);
+  bf16* sOSL = reinterpret_cast<bf16*>(smem + S::OSL);
+  bf16* xql = reinterpret_cast<bf16*>(smem + S::XQL);
+  bf16* xkl = reinterpret_cast<bf16*>(smem + S::XKL);
+  bf16* xol = reinterpret_cast<bf16*>(smem + S::XOL);
   const E* kin = static_cast<const E*>(p.k) + (int64_t)jb.h * D;
   const E* qin = static_cast<const E*>(p.q) + (int64_t)jb.h * D;
   const E* doin = static_cast<const E*>(p.d_out) + (int64_t)jb.hv * D + jb.vb;
@@ -466,11 +554,16 @@ __global__ void __launch_bounds__(128) bwd_dstate_kernel(BwdParams p) {
     unsigned char* base = smem + st * S::STAGE;
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
-    load_f32<C, CP>(reinterpret_cast<float*>(base + S::P), p.pm + item * C * C, C, C, tid, 128);
-    load_tokens_cols<VB, DOP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, tid, 128);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, tid, 128);
-    load_f32<D, WP>(reinterpret_cast<float*>(base + S::W), p.w + item * C * D, D, C, tid, 128);
+    const bf16* pp = reinterpret_cast<const bf16*>(p.pm) + item * 2 * C * C;
+    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PH), pp, C, 0, C, tid, kSeqThreads);
+    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PL), pp + C * C, C, 0, C, tid, kSeqThreads);
+    load_tokens_cols<VB, HP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, tid,
+                             kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
+    const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, tid, kSeqThreads);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
     if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
     else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rq + item * C + 4 * (tid - 16));
@@ -478,79 +571,120 @@ __global__ void __launch_bounds__(128) bwd_dstate_kernel(BwdParams p) {
   };
 
   const int64_t srow = (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
-  const int ns0 = warp * (D / 4);
+  const int ns0 = warp * (D / 8);
+  const int mu = 16 * (warp & 3), nu = 8 * (warp >> 2);
   float ds[1][NTS][4];
   wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { x = p.d_state ? p.d_state[srow + i * D + c] : 0.f; });
-  wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { sdS[i * WP + c] = x; });
+  auto store_grad = [&]() {
+    wm::for_each_pair(ds, 0, ns0, [&](int i, int c, float& x0, float& x1) {
+      wm::store_split2(sGH + i * DP + c, sGL + i * DP + c, x0, x1);
+    });
+  };
+  store_grad();
   if (jb.c1 > jb.c0) issue(jb.c1 - 1, 0);
   cp_async_commit();
 
   for (int c = jb.c1 - 1; c >= jb.c0; --c) {
-    const int stg = (jb.c1 - 1 - c) & 1;
+    const int stg = S::NST == 2 ? (jb.c1 - 1 - c) & 1 : 0;
     cp_async_wait<0>();
     __syncthreads();
-    if (c - 1 >= jb.c0) issue(c - 1, stg ^ 1);
+    if (S::NST == 2 && c - 1 >= jb.c0) issue(c - 1, stg ^ 1);
     cp_async_commit();
-    const unsigned char* base = smem + stg * S::STAGE;
-    const float* sP = reinterpret_cast<const float*>(base + S::P);
-    const E* sDO = reinterpret_cast<const E*>(base + S::DO);
-    const E* sK = reinterpret_cast<const E*>(base + S::K);
-    const E* sQ = reinterpret_cast<const E*>(base + S::Q);
-    const float* sW = reinterpret_cast<const float*>(base + S::W);
+    unsigned char* base = smem + stg * S::STAGE;
+    const bf16* sPH = reinterpret_cast<const bf16*>(base + S::PH);
+    const bf16* sPL = reinterpret_cast<const bf16*>(base + S::PL);
+    E* sDO = reinterpret_cast<E*>(base + S::DO);
+    E* sK = reinterpret_cast<E*>(base + S::K);
+    E* sQ = reinterpret_cast<E*>(base + S::Q);
+    const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
+    const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
     const float* vg = reinterpret_cast<const float*>(base + S::VEC);
     const float* vrq = vg + C;
     const float* vrk = vg + 2 * C;
     const int64_t item = (int64_t)c * p.HV + jb.hv;
+    if (XS) {
+      split_inplace<D, DP>(sQ, xql, C, tid, kSeqThreads);
+      split_inplace<D, DP>(sK, xkl, C, tid, kSeqThreads);
+      split_inplace<VB, HP>(sDO, xol, C, tid, kSeqThreads);
+      __syncthreads();
+    }
+    const bf16* qh = reinterpret_cast<const bf16*>(sQ);
+    const bf16* kh = reinterpret_cast<const bf16*>(sK);
+    const bf16* oh = reinterpret_cast<const bf16*>(sDO);
+    // a dO value of the tile (fp16 inputs: hi + lo, exactly)
+    auto dov = [&](int i, int cc) {
+      return XS ? __bfloat162float(oh[i * HP + cc]) + __bfloat162float(xol[i * HP + cc]) : to_f(sDO[i * HP + cc]);
+    };
 
     // the gradient of the state leaving this chunk
     float* dSo = p.ds_out + item * D * D + (int64_t)jb.vb * D;
     wm::for_each_pair(ds, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
       *reinterpret_cast<float2*>(dSo + i * D + cc) = make_float2(x0, x1);
     });
-    if (tid < C) {
-      vsk[tid] = expf(vg[C - 1] - vg[tid]) * vrk[tid];
-      vsq[tid] = p.scale * expf(vg[tid]) * vrq[tid];
-    }
-    // dU = scale P^T dO + diag(e^{g_C - g} / |k|) (K dS^T)   (C x VB): warp rows 16 warp
+    // dU = scale P^T dO + diag(e^{g_C - g}/|k|) (K dS^T)  (C x VB): the warp's 16 x 8 tile; also the
+    // planes of -dU and of scale diag(e^g/|q|) dO for the state-gradient update
     {
-      const int m0 = 16 * warp;
-      float a1[1][2][4], a2[1][2][4];
-      wm::zero(a1);
-      wm::zero(a2);
-      auto fa1 = [&](int m, int x) { return sP[x * CP + m]; };  // P^T: zero for x < m
-      auto fb1 = [&](int x, int n) { return to_f(sDO[x * DOP + n]); };
-      auto fa2 = [&](int m, int x) { return to_f(sK[m * DP + x]); };
-      auto fb2 = [&](int x, int n) { return sdS[n * WP + x]; };
-      wm::gemm<1, 2, true, XS>(a1, fa1, fb1, m0, 0, m0, C);
-      wm::gemm<1, 2, XS, true>(a2, fa2, fb2, m0, 0, 0, D);
-      __syncthreads();  // vsk written
+      float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int k0 = mu; k0 < C; k0 += 16) {  // P^T is upper triangular: rows mu.. need k >= mu
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        wm::lda_t(ah, sPH, PP, mu, k0);
+        wm::lda_t(al, sPL, PP, mu, k0);
+        wm::ldb1_t(bh, oh, HP, k0, nu);
+        if (XS) wm::ldb1_t(bl, xol, HP, k0, nu);
+        mma_terms<true, XS>(a1, ah, al, bh, bl);
+      }
+#pragma unroll
+      for (int k0 = 0; k0 < D; k0 += 16) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        wm::lda(ah, kh, DP, mu, k0);
+        if (XS) wm::lda(al, xkl, DP, mu, k0);
+        wm::ldb1(bh, sGH, DP, k0, nu);
+        wm::ldb1(bl, sGL, DP, k0, nu);
+        mma_terms<XS, true>(a2, ah, al, bh, bl);
+      }
       float* dUg = p.du + item * C * D + jb.vb;
-      const float sc = p.scale;
+      const float sc = p.scale, gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int i = m0 + r + 8 * hh, cc = 8 * jj + cl;
-          const float y0 = sc * a1[0][jj][2 * hh] + vsk[i] * a2[0][jj][2 * hh];
-          const float y1 = sc * a1[0][jj][2 * hh + 1] + vsk[i] * a2[0][jj][2 * hh + 1];
-          sdU[i * UP + cc] = y0;
-          sdU[i * UP + cc + 1] = y1;
-          *reinterpret_cast<float2*>(dUg + i * D + cc) = make_float2(y0, y1);
-        }
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = mu + r + 8 * hh, cc = nu + cl;
+        const float sk = expf(gC - vg[i]) * vrk[i];
+        const float y0 = sc * a1[2 * hh] + sk * a2[2 * hh];
+        const float y1 = sc * a1[2 * hh + 1] + sk * a2[2 * hh + 1];
+        *reinterpret_cast<float2*>(dUg + i * D + cc) = make_float2(y0, y1);
+        wm::store_split2(sNUH + i * HP + cc, sNUL + i * HP + cc, -y0, -y1);
+        const float sq = sc * expf(vg[i]) * vrq[i];
+        wm::store_split2(sOSH + i * HP + cc, sOSL + i * HP + cc, sq * dov(i, cc), sq * dov(i, cc + 1));
+      }
     }
     __syncthreads();
-    // dS = e^{g_C} dS + (scale diag(e^g / |q|) dO)^T Q - dU^T W<-   (VB x D)
+    // dS = e^{g_C} dS + (scale diag(e^g/|q|) dO)^T Q - dU^T W<-   (VB x D)
     {
       const float eC = expf(vg[C - 1]);
       wm::for_each(ds, 0, ns0, [&](int, int, float& x) { x *= eC; });
-      auto fa1 = [&](int m, int x) { return to_f(sDO[x * DOP + m]) * vsq[x]; };
-      auto fb1 = [&](int x, int n) { return to_f(sQ[x * DP + n]); };
-      auto fa2 = [&](int m, int x) { return -sdU[x * UP + m]; };
-      auto fb2 = [&](int x, int n) { return sW[x * WP + n]; };
-      wm::gemm<1, NTS, true, XS>(ds, fa1, fb1, 0, ns0, 0, C);
-      wm::gemm<1, NTS, true, true>(ds, fa2, fb2, 0, ns0, 0, C);
-      wm::for_each(ds, 0, ns0, [&](int i, int cc, float& x) { sdS[i * WP + cc] = x; });
+#pragma unroll
+      for (int k0 = 0; k0 < C; k0 += 16) {
+        uint32_t oh4[4], ol4[4], uh4[4], ul4[4];
+        wm::lda_t(oh4, sOSH, HP, 0, k0);
+        wm::lda_t(ol4, sOSL, HP, 0, k0);
+        wm::lda_t(uh4, sNUH, HP, 0, k0);
+        wm::lda_t(ul4, sNUL, HP, 0, k0);
+#pragma unroll
+        for (int j = 0; j < NTS; ++j) {
+          uint32_t bh[2], bl[2];
+          wm::ldb1_t(bh, qh, DP, k0, ns0 + 8 * j);
+          if (XS) wm::ldb1_t(bl, xql, DP, k0, ns0 + 8 * j);
+          mma_terms<true, XS>(ds[0][j], oh4, ol4, bh, bl);
+          wm::ldb1_t(bh, sWH, DP, k0, ns0 + 8 * j);
+          wm::ldb1_t(bl, sWL, DP, k0, ns0 + 8 * j);
+          mma_terms<true, true>(ds[0][j], uh4, ul4, bh, bl);
+        }
+      }
+      store_grad();
+    }
+    if (S::NST == 1 && c - 1 >= jb.c0) {  // one stage: refill it once this chunk is done with it
+      __syncthreads();
+      issue(c - 1, 0);
     }
   }
   float* dS0 = p.d_state_pool + srow;
@@ -683,10 +817,39 @@ struct LoSmem {
   static constexpr uint32_t C4 = C3 + CC;            // dP
   static constexpr uint32_t F1 = C4 + CC;            // U, then dW (fp32 [C][WP])
   static constexpr uint32_t F2 = F1 + C * WP * 4;    // dU
-  static constexpr uint32_t VEC = F2 + C * WP * 4;   // 20 vectors of C
-  static constexpr uint32_t bytes = VEC + 20 * C * 4;
+  static constexpr uint32_t VEC = F2 + C * WP * 4;   // 24 vectors of C
+  static constexpr uint32_t bytes = VEC + 24 * C * 4;
   static_assert(bytes <= 232448, "shared memory per CTA");
 };
+
+// x = x^ n with n = sqrt(|x|^2 + eps): dx = dx^ / n - x (x . dx^) / n^3, for the rows of the
+// accumulator tile (rows m0 .. m0 + 15 split over the two warps of a row block; `part` holds the
+// two warps' partial dot products). rn = 1/n per row; raw: the 16-bit rows of x. Every thread
+// of the CTA calls it (it synchronises the CTA).
+template <int D, int NT, typename E>
+__device__ __forceinline__ void norm_backward(float (&acc)[1][NT][4], const E* raw, const float* rn, float* part,
+                                              int m0, int nd, int len, float* out, int64_t ld) {
+  constexpr int DP = D + 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float pd[2] = {0.f, 0.f};
+  wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+    const float y = fmaf(to_f(raw[i * DP + c]), x0, to_f(raw[i * DP + c + 1]) * x1);
+    if (i - m0 < 8) pd[0] += y; else pd[1] += y;
+  });
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const float sdot = quad_sum(pd[hh]);
+    if ((lane & 3) == 0) part[(warp >> 2) * 64 + m0 + wm::lane_r() + 8 * hh] = sdot;
+  }
+  __syncthreads();
+  wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+    if (i < len) {
+      const float r = rn[i], f = (part[i] + part[64 + i]) * r * r * r;
+      *reinterpret_cast<float2*>(out + (int64_t)i * ld + c) =
+          make_float2(r * x0 - to_f(raw[i * DP + c]) * f, r * x1 - to_f(raw[i * DP + c + 1]) * f);
+    }
+  });
+}
 
 template <int D, typename E>
 __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
@@ -729,6 +892,9 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   float* vpA = vcol + C;        // [2][C] eg <k^, A^T dW>
   float* vpB = vpA + 2 * C;     // [2][C] dec <k^, dKr>
   float* vpC = vpB + 2 * C;     // [2][C] <dQa, q^>
+  float* vnk = vpC + 2 * C;     // [2][C] <k, dk^> (normalisation backward, ungrouped heads)
+  float* vnq = vnk + 2 * C;     // [2][C] <q, dq^>
+  const bool fused_norm = p.HV == p.H;
 
   load_tokens<D>(rq_t, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
   load_tokens<D>(rk_t, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
@@ -923,9 +1089,12 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     auto fa2 = [&](int m, int x) { return vrk[x] * (vbt[m] * X1[m * CP + x] + vbt[x] * X1[x * CP + m]); };
     auto fbk = [&](int x, int n) { return to_f(rk_t[x * DP + n]); };
     wm::gemm<1, NT, true, XS>(acc, fa2, fbk, m0, nd, 0, C);
-    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
-      if (i < len) *reinterpret_cast<float2*>(p.dkh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
-    });
+    if (fused_norm)
+      norm_backward<D, NT>(acc, rk_t, vrk, vnk, m0, nd, len, p.dk + (t0 * p.H + h) * D, (int64_t)p.H * D);
+    else
+      wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+        if (i < len) *reinterpret_cast<float2*>(p.dkh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+      });
   }
   {
     // dq^ = dQa + (Gamma . dP) diag(1/|k|) K
@@ -950,9 +1119,12 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     auto fa = [&](int m, int x) { return x <= m ? expf(vg[m] - vg[x]) * C4[m * CP + x] * vrk[x] : 0.f; };
     auto fbk = [&](int x, int n) { return to_f(rk_t[x * DP + n]); };
     wm::gemm<1, NT, true, XS>(acc, fa, fbk, m0, nd, 0, m0 + 16);
-    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
-      if (i < len) *reinterpret_cast<float2*>(p.dqh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
-    });
+    if (fused_norm)
+      norm_backward<D, NT>(acc, rq_t, vrq, vnq, m0, nd, len, p.dq + (t0 * p.H + h) * D, (int64_t)p.H * D);
+    else
+      wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+        if (i < len) *reinterpret_cast<float2*>(p.dqh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+      });
   }
   __syncthreads();
   if (tid < C) {
@@ -1063,10 +1235,13 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
   bwd_factor_kernel<D, E><<<items, 256, FacSmem<D>::bytes, s>>>(p);
   ++n;
   if (chains > 0) {
-    if ((e = set_smem(bwd_state_kernel<D, E>, StSmem<D>::bytes)) != cudaSuccess) return e;
-    bwd_state_kernel<D, E><<<chains, 128, StSmem<D>::bytes, s>>>(p);
-    if ((e = set_smem(bwd_dstate_kernel<D, E>, DsSmem<D>::bytes)) != cudaSuccess) return e;
-    bwd_dstate_kernel<D, E><<<chains, 128, DsSmem<D>::bytes, s>>>(p);
+    constexpr bool f16in = kSplitSrc<E>;
+    const uint32_t sb = f16in ? StSmem<D>::bytes_fp16 : StSmem<D>::bytes_bf16;
+    const uint32_t db = DsSmem<D, f16in>::bytes;
+    if ((e = set_smem(bwd_state_kernel<D, E>, sb)) != cudaSuccess) return e;
+    bwd_state_kernel<D, E><<<chains, kSeqThreads, sb, s>>>(p);
+    if ((e = set_smem(bwd_dstate_kernel<D, E>, db)) != cudaSuccess) return e;
+    bwd_dstate_kernel<D, E><<<chains, kSeqThreads, db, s>>>(p);
     n += 2;
   }
   if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D>::bytes)) != cudaSuccess) return e;
@@ -1075,7 +1250,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
   bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
   n += 2;
   const int64_t rows = p.T * p.H;
-  if (rows > 0) {
+  if (rows > 0 && p.HV != p.H) {  // grouped heads: sum the value heads' gradients, then the norm
     bwd_norm_kernel<D, E><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
     ++n;
   }

@@ -12,8 +12,9 @@ struct BwdLayout {
   size_t g, beta;                                   // fp32 [mc][HV][C] (gates kernel)
   size_t rq, rk;                                    // fp32 [mc][HV][C]: 1/|q|, 1/|k| (0 on padded rows)
   size_t minv;                                      // fp32 [mc][HV][C][C]: M^{-1}
-  size_t pm;                                        // fp32 [mc][HV][C][C]: P = Gamma . tril(Q^ K^^T)
-  size_t w, ut;                                     // fp32 [mc][HV][C][D]: W<-, U~
+  size_t pm;                                        // bf16 [mc][HV][2][C][C]: P = Gamma . tril(Q^ K^^T), hi and lo planes
+  size_t w;                                         // bf16 [mc][HV][2][C][D]: W<-, hi and lo planes
+  size_t ut;                                        // fp32 [mc][HV][C][D]: U~
   size_t s_in;                                      // fp32 [mc][HV][D][D]: state entering each chunk
   size_t u;                                         // fp32 [mc][HV][C][D]: U = U~ - W<- S^T
   size_t ds_out;                                    // fp32 [mc][HV][D][D]: gradient of the state leaving each chunk
@@ -56,7 +57,10 @@ struct BwdParams {
   int32_t* seq_chunk_off;
   int32_t* order;
   int4* chunk_tab;
-  float *g, *beta, *rq, *rk, *minv, *pm, *w, *ut, *s_in, *u, *ds_out, *du, *dqa, *dw, *dkr, *dgc, *dqh, *dkh, *dlala;
+  float *g, *beta, *rq, *rk, *minv;
+  void* pm;  // bf16 planes
+  void* w;   // bf16 planes
+  float *ut, *s_in, *u, *ds_out, *du, *dqa, *dw, *dkr, *dgc, *dqh, *dkh, *dlala;
 };
 
 // Launches the backward kernels after the schedule and gates kernels of the call have run on s.

@@ -119,5 +119,64 @@ __device__ __forceinline__ void for_each_pair(float (&acc)[MT][NT][4], int m0, i
       for (int h = 0; h < 2; ++h) f(m0 + 16 * i + r + 8 * h, n0 + 8 * j + c, acc[i][j][2 * h], acc[i][j][2 * h + 1]);
 }
 
+// ---- fragments straight from 16-bit planes in shared memory (ldmatrix). A plane holds an
+// operand's bf16 values (the hi part of an fp32 operand, or its lo part) with a row pitch of
+// ld elements (a multiple of 8, so that every row start is 16-byte aligned).
+
+// A (16 x 16) at (m0, k0) from [m][k] storage.
+__device__ __forceinline__ void lda(uint32_t (&a)[4], const bf16* base, int ld, int m0, int k0) {
+  const int l = threadIdx.x & 31;
+  const uint32_t addr = smem_u32(base + (m0 + (l & 15)) * ld + k0 + 8 * (l >> 4));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(addr));
+}
+// A (16 x 16) at (m0, k0) from [k][m] storage (A^T row-major).
+__device__ __forceinline__ void lda_t(uint32_t (&a)[4], const bf16* base, int ld, int m0, int k0) {
+  const int l = threadIdx.x & 31, mat = l >> 3;
+  const uint32_t addr = smem_u32(base + (k0 + (l & 7) + 8 * (mat >> 1)) * ld + m0 + 8 * (mat & 1));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(addr));
+}
+// B for the two 8-column tiles n0 and n0 + 8 (b[0..1]: tile n0, b[2..3]: tile n0 + 8) at k0,
+// from [n][k] storage (B^T row-major).
+__device__ __forceinline__ void ldb2(uint32_t (&b)[4], const bf16* base, int ld, int k0, int n0) {
+  const int l = threadIdx.x & 31, mat = l >> 3;
+  const uint32_t addr = smem_u32(base + (n0 + (l & 7) + 8 * (mat >> 1)) * ld + k0 + 8 * (mat & 1));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(addr));
+}
+// The same from [k][n] storage.
+__device__ __forceinline__ void ldb2_t(uint32_t (&b)[4], const bf16* base, int ld, int k0, int n0) {
+  const int l = threadIdx.x & 31, mat = l >> 3;
+  const uint32_t addr = smem_u32(base + (k0 + (l & 7) + 8 * (mat & 1)) * ld + n0 + 8 * (mat >> 1));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(addr));
+}
+// B for one 8-column tile n0 at k0, from [n][k] / [k][n] storage (lanes 16-31 repeat 0-15).
+__device__ __forceinline__ void ldb1(uint32_t (&b)[2], const bf16* base, int ld, int k0, int n0) {
+  const int l = threadIdx.x & 15;
+  const uint32_t addr = smem_u32(base + (n0 + (l & 7)) * ld + k0 + 8 * (l >> 3));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(b[0]), "=r"(b[1]) : "r"(addr));
+}
+__device__ __forceinline__ void ldb1_t(uint32_t (&b)[2], const bf16* base, int ld, int k0, int n0) {
+  const int l = threadIdx.x & 15;
+  const uint32_t addr = smem_u32(base + (k0 + l) * ld + n0);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(b[0]), "=r"(b[1]) : "r"(addr));
+}
+
+// x (fp32) as the bf16 pair hi + lo, stored to two planes.
+__device__ __forceinline__ void store_split(bf16* hi, bf16* lo, float x) {
+  const bf16 h = __float2bfloat16_rn(x);
+  *hi = h;
+  *lo = __float2bfloat16_rn(x - __bfloat162float(h));
+}
+__device__ __forceinline__ void store_split2(bf16* hi, bf16* lo, float x0, float x1) {
+  uint32_t h, l;
+  split2<bf16>(x0, x1, h, l);
+  *reinterpret_cast<uint32_t*>(hi) = h;
+  *reinterpret_cast<uint32_t*>(lo) = l;
+}
+
 }  // namespace wm
 }  // namespace gdn
