@@ -153,9 +153,12 @@ def test_backward_workspace_size_rules(lib):
     assert ws(100, 2, 2, 4, 128, 128, 32) == 0     # chunk size
     assert ws(100, 2, 1, 1 << 16, 64, 64, 64) == 0  # HV above the grid's y limit
     assert ws(1000, 2, 2, 4, 128, 128, 128) == ws(1000, 2, 2, 4, 128, 128, 64)
-    # fp32 intermediates: (C*C*2 + C*D*7 + D*D*2) floats per (chunk, value head) and 2*D + 1 per (token, value head)
+    # (C*C*2 + C*D*7 + D*D*2) 4-byte words per (chunk, value head); per (token, value head) one word, plus
+    # 2*D for the per-value-head q/k gradients when value heads share a q/k head
     per_item = (64 * 64 * 2 + 64 * 128 * 7 + 128 * 128 * 2) * 4
-    assert ws(65536, 1, 16, 16, 128, 128, 64) >= 1025 * 16 * per_item + 65536 * 16 * (2 * 128 + 1) * 4
+    assert ws(65536, 1, 16, 16, 128, 128, 64) >= 1025 * 16 * per_item + 65536 * 16 * 4
+    assert ws(65536, 1, 16, 16, 128, 128, 64) < 1025 * 16 * per_item + 65536 * 16 * 2 * 128 * 4
+    assert ws(65536, 1, 8, 16, 128, 128, 64) >= 1025 * 16 * per_item + 65536 * 16 * (2 * 128 + 1) * 4
 
 
 def _bwd(lib, **over):
