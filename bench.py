@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 
 METRIC = "GDN prefill tokens/s and TFLOP/s (% of GB300 bf16 peak), 1 GPU"
 METRIC_DECODE = "GDN single-token step (decode) tokens/s and state GB/s (% of GB300 HBM), 1 GPU"
+METRIC_BACKWARD = "GDN chunkwise backward tokens/s and gradient GB/s (% of GB300 HBM), 1 GPU"
 DEC_KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indices")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KEYS = ("q", "k", "v", "a", "b", "A_log", "dt_bias", "state_pool", "cache_indices", "cu_seqlens")
@@ -45,7 +46,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="long",
-                    help="workload name (tiny, varlen, long, throughput, wide; decode: the single-token step)")
+                    help="workload name (tiny, varlen, long, throughput, wide; decode: the single-token step; "
+                         "backward: the backward pass on the long workload)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
@@ -223,7 +225,8 @@ def _code_only(src: str) -> str:
 def kernel_source_hash(kernel: str) -> str:
     """Hash of the code (not the comments) of a kernel's sources and the shared headers."""
     files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu"], "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
-             "schedule": ["gdn_schedule.cu"], "decode": ["gdn_decode.cu", "gdn_decode.cuh"]}
+             "schedule": ["gdn_schedule.cu"], "decode": ["gdn_decode.cu", "gdn_decode.cuh"],
+             "backward": ["gdn_backward.cu", "gdn_backward.cuh", "gdn_mma.cuh"]}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
     h = hashlib.sha256()
     for f in files.get(kernel, []) + ["gdn_common.cuh", "gdn_tc.cuh"]:
@@ -527,11 +530,209 @@ def run_ours(args, dist):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- backward
+
+def backward_inputs(w):
+    """The long workload's inputs plus seeded gradients from above (d_out like v, d_state like the pool)."""
+    import torch
+    from gated_deltanet_chunkwise_gdn_gb300 import workloads as wl
+    d = wl.make_inputs(w)
+    gen = torch.Generator().manual_seed(1000 + w.seed)
+    d["d_out"] = torch.randn(d["v"].shape, generator=gen).to(w.dtype)
+    d["d_state"] = 0.1 * torch.randn(d["state_pool"].shape, generator=gen)
+    return d
+
+
+def backward_accounting(w, lengths):
+    """Algorithmic bytes of one backward call: q, k, v, d_out, a, b read once; dq, dk, dv (fp32), da, db
+    written once; each touched initial state and final-state gradient read once and the initial state's
+    gradient written once. FLOPs: twice the forward's algorithmic count (an estimate: the backward runs
+    about two forward-sized sets of products)."""
+    from gated_deltanet_chunkwise_gdn_gb300 import accounting as acc
+    T, B = sum(lengths), len(lengths)
+    H, HV, K, V = w.H, w.HV, w.K, w.V
+    nbytes = (T * H * K * 2 * 2 + T * HV * V * 2 * 2 + T * HV * 4 * 2 + T * H * K * 4 * 2 + T * HV * V * 4
+              + T * HV * 4 * 2 + B * HV * V * K * 4 * 3 + HV * 4 * 4)
+    return {"bytes": nbytes, "flops": 2.0 * acc.flop_count(lengths, H, HV, K, V, w.chunk_size)}
+
+
+def oracle_backward_sample(d, S):
+    """The gradient oracle (chain rule on the token recurrence, fp64 numpy) on the first S tokens of
+    sequence 0, all value heads. Returns seconds."""
+    import torch
+    from oracle import backward as bw
+    sub = {k: d[k][:S] for k in ("q", "k", "v", "a", "b", "d_out")}
+    idx = d["cache_indices"][:1]
+    t = time.perf_counter()
+    bw.gdn_backward(sub["q"], sub["k"], sub["v"], sub["a"], sub["b"], d["A_log"], d["dt_bias"], d["state_pool"],
+                    idx, torch.tensor([0, S], dtype=torch.int64), sub["d_out"].double(),
+                    d["d_state"].double().numpy()[idx.numpy()])
+    return time.perf_counter() - t
+
+
+def backward_cpu_sample(d, target_s):
+    L0 = int(d["cu_seqlens"][1] - d["cu_seqlens"][0])
+    probe = min(L0, 64)
+    dt = oracle_backward_sample(d, probe)
+    S = max(1, min(L0, int(probe * target_s / max(dt, 1e-6))))
+    return S, oracle_backward_sample(d, S)
+
+
+def run_backward(args, dist):
+    import torch
+    import gated_deltanet_chunkwise_gdn_gb300 as gdn
+    from gated_deltanet_chunkwise_gdn_gb300 import workloads as wl
+
+    w = wl.BY_NAME["long"]
+    if args.impl == "reference":
+        if dist.rank != 0:
+            return
+        d = backward_inputs(w)
+        per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+        S, _ = backward_cpu_sample(d, per_step)
+        for _ in range(args.warmup):
+            oracle_backward_sample(d, S)
+        el = sum(oracle_backward_sample(d, S) for _ in range(args.steps))
+        tok_s = S * args.steps / el
+        sample = f"first {S} tokens of sequence 0, all {w.HV} value heads, per step"
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC_BACKWARD, "value": round(tok_s, 1), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"backward of {w.name}: {w.note}", "sample": sample},
+            "cpu_baseline": {"value": round(tok_s, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(tok_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    dev = torch.device("cuda", dist.local_rank if dist.world > 1 else 0)
+    torch.cuda.set_device(dev)
+    d = backward_inputs(w)
+    lengths = wl.sequence_lengths(w)
+    T = sum(lengths)
+    keys = KEYS + ("d_out", "d_state")
+    g = {k: d[k].to(dev) for k in keys}
+    need = gdn.gdn_backward_workspace_size(T, len(lengths), w.H, w.HV, w.K, w.V, w.chunk_size)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    grads = gdn.GdnGrads(torch.empty((T, w.H, w.K), **f32), torch.empty((T, w.H, w.K), **f32),
+                         torch.empty((T, w.HV, w.V), **f32), torch.empty((T, w.HV), **f32),
+                         torch.empty((T, w.HV), **f32), torch.empty((w.HV,), **f32), torch.empty((w.HV,), **f32),
+                         torch.zeros_like(g["state_pool"]))
+    stream = torch.cuda.current_stream(dev)
+
+    def call(b, check=False):
+        gdn.gdn_chunkwise_backward(*[b[k] for k in KEYS], b["d_out"], b["d_state"], chunk_size=w.chunk_size,
+                                   workspace=ws, grads=grads, check=check)
+
+    call(g, check=True)
+    for _ in range(max(3, args.warmup)):
+        call(g)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(device_uuid(torch, dev))
+    sampler.wait_first()
+    for _ in range(max(3, args.warmup)):
+        call(g)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = gdn.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        call(g)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    dist.barrier()
+    launches = gdn.launch_count() - n0
+    time.sleep(0.1)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = dist.max(ms)
+    clocks = sampler.summary(t_host0, t_host1)
+    prof = gdn.KernelProfile(max_launches=4 * args.steps + 64)
+    prof.start()
+    for _ in range(args.steps):
+        call(g)
+    torch.cuda.synchronize(dev)
+    kernels = prof.stop()
+
+    # e2e: host buffers through the public API; every step uploads its inputs and the gradients
+    # from above, and reads every gradient back (the initial states stay resident)
+    e2e_steps = max(1, min(args.e2e_steps, args.steps, 10))
+    in_keys = ("q", "k", "v", "a", "b", "cache_indices", "cu_seqlens", "d_out", "d_state")
+    host_in = {k: d[k].pin_memory() for k in in_keys}
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in grads]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dbuf = dict(g, **{k: torch.empty_like(g[k]) for k in in_keys})
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dbuf[k].copy_(t, non_blocking=True)
+        call(dbuf)
+        for h, t in zip(host_out, grads):
+            h.copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist.max(f0.elapsed_time(f1))
+
+    if dist.rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    acct = backward_accounting(w, lengths)
+    tot_all = max(sum(v[0] for v in kernels.values()), 1e-9)
+    per_kernel = {name: {"ms_per_launch": round(tot / n, 4), "launches": n, "share": round(tot / tot_all, 4)}
+                  for name, (tot, n) in kernels.items() if n}
+    bt, bn = kernels["backward"]
+    roof = roofline_entry("backward", acct, bt / bn, peaks, peak_kind, "long")
+    step_ms = ms_max / args.steps
+    path = roofline_entry("path", acct, step_ms, peaks, peak_kind, "long")
+    path.pop("traffic", None)
+    tokens = T * args.steps * dist.world
+    line = {
+        "metric": METRIC_BACKWARD, "value": round(tokens / (ms_max * 1e-3), 1), "unit": "tokens/s",
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"backward of {w.name}: {w.note}; d_out ~ N(0,1), d_state ~ N(0, 0.1^2)",
+                   "global_batch": len(lengths) * dist.world, "seq_len": max(lengths), "total_tokens_per_gpu": T,
+                   "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (q,k,v,d_out %.0f MB > 129 MB), no flush" % (4 * T * w.H * w.K * 2 / 1e6)},
+        "tflops": round(acct["flops"] * args.steps * dist.world / (ms_max * 1e-3) / 1e12, 2),
+        "roofline": roof,
+        "path_roofline": path,
+        "kernels": per_kernel,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": {"value": round(T * e2e_steps * dist.world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "ms_per_step": round(e2e_ms / e2e_steps, 4)},
+    }
+    if dist.world == 1 and not args.no_cpu_baseline:
+        S, dt = backward_cpu_sample(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(S / dt, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {S} tokens of sequence 0, all {w.HV} value heads ({dt:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     dist = Dist()
     try:
-        if args.impl == "reference":
+        if args.config == "backward":
+            run_backward(args, dist)
+        elif args.impl == "reference":
             run_reference(args, dist)
         else:
             run_ours(args, dist)

@@ -20,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import GdnError
 
-__all__ = ["gdn_extend_chunkwise", "gdn_decode_step", "gdn_chunkwise_backward", "GdnGrads", "gdn_workspace_size",
+__all__ = ["gdn_extend_chunkwise", "gdn_decode_step", "gdn_chunkwise_backward", "GdnGrads", "GatedDeltaNetChunkwise",
+           "gdn_workspace_size",
            "gdn_backward_workspace_size", "gdn_get_device_status", "GdnError", "library_path", "version"]
 
 _ws_cache: dict = {}
@@ -157,7 +158,7 @@ def gdn_backward_workspace_size(total_tokens: int, batch: int, H: int, HV: int, 
 def gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, cu_seqlens, d_out,
                            d_state=None, chunk_size: int = 64, *, scale: float = 1.0, check: bool = False,
                            stream=None, workspace: torch.Tensor = None,
-                           d_state_pool: torch.Tensor = None) -> GdnGrads:
+                           d_state_pool: torch.Tensor = None, grads: GdnGrads = None) -> GdnGrads:
     """Gradients of :func:`gdn_extend_chunkwise` for ``L = <d_out, out> + <d_state, final states>``.
 
     Same inputs as the forward call, except that ``state_pool`` holds the INITIAL states (the pool
@@ -167,6 +168,8 @@ def gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indi
     batch's slots, or the given ``d_state_pool``, written at those slots only; that may be
     ``d_state`` itself, for a caller that carries the state gradient back through earlier calls.
     ``check=True`` waits and raises on a device-detected error (bad cache index or cu_seqlens).
+    ``grads``: a :class:`GdnGrads` of the right shapes to write into instead of new tensors (its
+    ``d_state_pool`` is then written at the batch's slots only).
     """
     dev = q.device
     if dev.type != "cuda":
@@ -208,9 +211,17 @@ def gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indi
     elif not hasattr(stream, "cuda_stream"):
         stream = torch.cuda.ExternalStream(int(stream), device=dev)
     sp = stream.cuda_stream
+    if grads is not None:
+        shapes = ((T, H, K), (T, H, K), (T, HV, V), (T, HV), (T, HV), (HV,), (HV,), tuple(state_pool.shape))
+        for name, t, shp in zip(GdnGrads._fields, grads, shapes):
+            _req(t, name, torch.float32, dev)
+            if tuple(t.shape) != shp:
+                raise ValueError(f"grads.{name} must have shape {shp}")
+        if d_state_pool is not None and d_state_pool.data_ptr() != grads.d_state_pool.data_ptr():
+            raise ValueError("give the state gradient's buffer once: as d_state_pool or in grads")
     with torch.cuda.stream(stream):
         f32 = dict(dtype=torch.float32, device=dev)
-        g = GdnGrads(torch.empty((T, H, K), **f32), torch.empty((T, H, K), **f32), torch.empty((T, HV, V), **f32),
+        g = grads if grads is not None else GdnGrads(torch.empty((T, H, K), **f32), torch.empty((T, H, K), **f32), torch.empty((T, HV, V), **f32),
                      torch.empty((T, HV), **f32), torch.empty((T, HV), **f32), torch.empty((HV,), **f32),
                      torch.empty((HV,), **f32),
                      d_state_pool if d_state_pool is not None else torch.zeros_like(state_pool))
@@ -233,6 +244,39 @@ def gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indi
     if check:
         _lib.check(L.gdn_get_device_status(ws_ptr, sp), "gdn_chunkwise_backward (device)")
     return g
+
+
+class GatedDeltaNetChunkwise(torch.autograd.Function):
+    """The chunkwise prefill as an autograd function: forward through gdn_extend_chunkwise, backward
+    through gdn_chunkwise_backward.
+
+    ``apply(q, k, v, a, b, A_log, dt_bias, initial_state, cu_seqlens, chunk_size=64, scale=1.0)`` with
+    ``initial_state [B, HV, V, K]`` fp32 (one state per sequence) returns ``(out [T, HV, V],
+    final_state [B, HV, V, K])``; gradients flow to q, k, v, a, b, A_log, dt_bias and initial_state
+    (q, k, v get their gradients in their own dtype, the rest in fp32).
+    """
+
+    @staticmethod
+    def forward(ctx, q, k, v, a, b, A_log, dt_bias, initial_state, cu_seqlens, chunk_size=64, scale=1.0):
+        B = initial_state.shape[0]
+        idx = torch.arange(B, dtype=torch.int64, device=q.device)
+        pool = initial_state.detach().clone().contiguous()
+        out = gdn_extend_chunkwise(q, k, v, a, b, A_log, dt_bias, pool, idx, cu_seqlens, chunk_size, scale=scale)
+        ctx.save_for_backward(q, k, v, a, b, A_log, dt_bias, initial_state, cu_seqlens, idx)
+        ctx.chunk_size, ctx.scale = chunk_size, scale
+        return out, pool
+
+    @staticmethod
+    def backward(ctx, d_out, d_final):
+        q, k, v, a, b, A_log, dt_bias, initial_state, cu_seqlens, idx = ctx.saved_tensors
+        if d_out is None:
+            d_out = torch.zeros(v.shape, dtype=v.dtype, device=v.device)
+        d_state = None if d_final is None else d_final.float().contiguous()
+        g = gdn_chunkwise_backward(q, k, v, a, b, A_log, dt_bias, initial_state.detach().contiguous(), idx,
+                                   cu_seqlens, d_out.to(v.dtype).contiguous(), d_state, ctx.chunk_size,
+                                   scale=ctx.scale)
+        return (g.dq.to(q.dtype), g.dk.to(k.dtype), g.dv.to(v.dtype), g.da, g.db, g.dA_log, g.ddt_bias,
+                g.d_state_pool, None, None, None)
 
 
 def gdn_decode_step(q, k, v, a, b, A_log, dt_bias, state_pool, cache_indices, *, scale: float = 1.0,

@@ -17,7 +17,8 @@ import numpy as np
 import pytest
 import torch
 
-from gated_deltanet_chunkwise_gdn_gb300 import GdnError, gdn_chunkwise_backward, workloads as wl
+from gated_deltanet_chunkwise_gdn_gb300 import (GatedDeltaNetChunkwise, GdnError, gdn_chunkwise_backward,
+                                                workloads as wl)
 from oracle import backward as bw
 from oracle import chunkwise_grad as cg
 
@@ -208,3 +209,28 @@ def test_backward_long_chains_sampled_heads():
         print(hv, {k: f"{v:.2e}" for k, v in errs.items()})
         for k, v in errs.items():
             assert v <= GRAD_TOL, (hv, k, v)
+
+
+def test_autograd_function_against_the_oracle():
+    """torch.autograd through GatedDeltaNetChunkwise: a weighted loss on the output and the final states,
+    gradients of every input compared with the fp64 oracle."""
+    d = wl.make_inputs(wl.custom("bwd_autograd", [150, 70], H=2, HV=2, K=64, V=64, chunk_size=64, seed=327,
+                                 index_rule="arange"))
+    d_out, d_state = upstream(d, 327)
+    B = 2
+    leaf = {k: d[k].cuda().requires_grad_(True) for k in ("q", "k", "v", "a", "b", "A_log", "dt_bias")}
+    init = d["state_pool"][:B].cuda().requires_grad_(True)
+    out, final = GatedDeltaNetChunkwise.apply(leaf["q"], leaf["k"], leaf["v"], leaf["a"], leaf["b"],
+                                              leaf["A_log"], leaf["dt_bias"], init, d["cu_seqlens"].cuda(), 64)
+    loss = (out.float() * d_out.float().cuda()).sum() + (final * d_state[:B].cuda()).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    ref = oracle_backward(d, d_out, d_state)
+    pairs = {"dq": leaf["q"], "dk": leaf["k"], "dv": leaf["v"], "da": leaf["a"], "db": leaf["b"],
+             "dA_log": leaf["A_log"], "ddt_bias": leaf["dt_bias"]}
+    for name, t in pairs.items():
+        e = rel(t.grad.double().cpu().numpy(), ref[name])
+        tol = 1e-2 if name in ("dq", "dk", "dv") else GRAD_TOL  # q, k, v gradients come back in bf16
+        assert e <= tol, (name, e)
+    e = rel(init.grad.double().cpu().numpy(), ref["d_state_pool"][:B])
+    assert e <= GRAD_TOL, e
