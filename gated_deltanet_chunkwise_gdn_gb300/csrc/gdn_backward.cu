@@ -160,25 +160,53 @@ __device__ __forceinline__ float col_sum(float x) {
 
 __device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
 
+// Splits an fp16 token tile (rows x W, pitch P) in place into bf16 planes: the hi plane
+// overwrites the tile, the lo plane goes to `lo` (same pitch).
+template <int W, int P>
+__device__ __forceinline__ void split_inplace(f16* tile, bf16* lo, int rows, int tid, int nthr) {
+  for (int e = tid; e < rows * W / 2; e += nthr) {
+    const int i = e / (W / 2), c = (e % (W / 2)) * 2;
+    const float x0 = __half2float(tile[i * P + c]), x1 = __half2float(tile[i * P + c + 1]);
+    wm::store_split2(reinterpret_cast<bf16*>(tile) + i * P + c, lo + i * P + c, x0, x1);
+  }
+}
+template <int W, int P>
+__device__ __forceinline__ void split_inplace(bf16*, bf16*, int, int, int) {}
+
 // ----------------------------------------------------------------------------- factor
 
-template <int D>
+// rows x W bf16 planes (W a multiple of 8) from a row-major array of row stride ld, pitch P.
+template <int W, int P>
+__device__ __forceinline__ void load_rows(bf16* dst, const bf16* src, int64_t ld, int rows, int tid, int nthr) {
+  constexpr int PER = W / 8;
+  for (int e = tid; e < rows * PER; e += nthr) {
+    const int i = e / PER, q = e % PER;
+    cp_async_16(dst + i * P + q * 8, src + i * ld + q * 8);
+  }
+}
+
+template <int D, bool XS>
 struct FacSmem {
-  static constexpr int DP = D + 8;
-  static constexpr uint32_t Q = 0;                    // 16-bit [C][DP] q, k, v tiles
-  static constexpr uint32_t K = Q + C * DP * 2;
-  static constexpr uint32_t V = K + C * DP * 2;
-  static constexpr uint32_t L = V + C * DP * 2;       // fp32 [C][CP]: beta_i k^_i . k^_j (j < i), then A
-  static constexpr uint32_t X = L + C * CP * 4;       // fp32 [C][CP]: M^{-1}
-  static constexpr uint32_t VEC = X + C * CP * 4;     // g, beta, 1/|q|, 1/|k|, e^g/|k|
+  static constexpr int DP = D + 8, PP = C + 8;
+  static constexpr uint32_t TILE = C * DP * 2;
+  static constexpr uint32_t PAIR = 2 * C * PP * 2;   // hi, lo planes of a C x C operand
+  static constexpr uint32_t Q = 0;                   // q, k, v tiles (fp16: their hi planes after the split)
+  static constexpr uint32_t K = Q + TILE;
+  static constexpr uint32_t V = K + TILE;
+  static constexpr uint32_t QL = V + TILE;           // fp16 only: lo planes of q, k, v
+  static constexpr uint32_t L = QL + (XS ? 3 * TILE : 0);  // fp32 [C][CP] beta k^_i . k^_j (j < i); then A planes
+  static constexpr uint32_t X = L + PAIR;            // fp32 [C][CP]: M^{-1}
+  static constexpr uint32_t AW = X + PAIR;           // planes of A diag(e^g / |k|)
+  static constexpr uint32_t VEC = AW + PAIR;         // g, beta, 1/|q|, 1/|k|, e^g/|k|
   static constexpr uint32_t bytes = VEC + 5 * C * 4;
+  static_assert(C * CP * 4 <= PAIR, "the fp32 C x C tiles fit the plane-pair regions");
 };
 
 template <int D, typename E>
 __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
-  using S = FacSmem<D>;
-  constexpr int DP = S::DP;
   constexpr bool XS = kSplitSrc<E>;
+  using S = FacSmem<D, XS>;
+  constexpr int DP = S::DP, PP = S::PP, PLN = C * PP;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
   const int j = blockIdx.x, hv = blockIdx.y;
@@ -191,8 +219,13 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   E* sq = reinterpret_cast<E*>(smem + S::Q);
   E* sk = reinterpret_cast<E*>(smem + S::K);
   E* sv = reinterpret_cast<E*>(smem + S::V);
+  bf16* ql = reinterpret_cast<bf16*>(smem + S::QL);
+  bf16* kl = ql + C * DP;
+  bf16* vl = kl + C * DP;
   float* sL = reinterpret_cast<float*>(smem + S::L);
   float* sX = reinterpret_cast<float*>(smem + S::X);
+  bf16* sA = reinterpret_cast<bf16*>(smem + S::L);
+  bf16* sAW = reinterpret_cast<bf16*>(smem + S::AW);
   float* vg = reinterpret_cast<float*>(smem + S::VEC);
   float* vb = vg + C;
   float* vrq = vb + C;
@@ -210,11 +243,23 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   }
   cp_async_wait<0>();
   __syncthreads();
+  if (XS) {
+    split_inplace<D, DP>(sq, ql, C, tid, 256);
+    split_inplace<D, DP>(sk, kl, C, tid, 256);
+    split_inplace<D, DP>(sv, vl, C, tid, 256);
+    __syncthreads();
+  }
+  const bf16* qh = reinterpret_cast<const bf16*>(sq);
+  const bf16* kh = reinterpret_cast<const bf16*>(sk);
+  const bf16* vh = reinterpret_cast<const bf16*>(sv);
+  auto val = [&](const bf16* hi, const bf16* lo, int o) {
+    return XS ? __bfloat162float(hi[o]) + __bfloat162float(lo[o]) : __bfloat162float(hi[o]);
+  };
 
   for (int i = warp * 8; i < warp * 8 + 8; ++i) {  // row norms, one warp per 8 rows
     float s2q = 0.f, s2k = 0.f;
     for (int d = lane; d < D; d += 32) {
-      const float x = to_f(sq[i * DP + d]), y = to_f(sk[i * DP + d]);
+      const float x = val(qh, ql, i * DP + d), y = val(kh, kl, i * DP + d);
       s2q = fmaf(x, x, s2q);
       s2k = fmaf(y, y, s2k);
     }
@@ -238,11 +283,8 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
     float kk[1][4][4], qk[1][4][4];
     wm::zero(kk);
     wm::zero(qk);
-    auto fk = [&](int m, int x) { return to_f(sk[m * DP + x]); };
-    auto fq = [&](int m, int x) { return to_f(sq[m * DP + x]); };
-    auto fkt = [&](int x, int n) { return to_f(sk[n * DP + x]); };
-    wm::gemm<1, 4, XS, XS>(kk, fk, fkt, m0, n0, 0, D);
-    wm::gemm<1, 4, XS, XS>(qk, fq, fkt, m0, n0, 0, D);
+    wm::pgemm<1, 4, false, false, XS, XS>(kk, kh, kl, DP, kh, kl, DP, m0, n0, 0, D);
+    wm::pgemm<1, 4, false, false, XS, XS>(qk, qh, ql, DP, kh, kl, DP, m0, n0, 0, D);
     wm::for_each(kk, m0, n0, [&](int i, int c, float& x) {
       sL[i * CP + c] = c < i ? vb[i] * vrk[i] * vrk[c] * x : 0.f;
     });
@@ -255,28 +297,36 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   }
   __syncthreads();
 
-  // M^{-1} = (I + L)^{-1}: forward substitution, one column per thread
+  // M^{-1} = (I + L)^{-1}: forward substitution, one column per thread, four partial sums
   if (tid < C) {
     const int c = tid;
     for (int i = 0; i < c; ++i) sX[i * CP + c] = 0.f;
     sX[c * CP + c] = 1.f;
     for (int i = c + 1; i < C; ++i) {
-      float s = 0.f;
-      for (int x = c; x < i; ++x) s = fmaf(sL[i * CP + x], sX[x * CP + c], s);
-      sX[i * CP + c] = -s;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int x = c;
+      for (; x + 3 < i; x += 4) {
+        s0 = fmaf(sL[i * CP + x], sX[x * CP + c], s0);
+        s1 = fmaf(sL[i * CP + x + 1], sX[(x + 1) * CP + c], s1);
+        s2 = fmaf(sL[i * CP + x + 2], sX[(x + 2) * CP + c], s2);
+        s3 = fmaf(sL[i * CP + x + 3], sX[(x + 3) * CP + c], s3);
+      }
+      for (; x < i; ++x) s0 = fmaf(sL[i * CP + x], sX[x * CP + c], s0);
+      sX[i * CP + c] = -((s0 + s1) + (s2 + s3));
     }
   }
   __syncthreads();
   {
-    float* MI = p.minv + item * C * C;
-    for (int e = tid; e < C * C / 4; e += 256) {
-      const int i = e / (C / 4), c = (e % (C / 4)) * 4;
-      *reinterpret_cast<float4*>(MI + i * C + c) =
-          make_float4(sX[i * CP + c], sX[i * CP + c + 1], sX[i * CP + c + 2], sX[i * CP + c + 3]);
-    }
-    for (int e = tid; e < C * C; e += 256) {  // A = (Gamma . M^{-1}) diag(beta), lower triangular
-      const int i = e / C, c = e % C;
-      sL[i * CP + c] = c <= i ? expf(vg[i] - vg[c]) * sX[i * CP + c] * vb[c] : 0.f;
+    // M^{-1} planes for the local kernel; A = (Gamma . M^{-1}) diag(beta) and A diag(e^g / |k|) as planes
+    bf16* MI = reinterpret_cast<bf16*>(p.minv) + item * 2 * C * C;
+    for (int e = tid; e < C * C / 2; e += 256) {
+      const int i = e / (C / 2), c = (e % (C / 2)) * 2;
+      const float m0v = sX[i * CP + c], m1v = sX[i * CP + c + 1];
+      wm::store_split2(MI + i * C + c, MI + C * C + i * C + c, m0v, m1v);
+      const float a0 = c <= i ? expf(vg[i] - vg[c]) * m0v * vb[c] : 0.f;
+      const float a1 = c + 1 <= i ? expf(vg[i] - vg[c + 1]) * m1v * vb[c + 1] : 0.f;
+      wm::store_split2(sA + i * PP + c, sA + PLN + i * PP + c, a0, a1);
+      wm::store_split2(sAW + i * PP + c, sAW + PLN + i * PP + c, a0 * vek[c], a1 * vek[c + 1]);
     }
   }
   __syncthreads();
@@ -285,14 +335,10 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   // triangular, so rows m0 .. m0 + 15 need k < m0 + 16 only.
   constexpr int NT = D / 16;
   const int nw = (D / 2) * (warp >> 2);
-  auto fa_w = [&](int m, int x) { return sL[m * CP + x] * vek[x]; };
-  auto fa_u = [&](int m, int x) { return sL[m * CP + x]; };
-  auto fb_k = [&](int x, int n) { return to_f(sk[x * DP + n]); };
-  auto fb_v = [&](int x, int n) { return to_f(sv[x * DP + n]); };
   {
     float acc[1][NT][4];
     wm::zero(acc);
-    wm::gemm<1, NT, true, XS>(acc, fa_w, fb_k, m0, nw, 0, m0 + 16);
+    wm::pgemm<1, NT, false, true, true, XS>(acc, sAW, sAW + PLN, PP, kh, kl, DP, m0, nw, 0, m0 + 16);
     bf16* Wg = reinterpret_cast<bf16*>(p.w) + item * 2 * C * D;  // hi, lo planes
     wm::for_each_pair(acc, m0, nw, [&](int i, int c, float& x0, float& x1) {
       wm::store_split2(Wg + i * D + c, Wg + C * D + i * D + c, x0, x1);
@@ -301,7 +347,7 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   {
     float acc[1][NT][4];
     wm::zero(acc);
-    wm::gemm<1, NT, true, XS>(acc, fa_u, fb_v, m0, nw, 0, m0 + 16);
+    wm::pgemm<1, NT, false, true, true, XS>(acc, sA, sA + PLN, PP, vh, vl, DP, m0, nw, 0, m0 + 16);
     float* Ug = p.ut + item * C * D;
     wm::for_each_pair(acc, m0, nw, [&](int i, int c, float& x0, float& x1) {
       *reinterpret_cast<float2*>(Ug + i * D + c) = make_float2(x0, x1);
@@ -316,32 +362,6 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
 // planes from the factor kernel; the state (or its gradient) and the chunk's small C x VB
 // operands are split into planes once per chunk. fp16 q/k/dO tiles are split into bf16 planes
 // after they land (an fp16 value is exactly hi + lo).
-
-// Splits an fp16 token tile (rows x W, pitch P) in place into bf16 planes: the hi plane
-// overwrites the tile, the lo plane goes to `lo` (same pitch).
-template <int W, int P>
-__device__ __forceinline__ void split_inplace(f16* tile, bf16* lo, int rows, int tid, int nthr) {
-  for (int e = tid; e < rows * W / 2; e += nthr) {
-    const int i = e / (W / 2), c = (e % (W / 2)) * 2;
-    const float x0 = __half2float(tile[i * P + c]), x1 = __half2float(tile[i * P + c + 1]);
-    wm::store_split2(reinterpret_cast<bf16*>(tile) + i * P + c, lo + i * P + c, x0, x1);
-  }
-}
-template <int W, int P>
-__device__ __forceinline__ void split_inplace(bf16*, bf16*, int, int, int) {}
-
-// MMA terms of one product: hi*hi, hi*lo (B has lo), lo*hi (A has lo).
-template <bool AL, bool BL>
-__device__ __forceinline__ void mma_terms(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
-                                          const uint32_t* bh, const uint32_t* bl) {
-  const uint32_t b0[2] = {bh[0], bh[1]};
-  wm::mma(d, ah, b0);
-  if (BL) {
-    const uint32_t b1[2] = {bl[0], bl[1]};
-    wm::mma(d, ah, b1);
-  }
-  if (AL) wm::mma(d, al, b0);
-}
 
 template <int D>
 struct StSmem {
@@ -445,10 +465,10 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
     const int64_t item = (int64_t)c * p.HV + jb.hv;
     split_inplace<D, DP>(sK, sKL, XS ? C : 0, tid, kSeqThreads);
 
-    // the state entering this chunk
-    float* Sin = p.s_in + item * D * D + (int64_t)jb.vb * D;
+    // the state entering this chunk (hi, lo planes)
+    bf16* Sin = reinterpret_cast<bf16*>(p.s_in) + item * 2 * D * D + (int64_t)jb.vb * D;
     wm::for_each_pair(st, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
-      *reinterpret_cast<float2*>(Sin + i * D + cc) = make_float2(x0, x1);
+      wm::store_split2(Sin + i * D + cc, Sin + D * D + i * D + cc, x0, x1);
     });
     // U = U~ - W<- S^T (C x VB); then diag(e^{g_C - g}/|k|) U as planes for the state update
     {
@@ -460,16 +480,16 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
         wm::lda(al, sWL, DP, mu, k0);
         wm::ldb1(bh, sSH, DP, k0, nu);
         wm::ldb1(bl, sSL, DP, k0, nu);
-        mma_terms<true, true>(ua, ah, al, bh, bl);
+        wm::mma_terms<true, true>(ua, ah, al, bh, bl);
       }
-      float* Ug = p.u + item * C * D + jb.vb;
+      bf16* Ug = reinterpret_cast<bf16*>(p.u) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = mu + r + 8 * hh, cc = nu + cl;
         const float u0 = sUT[i * UP + cc] - ua[2 * hh], u1 = sUT[i * UP + cc + 1] - ua[2 * hh + 1];
-        *reinterpret_cast<float2*>(Ug + i * D + cc) = make_float2(u0, u1);
+        wm::store_split2(Ug + i * D + cc, Ug + C * D + i * D + cc, u0, u1);
         const float sk = expf(gC - vg[i]) * vrk[i];
         wm::store_split2(sUKH + i * HP + cc, sUKL + i * HP + cc, sk * u0, sk * u1);
       }
@@ -490,7 +510,7 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
           uint32_t bh[2], bl[2];
           wm::ldb1_t(bh, kh, DP, k0, ns0 + 8 * j);
           if (XS) wm::ldb1_t(bl, sKL, DP, k0, ns0 + 8 * j);
-          mma_terms<true, XS>(st[0][j], ah, al, bh, bl);
+          wm::mma_terms<true, XS>(st[0][j], ah, al, bh, bl);
         }
       }
       store_state();
@@ -616,10 +636,10 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
       return XS ? __bfloat162float(oh[i * HP + cc]) + __bfloat162float(xol[i * HP + cc]) : to_f(sDO[i * HP + cc]);
     };
 
-    // the gradient of the state leaving this chunk
-    float* dSo = p.ds_out + item * D * D + (int64_t)jb.vb * D;
+    // the gradient of the state leaving this chunk (hi, lo planes)
+    bf16* dSo = reinterpret_cast<bf16*>(p.ds_out) + item * 2 * D * D + (int64_t)jb.vb * D;
     wm::for_each_pair(ds, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
-      *reinterpret_cast<float2*>(dSo + i * D + cc) = make_float2(x0, x1);
+      wm::store_split2(dSo + i * D + cc, dSo + D * D + i * D + cc, x0, x1);
     });
     // dU = scale P^T dO + diag(e^{g_C - g}/|k|) (K dS^T)  (C x VB): the warp's 16 x 8 tile; also the
     // planes of -dU and of scale diag(e^g/|q|) dO for the state-gradient update
@@ -631,7 +651,7 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
         wm::lda_t(al, sPL, PP, mu, k0);
         wm::ldb1_t(bh, oh, HP, k0, nu);
         if (XS) wm::ldb1_t(bl, xol, HP, k0, nu);
-        mma_terms<true, XS>(a1, ah, al, bh, bl);
+        wm::mma_terms<true, XS>(a1, ah, al, bh, bl);
       }
 #pragma unroll
       for (int k0 = 0; k0 < D; k0 += 16) {
@@ -640,9 +660,9 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
         if (XS) wm::lda(al, xkl, DP, mu, k0);
         wm::ldb1(bh, sGH, DP, k0, nu);
         wm::ldb1(bl, sGL, DP, k0, nu);
-        mma_terms<XS, true>(a2, ah, al, bh, bl);
+        wm::mma_terms<XS, true>(a2, ah, al, bh, bl);
       }
-      float* dUg = p.du + item * C * D + jb.vb;
+      bf16* dUg = reinterpret_cast<bf16*>(p.du) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float sc = p.scale, gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
 #pragma unroll
@@ -651,7 +671,7 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
         const float sk = expf(gC - vg[i]) * vrk[i];
         const float y0 = sc * a1[2 * hh] + sk * a2[2 * hh];
         const float y1 = sc * a1[2 * hh + 1] + sk * a2[2 * hh + 1];
-        *reinterpret_cast<float2*>(dUg + i * D + cc) = make_float2(y0, y1);
+        wm::store_split2(dUg + i * D + cc, dUg + C * D + i * D + cc, y0, y1);
         wm::store_split2(sNUH + i * HP + cc, sNUL + i * HP + cc, -y0, -y1);
         const float sq = sc * expf(vg[i]) * vrq[i];
         wm::store_split2(sOSH + i * HP + cc, sOSL + i * HP + cc, sq * dov(i, cc), sq * dov(i, cc + 1));
@@ -674,10 +694,10 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
           uint32_t bh[2], bl[2];
           wm::ldb1_t(bh, qh, DP, k0, ns0 + 8 * j);
           if (XS) wm::ldb1_t(bl, xql, DP, k0, ns0 + 8 * j);
-          mma_terms<true, XS>(ds[0][j], oh4, ol4, bh, bl);
+          wm::mma_terms<true, XS>(ds[0][j], oh4, ol4, bh, bl);
           wm::ldb1_t(bh, sWH, DP, k0, ns0 + 8 * j);
           wm::ldb1_t(bl, sWL, DP, k0, ns0 + 8 * j);
-          mma_terms<true, true>(ds[0][j], uh4, ul4, bh, bl);
+          wm::mma_terms<true, true>(ds[0][j], uh4, ul4, bh, bl);
         }
       }
       store_grad();
@@ -695,85 +715,111 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
 
 // ----------------------------------------------------------------------------- sgrad
 
-template <int D>
+template <int D, bool XS>
 struct SgSmem {
-  static constexpr int DP = D + 8, WP = D + 4;
-  static constexpr uint32_t SB = 0;                  // fp32 [D][WP]: S_in, then dS_out
-  static constexpr uint32_t DO = SB + D * WP * 4;    // dO 16-bit [C][DP]
-  static constexpr uint32_t DU = DO + C * DP * 2;    // dU fp32 [C][WP]
-  static constexpr uint32_t U = DU + C * WP * 4;     // U fp32 [C][WP]
-  static constexpr uint32_t VEC = U + C * WP * 4;    // g; 8 warp partials
+  static constexpr int DP = D + 8;
+  static constexpr uint32_t PLS = D * DP * 2;        // one D x D plane
+  static constexpr uint32_t PLC = C * DP * 2;        // one C x D plane or tile
+  static constexpr uint32_t SH = 0;                  // S_in planes, then dS_out planes
+  static constexpr uint32_t SL = SH + PLS;
+  static constexpr uint32_t DO = SL + PLS;           // dO tile (fp16: its hi plane after the split)
+  static constexpr uint32_t DUH = DO + PLC;          // dU planes
+  static constexpr uint32_t DUL = DUH + PLC;
+  static constexpr uint32_t UH = DUL + PLC;          // U planes
+  static constexpr uint32_t UL = UH + PLC;
+  static constexpr uint32_t DOL = UL + PLC;          // fp16 only: lo plane of dO
+  static constexpr uint32_t VEC = DOL + (XS ? PLC : 0);  // g; 8 warp partials
   static constexpr uint32_t bytes = VEC + C * 4 + 8 * 4;
 };
 
 template <int D, typename E>
-__global__ void __launch_bounds__(256) bwd_sgrad_kernel(BwdParams p) {
-  using S = SgSmem<D>;
-  constexpr int DP = S::DP, WP = S::WP;
+__global__ void __launch_bounds__(256, 1) bwd_sgrad_kernel(BwdParams p) {
   constexpr bool XS = kSplitSrc<E>;
+  using S = SgSmem<D, XS>;
+  constexpr int DP = S::DP;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
   const int j = blockIdx.x, hv = blockIdx.y;
   if (j >= p.status[1]) return;
   const int4 ct = p.chunk_tab[j];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* sSB = reinterpret_cast<float*>(smem + S::SB);
+  bf16* sSH = reinterpret_cast<bf16*>(smem + S::SH);
+  bf16* sSL = reinterpret_cast<bf16*>(smem + S::SL);
   E* sDO = reinterpret_cast<E*>(smem + S::DO);
-  float* sDU = reinterpret_cast<float*>(smem + S::DU);
-  float* sU = reinterpret_cast<float*>(smem + S::U);
+  bf16* sDUH = reinterpret_cast<bf16*>(smem + S::DUH);
+  bf16* sDUL = reinterpret_cast<bf16*>(smem + S::DUL);
+  bf16* sUH = reinterpret_cast<bf16*>(smem + S::UH);
+  bf16* sUL = reinterpret_cast<bf16*>(smem + S::UL);
+  bf16* sDOL = reinterpret_cast<bf16*>(smem + S::DOL);
   float* vg = reinterpret_cast<float*>(smem + S::VEC);
   float* vred = vg + C;
   const int64_t item = (int64_t)j * p.HV + hv;
+  const bf16* sin_g = reinterpret_cast<const bf16*>(p.s_in) + item * 2 * D * D;
+  const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
+  const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
 
-  load_f32<D, WP>(sSB, p.s_in + item * D * D, D, D, tid, 256);
+  load_rows<D, DP>(sSH, sin_g, D, D, tid, 256);
+  load_rows<D, DP>(sSL, sin_g + D * D, D, D, tid, 256);
   load_tokens<D>(sDO, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, ct.y, ct.z, tid, 256);
-  load_f32<D, WP>(sDU, p.du + item * C * D, D, C, tid, 256);
-  load_f32<D, WP>(sU, p.u + item * C * D, D, C, tid, 256);
+  load_rows<D, DP>(sDUH, du_g, D, C, tid, 256);
+  load_rows<D, DP>(sDUL, du_g + C * D, D, C, tid, 256);
+  load_rows<D, DP>(sUH, u_g, D, C, tid, 256);
+  load_rows<D, DP>(sUL, u_g + C * D, D, C, tid, 256);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
+  if (XS) {
+    split_inplace<D, DP>(sDO, sDOL, C, tid, 256);
+    __syncthreads();
+  }
+  const bf16* doh = reinterpret_cast<const bf16*>(sDO);
 
-  // [dO; dU] S_in: warps 0-3 rows 16 w of dO, warps 4-7 rows 16 (w - 4) of dU; all D columns
+  // [dO; dU] S_in: warp tiles of 32 rows x D/2 columns; row blocks 0, 1 of dO and 0, 1 of dU
   {
-    constexpr int NT = D / 8;
-    const int m0 = 16 * (warp & 3);
-    float acc[1][NT][4];
+    constexpr int NT = D / 16;
+    const int rb = warp & 3, m0 = 32 * (rb & 1), n0 = (D / 2) * (warp >> 2);
+    float acc[2][NT][4];
     wm::zero(acc);
-    auto fb = [&](int x, int n) { return sSB[x * WP + n]; };
-    if (warp < 4) {
-      auto fa = [&](int m, int x) { return to_f(sDO[m * DP + x]); };
-      wm::gemm<1, NT, XS, true>(acc, fa, fb, m0, 0, 0, D);
+    if (rb < 2) {
+      wm::pgemm<2, NT, false, true, XS, true>(acc, doh, sDOL, DP, sSH, sSL, DP, m0, n0, 0, D);
       float* out = p.dqa + item * C * D;
       const float sc = p.scale;
-      wm::for_each_pair(acc, m0, 0, [&](int i, int c, float& x0, float& x1) {
+      wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
         const float f = sc * expf(vg[i]);
         *reinterpret_cast<float2*>(out + i * D + c) = make_float2(f * x0, f * x1);
       });
     } else {
-      auto fa = [&](int m, int x) { return sDU[m * WP + x]; };
-      wm::gemm<1, NT, true, true>(acc, fa, fb, m0, 0, 0, D);
-      float* out = p.dw + item * C * D;
-      wm::for_each_pair(acc, m0, 0, [&](int i, int c, float& x0, float& x1) {
-        *reinterpret_cast<float2*>(out + i * D + c) = make_float2(-x0, -x1);
+      wm::pgemm<2, NT, false, true, true, true>(acc, sDUH, sDUL, DP, sSH, sSL, DP, m0, n0, 0, D);
+      bf16* out = reinterpret_cast<bf16*>(p.dw) + item * 2 * C * D;  // -dU S_in as planes
+      wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
+        wm::store_split2(out + i * D + c, out + C * D + i * D + c, -x0, -x1);
       });
     }
   }
   __syncthreads();
-  // dS_out over S_in, with <dS_out, S_in>
+  // dS_out planes over the S_in planes, with <dS_out, S_in>
   {
-    const float* src = p.ds_out + item * D * D;
+    const bf16* src = reinterpret_cast<const bf16*>(p.ds_out) + item * 2 * D * D;
     float part = 0.f;
-    for (int e = tid; e < D * D / 4; e += 256) {
-      const int i = e / (D / 4), c = (e % (D / 4)) * 4;
-      const float4 x = *reinterpret_cast<const float4*>(src + i * D + c);
-      float4* y = reinterpret_cast<float4*>(sSB + i * WP + c);
-      const float4 s = *y;
-      part = fmaf(x.x, s.x, part);
-      part = fmaf(x.y, s.y, part);
-      part = fmaf(x.z, s.z, part);
-      part = fmaf(x.w, s.w, part);
-      *y = x;
+    for (int e = tid; e < D * D / 8; e += 256) {
+      const int i = e / (D / 8), c = (e % (D / 8)) * 8;
+      const uint4 gh = *reinterpret_cast<const uint4*>(src + i * D + c);
+      const uint4 gl = *reinterpret_cast<const uint4*>(src + D * D + i * D + c);
+      uint4* yh = reinterpret_cast<uint4*>(sSH + i * DP + c);
+      uint4* yl = reinterpret_cast<uint4*>(sSL + i * DP + c);
+      const uint4 sh = *yh, sl = *yl;
+      const uint32_t a[4] = {gh.x, gh.y, gh.z, gh.w}, b[4] = {gl.x, gl.y, gl.z, gl.w};
+      const uint32_t x[4] = {sh.x, sh.y, sh.z, sh.w}, y[4] = {sl.x, sl.y, sl.z, sl.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 g0 = ElemT<bf16>::unpack(a[u]), g1 = ElemT<bf16>::unpack(b[u]);
+        const float2 s0 = ElemT<bf16>::unpack(x[u]), s1 = ElemT<bf16>::unpack(y[u]);
+        part = fmaf(g0.x + g1.x, s0.x + s1.x, part);
+        part = fmaf(g0.y + g1.y, s0.y + s1.y, part);
+      }
+      *yh = gh;
+      *yl = gl;
     }
     part = warp_sum(part);
     if (lane == 0) vred[warp] = part;
@@ -784,15 +830,13 @@ __global__ void __launch_bounds__(256) bwd_sgrad_kernel(BwdParams p) {
     for (int w = 0; w < 8; ++w) s += vred[w];
     p.dgc[item] = expf(vg[C - 1]) * s;
   }
-  // U dS_out (C x D): warp rows 16 (w & 3), columns (D/2) (w >> 2)
+  // U dS_out (C x D): warp tiles of 32 rows x D/4 columns
   {
-    constexpr int NT = D / 16;
-    const int m0 = 16 * (warp & 3), n0 = (D / 2) * (warp >> 2);
-    float acc[1][NT][4];
+    constexpr int NT = D / 32;
+    const int m0 = 32 * (warp & 1), n0 = (D / 4) * (warp >> 1);
+    float acc[2][NT][4];
     wm::zero(acc);
-    auto fa = [&](int m, int x) { return sU[m * WP + x]; };
-    auto fb = [&](int x, int n) { return sSB[x * WP + n]; };
-    wm::gemm<1, NT, true, true>(acc, fa, fb, m0, n0, 0, D);
+    wm::pgemm<2, NT, false, true, true, true>(acc, sUH, sUL, DP, sSH, sSL, DP, m0, n0, 0, D);
     float* out = p.dkr + item * C * D;
     wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
       *reinterpret_cast<float2*>(out + i * D + c) = make_float2(x0, x1);
@@ -804,7 +848,7 @@ __global__ void __launch_bounds__(256) bwd_sgrad_kernel(BwdParams p) {
 
 template <int D>
 struct LoSmem {
-  static constexpr int DP = D + 8, WP = D + 4;
+  static constexpr int DP = D + 8;
   static constexpr uint32_t TOK = C * DP * 2;        // one 16-bit token tile
   static constexpr uint32_t CC = C * CP * 4;         // one fp32 C x C tile
   static constexpr uint32_t RQ = 0;                  // q, k tiles (whole kernel)
@@ -815,9 +859,10 @@ struct LoSmem {
   static constexpr uint32_t C2 = C1 + CC;            // Q^K^^T, then dGamma
   static constexpr uint32_t C3 = C2 + CC;            // K^K^^T
   static constexpr uint32_t C4 = C3 + CC;            // dP
-  static constexpr uint32_t F1 = C4 + CC;            // U, then dW (fp32 [C][WP])
-  static constexpr uint32_t F2 = F1 + C * WP * 4;    // dU
-  static constexpr uint32_t VEC = F2 + C * WP * 4;   // 24 vectors of C
+  static constexpr uint32_t PAIRD = 2 * C * DP * 2;  // hi, lo planes of a C x D operand
+  static constexpr uint32_t F1 = C4 + CC;            // U, then dW (planes)
+  static constexpr uint32_t F2 = F1 + PAIRD;         // dU (planes)
+  static constexpr uint32_t VEC = F2 + PAIRD;        // 24 vectors of C
   static constexpr uint32_t bytes = VEC + 24 * C * 4;
   static_assert(bytes <= 232448, "shared memory per CTA");
 };
@@ -854,7 +899,7 @@ __device__ __forceinline__ void norm_backward(float (&acc)[1][NT][4], const E* r
 template <int D, typename E>
 __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   using S = LoSmem<D>;
-  constexpr int DP = S::DP, WP = S::WP;
+  constexpr int DP = S::DP;
   constexpr bool XS = kSplitSrc<E>;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
@@ -876,8 +921,9 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   float* C2 = reinterpret_cast<float*>(smem + S::C2);
   float* C3 = reinterpret_cast<float*>(smem + S::C3);
   float* C4 = reinterpret_cast<float*>(smem + S::C4);
-  float* F1 = reinterpret_cast<float*>(smem + S::F1);
-  float* F2 = reinterpret_cast<float*>(smem + S::F2);
+  bf16* F1 = reinterpret_cast<bf16*>(smem + S::F1);
+  bf16* F2 = reinterpret_cast<bf16*>(smem + S::F2);
+  constexpr int64_t FPL = C * DP;  // elements from a hi plane to its lo plane
   float* vg = reinterpret_cast<float*>(smem + S::VEC);
   float* vbt = vg + C;
   float* vrq = vbt + C;
@@ -900,9 +946,14 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   load_tokens<D>(rk_t, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
   load_tokens<D>(rv_t, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
   load_tokens<D>(rdo_t, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
-  load_f32<D, WP>(F1, p.u + item * C * D, D, C, tid, 256);
-  load_f32<D, WP>(F2, p.du + item * C * D, D, C, tid, 256);
-  load_f32<C, CP>(C1, p.minv + item * C * C, C, C, tid, 256);
+  const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
+  const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
+  load_rows<D, DP>(F1, u_g, D, C, tid, 256);
+  load_rows<D, DP>(F1 + FPL, u_g + C * D, D, C, tid, 256);
+  load_rows<D, DP>(F2, du_g, D, C, tid, 256);
+  load_rows<D, DP>(F2 + FPL, du_g + C * D, D, C, tid, 256);
+  bf16* mi_s = reinterpret_cast<bf16*>(C3);  // M^{-1} planes land in C3 (written later) and widen into C1
+  load_rows<C, C>(mi_s, reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C, C, 2 * C, tid, 256);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
   else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
@@ -914,6 +965,8 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     veg[tid] = expf(vg[tid]);
     vdec[tid] = expf(vg[C - 1] - vg[tid]);
   }
+  for (int e = tid; e < C * C; e += 256) C1[(e / C) * CP + e % C] = wm::plane_val(mi_s, e, C * C);
+  __syncthreads();
 
   // C x C warp tiles: rows m0 .. m0 + 15, columns n0 .. n0 + 31
   const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
@@ -931,10 +984,10 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     wm::gemm<1, 4, XS, XS>(kk, fk, fkt, m0, n0, 0, D);
     // dP = scale tril(dO U^T)
     auto fdo = [&](int m, int x) { return to_f(rdo_t[m * DP + x]); };
-    auto fut = [&](int x, int n) { return F1[n * WP + x]; };
+    auto fut = [&](int x, int n) { return wm::plane_val(F1, n * DP + x, FPL); };
     wm::gemm<1, 4, XS, true>(dp, fdo, fut, m0, n0, 0, D);
     // dU V^T
-    auto fdu = [&](int m, int x) { return F2[m * WP + x]; };
+    auto fdu = [&](int m, int x) { return wm::plane_val(F2, m * DP + x, FPL); };
     auto fvt = [&](int x, int n) { return to_f(rv_t[n * DP + x]); };
     wm::gemm<1, 4, true, XS>(da1, fdu, fvt, m0, n0, 0, D);
     const float sc = p.scale;
@@ -943,7 +996,9 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     wm::for_each(dp, m0, n0, [&](int i, int c, float& x) { C4[i * CP + c] = c <= i ? sc * x : 0.f; });
   }
   __syncthreads();  // U, v and dO tiles no longer read
-  load_f32<D, WP>(F1, p.dw + item * C * D, D, C, tid, 256);
+  const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
+  load_rows<D, DP>(F1, dw_g, D, C, tid, 256);
+  load_rows<D, DP>(F1 + FPL, dw_g + C * D, D, C, tid, 256);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
@@ -951,7 +1006,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     // dA = dU V^T + dW (diag(e^g/|k|) K)^T on and below the diagonal; then dZ, d beta, dGamma, dM^{-1}
     float da2[1][4][4];
     wm::zero(da2);
-    auto fdw = [&](int m, int x) { return F1[m * WP + x]; };
+    auto fdw = [&](int m, int x) { return wm::plane_val(F1, m * DP + x, FPL); };
     auto fkt = [&](int x, int n) { return to_f(rk_t[n * DP + x]); };
     wm::gemm<1, 4, true, XS>(da2, fdw, fkt, m0, n0, 0, D);
     float colp[4][2];
@@ -1045,7 +1100,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     // dv = A^T dU
     float acc[1][NT][4];
     wm::zero(acc);
-    auto fb = [&](int x, int n) { return F2[x * WP + n]; };
+    auto fb = [&](int x, int n) { return wm::plane_val(F2, x * DP + n, FPL); };
     wm::gemm<1, NT, true, true>(acc, fat, fb, m0, nd, m0, C);
     wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
       if (i < len) *reinterpret_cast<float2*>(p.dv + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
@@ -1055,7 +1110,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
     // dk^ = diag(e^g) A^T dW + diag(dec) dKr + (Gamma . dP)^T Q^ + diag(beta) X K^ + X^T diag(beta) K^
     float acc[1][NT][4];
     wm::zero(acc);
-    auto fb = [&](int x, int n) { return F1[x * WP + n]; };
+    auto fb = [&](int x, int n) { return wm::plane_val(F1, x * DP + n, FPL); };
     wm::gemm<1, NT, true, true>(acc, fat, fb, m0, nd, m0, C);
     const float* dkr = p.dkr + item * C * D;
     float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
@@ -1158,6 +1213,356 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   }
 }
 
+// The local kernel for bf16 inputs: every product takes its operands from bf16 planes through
+// ldmatrix. The C x C operands that the products need scaled or combined (Gamma . dP with the
+// key or query norms, A, X's symmetric combination) are materialised as planes once; the
+// element-wise steps run on the accumulators where the fragments already sit.
+template <int D>
+struct LoFastSmem {
+  static constexpr int DP = D + 8, PP = C + 8;
+  static constexpr uint32_t TILE = C * DP * 2;
+  static constexpr uint32_t PAIR = 2 * C * PP * 2;   // hi, lo planes of a C x C operand
+  static constexpr uint32_t TQ = 0;                  // q, k tiles (whole kernel)
+  static constexpr uint32_t TK = TQ + TILE;
+  static constexpr uint32_t R1 = TK + TILE;          // v, dO tiles; after their last use: pairs P1, P2
+  static constexpr uint32_t R1B = 2 * TILE > 2 * PAIR ? 2 * TILE : 2 * PAIR;
+  static constexpr uint32_t PU = R1 + R1B;           // U planes, then dW planes
+  static constexpr uint32_t PDU = PU + 2 * TILE;     // dU planes
+  static constexpr uint32_t CM = PDU + 2 * TILE;     // M^{-1} planes, then A planes
+  static constexpr uint32_t P3 = CM + PAIR;
+  static constexpr uint32_t P4 = P3 + PAIR;
+  static constexpr int NVEC = 26;                     // vectors of C floats (carved below, in order)
+  static constexpr uint32_t VEC = P4 + PAIR;
+  static constexpr uint32_t bytes = VEC + NVEC * C * 4;
+  static_assert(bytes <= 232448, "shared memory per CTA");
+};
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
+  using S = LoFastSmem<D>;
+  constexpr int DP = S::DP, PP = S::PP, PLN = C * PP;
+  constexpr int64_t TPL = C * DP;  // elements from a C x D hi plane to its lo plane
+  extern __shared__ __align__(128) unsigned char smem[];
+  if (p.status[0] != GDN_OK) return;
+  const int j = blockIdx.x, hv = blockIdx.y;
+  if (j >= p.status[1]) return;
+  const int4 ct = p.chunk_tab[j];
+  const int64_t t0 = ct.y;
+  const int len = ct.z;
+  const int h = hv / (p.HV / p.H);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t item = (int64_t)j * p.HV + hv;
+  bf16* tq = reinterpret_cast<bf16*>(smem + S::TQ);
+  bf16* tk = reinterpret_cast<bf16*>(smem + S::TK);
+  bf16* tv = reinterpret_cast<bf16*>(smem + S::R1);
+  bf16* tdo = reinterpret_cast<bf16*>(smem + S::R1 + S::TILE);
+  bf16* p1 = reinterpret_cast<bf16*>(smem + S::R1);           // dM^{-1}, then X
+  bf16* p2 = reinterpret_cast<bf16*>(smem + S::R1 + S::PAIR);  // (Gamma . dP) diag(1/|k|)
+  bf16* pu = reinterpret_cast<bf16*>(smem + S::PU);
+  bf16* pdu = reinterpret_cast<bf16*>(smem + S::PDU);
+  bf16* cm = reinterpret_cast<bf16*>(smem + S::CM);
+  bf16* p3 = reinterpret_cast<bf16*>(smem + S::P3);  // diag(1/|q|) (Gamma . dP)
+  bf16* p4 = reinterpret_cast<bf16*>(smem + S::P4);  // T1, then the symmetric X combination
+  float* vg = reinterpret_cast<float*>(smem + S::VEC);
+  float* vbt = vg + C;
+  float* vrq = vbt + C;
+  float* vrk = vrq + C;
+  float* veg = vrk + C;      // e^g
+  float* vdec = veg + C;     // e^{g_C - g}
+  float* vdb = vdec + C;     // d beta
+  float* vdg = vdb + C;      // d g
+  float* vcolp = vdg + C;    // [4][C] column partials (d beta, then the column sums of dGamma . Gamma)
+  float* vrow = vcolp + 4 * C;  // [2][C] row sums of dGamma . Gamma
+  float* vxb = vrow + 2 * C;    // [2][C] row sums of X . K^K^^T
+  float* vpA = vxb + 2 * C;     // [2][C] eg <k^, A^T dW>
+  float* vpB = vpA + 2 * C;     // [2][C] dec <k^, dKr>
+  float* vpC = vpB + 2 * C;     // [2][C] <dQa, q^>
+  float* vnk = vpC + 2 * C;     // [2][C] <k, dk^>
+  float* vnq = vnk + 2 * C;     // [2][C] <q, dq^>
+  static_assert(S::NVEC == 26, "vg .. vnq: 8 single vectors, vcolp 4, vrow, vxb, vpA, vpB, vpC, vnk, vnq 2 each");
+  const bool fused_norm = p.HV == p.H;
+
+  const bf16* qin = static_cast<const bf16*>(p.q) + (int64_t)h * D;
+  const bf16* kin = static_cast<const bf16*>(p.k) + (int64_t)h * D;
+  load_tokens<D>(tq, qin, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(tk, kin, (int64_t)p.H * D, t0, len, tid, 256);
+  load_tokens<D>(tv, static_cast<const bf16*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_tokens<D>(tdo, static_cast<const bf16*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
+  const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
+  const bf16* mi_g = reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C;
+  load_rows<D, DP>(pu, u_g, D, C, tid, 256);
+  load_rows<D, DP>(pu + TPL, u_g + C * D, D, C, tid, 256);
+  load_rows<D, DP>(pdu, du_g, D, C, tid, 256);
+  load_rows<D, DP>(pdu + TPL, du_g + C * D, D, C, tid, 256);
+  load_rows<C, PP>(cm, mi_g, C, C, tid, 256);
+  load_rows<C, PP>(cm + PLN, mi_g + C * C, C, C, tid, 256);
+  if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
+  else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
+  else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
+  else if (tid < 64) cp_async_16(vrk + 4 * (tid - 48), p.rk + item * C + 4 * (tid - 48));
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < C) {
+    veg[tid] = expf(vg[tid]);
+    vdec[tid] = expf(vg[C - 1] - vg[tid]);
+  }
+
+  // ---- C x C stage: warp tiles rows m0 .. m0 + 15, columns n0 .. n0 + 31
+  const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+  const int r = wm::lane_r(), cl = wm::lane_c();
+  float qk[1][4][4], kk[1][4][4], dp[1][4][4], da[1][4][4];
+  wm::zero(qk);
+  wm::zero(kk);
+  wm::zero(dp);
+  wm::zero(da);
+  wm::pgemm<1, 4, false, false, false, false>(qk, tq, tq, DP, tk, tk, DP, m0, n0, 0, D);
+  wm::pgemm<1, 4, false, false, false, false>(kk, tk, tk, DP, tk, tk, DP, m0, n0, 0, D);
+  wm::pgemm<1, 4, false, false, false, true>(dp, tdo, tdo, DP, pu, pu + TPL, DP, m0, n0, 0, D);  // dO U^T
+  wm::pgemm<1, 4, false, false, true, false>(da, pdu, pdu + TPL, DP, tv, tv, DP, m0, n0, 0, D);  // dU V^T
+  __syncthreads();  // U, v and dO no longer read; veg, vdec visible
+  {
+    const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
+    load_rows<D, DP>(pu, dw_g, D, C, tid, 256);
+    load_rows<D, DP>(pu + TPL, dw_g + C * D, D, C, tid, 256);
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  {
+    float da2[1][4][4];
+    wm::zero(da2);
+    wm::pgemm<1, 4, false, false, true, false>(da2, pu, pu + TPL, DP, tk, tk, DP, m0, n0, 0, D);  // dW K^T
+    // dA (on and below the diagonal), Z = Gamma . M^{-1}, d beta (columns), dZ, dGamma (kept in qk),
+    // dM^{-1} -> p1, (Gamma . dP) diag(1/|k|) -> p2, diag(1/|q|) (Gamma . dP) -> p3
+    const float sc = p.scale;
+    float colp[4][2];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      colp[jj][0] = colp[jj][1] = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = m0 + r + 8 * hh, c = n0 + 8 * jj + cl;
+        float dm[2], g1k[2], g1q[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int e = 2 * hh + u, cc = c + u;
+          const bool low = cc <= i;
+          const float gam = low ? expf(vg[i] - vg[cc]) : 0.f;
+          const float mv = wm::plane_val(cm, i * PP + cc, PLN);
+          const float dA = low ? da[0][jj][e] + da2[0][jj][e] * veg[cc] * vrk[cc] : 0.f;
+          const float dP = low ? sc * dp[0][jj][e] : 0.f;
+          colp[jj][u] += dA * gam * mv;
+          const float dZ = dA * vbt[cc];
+          qk[0][jj][e] = low ? dP * qk[0][jj][e] * vrq[i] * vrk[cc] + dZ * mv : 0.f;  // dGamma
+          dm[u] = dZ * gam;
+          g1k[u] = gam * dP * vrk[cc];
+          g1q[u] = gam * dP * vrq[i];
+        }
+        wm::store_split2(p1 + i * PP + c, p1 + PLN + i * PP + c, dm[0], dm[1]);
+        wm::store_split2(p2 + i * PP + c, p2 + PLN + i * PP + c, g1k[0], g1k[1]);
+        wm::store_split2(p3 + i * PP + c, p3 + PLN + i * PP + c, g1q[0], g1q[1]);
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float s = col_sum(colp[jj][u]);
+        if (lane < 4) vcolp[(warp & 3) * C + n0 + 8 * jj + cl + u] = s;
+      }
+  }
+  __syncthreads();
+  if (tid < C) vdb[tid] = vcolp[tid] + vcolp[C + tid] + vcolp[2 * C + tid] + vcolp[3 * C + tid];
+  {
+    // T1 = M^{-T} dM^{-1} -> p4 (M^{-T}[i][l] = M^{-1}[l][i], zero for l < i)
+    float t1[1][4][4];
+    wm::zero(t1);
+    wm::pgemm<1, 4, true, true, true, true>(t1, cm, cm + PLN, PP, p1, p1 + PLN, PP, m0, n0, m0, C);
+    wm::for_each_pair(t1, m0, n0, [&](int i, int c, float& x0, float& x1) {
+      wm::store_split2(p4 + i * PP + c, p4 + PLN + i * PP + c, x0, x1);
+    });
+  }
+  __syncthreads();
+  {
+    // X = -T1 M^{-T}, strictly lower (M^{-T}[l][c] = M^{-1}[c][l], zero for l > c) -> p1; with the row sums
+    // of X . K^K^^T (d beta) and the row and column sums of dGamma . Gamma (d g)
+    float xx[1][4][4];
+    wm::zero(xx);
+    wm::pgemm<1, 4, false, false, true, true>(xx, p4, p4 + PLN, PP, cm, cm + PLN, PP, m0, n0, 0, n0 + 32);
+    float xb[2] = {0.f, 0.f}, wr[2] = {0.f, 0.f}, wc[4][2];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      wc[jj][0] = wc[jj][1] = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = m0 + r + 8 * hh, c = n0 + 8 * jj + cl;
+        float xv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int e = 2 * hh + u, cc = c + u;
+          xv[u] = cc < i ? -xx[0][jj][e] : 0.f;
+          xb[hh] += xv[u] * kk[0][jj][e] * vrk[i] * vrk[cc];
+          const float w = cc <= i ? qk[0][jj][e] * expf(vg[i] - vg[cc]) : 0.f;
+          wr[hh] += w;
+          wc[jj][u] += w;
+        }
+        wm::store_split2(p1 + i * PP + c, p1 + PLN + i * PP + c, xv[0], xv[1]);
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float a = quad_sum(xb[hh]), b2 = quad_sum(wr[hh]);
+      if ((lane & 3) == 0) {
+        vxb[(warp >> 2) * C + m0 + r + 8 * hh] = a;
+        vrow[(warp >> 2) * C + m0 + r + 8 * hh] = b2;
+      }
+    }
+    __syncthreads();  // vcolp free again (d beta read it above)
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float s = col_sum(wc[jj][u]);
+        if (lane < 4) vcolp[(warp & 3) * C + n0 + 8 * jj + cl + u] = s;
+      }
+  }
+  __syncthreads();
+  // A = (Gamma . M^{-1}) diag(beta) in place of M^{-1}; Y = diag(1/|k|) combination of X for the key
+  // gradient: Y[i][c] = (beta_i X_ic + beta_c X_ci) / |k_c| -> p4; d beta and the row/column sums of d g
+  for (int e = tid; e < C * C / 2; e += 256) {
+    const int i = e / (C / 2), c = (e % (C / 2)) * 2;
+    float a2[2], y2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int cc = c + u;
+      const float mv = wm::plane_val(cm, i * PP + cc, PLN);
+      a2[u] = cc <= i ? expf(vg[i] - vg[cc]) * mv * vbt[cc] : 0.f;
+      y2[u] = vrk[cc] * (vbt[i] * wm::plane_val(p1, i * PP + cc, PLN) + vbt[cc] * wm::plane_val(p1, cc * PP + i, PLN));
+    }
+    wm::store_split2(cm + i * PP + c, cm + PLN + i * PP + c, a2[0], a2[1]);
+    wm::store_split2(p4 + i * PP + c, p4 + PLN + i * PP + c, y2[0], y2[1]);
+  }
+  if (tid < C) {
+    const int i = tid;
+    vdb[i] += vxb[i] + vxb[C + i];
+    vdg[i] = (vrow[i] + vrow[C + i]) - (vcolp[i] + vcolp[C + i] + vcolp[2 * C + i] + vcolp[3 * C + i]);
+  }
+  __syncthreads();
+
+  // ---- C x D stage: warp tiles rows m0 .. m0 + 15, columns nd .. nd + D/2
+  constexpr int NT = D / 16;
+  const int nd = (D / 2) * (warp >> 2);
+  {
+    // dv = A^T dU   (A^T[j][i] = A[i][j], zero for i < j)
+    float acc[1][NT][4];
+    wm::zero(acc);
+    wm::pgemm<1, NT, true, true, true, true>(acc, cm, cm + PLN, PP, pdu, pdu + TPL, DP, m0, nd, m0, C);
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      if (i < len) *reinterpret_cast<float2*>(p.dv + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+    });
+  }
+  {
+    // dk^ = diag(e^g) A^T dW + diag(dec) dKr + (diag(1/|q|) (Gamma . dP))^T Q + Y K
+    float acc[1][NT][4];
+    wm::zero(acc);
+    wm::pgemm<1, NT, true, true, true, true>(acc, cm, cm + PLN, PP, pu, pu + TPL, DP, m0, nd, m0, C);
+    const float* dkr = p.dkr + item * C * D;
+    float pa[2] = {0.f, 0.f}, pb[2] = {0.f, 0.f};
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      const bool lo8 = i - m0 < 8;
+      const float k0 = __bfloat162float(tk[i * DP + c]) * vrk[i], k1 = __bfloat162float(tk[i * DP + c + 1]) * vrk[i];
+      const float2 kr = *reinterpret_cast<const float2*>(dkr + i * D + c);
+      const float ya = fmaf(k0, x0, k1 * x1), yb = fmaf(k0, kr.x, k1 * kr.y);
+      if (lo8) {
+        pa[0] += ya;
+        pb[0] += yb;
+      } else {
+        pa[1] += ya;
+        pb[1] += yb;
+      }
+      x0 = veg[i] * x0 + vdec[i] * kr.x;
+      x1 = veg[i] * x1 + vdec[i] * kr.y;
+    });
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float a = quad_sum(pa[hh]), b2 = quad_sum(pb[hh]);
+      if ((lane & 3) == 0) {
+        const int i = m0 + r + 8 * hh;
+        vpA[(warp >> 2) * C + i] = veg[i] * a;
+        vpB[(warp >> 2) * C + i] = vdec[i] * b2;
+      }
+    }
+    wm::pgemm<1, NT, true, true, true, false>(acc, p3, p3 + PLN, PP, tq, tq, DP, m0, nd, m0, C);
+    wm::pgemm<1, NT, false, true, true, false>(acc, p4, p4 + PLN, PP, tk, tk, DP, m0, nd, 0, C);
+    if (fused_norm)
+      norm_backward<D, NT>(acc, tk, vrk, vnk, m0, nd, len, p.dk + (t0 * p.H + h) * D, (int64_t)p.H * D);
+    else
+      wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+        if (i < len) *reinterpret_cast<float2*>(p.dkh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+      });
+  }
+  {
+    // dq^ = dQa + ((Gamma . dP) diag(1/|k|)) K
+    float acc[1][NT][4];
+    const float* dqa = p.dqa + item * C * D;
+    float pc[2] = {0.f, 0.f};
+    wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+      const float2 a = *reinterpret_cast<const float2*>(dqa + i * D + c);
+      x0 = a.x;
+      x1 = a.y;
+      const float y = fmaf(__bfloat162float(tq[i * DP + c]), a.x, __bfloat162float(tq[i * DP + c + 1]) * a.y);
+      if (i - m0 < 8) pc[0] += y; else pc[1] += y;
+    });
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float s = quad_sum(pc[hh]);
+      if ((lane & 3) == 0) {
+        const int i = m0 + r + 8 * hh;
+        vpC[(warp >> 2) * C + i] = vrq[i] * s;
+      }
+    }
+    wm::pgemm<1, NT, false, true, true, false>(acc, p2, p2 + PLN, PP, tk, tk, DP, m0, nd, 0, m0 + 16);
+    if (fused_norm)
+      norm_backward<D, NT>(acc, tq, vrq, vnq, m0, nd, len, p.dq + (t0 * p.H + h) * D, (int64_t)p.H * D);
+    else
+      wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
+        if (i < len) *reinterpret_cast<float2*>(p.dqh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
+      });
+  }
+  __syncthreads();
+  if (tid < C) {
+    const int i = tid;
+    const float rb = vpB[i] + vpB[C + i];
+    vdg[i] += (vpC[i] + vpC[C + i]) - rb + (vpA[i] + vpA[C + i]);
+    vrow[i] = rb;  // r_i, for the chunk-end term
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float sr = 0.f;
+    for (int i = 0; i < C; ++i) sr += vrow[i];
+    vdg[C - 1] += sr + p.dgc[item];
+    float run = 0.f;  // d log alpha_i = sum_{i' >= i} dg_i'
+    for (int i = C - 1; i >= 0; --i) {
+      run += vdg[i];
+      vdg[i] = run;
+    }
+  }
+  __syncthreads();
+  if (tid < len) {
+    const int64_t t = t0 + tid;
+    const float dla = vdg[tid];
+    const float x = p.a[t * p.HV + hv] + p.dt_bias[hv];
+    const float eA = expf(p.A_log[hv]);
+    const float sig = 1.f / (1.f + expf(-x));
+    const float bt = vbt[tid];
+    p.da[t * p.HV + hv] = dla * (-eA) * sig;
+    p.db[t * p.HV + hv] = vdb[tid] * bt * (1.f - bt);
+    p.dlala[t * p.HV + hv] = dla * (-eA * softplus_f(x));
+  }
+}
+
 // ----------------------------------------------------------------------------- norm, gate sums
 
 template <int D, typename E>
@@ -1231,11 +1636,11 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
   int n = 0;
   const dim3 items((unsigned)p.max_chunks, (unsigned)p.HV);
   const unsigned chains = (unsigned)((int64_t)p.B * p.HV * (D / VB));
-  if ((e = set_smem(bwd_factor_kernel<D, E>, FacSmem<D>::bytes)) != cudaSuccess) return e;
-  bwd_factor_kernel<D, E><<<items, 256, FacSmem<D>::bytes, s>>>(p);
+  constexpr bool f16in = kSplitSrc<E>;
+  if ((e = set_smem(bwd_factor_kernel<D, E>, FacSmem<D, f16in>::bytes)) != cudaSuccess) return e;
+  bwd_factor_kernel<D, E><<<items, 256, FacSmem<D, f16in>::bytes, s>>>(p);
   ++n;
   if (chains > 0) {
-    constexpr bool f16in = kSplitSrc<E>;
     const uint32_t sb = f16in ? StSmem<D>::bytes_fp16 : StSmem<D>::bytes_bf16;
     const uint32_t db = DsSmem<D, f16in>::bytes;
     if ((e = set_smem(bwd_state_kernel<D, E>, sb)) != cudaSuccess) return e;
@@ -1244,10 +1649,15 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
     bwd_dstate_kernel<D, E><<<chains, kSeqThreads, db, s>>>(p);
     n += 2;
   }
-  if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D>::bytes)) != cudaSuccess) return e;
-  bwd_sgrad_kernel<D, E><<<items, 256, SgSmem<D>::bytes, s>>>(p);
-  if ((e = set_smem(bwd_local_kernel<D, E>, LoSmem<D>::bytes)) != cudaSuccess) return e;
-  bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
+  if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D, f16in>::bytes)) != cudaSuccess) return e;
+  bwd_sgrad_kernel<D, E><<<items, 256, SgSmem<D, f16in>::bytes, s>>>(p);
+  if (f16in) {  // fp16 inputs: the generic local kernel
+    if ((e = set_smem(bwd_local_kernel<D, E>, LoSmem<D>::bytes)) != cudaSuccess) return e;
+    bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
+  } else {
+    if ((e = set_smem(bwd_local_fast_kernel<D>, LoFastSmem<D>::bytes)) != cudaSuccess) return e;
+    bwd_local_fast_kernel<D><<<items, 256, LoFastSmem<D>::bytes, s>>>(p);
+  }
   n += 2;
   const int64_t rows = p.T * p.H;
   if (rows > 0 && p.HV != p.H) {  // grouped heads: sum the value heads' gradients, then the norm

@@ -11,15 +11,16 @@ struct BwdLayout {
   size_t status, seq_chunk_off, order, chunk_tab;  // as in the forward (schedule kernel)
   size_t g, beta;                                   // fp32 [mc][HV][C] (gates kernel)
   size_t rq, rk;                                    // fp32 [mc][HV][C]: 1/|q|, 1/|k| (0 on padded rows)
-  size_t minv;                                      // fp32 [mc][HV][C][C]: M^{-1}
+  size_t minv;                                      // bf16 [mc][HV][2][C][C]: M^{-1}, hi and lo planes
   size_t pm;                                        // bf16 [mc][HV][2][C][C]: P = Gamma . tril(Q^ K^^T), hi and lo planes
   size_t w;                                         // bf16 [mc][HV][2][C][D]: W<-, hi and lo planes
   size_t ut;                                        // fp32 [mc][HV][C][D]: U~
-  size_t s_in;                                      // fp32 [mc][HV][D][D]: state entering each chunk
-  size_t u;                                         // fp32 [mc][HV][C][D]: U = U~ - W<- S^T
-  size_t ds_out;                                    // fp32 [mc][HV][D][D]: gradient of the state leaving each chunk
-  size_t du;                                        // fp32 [mc][HV][C][D]: gradient of U
-  size_t dqa, dw, dkr;                              // fp32 [mc][HV][C][D]: the state-operand products
+  size_t s_in;                                      // bf16 [mc][HV][2][D][D]: state entering each chunk (planes)
+  size_t u;                                         // bf16 [mc][HV][2][C][D]: U = U~ - W<- S^T (planes)
+  size_t ds_out;                                    // bf16 [mc][HV][2][D][D]: gradient of the state leaving each chunk
+  size_t du;                                        // bf16 [mc][HV][2][C][D]: gradient of U (planes)
+  size_t dqa, dkr;                                  // fp32 [mc][HV][C][D]: scale e^g (dO S_in), U dS_out
+  size_t dw;                                        // bf16 [mc][HV][2][C][D]: -dU S_in (planes)
   size_t dgc;                                       // fp32 [mc][HV]: exp(g_C) <dS_out, S_in>
   size_t dqh, dkh;                                  // fp32 [T][HV][D]: gradients of q^, k^ per value head
   size_t dlala;                                     // fp32 [T][HV]: d log alpha * log alpha
@@ -57,10 +58,13 @@ struct BwdParams {
   int32_t* seq_chunk_off;
   int32_t* order;
   int4* chunk_tab;
-  float *g, *beta, *rq, *rk, *minv;
-  void* pm;  // bf16 planes
-  void* w;   // bf16 planes
-  float *ut, *s_in, *u, *ds_out, *du, *dqa, *dw, *dkr, *dgc, *dqh, *dkh, *dlala;
+  float *g, *beta, *rq, *rk;
+  void *minv, *pm, *w;           // bf16 hi, lo planes
+  float* ut;
+  void *s_in, *u, *ds_out, *du;  // bf16 hi, lo planes
+  float* dqa;
+  void* dw;                      // bf16 hi, lo planes
+  float *dkr, *dgc, *dqh, *dkh, *dlala;
 };
 
 // Launches the backward kernels after the schedule and gates kernels of the call have run on s.

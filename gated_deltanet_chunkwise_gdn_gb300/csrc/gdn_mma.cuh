@@ -165,6 +165,57 @@ __device__ __forceinline__ void ldb1_t(uint32_t (&b)[2], const bf16* base, int l
                : "=r"(b[0]), "=r"(b[1]) : "r"(addr));
 }
 
+// MMA terms of one product: hi*hi, hi*lo (B has lo), lo*hi (A has lo). bh, bl: two registers each.
+template <bool AL, bool BL>
+__device__ __forceinline__ void mma_terms(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                          const uint32_t* bh, const uint32_t* bl) {
+  const uint32_t b0[2] = {bh[0], bh[1]};
+  mma(d, ah, b0);
+  if (BL) {
+    const uint32_t b1[2] = {bl[0], bl[1]};
+    mma(d, ah, b1);
+  }
+  if (AL) mma(d, al, b0);
+}
+
+// acc[i][j] (the 16 x 8 tile at rows m0 + 16 i, columns n0 + 8 j) += A B over k in [k_lo, k_hi), both
+// operands from bf16 planes through ldmatrix. A: planes ah (+ al when AL) in [m][k] storage, or
+// [k][m] when AKM; B: planes bh (+ bl when BL) in [n][k] storage, or [k][n] when BKN. NT even.
+template <int MT, int NT, bool AKM, bool BKN, bool AL, bool BL>
+__device__ __forceinline__ void pgemm(float (&acc)[MT][NT][4], const bf16* ah, const bf16* al, int lda_,
+                                      const bf16* bh, const bf16* bl, int ldb_, int m0, int n0, int k_lo,
+                                      int k_hi) {
+  static_assert(NT % 2 == 0, "B fragments are loaded two tiles at a time");
+  for (int k0 = k_lo; k0 < k_hi; k0 += 16) {
+    uint32_t a_h[MT][4], a_l[MT][4];
+#pragma unroll
+    for (int i = 0; i < MT; ++i) {
+      if (AKM) lda_t(a_h[i], ah, lda_, m0 + 16 * i, k0); else lda(a_h[i], ah, lda_, m0 + 16 * i, k0);
+      if (AL) {
+        if (AKM) lda_t(a_l[i], al, lda_, m0 + 16 * i, k0); else lda(a_l[i], al, lda_, m0 + 16 * i, k0);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; j += 2) {
+      uint32_t b_h[4], b_l[4];
+      if (BKN) ldb2_t(b_h, bh, ldb_, k0, n0 + 8 * j); else ldb2(b_h, bh, ldb_, k0, n0 + 8 * j);
+      if (BL) {
+        if (BKN) ldb2_t(b_l, bl, ldb_, k0, n0 + 8 * j); else ldb2(b_l, bl, ldb_, k0, n0 + 8 * j);
+      }
+#pragma unroll
+      for (int i = 0; i < MT; ++i) {
+        mma_terms<AL, BL>(acc[i][j], a_h[i], a_l[i], b_h, b_l);
+        mma_terms<AL, BL>(acc[i][j + 1], a_h[i], a_l[i], b_h + 2, b_l + 2);
+      }
+    }
+  }
+}
+
+// hi + lo of the planes at offset off (lo plane `plane` elements after hi).
+__device__ __forceinline__ float plane_val(const bf16* hi, int64_t off, int64_t plane) {
+  return __bfloat162float(hi[off]) + __bfloat162float(hi[off + plane]);
+}
+
 // x (fp32) as the bf16 pair hi + lo, stored to two planes.
 __device__ __forceinline__ void store_split(bf16* hi, bf16* lo, float x) {
   const bf16 h = __float2bfloat16_rn(x);
