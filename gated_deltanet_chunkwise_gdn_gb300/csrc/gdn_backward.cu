@@ -38,6 +38,7 @@
 #include <type_traits>
 
 #include "gdn_backward.cuh"
+#include "gdn_inverse.cuh"
 #include "gdn_mma.cuh"
 
 namespace gdn {
@@ -297,31 +298,18 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   }
   __syncthreads();
 
-  // M^{-1} = (I + L)^{-1}: forward substitution, one column per thread, four partial sums
-  if (tid < C) {
-    const int c = tid;
-    for (int i = 0; i < c; ++i) sX[i * CP + c] = 0.f;
-    sX[c * CP + c] = 1.f;
-    for (int i = c + 1; i < C; ++i) {
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      int x = c;
-      for (; x + 3 < i; x += 4) {
-        s0 = fmaf(sL[i * CP + x], sX[x * CP + c], s0);
-        s1 = fmaf(sL[i * CP + x + 1], sX[(x + 1) * CP + c], s1);
-        s2 = fmaf(sL[i * CP + x + 2], sX[(x + 2) * CP + c], s2);
-        s3 = fmaf(sL[i * CP + x + 3], sX[(x + 3) * CP + c], s3);
-      }
-      for (; x < i; ++x) s0 = fmaf(sL[i * CP + x], sX[x * CP + c], s0);
-      sX[i * CP + c] = -((s0 + s1) + (s2 + s3));
-    }
-  }
+  // M^{-1} = (I + L)^{-1} in 16 x 16 blocks: diagonal blocks by an fp32 column sweep (warps 0, 1),
+  // off-diagonal blocks on the tensor cores (warps 0-3); only the blocks on and below the diagonal
+  // are written
+  if (warp < 2) inv::diag_blocks<CP>(sL, sX, warp);
   __syncthreads();
+  inv::offdiag_blocks<CP>(sL, sX);
   {
     // M^{-1} planes for the local kernel; A = (Gamma . M^{-1}) diag(beta) and A diag(e^g / |k|) as planes
     bf16* MI = reinterpret_cast<bf16*>(p.minv) + item * 2 * C * C;
     for (int e = tid; e < C * C / 2; e += 256) {
       const int i = e / (C / 2), c = (e % (C / 2)) * 2;
-      const float m0v = sX[i * CP + c], m1v = sX[i * CP + c + 1];
+      const float m0v = c <= i ? sX[i * CP + c] : 0.f, m1v = c + 1 <= i ? sX[i * CP + c + 1] : 0.f;
       wm::store_split2(MI + i * C + c, MI + C * C + i * C + c, m0v, m1v);
       const float a0 = c <= i ? expf(vg[i] - vg[c]) * m0v * vb[c] : 0.f;
       const float a1 = c + 1 <= i ? expf(vg[i] - vg[c + 1]) * m1v * vb[c + 1] : 0.f;
@@ -472,16 +460,23 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
     });
     // U = U~ - W<- S^T (C x VB); then diag(e^{g_C - g}/|k|) U as planes for the state update
     {
-      float ua[4] = {0.f, 0.f, 0.f, 0.f};
+      float ua[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps
 #pragma unroll
-      for (int k0 = 0; k0 < D; k0 += 16) {
+      for (int k0 = 0; k0 < D; k0 += 32) {
         uint32_t ah[4], al[4], bh[2], bl[2];
         wm::lda(ah, sWH, DP, mu, k0);
         wm::lda(al, sWL, DP, mu, k0);
         wm::ldb1(bh, sSH, DP, k0, nu);
         wm::ldb1(bl, sSL, DP, k0, nu);
         wm::mma_terms<true, true>(ua, ah, al, bh, bl);
+        wm::lda(ah, sWH, DP, mu, k0 + 16);
+        wm::lda(al, sWL, DP, mu, k0 + 16);
+        wm::ldb1(bh, sSH, DP, k0 + 16, nu);
+        wm::ldb1(bl, sSL, DP, k0 + 16, nu);
+        wm::mma_terms<true, true>(ub, ah, al, bh, bl);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ua[e] += ub[e];
       bf16* Ug = reinterpret_cast<bf16*>(p.u) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
@@ -653,15 +648,23 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
         if (XS) wm::ldb1_t(bl, xol, HP, k0, nu);
         wm::mma_terms<true, XS>(a1, ah, al, bh, bl);
       }
+      float a3[4] = {0.f, 0.f, 0.f, 0.f};  // odd k-steps of a2
 #pragma unroll
-      for (int k0 = 0; k0 < D; k0 += 16) {
+      for (int k0 = 0; k0 < D; k0 += 32) {
         uint32_t ah[4], al[4], bh[2], bl[2];
         wm::lda(ah, kh, DP, mu, k0);
         if (XS) wm::lda(al, xkl, DP, mu, k0);
         wm::ldb1(bh, sGH, DP, k0, nu);
         wm::ldb1(bl, sGL, DP, k0, nu);
         wm::mma_terms<XS, true>(a2, ah, al, bh, bl);
+        wm::lda(ah, kh, DP, mu, k0 + 16);
+        if (XS) wm::lda(al, xkl, DP, mu, k0 + 16);
+        wm::ldb1(bh, sGH, DP, k0 + 16, nu);
+        wm::ldb1(bl, sGL, DP, k0 + 16, nu);
+        wm::mma_terms<XS, true>(a3, ah, al, bh, bl);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a2[e] += a3[e];
       bf16* dUg = reinterpret_cast<bf16*>(p.du) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float sc = p.scale, gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
@@ -682,6 +685,8 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
     {
       const float eC = expf(vg[C - 1]);
       wm::for_each(ds, 0, ns0, [&](int, int, float& x) { x *= eC; });
+      float dw2[1][NTS][4];  // the -dU^T W<- product, added at the end
+      wm::zero(dw2);
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {
         uint32_t oh4[4], ol4[4], uh4[4], ul4[4];
@@ -697,9 +702,13 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
           wm::mma_terms<true, XS>(ds[0][j], oh4, ol4, bh, bl);
           wm::ldb1_t(bh, sWH, DP, k0, ns0 + 8 * j);
           wm::ldb1_t(bl, sWL, DP, k0, ns0 + 8 * j);
-          wm::mma_terms<true, true>(ds[0][j], uh4, ul4, bh, bl);
+          wm::mma_terms<true, true>(dw2[0][j], uh4, ul4, bh, bl);
         }
       }
+#pragma unroll
+      for (int j = 0; j < NTS; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ds[0][j][e] += dw2[0][j][e];
       store_grad();
     }
     if (S::NST == 1 && c - 1 >= jb.c0) {  // one stage: refill it once this chunk is done with it
