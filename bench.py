@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--config", default="long",
                     help="workload name (tiny, varlen, long, throughput, wide; decode: the single-token step; "
                          "backward: the backward pass on the long workload)")
+    ap.add_argument("--backward-of", default="long",
+                    help="with --config backward: the workload whose backward is timed (default: long)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
@@ -224,9 +226,11 @@ def _code_only(src: str) -> str:
 
 def kernel_source_hash(kernel: str) -> str:
     """Hash of the code (not the comments) of a kernel's sources and the shared headers."""
-    files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu"], "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
+    files = {"gates": ["gdn_gates.cu"], "intra": ["gdn_intra.cu", "gdn_inverse.cuh"],
+             "scan": ["gdn_scan.cu", "gdn_scan_affine.cu"],
              "schedule": ["gdn_schedule.cu"], "decode": ["gdn_decode.cu", "gdn_decode.cuh"],
-             "backward": ["gdn_backward.cu", "gdn_backward.cuh", "gdn_mma.cuh"]}
+             "backward": ["gdn_backward.cu", "gdn_backward.cuh", "gdn_mma.cuh", "gdn_inverse.cuh",
+                          "gdn_gates.cu", "gdn_schedule.cu"]}
     csrc = os.path.join(ROOT, "gated_deltanet_chunkwise_gdn_gb300", "csrc")
     h = hashlib.sha256()
     for f in files.get(kernel, []) + ["gdn_common.cuh", "gdn_tc.cuh"]:
@@ -583,7 +587,9 @@ def run_backward(args, dist):
     import gated_deltanet_chunkwise_gdn_gb300 as gdn
     from gated_deltanet_chunkwise_gdn_gb300 import workloads as wl
 
-    w = wl.BY_NAME["long"]
+    w = wl.BY_NAME[args.backward_of]
+    if w.K not in (64, 128) or w.K != w.V:
+        raise SystemExit(f"the backward is built for K = V in {{64, 128}}; {w.name} has K={w.K}, V={w.V}")
     if args.impl == "reference":
         if dist.rank != 0:
             return
@@ -696,9 +702,9 @@ def run_backward(args, dist):
     per_kernel = {name: {"ms_per_launch": round(tot / n, 4), "launches": n, "share": round(tot / tot_all, 4)}
                   for name, (tot, n) in kernels.items() if n}
     bt, bn = kernels["backward"]
-    roof = roofline_entry("backward", acct, bt / bn, peaks, peak_kind, "long")
+    roof = roofline_entry("backward", acct, bt / bn, peaks, peak_kind, w.name)
     step_ms = ms_max / args.steps
-    path = roofline_entry("path", acct, step_ms, peaks, peak_kind, "long")
+    path = roofline_entry("path", acct, step_ms, peaks, peak_kind, w.name)
     path.pop("traffic", None)
     tokens = T * args.steps * dist.world
     line = {

@@ -234,3 +234,76 @@ def test_autograd_function_against_the_oracle():
         assert e <= tol, (name, e)
     e = rel(init.grad.double().cpu().numpy(), ref["d_state_pool"][:B])
     assert e <= GRAD_TOL, e
+
+
+def _guarded(shape, fill, guard=4096):
+    """A tensor of `shape` inside a larger buffer with `guard` elements of `fill` on each side."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * guard,), fill, dtype=torch.float32, device="cuda")
+    return buf, buf[guard:guard + n].view(shape)
+
+
+def test_backward_writes_nothing_outside_its_buffers():
+    """Guard regions around every gradient buffer and around the workspace stay as they were."""
+    from gated_deltanet_chunkwise_gdn_gb300 import GdnGrads, gdn_backward_workspace_size
+    d = wl.make_inputs(wl.custom("bwd_guard", [130, 64, 5], H=2, HV=4, K=128, V=128, chunk_size=64, seed=328))
+    d_out, d_state = upstream(d, 328)
+    g = {k: d[k].cuda() for k in KEYS}
+    T, H, K = d["q"].shape
+    HV = d["v"].shape[1]
+    shapes = ((T, H, K), (T, H, K), (T, HV, K), (T, HV), (T, HV), (HV,), (HV,), tuple(d["state_pool"].shape))
+    bufs = [_guarded(s, 11.0) for s in shapes]
+    grads = GdnGrads(*[v for _, v in bufs])
+    need = gdn_backward_workspace_size(T, 3, H, HV, K, K, 64)
+    guard = 1 << 16
+    ws_buf = torch.full((need + 2 * guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = ws_buf[guard:guard + need]
+    gdn_chunkwise_backward(*[g[k] for k in KEYS], d_out.cuda(), d_state.cuda(), chunk_size=64, check=True,
+                           workspace=ws, grads=grads)
+    torch.cuda.synchronize()
+    for buf, view in bufs:
+        n = view.numel()
+        assert torch.all(buf[:4096] == 11.0) and torch.all(buf[4096 + n:] == 11.0)
+    assert torch.all(ws_buf[:guard] == 0x5A) and torch.all(ws_buf[guard + need:] == 0x5A)
+    got = {k: getattr(grads, k).cpu().double().numpy() for k in grads._fields}
+    compare(d, got, oracle_backward(d, d_out, d_state))
+
+
+def test_backward_replays_in_a_cuda_graph():
+    """With its workspace and gradient buffers given, the backward call is captured in a CUDA graph and
+    replayed on new input contents; the replay equals a direct call bit for bit."""
+    from gated_deltanet_chunkwise_gdn_gb300 import GdnGrads, gdn_backward_workspace_size
+    d1 = wl.make_inputs(wl.custom("bwd_graph", [150, 90], H=2, HV=2, K=64, V=64, chunk_size=64, seed=329))
+    d2 = wl.make_inputs(wl.custom("bwd_graph", [150, 90], H=2, HV=2, K=64, V=64, chunk_size=64, seed=330))
+    o1, s1 = upstream(d1, 329)
+    o2, s2 = upstream(d2, 330)
+    T, H, K = d1["q"].shape
+    HV = d1["v"].shape[1]
+    g = {k: d1[k].cuda() for k in KEYS}
+    d_out, d_state = o1.cuda(), s1.cuda()
+    ws = torch.empty(gdn_backward_workspace_size(T, 2, H, HV, K, K, 64), dtype=torch.uint8, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    grads = GdnGrads(torch.empty((T, H, K), **f32), torch.empty((T, H, K), **f32), torch.empty((T, HV, K), **f32),
+                     torch.empty((T, HV), **f32), torch.empty((T, HV), **f32), torch.empty((HV,), **f32),
+                     torch.empty((HV,), **f32), torch.zeros_like(g["state_pool"]))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside the capture (kernel attributes are set on first use)
+        gdn_chunkwise_backward(*[g[k] for k in KEYS], d_out, d_state, chunk_size=64, workspace=ws, grads=grads)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gdn_chunkwise_backward(*[g[k] for k in KEYS], d_out, d_state, chunk_size=64, workspace=ws, grads=grads)
+    for k in KEYS:
+        g[k].copy_(d2[k])
+    d_out.copy_(o2)
+    d_state.copy_(s2)
+    graph.replay()
+    torch.cuda.synchronize()
+    replay = {k: getattr(grads, k).cpu().numpy().copy() for k in grads._fields}
+    direct = run_backward(d2, o2, s2)
+    idx2 = d2["cache_indices"].numpy()
+    replay["d_state_pool"], direct["d_state_pool"] = replay["d_state_pool"][idx2], direct["d_state_pool"][idx2]
+    for k in replay:
+        assert np.array_equal(replay[k].astype(np.float64), direct[k]), k
