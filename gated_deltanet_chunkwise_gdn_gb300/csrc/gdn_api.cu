@@ -231,7 +231,8 @@ gdn_status gdn_chunkwise_backward(const void* q, const void* k, const void* v, g
   if (total_tokens > 0 && (!q || !k || !v || !a || !b || !d_out || !dq || !dk || !dv || !da || !db))
     return GDN_ERR_INVALID_ARG;
   auto al = [](const void* x, uintptr_t n) { return (reinterpret_cast<uintptr_t>(x) & (n - 1)) == 0; };
-  if (total_tokens > 0 && !(al(q, 16) && al(k, 16) && al(v, 16) && al(d_out, 16) && al(dv, 8)))
+  if (total_tokens > 0 &&
+      !(al(q, 16) && al(k, 16) && al(v, 16) && al(d_out, 16) && al(dq, 16) && al(dk, 16) && al(dv, 8)))
     return GDN_ERR_INVALID_ARG;
   if (batch > 0 && !(al(state_pool, 8) && al(d_state_pool, 8) && al(d_state, 8))) return GDN_ERR_INVALID_ARG;
   const size_t need = gdn_backward_workspace_size(total_tokens, batch, H, HV, K, V, chunk_size);

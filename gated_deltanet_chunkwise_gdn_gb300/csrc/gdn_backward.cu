@@ -365,7 +365,9 @@ struct StSmem {
   static constexpr uint32_t SL = SH + VB * DP * 2;
   static constexpr uint32_t UKH = SL + VB * DP * 2;  // diag(e^{g_C - g}/|k|) U, hi, lo planes [C][HP]
   static constexpr uint32_t UKL = UKH + C * HP * 2;
-  static constexpr uint32_t KL = UKL + C * HP * 2;   // fp16 inputs: the lo plane of k (its hi plane
+  static constexpr uint32_t UH = UKL + C * HP * 2;   // U, hi, lo planes [C][HP] (copied out by the producers)
+  static constexpr uint32_t UL = UH + C * HP * 2;
+  static constexpr uint32_t KL = UL + C * HP * 2;    // fp16 inputs: the lo plane of k (its hi plane
                                                      // overwrites the stage's k tile)
   static constexpr uint32_t bytes_bf16 = KL;
   static constexpr uint32_t bytes_fp16 = KL + TILE;
@@ -392,74 +394,100 @@ __device__ __forceinline__ ChainJob chain_job(const BwdParams& p) {
   return jb;
 }
 
+// rows x W bf16 plane rows (pitch P in shared memory) to a row-major global plane of row stride ld,
+// 16 bytes at a time; `neg` flips the sign of every value (exact for a hi/lo pair).
+template <int W, int P>
+__device__ __forceinline__ void copy_rows_out(bf16* dst, const bf16* src, int64_t ld, int rows, bool neg, int tid,
+                                              int nthr) {
+  constexpr int PER = W / 8;
+  const uint32_t flip = neg ? 0x80008000u : 0u;
+  for (int e = tid; e < rows * PER; e += nthr) {
+    const int i = e / PER, q = e % PER;
+    uint4 x = *reinterpret_cast<const uint4*>(src + i * P + q * 8);
+    x.x ^= flip;
+    x.y ^= flip;
+    x.z ^= flip;
+    x.w ^= flip;
+    *reinterpret_cast<uint4*>(dst + i * ld + q * 8) = x;
+  }
+}
+
+// Warps 0-7 (consumers) run the chunk step; warps 8-15 (producers) fetch the next chunk's tiles and
+// write this chunk's S_in and U planes out, so neither sits on the step's critical path.
 template <int D, typename E>
-__global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
+__global__ void __launch_bounds__(2 * kSeqThreads) bwd_state_kernel(BwdParams p) {
   using S = StSmem<D>;
   constexpr int DP = S::DP, HP = S::HP;
   constexpr bool XS = kSplitSrc<E>;
-  constexpr int NTS = D / 64;  // 8-column tiles per warp of the VB x D state (8 warps)
+  constexpr int NTS = D / 64;  // 8-column tiles per consumer warp of the VB x D state
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
   const ChainJob jb = chain_job<D>(p);
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool producer = tid >= kSeqThreads;
+  const int ptid = tid - kSeqThreads;
   bf16* sSH = reinterpret_cast<bf16*>(smem + S::SH);
   bf16* sSL = reinterpret_cast<bf16*>(smem + S::SL);
   bf16* sUKH = reinterpret_cast<bf16*>(smem + S::UKH);
   bf16* sUKL = reinterpret_cast<bf16*>(smem + S::UKL);
+  bf16* sUH = reinterpret_cast<bf16*>(smem + S::UH);
+  bf16* sUL = reinterpret_cast<bf16*>(smem + S::UL);
   bf16* sKL = reinterpret_cast<bf16*>(smem + S::KL);
   const E* kin = static_cast<const E*>(p.k) + (int64_t)jb.h * D;
 
-  auto issue = [&](int c, int st) {
+  auto issue = [&](int c, int st) {  // producers
     unsigned char* base = smem + st * S::STAGE;
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
     const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, tid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, tid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
-    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
+    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, ptid,
+                     kSeqThreads);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
-    if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
-    else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rk + item * C + 4 * (tid - 16));
+    if (ptid < 16) cp_async_16(vec + 4 * ptid, p.g + item * C + 4 * ptid);
+    else if (ptid < 32) cp_async_16(vec + C + 4 * (ptid - 16), p.rk + item * C + 4 * (ptid - 16));
   };
 
   const float* S0 = p.state_pool + (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
-  const int ns0 = warp * (D / 8);                         // the warp's state columns
-  const int mu = 16 * (warp & 3), nu = 8 * (warp >> 2);  // the warp's 16 x 8 tile of U (C x VB)
+  const int ns0 = (warp & 7) * (D / 8);                         // the consumer warp's state columns
+  const int mu = 16 * (warp & 3), nu = 8 * ((warp >> 2) & 1);  // its 16 x 8 tile of U (C x VB)
   float st[1][NTS][4];
-  wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { x = S0[i * D + c]; });
   auto store_state = [&]() {
     wm::for_each_pair(st, 0, ns0, [&](int i, int c, float& x0, float& x1) {
       wm::store_split2(sSH + i * DP + c, sSL + i * DP + c, x0, x1);
     });
   };
-  store_state();
-  if (jb.c1 > jb.c0) issue(jb.c0, 0);
-  cp_async_commit();
+  if (!producer) {
+    wm::for_each(st, 0, ns0, [&](int i, int c, float& x) { x = S0[i * D + c]; });
+    store_state();
+  } else {
+    if (jb.c1 > jb.c0) issue(jb.c0, 0);
+    cp_async_commit();
+  }
 
   for (int c = jb.c0; c < jb.c1; ++c) {
     const int stg = (c - jb.c0) & 1;
-    cp_async_wait<0>();
-    __syncthreads();
-    if (c + 1 < jb.c1) issue(c + 1, stg ^ 1);
-    cp_async_commit();
-    const unsigned char* base = smem + stg * S::STAGE;
-    const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
-    const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
-    E* sK = reinterpret_cast<E*>(smem + stg * S::STAGE + S::K);
-    const float* sUT = reinterpret_cast<const float*>(base + S::UT);
-    const float* vg = reinterpret_cast<const float*>(base + S::VEC);
-    const float* vrk = vg + C;
+    if (producer) cp_async_wait<0>();
+    __syncthreads();  // this chunk's tiles have landed; the state planes hold the entering state
+    unsigned char* base = smem + stg * S::STAGE;
     const int64_t item = (int64_t)c * p.HV + jb.hv;
-    split_inplace<D, DP>(sK, sKL, XS ? C : 0, tid, kSeqThreads);
-
-    // the state entering this chunk (hi, lo planes)
-    bf16* Sin = reinterpret_cast<bf16*>(p.s_in) + item * 2 * D * D + (int64_t)jb.vb * D;
-    wm::for_each_pair(st, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
-      wm::store_split2(Sin + i * D + cc, Sin + D * D + i * D + cc, x0, x1);
-    });
-    // U = U~ - W<- S^T (C x VB); then diag(e^{g_C - g}/|k|) U as planes for the state update
-    {
+    if (producer) {
+      if (c + 1 < jb.c1) issue(c + 1, stg ^ 1);
+      cp_async_commit();
+      bf16* Sin = reinterpret_cast<bf16*>(p.s_in) + item * 2 * D * D + (int64_t)jb.vb * D;
+      copy_rows_out<D, DP>(Sin, sSH, D, VB, false, ptid, kSeqThreads);
+      copy_rows_out<D, DP>(Sin + D * D, sSL, D, VB, false, ptid, kSeqThreads);
+    } else {
+      const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
+      const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
+      E* sK = reinterpret_cast<E*>(base + S::K);
+      const float* sUT = reinterpret_cast<const float*>(base + S::UT);
+      const float* vg = reinterpret_cast<const float*>(base + S::VEC);
+      const float* vrk = vg + C;
+      split_inplace<D, DP>(sK, sKL, XS ? C : 0, tid, kSeqThreads);
+      // U = U~ - W<- S^T (C x VB); U and diag(e^{g_C - g}/|k|) U as planes
       float ua[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps
 #pragma unroll
       for (int k0 = 0; k0 < D; k0 += 32) {
@@ -475,26 +503,29 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_state_kernel(BwdParams p) {
         wm::ldb1(bl, sSL, DP, k0 + 16, nu);
         wm::mma_terms<true, true>(ub, ah, al, bh, bl);
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) ua[e] += ub[e];
-      bf16* Ug = reinterpret_cast<bf16*>(p.u) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = mu + r + 8 * hh, cc = nu + cl;
-        const float u0 = sUT[i * UP + cc] - ua[2 * hh], u1 = sUT[i * UP + cc + 1] - ua[2 * hh + 1];
-        wm::store_split2(Ug + i * D + cc, Ug + C * D + i * D + cc, u0, u1);
+        const float u0 = sUT[i * UP + cc] - (ua[2 * hh] + ub[2 * hh]);
+        const float u1 = sUT[i * UP + cc + 1] - (ua[2 * hh + 1] + ub[2 * hh + 1]);
+        wm::store_split2(sUH + i * HP + cc, sUL + i * HP + cc, u0, u1);
         const float sk = expf(gC - vg[i]) * vrk[i];
         wm::store_split2(sUKH + i * HP + cc, sUKL + i * HP + cc, sk * u0, sk * u1);
       }
     }
-    __syncthreads();
-    // S = e^{g_C} S + (diag(e^{g_C - g}/|k|) U)^T K
-    {
+    __syncthreads();  // U planes complete; the producers have copied the entering state out
+    if (producer) {
+      bf16* Ug = reinterpret_cast<bf16*>(p.u) + item * 2 * C * D + jb.vb;
+      copy_rows_out<VB, HP>(Ug, sUH, D, C, false, ptid, kSeqThreads);
+      copy_rows_out<VB, HP>(Ug + C * D, sUL, D, C, false, ptid, kSeqThreads);
+    } else {
+      // S = e^{g_C} S + (diag(e^{g_C - g}/|k|) U)^T K
+      const float* vg = reinterpret_cast<const float*>(base + S::VEC);
       const float eC = expf(vg[C - 1]);
       wm::for_each(st, 0, ns0, [&](int, int, float& x) { x *= eC; });
-      const bf16* kh = reinterpret_cast<const bf16*>(sK);
+      const bf16* kh = reinterpret_cast<const bf16*>(base + S::K);
 #pragma unroll
       for (int k0 = 0; k0 < C; k0 += 16) {
         uint32_t ah[4], al[4];
@@ -543,7 +574,7 @@ struct DsSmem {
 };
 
 template <int D, typename E>
-__global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
+__global__ void __launch_bounds__(2 * kSeqThreads) bwd_dstate_kernel(BwdParams p) {
   constexpr bool XS = kSplitSrc<E>;
   using S = DsSmem<D, XS>;
   constexpr int DP = S::DP, HP = S::HP, PP = S::PP;
@@ -552,6 +583,8 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
   if (p.status[0] != GDN_OK) return;
   const ChainJob jb = chain_job<D>(p);
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool producer = tid >= kSeqThreads;  // warps 8-15: tile fetches and the per-chunk outputs
+  const int ptid = tid - kSeqThreads;
   bf16* sGH = reinterpret_cast<bf16*>(smem + S::GH);
   bf16* sGL = reinterpret_cast<bf16*>(smem + S::GL);
   bf16* sNUH = reinterpret_cast<bf16*>(smem + S::NUH);
@@ -565,80 +598,78 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
   const E* qin = static_cast<const E*>(p.q) + (int64_t)jb.h * D;
   const E* doin = static_cast<const E*>(p.d_out) + (int64_t)jb.hv * D + jb.vb;
 
-  auto issue = [&](int c, int st) {
+  auto issue = [&](int c, int st) {  // producers
     unsigned char* base = smem + st * S::STAGE;
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
     const bf16* pp = reinterpret_cast<const bf16*>(p.pm) + item * 2 * C * C;
-    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PH), pp, C, 0, C, tid, kSeqThreads);
-    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PL), pp + C * C, C, 0, C, tid, kSeqThreads);
-    load_tokens_cols<VB, HP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, tid,
+    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PH), pp, C, 0, C, ptid, kSeqThreads);
+    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PL), pp + C * C, C, 0, C, ptid, kSeqThreads);
+    load_tokens_cols<VB, HP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, ptid,
                              kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
     const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, tid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, tid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid, kSeqThreads);
+    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid, kSeqThreads);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
-    if (tid < 16) cp_async_16(vec + 4 * tid, p.g + item * C + 4 * tid);
-    else if (tid < 32) cp_async_16(vec + C + 4 * (tid - 16), p.rq + item * C + 4 * (tid - 16));
-    else if (tid < 48) cp_async_16(vec + 2 * C + 4 * (tid - 32), p.rk + item * C + 4 * (tid - 32));
+    if (ptid < 16) cp_async_16(vec + 4 * ptid, p.g + item * C + 4 * ptid);
+    else if (ptid < 32) cp_async_16(vec + C + 4 * (ptid - 16), p.rq + item * C + 4 * (ptid - 16));
+    else if (ptid < 48) cp_async_16(vec + 2 * C + 4 * (ptid - 32), p.rk + item * C + 4 * (ptid - 32));
   };
 
   const int64_t srow = (jb.slot * p.HV + jb.hv) * (int64_t)D * D + (int64_t)jb.vb * D;
-  const int ns0 = warp * (D / 8);
-  const int mu = 16 * (warp & 3), nu = 8 * (warp >> 2);
+  const int ns0 = (warp & 7) * (D / 8);
+  const int mu = 16 * (warp & 3), nu = 8 * ((warp >> 2) & 1);
   float ds[1][NTS][4];
-  wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { x = p.d_state ? p.d_state[srow + i * D + c] : 0.f; });
   auto store_grad = [&]() {
     wm::for_each_pair(ds, 0, ns0, [&](int i, int c, float& x0, float& x1) {
       wm::store_split2(sGH + i * DP + c, sGL + i * DP + c, x0, x1);
     });
   };
-  store_grad();
-  if (jb.c1 > jb.c0) issue(jb.c1 - 1, 0);
-  cp_async_commit();
+  if (!producer) {
+    wm::for_each(ds, 0, ns0, [&](int i, int c, float& x) { x = p.d_state ? p.d_state[srow + i * D + c] : 0.f; });
+    store_grad();
+  } else {
+    if (jb.c1 > jb.c0) issue(jb.c1 - 1, 0);
+    cp_async_commit();
+  }
 
   for (int c = jb.c1 - 1; c >= jb.c0; --c) {
     const int stg = S::NST == 2 ? (jb.c1 - 1 - c) & 1 : 0;
-    cp_async_wait<0>();
-    __syncthreads();
-    if (S::NST == 2 && c - 1 >= jb.c0) issue(c - 1, stg ^ 1);
-    cp_async_commit();
+    if (producer) cp_async_wait<0>();
+    __syncthreads();  // this chunk's tiles have landed; the gradient planes hold dS leaving this chunk
     unsigned char* base = smem + stg * S::STAGE;
-    const bf16* sPH = reinterpret_cast<const bf16*>(base + S::PH);
-    const bf16* sPL = reinterpret_cast<const bf16*>(base + S::PL);
-    E* sDO = reinterpret_cast<E*>(base + S::DO);
-    E* sK = reinterpret_cast<E*>(base + S::K);
-    E* sQ = reinterpret_cast<E*>(base + S::Q);
-    const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
-    const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
     const float* vg = reinterpret_cast<const float*>(base + S::VEC);
-    const float* vrq = vg + C;
-    const float* vrk = vg + 2 * C;
     const int64_t item = (int64_t)c * p.HV + jb.hv;
-    if (XS) {
-      split_inplace<D, DP>(sQ, xql, C, tid, kSeqThreads);
-      split_inplace<D, DP>(sK, xkl, C, tid, kSeqThreads);
-      split_inplace<VB, HP>(sDO, xol, C, tid, kSeqThreads);
-      __syncthreads();
-    }
-    const bf16* qh = reinterpret_cast<const bf16*>(sQ);
-    const bf16* kh = reinterpret_cast<const bf16*>(sK);
-    const bf16* oh = reinterpret_cast<const bf16*>(sDO);
-    // a dO value of the tile (fp16 inputs: hi + lo, exactly)
-    auto dov = [&](int i, int cc) {
-      return XS ? __bfloat162float(oh[i * HP + cc]) + __bfloat162float(xol[i * HP + cc]) : to_f(sDO[i * HP + cc]);
-    };
-
-    // the gradient of the state leaving this chunk (hi, lo planes)
-    bf16* dSo = reinterpret_cast<bf16*>(p.ds_out) + item * 2 * D * D + (int64_t)jb.vb * D;
-    wm::for_each_pair(ds, 0, ns0, [&](int i, int cc, float& x0, float& x1) {
-      wm::store_split2(dSo + i * D + cc, dSo + D * D + i * D + cc, x0, x1);
-    });
-    // dU = scale P^T dO + diag(e^{g_C - g}/|k|) (K dS^T)  (C x VB): the warp's 16 x 8 tile; also the
-    // planes of -dU and of scale diag(e^g/|q|) dO for the state-gradient update
-    {
+    if (producer) {
+      if (S::NST == 2 && c - 1 >= jb.c0) issue(c - 1, stg ^ 1);
+      cp_async_commit();
+      bf16* dSo = reinterpret_cast<bf16*>(p.ds_out) + item * 2 * D * D + (int64_t)jb.vb * D;
+      copy_rows_out<D, DP>(dSo, sGH, D, VB, false, ptid, kSeqThreads);
+      copy_rows_out<D, DP>(dSo + D * D, sGL, D, VB, false, ptid, kSeqThreads);
+    } else {
+      const bf16* sPH = reinterpret_cast<const bf16*>(base + S::PH);
+      const bf16* sPL = reinterpret_cast<const bf16*>(base + S::PL);
+      E* sDO = reinterpret_cast<E*>(base + S::DO);
+      E* sK = reinterpret_cast<E*>(base + S::K);
+      E* sQ = reinterpret_cast<E*>(base + S::Q);
+      const float* vrq = vg + C;
+      const float* vrk = vg + 2 * C;
+      if (XS) {
+        split_inplace<D, DP>(sQ, xql, C, tid, kSeqThreads);
+        split_inplace<D, DP>(sK, xkl, C, tid, kSeqThreads);
+        split_inplace<VB, HP>(sDO, xol, C, tid, kSeqThreads);
+        tc::named_sync(1, kSeqThreads);  // consumers only
+      }
+      const bf16* kh = reinterpret_cast<const bf16*>(sK);
+      const bf16* oh = reinterpret_cast<const bf16*>(sDO);
+      // a dO value of the tile (fp16 inputs: hi + lo, exactly)
+      auto dov = [&](int i, int cc) {
+        return XS ? __bfloat162float(oh[i * HP + cc]) + __bfloat162float(xol[i * HP + cc]) : to_f(sDO[i * HP + cc]);
+      };
+      // dU = scale P^T dO + diag(e^{g_C - g}/|k|) (K dS^T)  (C x VB): the warp's 16 x 8 tile, kept as planes
+      // of -dU; and the planes of scale diag(e^g/|q|) dO for the state-gradient update
       float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};
       for (int k0 = mu; k0 < C; k0 += 16) {  // P^T is upper triangular: rows mu.. need k >= mu
         uint32_t ah[4], al[4], bh[2], bl[2];
@@ -663,26 +694,29 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
         wm::ldb1(bl, sGL, DP, k0 + 16, nu);
         wm::mma_terms<XS, true>(a3, ah, al, bh, bl);
       }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) a2[e] += a3[e];
-      bf16* dUg = reinterpret_cast<bf16*>(p.du) + item * 2 * C * D + jb.vb;  // hi, lo planes
       const float sc = p.scale, gC = vg[C - 1];
       const int r = wm::lane_r(), cl = wm::lane_c();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = mu + r + 8 * hh, cc = nu + cl;
         const float sk = expf(gC - vg[i]) * vrk[i];
-        const float y0 = sc * a1[2 * hh] + sk * a2[2 * hh];
-        const float y1 = sc * a1[2 * hh + 1] + sk * a2[2 * hh + 1];
-        wm::store_split2(dUg + i * D + cc, dUg + C * D + i * D + cc, y0, y1);
+        const float y0 = sc * a1[2 * hh] + sk * (a2[2 * hh] + a3[2 * hh]);
+        const float y1 = sc * a1[2 * hh + 1] + sk * (a2[2 * hh + 1] + a3[2 * hh + 1]);
         wm::store_split2(sNUH + i * HP + cc, sNUL + i * HP + cc, -y0, -y1);
         const float sq = sc * expf(vg[i]) * vrq[i];
         wm::store_split2(sOSH + i * HP + cc, sOSL + i * HP + cc, sq * dov(i, cc), sq * dov(i, cc + 1));
       }
     }
-    __syncthreads();
-    // dS = e^{g_C} dS + (scale diag(e^g/|q|) dO)^T Q - dU^T W<-   (VB x D)
-    {
+    __syncthreads();  // -dU and the scaled dO planes complete; dS_out copied out
+    if (producer) {
+      bf16* dUg = reinterpret_cast<bf16*>(p.du) + item * 2 * C * D + jb.vb;  // dU = -(the -dU planes)
+      copy_rows_out<VB, HP>(dUg, sNUH, D, C, true, ptid, kSeqThreads);
+      copy_rows_out<VB, HP>(dUg + C * D, sNUL, D, C, true, ptid, kSeqThreads);
+    } else {
+      // dS = e^{g_C} dS + (scale diag(e^g/|q|) dO)^T Q - dU^T W<-   (VB x D)
+      const bf16* qh = reinterpret_cast<const bf16*>(base + S::Q);
+      const bf16* sWH = reinterpret_cast<const bf16*>(base + S::WH);
+      const bf16* sWL = reinterpret_cast<const bf16*>(base + S::WL);
       const float eC = expf(vg[C - 1]);
       wm::for_each(ds, 0, ns0, [&](int, int, float& x) { x *= eC; });
       float dw2[1][NTS][4];  // the -dU^T W<- product, added at the end
@@ -713,13 +747,15 @@ __global__ void __launch_bounds__(kSeqThreads) bwd_dstate_kernel(BwdParams p) {
     }
     if (S::NST == 1 && c - 1 >= jb.c0) {  // one stage: refill it once this chunk is done with it
       __syncthreads();
-      issue(c - 1, 0);
+      if (producer) issue(c - 1, 0);
     }
   }
-  float* dS0 = p.d_state_pool + srow;
-  wm::for_each_pair(ds, 0, ns0, [&](int i, int c, float& x0, float& x1) {
-    *reinterpret_cast<float2*>(dS0 + i * D + c) = make_float2(x0, x1);
-  });
+  if (!producer) {
+    float* dS0 = p.d_state_pool + srow;
+    wm::for_each_pair(ds, 0, ns0, [&](int i, int c, float& x0, float& x1) {
+      *reinterpret_cast<float2*>(dS0 + i * D + c) = make_float2(x0, x1);
+    });
+  }
 }
 
 // ----------------------------------------------------------------------------- sgrad
@@ -1574,6 +1610,8 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
 
 // ----------------------------------------------------------------------------- norm, gate sums
 
+// One warp per (token, q/k head); each lane owns 4 consecutive elements of the row (lanes past D/4
+// idle), so every load is 16 bytes, and all loads of the row are issued before the reductions.
 template <int D, typename E>
 __global__ void __launch_bounds__(256) bwd_norm_kernel(BwdParams p) {
   if (p.status[0] != GDN_OK) return;
@@ -1582,29 +1620,53 @@ __global__ void __launch_bounds__(256) bwd_norm_kernel(BwdParams p) {
   if (wid >= p.T * p.H) return;
   const int64_t t = wid / p.H;
   const int h = (int)(wid % p.H), r = p.HV / p.H;
-  constexpr int U = D / 32;
+  const bool on = 4 * lane < D;
+  const int d0 = on ? 4 * lane : 0;
+  float x[2][4], g[2][4], n2[2], dot[2];
 #pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const E* x = static_cast<const E*>(which == 0 ? p.q : p.k) + (t * p.H + h) * D;
-    const float* gh = (which == 0 ? p.dqh : p.dkh) + (t * p.HV + (int64_t)h * r) * D;
-    float* out = (which == 0 ? p.dq : p.dk) + (t * p.H + h) * D;
-    float xv[U], gv[U], n2 = 0.f, dot = 0.f;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int d = lane + 32 * u;
-      xv[u] = to_f(x[d]);
-      float s = 0.f;
-      for (int e = 0; e < r; ++e) s += gh[(int64_t)e * D + d];
-      gv[u] = s;
-      n2 = fmaf(xv[u], xv[u], n2);
-      dot = fmaf(xv[u], s, dot);
+  for (int w = 0; w < 2; ++w) {
+    const E* src = static_cast<const E*>(w == 0 ? p.q : p.k) + (t * p.H + h) * D + d0;
+    const float* gh = (w == 0 ? p.dqh : p.dkh) + (t * p.HV + (int64_t)h * r) * D + d0;
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);  // four 16-bit values
+    const float2 a = ElemT<E>::unpack(raw.x), b = ElemT<E>::unpack(raw.y);
+    x[w][0] = a.x;
+    x[w][1] = a.y;
+    x[w][2] = b.x;
+    x[w][3] = b.y;
+    float4 s = *reinterpret_cast<const float4*>(gh);
+    for (int e = 1; e < r; ++e) {
+      const float4 y = *reinterpret_cast<const float4*>(gh + (int64_t)e * D);
+      s.x += y.x;
+      s.y += y.y;
+      s.z += y.z;
+      s.w += y.w;
     }
-    n2 = warp_sum(n2);
-    dot = warp_sum(dot);
-    const float n = sqrtf(n2 + kNormEps);
-    const float inv = 1.f / n, c3 = dot / (n * n * n);
+    g[w][0] = s.x;
+    g[w][1] = s.y;
+    g[w][2] = s.z;
+    g[w][3] = s.w;
+  }
 #pragma unroll
-    for (int u = 0; u < U; ++u) out[lane + 32 * u] = gv[u] * inv - xv[u] * c3;
+  for (int w = 0; w < 2; ++w) {
+    n2[w] = dot[w] = 0.f;
+    if (on)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        n2[w] = fmaf(x[w][u], x[w][u], n2[w]);
+        dot[w] = fmaf(x[w][u], g[w][u], dot[w]);
+      }
+    n2[w] = warp_sum(n2[w]);
+    dot[w] = warp_sum(dot[w]);
+  }
+  if (!on) return;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    float* out = (w == 0 ? p.dq : p.dk) + (t * p.H + h) * D + d0;
+    const float n = sqrtf(n2[w] + kNormEps);
+    const float inv = 1.f / n, c3 = dot[w] / (n * n * n);
+    *reinterpret_cast<float4*>(out) =
+        make_float4(g[w][0] * inv - x[w][0] * c3, g[w][1] * inv - x[w][1] * c3, g[w][2] * inv - x[w][2] * c3,
+                    g[w][3] * inv - x[w][3] * c3);
   }
 }
 
@@ -1653,9 +1715,9 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
     const uint32_t sb = f16in ? StSmem<D>::bytes_fp16 : StSmem<D>::bytes_bf16;
     const uint32_t db = DsSmem<D, f16in>::bytes;
     if ((e = set_smem(bwd_state_kernel<D, E>, sb)) != cudaSuccess) return e;
-    bwd_state_kernel<D, E><<<chains, kSeqThreads, sb, s>>>(p);
+    bwd_state_kernel<D, E><<<chains, 2 * kSeqThreads, sb, s>>>(p);
     if ((e = set_smem(bwd_dstate_kernel<D, E>, db)) != cudaSuccess) return e;
-    bwd_dstate_kernel<D, E><<<chains, kSeqThreads, db, s>>>(p);
+    bwd_dstate_kernel<D, E><<<chains, 2 * kSeqThreads, db, s>>>(p);
     n += 2;
   }
   if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D, f16in>::bytes)) != cudaSuccess) return e;

@@ -235,7 +235,7 @@ GDN_API size_t gdn_backward_workspace_size(int64_t total_tokens, int32_t batch, 
  *
  * Supported: K = V in {64, 128}; chunk_size 64 or 128 (the kernels work on 64-token WY
  * blocks; the gradients do not depend on the block length in exact arithmetic).
- * q, k, v, d_out 16-byte aligned; dv, state_pool, d_state, d_state_pool 8-byte aligned.
+ * q, k, v, d_out, dq, dk 16-byte aligned; dv, state_pool, d_state, d_state_pool 8-byte aligned.
  * Host-detectable errors return before anything is enqueued. Device-detected errors
  * (cu_seqlens, cache_indices: as for gdn_extend_chunkwise) are recorded in the
  * workspace's status word, read by gdn_get_device_status(workspace, stream); the

@@ -182,6 +182,7 @@ def test_backward_host_side_errors_return_before_any_device_work(lib):
     assert _bwd(lib, dtype=3) == 1
     assert _bwd(lib, q=24) == 1              # tiles are copied in 16-byte pieces
     assert _bwd(lib, dv=12) == 1             # 8-byte stores
+    assert _bwd(lib, dq=24) == 1             # 16-byte stores
     assert _bwd(lib, K=256, V=256) == 2      # not built for the backward
     assert _bwd(lib, C=32) == 2
     assert _bwd(lib, ws=None) == 4
