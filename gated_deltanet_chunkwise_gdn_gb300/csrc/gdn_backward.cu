@@ -75,7 +75,7 @@ BwdLayout make_bwd_layout(int64_t T, int B, int H, int HV, int D) {
   L.dqa = take(per * C * D * sizeof(float));
   L.dw = take(per * C * D * sizeof(float));
   L.dkr = take(per * C * D * sizeof(float));
-  L.dgc = take(per * sizeof(float));
+  L.dgc = take(per * 2 * sizeof(float));
   // gradients of q^, k^ per value head: only with grouped heads (otherwise the local kernel
   // applies the normalisation's backward itself)
   const size_t per_head_grads = HV != H ? (size_t)T * HV * D * sizeof(float) : 0;
@@ -760,56 +760,56 @@ __global__ void __launch_bounds__(2 * kSeqThreads) bwd_dstate_kernel(BwdParams p
 
 // ----------------------------------------------------------------------------- sgrad
 
+// Two CTAs per (chunk, value head), each computing one half of the output columns (the key
+// dimension), so that two CTAs fit on an SM and one's loads overlap the other's products.
 template <int D, bool XS>
 struct SgSmem {
-  static constexpr int DP = D + 8;
-  static constexpr uint32_t PLS = D * DP * 2;        // one D x D plane
+  static constexpr int DP = D + 8;                   // pitch of C x D tiles and planes
+  static constexpr int HD = D / 2, HPD = HD + 8;     // the CTA's half of the key columns, its pitch
+  static constexpr uint32_t PLS = D * HPD * 2;       // one D x D/2 plane
   static constexpr uint32_t PLC = C * DP * 2;        // one C x D plane or tile
-  static constexpr uint32_t SH = 0;                  // S_in planes, then dS_out planes
+  static constexpr uint32_t SH = 0;                  // S_in half planes, then dS_out half planes
   static constexpr uint32_t SL = SH + PLS;
   static constexpr uint32_t DO = SL + PLS;           // dO tile (fp16: its hi plane after the split)
-  static constexpr uint32_t DUH = DO + PLC;          // dU planes
+  static constexpr uint32_t DUH = DO + PLC;          // dU planes; after the first product: U planes at DO
   static constexpr uint32_t DUL = DUH + PLC;
-  static constexpr uint32_t UH = DUL + PLC;          // U planes
-  static constexpr uint32_t UL = UH + PLC;
-  static constexpr uint32_t DOL = UL + PLC;          // fp16 only: lo plane of dO
+  static constexpr uint32_t DOL = DUL + PLC;         // fp16 only: lo plane of dO
   static constexpr uint32_t VEC = DOL + (XS ? PLC : 0);  // g; 8 warp partials
   static constexpr uint32_t bytes = VEC + C * 4 + 8 * 4;
 };
 
 template <int D, typename E>
-__global__ void __launch_bounds__(256, 1) bwd_sgrad_kernel(BwdParams p) {
+__global__ void __launch_bounds__(256, 2) bwd_sgrad_kernel(BwdParams p) {
   constexpr bool XS = kSplitSrc<E>;
   using S = SgSmem<D, XS>;
-  constexpr int DP = S::DP;
+  constexpr int DP = S::DP, HD = S::HD, HPD = S::HPD;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
-  const int j = blockIdx.x, hv = blockIdx.y;
+  const int j = blockIdx.x, hv = blockIdx.y, half = blockIdx.z;
   if (j >= p.status[1]) return;
   const int4 ct = p.chunk_tab[j];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int col0 = half * HD;  // the CTA's key columns: col0 .. col0 + D/2
   bf16* sSH = reinterpret_cast<bf16*>(smem + S::SH);
   bf16* sSL = reinterpret_cast<bf16*>(smem + S::SL);
   E* sDO = reinterpret_cast<E*>(smem + S::DO);
   bf16* sDUH = reinterpret_cast<bf16*>(smem + S::DUH);
   bf16* sDUL = reinterpret_cast<bf16*>(smem + S::DUL);
-  bf16* sUH = reinterpret_cast<bf16*>(smem + S::UH);
-  bf16* sUL = reinterpret_cast<bf16*>(smem + S::UL);
+  bf16* sUH = reinterpret_cast<bf16*>(smem + S::DO);  // after the first product
+  bf16* sUL = sUH + C * DP;
   bf16* sDOL = reinterpret_cast<bf16*>(smem + S::DOL);
   float* vg = reinterpret_cast<float*>(smem + S::VEC);
   float* vred = vg + C;
   const int64_t item = (int64_t)j * p.HV + hv;
-  const bf16* sin_g = reinterpret_cast<const bf16*>(p.s_in) + item * 2 * D * D;
+  const bf16* sin_g = reinterpret_cast<const bf16*>(p.s_in) + item * 2 * D * D + col0;
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
 
-  load_rows<D, DP>(sSH, sin_g, D, D, tid, 256);
-  load_rows<D, DP>(sSL, sin_g + D * D, D, D, tid, 256);
+  load_rows<HD, HPD>(sSH, sin_g, D, D, tid, 256);
+  load_rows<HD, HPD>(sSL, sin_g + D * D, D, D, tid, 256);
   load_tokens<D>(sDO, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, ct.y, ct.z, tid, 256);
   load_rows<D, DP>(sDUH, du_g, D, C, tid, 256);
   load_rows<D, DP>(sDUL, du_g + C * D, D, C, tid, 256);
-  load_rows<D, DP>(sUH, u_g, D, C, tid, 256);
-  load_rows<D, DP>(sUL, u_g + C * D, D, C, tid, 256);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   cp_async_commit();
   cp_async_wait<0>();
@@ -820,39 +820,42 @@ __global__ void __launch_bounds__(256, 1) bwd_sgrad_kernel(BwdParams p) {
   }
   const bf16* doh = reinterpret_cast<const bf16*>(sDO);
 
-  // [dO; dU] S_in: warp tiles of 32 rows x D/2 columns; row blocks 0, 1 of dO and 0, 1 of dU
+  // [dO; dU] S_in[:, half]: warp tiles of 32 rows x D/4 columns; row blocks 0, 1 of dO and 0, 1 of dU
   {
-    constexpr int NT = D / 16;
-    const int rb = warp & 3, m0 = 32 * (rb & 1), n0 = (D / 2) * (warp >> 2);
+    constexpr int NT = D / 32;
+    const int rb = warp & 3, m0 = 32 * (rb & 1), n0 = (D / 4) * (warp >> 2);
     float acc[2][NT][4];
     wm::zero(acc);
     if (rb < 2) {
-      wm::pgemm<2, NT, false, true, XS, true>(acc, doh, sDOL, DP, sSH, sSL, DP, m0, n0, 0, D);
-      float* out = p.dqa + item * C * D;
+      wm::pgemm<2, NT, false, true, XS, true>(acc, doh, sDOL, DP, sSH, sSL, HPD, m0, n0, 0, D);
+      float* out = p.dqa + item * C * D + col0;
       const float sc = p.scale;
       wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
         const float f = sc * expf(vg[i]);
         *reinterpret_cast<float2*>(out + i * D + c) = make_float2(f * x0, f * x1);
       });
     } else {
-      wm::pgemm<2, NT, false, true, true, true>(acc, sDUH, sDUL, DP, sSH, sSL, DP, m0, n0, 0, D);
-      bf16* out = reinterpret_cast<bf16*>(p.dw) + item * 2 * C * D;  // -dU S_in as planes
+      wm::pgemm<2, NT, false, true, true, true>(acc, sDUH, sDUL, DP, sSH, sSL, HPD, m0, n0, 0, D);
+      bf16* out = reinterpret_cast<bf16*>(p.dw) + item * 2 * C * D + col0;  // -dU S_in as planes
       wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
         wm::store_split2(out + i * D + c, out + C * D + i * D + c, -x0, -x1);
       });
     }
   }
   __syncthreads();
-  // dS_out planes over the S_in planes, with <dS_out, S_in>
+  // U planes over dO and dU; dS_out half planes over the S_in half planes, with <dS_out, S_in> on the half
+  load_rows<D, DP>(sUH, u_g, D, C, tid, 256);
+  load_rows<D, DP>(sUL, u_g + C * D, D, C, tid, 256);
+  cp_async_commit();
   {
-    const bf16* src = reinterpret_cast<const bf16*>(p.ds_out) + item * 2 * D * D;
+    const bf16* src = reinterpret_cast<const bf16*>(p.ds_out) + item * 2 * D * D + col0;
     float part = 0.f;
-    for (int e = tid; e < D * D / 8; e += 256) {
-      const int i = e / (D / 8), c = (e % (D / 8)) * 8;
+    for (int e = tid; e < D * HD / 8; e += 256) {
+      const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
       const uint4 gh = *reinterpret_cast<const uint4*>(src + i * D + c);
       const uint4 gl = *reinterpret_cast<const uint4*>(src + D * D + i * D + c);
-      uint4* yh = reinterpret_cast<uint4*>(sSH + i * DP + c);
-      uint4* yl = reinterpret_cast<uint4*>(sSL + i * DP + c);
+      uint4* yh = reinterpret_cast<uint4*>(sSH + i * HPD + c);
+      uint4* yl = reinterpret_cast<uint4*>(sSL + i * HPD + c);
       const uint4 sh = *yh, sl = *yl;
       const uint32_t a[4] = {gh.x, gh.y, gh.z, gh.w}, b[4] = {gl.x, gl.y, gl.z, gl.w};
       const uint32_t x[4] = {sh.x, sh.y, sh.z, sh.w}, y[4] = {sl.x, sl.y, sl.z, sl.w};
@@ -869,20 +872,21 @@ __global__ void __launch_bounds__(256, 1) bwd_sgrad_kernel(BwdParams p) {
     part = warp_sum(part);
     if (lane == 0) vred[warp] = part;
   }
+  cp_async_wait<0>();
   __syncthreads();
   if (tid == 0) {
     float s = 0.f;
     for (int w = 0; w < 8; ++w) s += vred[w];
-    p.dgc[item] = expf(vg[C - 1]) * s;
+    p.dgc[item * 2 + half] = expf(vg[C - 1]) * s;  // the local kernel adds the two halves
   }
-  // U dS_out (C x D): warp tiles of 32 rows x D/4 columns
+  // U dS_out[:, half] (C x D/2): warp tiles of 16 rows x D/4 columns
   {
     constexpr int NT = D / 32;
-    const int m0 = 32 * (warp & 1), n0 = (D / 4) * (warp >> 1);
-    float acc[2][NT][4];
+    const int m0 = 16 * (warp & 3), n0 = (D / 4) * (warp >> 2);
+    float acc[1][NT][4];
     wm::zero(acc);
-    wm::pgemm<2, NT, false, true, true, true>(acc, sUH, sUL, DP, sSH, sSL, DP, m0, n0, 0, D);
-    float* out = p.dkr + item * C * D;
+    wm::pgemm<1, NT, false, true, true, true>(acc, sUH, sUL, DP, sSH, sSL, HPD, m0, n0, 0, D);
+    float* out = p.dkr + item * C * D + col0;
     wm::for_each_pair(acc, m0, n0, [&](int i, int c, float& x0, float& x1) {
       *reinterpret_cast<float2*>(out + i * D + c) = make_float2(x0, x1);
     });
@@ -1237,7 +1241,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   if (tid == 0) {
     float sr = 0.f;
     for (int i = 0; i < C; ++i) sr += vrow[i];
-    vdg[C - 1] += sr + p.dgc[item];
+    vdg[C - 1] += sr + (p.dgc[2 * item] + p.dgc[2 * item + 1]);
     float run = 0.f;  // d log alpha_i = sum_{i' >= i} dg_i'
     for (int i = C - 1; i >= 0; --i) {
       run += vdg[i];
@@ -1587,7 +1591,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   if (tid == 0) {
     float sr = 0.f;
     for (int i = 0; i < C; ++i) sr += vrow[i];
-    vdg[C - 1] += sr + p.dgc[item];
+    vdg[C - 1] += sr + (p.dgc[2 * item] + p.dgc[2 * item + 1]);
     float run = 0.f;  // d log alpha_i = sum_{i' >= i} dg_i'
     for (int i = C - 1; i >= 0; --i) {
       run += vdg[i];
@@ -1721,7 +1725,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
     n += 2;
   }
   if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D, f16in>::bytes)) != cudaSuccess) return e;
-  bwd_sgrad_kernel<D, E><<<items, 256, SgSmem<D, f16in>::bytes, s>>>(p);
+  bwd_sgrad_kernel<D, E><<<dim3(items.x, items.y, 2), 256, SgSmem<D, f16in>::bytes, s>>>(p);
   if (f16in) {  // fp16 inputs: the generic local kernel
     if ((e = set_smem(bwd_local_kernel<D, E>, LoSmem<D>::bytes)) != cudaSuccess) return e;
     bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);

@@ -21,7 +21,7 @@ struct BwdLayout {
   size_t du;                                        // bf16 [mc][HV][2][C][D]: gradient of U (planes)
   size_t dqa, dkr;                                  // fp32 [mc][HV][C][D]: scale e^g (dO S_in), U dS_out
   size_t dw;                                        // bf16 [mc][HV][2][C][D]: -dU S_in (planes)
-  size_t dgc;                                       // fp32 [mc][HV]: exp(g_C) <dS_out, S_in>
+  size_t dgc;                                       // fp32 [mc][HV][2]: exp(g_C) <dS_out, S_in>, by key-column half
   size_t dqh, dkh;                                  // fp32 [T][HV][D]: gradients of q^, k^ per value head
   size_t dlala;                                     // fp32 [T][HV]: d log alpha * log alpha
   size_t total;
