@@ -307,3 +307,20 @@ def test_backward_replays_in_a_cuda_graph():
     replay["d_state_pool"], direct["d_state_pool"] = replay["d_state_pool"][idx2], direct["d_state_pool"][idx2]
     for k in replay:
         assert np.array_equal(replay[k].astype(np.float64), direct[k]), k
+
+
+def test_backward_of_a_call_without_tokens():
+    """Every sequence empty (total_tokens = 0): each slot's state gradient passes through unchanged, and the
+    gate-parameter gradients are zero."""
+    d = wl.make_inputs(wl.custom("bwd_empty_all", [0, 0, 0], H=2, HV=2, K=64, V=64, chunk_size=64, seed=331,
+                                 pool_size=5))
+    d_out, d_state = upstream(d, 331)
+    g = {k: d[k].cuda() for k in KEYS}
+    res = gdn_chunkwise_backward(*[g[k] for k in KEYS], d_out.cuda(), d_state.cuda(), chunk_size=64, check=True)
+    torch.cuda.synchronize()
+    idx = d["cache_indices"].tolist()
+    for slot in range(5):
+        want = d_state[slot] if slot in idx else torch.zeros_like(d_state[slot])
+        assert torch.equal(res.d_state_pool[slot].cpu(), want)
+    assert torch.all(res.dA_log == 0) and torch.all(res.ddt_bias == 0)
+    assert res.dq.shape[0] == 0 and res.dv.shape[0] == 0
