@@ -47,7 +47,7 @@ __device__ __forceinline__ float softplus_d(float x) { return fmaxf(x, 0.f) + lo
 
 // cache_indices: every slot in [0, pool_size) and no slot twice, for B <= 1024 in one block of
 // 32 ceil(B/32) threads: thread i compares its slot with those of every j < i (branch-free, to
-// its warp's last index) and the block writes the verdict to the status word, GDN_OK included.
+// its warp's last index) and the block writes the outcome to the status word, GDN_OK included.
 __global__ void __launch_bounds__(kCheckOneBlock) decode_check_one_block_kernel(const int64_t* idx, int B,
                                                                                int64_t pool_size, int32_t* status) {
   __shared__ int64_t s_idx[kCheckOneBlock];

@@ -85,7 +85,7 @@ __device__ __forceinline__ void load_gates(const Params& p, int64_t jh, float* s
   __syncthreads();
 }
 
-// All threads: bounded wait; every thread leaves with the same verdict.
+// All threads: bounded wait; every thread leaves with the same outcome.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* status, long long budget) {
   const bool ok = tc::mbar_wait(bar, parity, budget);
   const bool all = __syncthreads_and(ok);

@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       cp_async_commit();
     };
-    // bounded wait with one verdict per warp (the warp then stays converged)
+    // bounded wait with one outcome per warp (the warp then stays converged)
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) {
       const bool ok = wait_or_fail(bar, parity, fail, p.wait_budget);
       return __all_sync(0xffffffffu, ok);

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *fail = 1;
     set_status(p.status, GDN_ERR_TIMEOUT);
   };
-  // bounded wait with one verdict per warp (the warp then stays converged)
+  // bounded wait with one outcome per warp (the warp then stays converged)
   auto wait_warp = [&](int b, uint32_t parity) {
     const bool ok = wait_or_fail(&bars[b], parity, fail, p.wait_budget);
     return __all_sync(0xffffffffu, ok);
