@@ -26,15 +26,21 @@
 //   factor   per (chunk, value head): 1/|q|, 1/|k|, M^{-1}, P, W<-, U~     (parallel)
 //   state    per (chain, block of 16 state rows): S_in of every chunk, U    (sequential in chunks)
 //   dstate   per (chain, block of 16 state rows): dS_out of every chunk, dU, dS_0 (sequential, reversed)
-//   sgrad    per (chunk, value head): scale e^g (dO S_in), -dU S_in, U dS_out, e^{g_C} <dS_out, S_in>
-//   local    per (chunk, value head): dv, db, da, the gradients of q^ and k^ for this value head
-//   norm     per (token, q/k head): the value heads' gradients of q^, k^ summed, through the norm
+//   sgrad    per (chunk, value head, half of the key columns): scale e^g (dO S_in), -dU S_in, U dS_out,
+//            e^{g_C} <dS_out, S_in>
+//   local    per (chunk, value head): dv, db, da, the gradients of q^ and k^ (through the norm when no
+//            value heads share a q/k head)
+//   norm     per (token, q/k head), grouped heads only: the group's gradients of q^, k^ summed, through
+//            the norm
 //   gate_sum per value head: dA_log and ddt_bias, summed over tokens in a fixed order
 // The state rows are independent in both sequential passes (the contractions run over the key
-// dimension and the chunk's tokens), so their CTAs split the value dimension. Every product
-// runs on the tensor cores as warp-level m16n8k16 MMAs (gdn_mma.cuh) with fp32 operands carried
-// as bf16 hi + lo pairs, so the backward keeps about fp32 accuracy; the intermediates between
-// kernels are fp32. Every sum is taken in a fixed order, so the results are deterministic.
+// dimension and the chunk's tokens), so their CTAs split the value dimension; in each CTA eight
+// warps run the chunk step and eight fetch the next chunk's tiles and write the per-chunk
+// outputs. Every product runs on the tensor cores as warp-level m16n8k16 MMAs (gdn_mma.cuh) with
+// fp32 operands carried as bf16 hi + lo pairs, so the backward keeps about fp32 accuracy. The
+// intermediates that later products consume are stored as such pairs (two bf16 planes in the
+// bytes of fp32) and loaded by ldmatrix; the rest are fp32. Every sum is taken in a fixed order,
+// so the results are deterministic.
 #include <type_traits>
 
 #include "gdn_backward.cuh"
