@@ -114,8 +114,10 @@ def test_backward_matches_oracle(name):
     compare(d, got, oracle_backward(d, d_out, d_state))
 
 
-def test_backward_fp16_inputs():
-    d = wl.make_inputs(wl.custom("bwd_fp16", [150, 40], H=2, HV=2, K=128, V=128, chunk_size=64, seed=320,
+@pytest.mark.parametrize("H,HV,K", [(2, 2, 128), (1, 2, 64), (2, 4, 128)])
+def test_backward_fp16_inputs(H, HV, K):
+    """fp16 q, k, v, dO: the generic local kernel, and with grouped heads the norm kernel."""
+    d = wl.make_inputs(wl.custom("bwd_fp16", [150, 40], H=H, HV=HV, K=K, V=K, chunk_size=64, seed=320 + HV + K,
                                  dtype=torch.float16))
     d_out, d_state = upstream(d, 320)
     compare(d, run_backward(d, d_out, d_state), oracle_backward(d, d_out, d_state))
