@@ -209,7 +209,8 @@ size_t gdn_backward_workspace_size(int64_t total_tokens, int32_t batch, int32_t 
       HV > 65535)
     return 0;
   if (!supported_backward_shape(K, V, chunk_size)) return 0;
-  if ((int64_t)batch * HV * (K / 16) > (int64_t)INT32_MAX) return 0;
+  if ((int64_t)batch * HV * (K / 16) > (int64_t)INT32_MAX) return 0;  // grid of the sequential passes
+  if ((total_tokens * H + 7) / 8 > (int64_t)INT32_MAX) return 0;       // grid of the grouped-heads norm kernel
   return gdn::make_bwd_layout(total_tokens, batch, H, HV, K).total;
 }
 

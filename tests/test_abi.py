@@ -152,6 +152,7 @@ def test_backward_workspace_size_rules(lib):
     assert ws(100, 2, 2, 4, 128, 64, 64) == 0      # K != V
     assert ws(100, 2, 2, 4, 128, 128, 32) == 0     # chunk size
     assert ws(100, 2, 1, 1 << 16, 64, 64, 64) == 0  # HV above the grid's y limit
+    assert ws((1 << 31) - 64, 1, 16, 16, 64, 64, 64) == 0  # (T H + 7) / 8 norm blocks above the grid limit
     assert ws(1000, 2, 2, 4, 128, 128, 128) == ws(1000, 2, 2, 4, 128, 128, 64)
     # (C*C*2 + C*D*7 + D*D*2) 4-byte words per (chunk, value head); per (token, value head) one word, plus
     # 2*D for the per-value-head q/k gradients when value heads share a q/k head
