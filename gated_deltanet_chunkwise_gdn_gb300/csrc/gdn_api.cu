@@ -68,6 +68,17 @@ void prof_end(int rec, cudaStream_t s, int kernels = 1) {
   cudaEventRecord(g_prof.recs[rec].stop, s);
 }
 
+// The enqueue of one kernel group of a call: an NVTX range named after the group (nested in the
+// call's range, closed when the scope ends, error returns included) and, while the profiler is on,
+// the group's CUDA-event pair; done() records the end event and counts the group's launches.
+struct LaunchScope {
+  NvtxRange range;
+  int rec;
+  cudaStream_t s;
+  LaunchScope(int id, cudaStream_t stream) : range(kKernelNames[id]), rec(prof_begin(id, stream)), s(stream) {}
+  void done(int kernels = 1) { prof_end(rec, s, kernels); }
+};
+
 bool supported_shape(int K, int V, int C) {
   if (K != V) return false;
   return (K == 64 || K == 128 || K == 256) && (C == 64 || C == 128);
@@ -95,6 +106,32 @@ bool supported_backward_shape(int K, int V, int C) {
 // Largest batch of one single-token step. Above 1024 sequences the slot check runs one block
 // per pair of 256-index tiles: 2^20 sequences take 8.4 M blocks, far inside the grid limit.
 constexpr int32_t kMaxDecodeBatch = 1 << 20;
+
+// K0 of a prefill or backward call: for batches above kScheduleSortMax the multi-block slot check
+// first (it records errors in the zeroed status word), then schedule_kernel.
+gdn_status launch_schedule(const gdn::Params& p, int32_t batch, int64_t pool_size, const int64_t* cache_indices,
+                           cudaStream_t s) {
+  LaunchScope ls(kKernSchedule, s);
+  const bool pre_check = batch > gdn::kScheduleSortMax;
+  if (pre_check) {
+    gdn::DecodeParams dp{};
+    dp.cache_indices = cache_indices;
+    dp.pool_size = pool_size;
+    dp.B = batch;
+    dp.status = p.status;
+    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+    if (gdn::launch_decode_check(dp, s) != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  const size_t sched_smem = gdn::schedule_smem_bytes(batch);
+  if (sched_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(gdn::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sched_smem) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  gdn::schedule_kernel<<<1, 512, sched_smem, s>>>(p, kWyBlock, pre_check ? 1 : 0);
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  ls.done(pre_check ? 2 : 1);
+  return GDN_OK;
+}
 
 }  // namespace
 
@@ -171,35 +208,23 @@ gdn_status gdn_extend_chunkwise(const void* q, const void* k, const void* v, gdn
   p.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
   p.stall = g_stall.load(std::memory_order_relaxed);
 
-  int rec = prof_begin(kKernSchedule, s);
-  const bool pre_check = batch > gdn::kScheduleSortMax;
-  if (pre_check) {  // large batch: the multi-block slot check records errors in the zeroed status word
-    gdn::DecodeParams dp{};
-    dp.cache_indices = cache_indices;
-    dp.pool_size = pool_size;
-    dp.B = batch;
-    dp.status = p.status;
-    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_decode_check(dp, s) != cudaSuccess) return GDN_ERR_CUDA;
-  }
-  const size_t sched_smem = gdn::schedule_smem_bytes(batch);
-  if (sched_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(gdn::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sched_smem) !=
-          cudaSuccess)
-    return GDN_ERR_CUDA;
-  gdn::schedule_kernel<<<1, 512, sched_smem, s>>>(p, kWyBlock, pre_check ? 1 : 0);
-  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s, pre_check ? 2 : 1);
+  if (launch_schedule(p, batch, pool_size, cache_indices, s) != GDN_OK) return GDN_ERR_CUDA;
   if (total_tokens == 0 || batch == 0) return GDN_OK;
-  rec = prof_begin(kKernGates, s);
-  if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
-  rec = prof_begin(kKernIntra, s);
-  if (gdn::launch_intra(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
-  rec = prof_begin(kKernScan, s);
-  if (gdn::launch_scan(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s, p.nseg <= 1 ? 1 : (p.nseg == 2 ? 2 : 3));  // segmented: maps, combine, segments
+  {
+    LaunchScope ls(kKernGates, s);
+    if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done();
+  }
+  {
+    LaunchScope ls(kKernIntra, s);
+    if (gdn::launch_intra(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done();
+  }
+  {
+    LaunchScope ls(kKernScan, s);
+    if (gdn::launch_scan(p, K, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done(p.nseg <= 1 ? 1 : (p.nseg == 2 ? 2 : 3));  // segmented: maps, combine, segments
+  }
   return GDN_OK;
 }
 
@@ -266,30 +291,12 @@ gdn_status gdn_chunkwise_backward(const void* q, const void* k, const void* v, g
   p.beta = reinterpret_cast<float*>(ws + L.beta);
   p.wait_budget = g_wait_budget.load(std::memory_order_relaxed);
 
-  int rec = prof_begin(kKernSchedule, s);
-  const bool pre_check = batch > gdn::kScheduleSortMax;
-  if (pre_check) {
-    gdn::DecodeParams dp{};
-    dp.cache_indices = cache_indices;
-    dp.pool_size = pool_size;
-    dp.B = batch;
-    dp.status = p.status;
-    if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
-    if (gdn::launch_decode_check(dp, s) != cudaSuccess) return GDN_ERR_CUDA;
-  }
-  const size_t sched_smem = gdn::schedule_smem_bytes(batch);
-  if (sched_smem > 48 * 1024 &&
-      cudaFuncSetAttribute(gdn::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sched_smem) !=
-          cudaSuccess)
-    return GDN_ERR_CUDA;
-  gdn::schedule_kernel<<<1, 512, sched_smem, s>>>(p, kWyBlock, pre_check ? 1 : 0);
-  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s, pre_check ? 2 : 1);
+  if (launch_schedule(p, batch, pool_size, cache_indices, s) != GDN_OK) return GDN_ERR_CUDA;
   if (batch == 0) return GDN_OK;
   if (total_tokens > 0) {
-    rec = prof_begin(kKernGates, s);
+    LaunchScope ls(kKernGates, s);
     if (gdn::launch_gates(p, kWyBlock, s) != cudaSuccess) return GDN_ERR_CUDA;
-    prof_end(rec, s);
+    ls.done();
   }
 
   gdn::BwdParams bp{};
@@ -342,10 +349,12 @@ gdn_status gdn_chunkwise_backward(const void* q, const void* k, const void* v, g
   bp.dqh = f(L.dqh);
   bp.dkh = f(L.dkh);
   bp.dlala = f(L.dlala);
-  rec = prof_begin(kKernBackward, s);
-  int kernels = 0;
-  if (gdn::launch_backward(bp, K, dtype == GDN_FP16, s, &kernels) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s, kernels);
+  {
+    LaunchScope ls(kKernBackward, s);
+    int kernels = 0;
+    if (gdn::launch_backward(bp, K, dtype == GDN_FP16, s, &kernels) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done(kernels);
+  }
   return GDN_OK;
 }
 
@@ -389,12 +398,16 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, gdn_dtyp
     if (cudaMemsetAsync(device_status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
     if (batch == 0) return GDN_OK;
   }
-  int rec = prof_begin(kKernDecodeCheck, s);
-  if (gdn::launch_decode_check(p, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
-  rec = prof_begin(kKernDecode, s);
-  if (gdn::launch_decode(p, K, s) != cudaSuccess) return GDN_ERR_CUDA;
-  prof_end(rec, s);
+  {
+    LaunchScope ls(kKernDecodeCheck, s);
+    if (gdn::launch_decode_check(p, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done();
+  }
+  {
+    LaunchScope ls(kKernDecode, s);
+    if (gdn::launch_decode(p, K, s) != cudaSuccess) return GDN_ERR_CUDA;
+    ls.done();
+  }
   return GDN_OK;
 }
 
