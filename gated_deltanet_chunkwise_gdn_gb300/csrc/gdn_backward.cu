@@ -97,6 +97,8 @@ namespace {
 constexpr int C = 64;   // WY block (tokens per chunk)
 constexpr int VB = 16;  // state rows per CTA of the sequential passes
 constexpr int kSeqThreads = 256;  // 8 warps per CTA of the sequential passes
+constexpr int kLocalThreads = 512;  // 16 warps per CTA of the bf16 local kernel
+constexpr int NCW = 4;  // its column warps per 16-row block
 constexpr int CP = C + 4;   // pitch (floats) of C x C fp32 tiles
 constexpr int UP = VB + 4;  // pitch (floats) of C x VB fp32 tiles
 
@@ -926,7 +928,7 @@ struct LoSmem {
 // accumulator tile (rows m0 .. m0 + 15 split over the two warps of a row block; `part` holds the
 // two warps' partial dot products). rn = 1/n per row; raw: the 16-bit rows of x. Every thread
 // of the CTA calls it (it synchronises the CTA).
-template <int D, int NT, typename E>
+template <int D, int NT, int NCW = 2, typename E>
 __device__ __forceinline__ void norm_backward(float (&acc)[1][NT][4], const E* raw, const float* rn, float* part,
                                               int m0, int nd, int len, float* out, int64_t ld) {
   constexpr int DP = D + 8;
@@ -944,7 +946,10 @@ __device__ __forceinline__ void norm_backward(float (&acc)[1][NT][4], const E* r
   __syncthreads();
   wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
     if (i < len) {
-      const float r = rn[i], f = (part[i] + part[64 + i]) * r * r * r;
+      float dot = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) dot += part[64 * w + i];
+      const float r = rn[i], f = dot * r * r * r;
       *reinterpret_cast<float2*>(out + (int64_t)i * ld + c) =
           make_float2(r * x0 - to_f(raw[i * DP + c]) * f, r * x1 - to_f(raw[i * DP + c + 1]) * f);
     }
@@ -1286,14 +1291,14 @@ struct LoFastSmem {
   static constexpr uint32_t CM = PDU + 2 * TILE;     // M^{-1} planes, then A planes
   static constexpr uint32_t P3 = CM + PAIR;
   static constexpr uint32_t P4 = P3 + PAIR;
-  static constexpr int NVEC = 26;                     // vectors of C floats (carved below, in order)
+  static constexpr int NVEC = 40;                     // vectors of C floats (carved below, in order)
   static constexpr uint32_t VEC = P4 + PAIR;
   static constexpr uint32_t bytes = VEC + NVEC * C * 4;
   static_assert(bytes <= 232448, "shared memory per CTA");
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdParams p) {
   using S = LoFastSmem<D>;
   constexpr int DP = S::DP, PP = S::PP, PLN = C * PP;
   constexpr int64_t TPL = C * DP;  // elements from a C x D hi plane to its lo plane
@@ -1327,31 +1332,33 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   float* vdb = vdec + C;     // d beta
   float* vdg = vdb + C;      // d g
   float* vcolp = vdg + C;    // [4][C] column partials (d beta, then the column sums of dGamma . Gamma)
-  float* vrow = vcolp + 4 * C;  // [2][C] row sums of dGamma . Gamma
-  float* vxb = vrow + 2 * C;    // [2][C] row sums of X . K^K^^T
-  float* vpA = vxb + 2 * C;     // [2][C] eg <k^, A^T dW>
-  float* vpB = vpA + 2 * C;     // [2][C] dec <k^, dKr>
-  float* vpC = vpB + 2 * C;     // [2][C] <dQa, q^>
-  float* vnk = vpC + 2 * C;     // [2][C] <k, dk^>
-  float* vnq = vnk + 2 * C;     // [2][C] <q, dq^>
-  static_assert(S::NVEC == 26, "vg .. vnq: 8 single vectors, vcolp 4, vrow, vxb, vpA, vpB, vpC, vnk, vnq 2 each");
+  // row partials below come from the NCW = 4 column warps of a row block
+  float* vrow = vcolp + 4 * C;      // [4][C] row sums of dGamma . Gamma
+  float* vxb = vrow + NCW * C;      // [4][C] row sums of X . K^K^^T
+  float* vpA = vxb + NCW * C;       // [4][C] eg <k^, A^T dW>
+  float* vpB = vpA + NCW * C;       // [4][C] dec <k^, dKr>
+  float* vpC = vpB + NCW * C;       // [4][C] <dQa, q^>
+  float* vnk = vpC + NCW * C;       // [4][C] <k, dk^>
+  float* vnq = vnk + NCW * C;       // [4][C] <q, dq^>
+  static_assert(S::NVEC == 8 + 4 + 7 * NCW, "vg .. vdg single vectors, vcolp 4, the seven partial arrays NCW each");
+  auto sum4 = [&](const float* a, int i) { return (a[i] + a[C + i]) + (a[2 * C + i] + a[3 * C + i]); };
   const bool fused_norm = p.HV == p.H;
 
   const bf16* qin = static_cast<const bf16*>(p.q) + (int64_t)h * D;
   const bf16* kin = static_cast<const bf16*>(p.k) + (int64_t)h * D;
-  load_tokens<D>(tq, qin, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(tk, kin, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(tv, static_cast<const bf16*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
-  load_tokens<D>(tdo, static_cast<const bf16*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_tokens<D>(tq, qin, (int64_t)p.H * D, t0, len, tid, kLocalThreads);
+  load_tokens<D>(tk, kin, (int64_t)p.H * D, t0, len, tid, kLocalThreads);
+  load_tokens<D>(tv, static_cast<const bf16*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, kLocalThreads);
+  load_tokens<D>(tdo, static_cast<const bf16*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, kLocalThreads);
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
   const bf16* mi_g = reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C;
-  load_rows<D, DP>(pu, u_g, D, C, tid, 256);
-  load_rows<D, DP>(pu + TPL, u_g + C * D, D, C, tid, 256);
-  load_rows<D, DP>(pdu, du_g, D, C, tid, 256);
-  load_rows<D, DP>(pdu + TPL, du_g + C * D, D, C, tid, 256);
-  load_rows<C, PP>(cm, mi_g, C, C, tid, 256);
-  load_rows<C, PP>(cm + PLN, mi_g + C * C, C, C, tid, 256);
+  load_rows<D, DP>(pu, u_g, D, C, tid, kLocalThreads);
+  load_rows<D, DP>(pu + TPL, u_g + C * D, D, C, tid, kLocalThreads);
+  load_rows<D, DP>(pdu, du_g, D, C, tid, kLocalThreads);
+  load_rows<D, DP>(pdu + TPL, du_g + C * D, D, C, tid, kLocalThreads);
+  load_rows<C, PP>(cm, mi_g, C, C, tid, kLocalThreads);
+  load_rows<C, PP>(cm + PLN, mi_g + C * C, C, C, tid, kLocalThreads);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
   else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
@@ -1365,36 +1372,36 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   }
 
   // ---- C x C stage: warp tiles rows m0 .. m0 + 15, columns n0 .. n0 + 31
-  const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+  const int m0 = 16 * (warp & 3), n0 = 16 * (warp >> 2);
   const int r = wm::lane_r(), cl = wm::lane_c();
-  float qk[1][4][4], kk[1][4][4], dp[1][4][4], da[1][4][4];
+  float qk[1][2][4], kk[1][2][4], dp[1][2][4], da[1][2][4];
   wm::zero(qk);
   wm::zero(kk);
   wm::zero(dp);
   wm::zero(da);
-  wm::pgemm<1, 4, false, false, false, false>(qk, tq, tq, DP, tk, tk, DP, m0, n0, 0, D);
-  wm::pgemm<1, 4, false, false, false, false>(kk, tk, tk, DP, tk, tk, DP, m0, n0, 0, D);
-  wm::pgemm<1, 4, false, false, false, true>(dp, tdo, tdo, DP, pu, pu + TPL, DP, m0, n0, 0, D);  // dO U^T
-  wm::pgemm<1, 4, false, false, true, false>(da, pdu, pdu + TPL, DP, tv, tv, DP, m0, n0, 0, D);  // dU V^T
+  wm::pgemm<1, 2, false, false, false, false>(qk, tq, tq, DP, tk, tk, DP, m0, n0, 0, D);
+  wm::pgemm<1, 2, false, false, false, false>(kk, tk, tk, DP, tk, tk, DP, m0, n0, 0, D);
+  wm::pgemm<1, 2, false, false, false, true>(dp, tdo, tdo, DP, pu, pu + TPL, DP, m0, n0, 0, D);  // dO U^T
+  wm::pgemm<1, 2, false, false, true, false>(da, pdu, pdu + TPL, DP, tv, tv, DP, m0, n0, 0, D);  // dU V^T
   __syncthreads();  // U, v and dO no longer read; veg, vdec visible
   {
     const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
-    load_rows<D, DP>(pu, dw_g, D, C, tid, 256);
-    load_rows<D, DP>(pu + TPL, dw_g + C * D, D, C, tid, 256);
+    load_rows<D, DP>(pu, dw_g, D, C, tid, kLocalThreads);
+    load_rows<D, DP>(pu + TPL, dw_g + C * D, D, C, tid, kLocalThreads);
     cp_async_commit();
     cp_async_wait<0>();
   }
   __syncthreads();
   {
-    float da2[1][4][4];
+    float da2[1][2][4];
     wm::zero(da2);
-    wm::pgemm<1, 4, false, false, true, false>(da2, pu, pu + TPL, DP, tk, tk, DP, m0, n0, 0, D);  // dW K^T
+    wm::pgemm<1, 2, false, false, true, false>(da2, pu, pu + TPL, DP, tk, tk, DP, m0, n0, 0, D);  // dW K^T
     // dA (on and below the diagonal), Z = Gamma . M^{-1}, d beta (columns), dZ, dGamma (kept in qk),
     // dM^{-1} -> p1, (Gamma . dP) diag(1/|k|) -> p2, diag(1/|q|) (Gamma . dP) -> p3
     const float sc = p.scale;
-    float colp[4][2];
+    float colp[2][2];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < 2; ++jj) {
       colp[jj][0] = colp[jj][1] = 0.f;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1421,7 +1428,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
       }
     }
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
+    for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float s = col_sum(colp[jj][u]);
@@ -1432,9 +1439,9 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   if (tid < C) vdb[tid] = vcolp[tid] + vcolp[C + tid] + vcolp[2 * C + tid] + vcolp[3 * C + tid];
   {
     // T1 = M^{-T} dM^{-1} -> p4 (M^{-T}[i][l] = M^{-1}[l][i], zero for l < i)
-    float t1[1][4][4];
+    float t1[1][2][4];
     wm::zero(t1);
-    wm::pgemm<1, 4, true, true, true, true>(t1, cm, cm + PLN, PP, p1, p1 + PLN, PP, m0, n0, m0, C);
+    wm::pgemm<1, 2, true, true, true, true>(t1, cm, cm + PLN, PP, p1, p1 + PLN, PP, m0, n0, m0, C);
     wm::for_each_pair(t1, m0, n0, [&](int i, int c, float& x0, float& x1) {
       wm::store_split2(p4 + i * PP + c, p4 + PLN + i * PP + c, x0, x1);
     });
@@ -1443,12 +1450,12 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   {
     // X = -T1 M^{-T}, strictly lower (M^{-T}[l][c] = M^{-1}[c][l], zero for l > c) -> p1; with the row sums
     // of X . K^K^^T (d beta) and the row and column sums of dGamma . Gamma (d g)
-    float xx[1][4][4];
+    float xx[1][2][4];
     wm::zero(xx);
-    wm::pgemm<1, 4, false, false, true, true>(xx, p4, p4 + PLN, PP, cm, cm + PLN, PP, m0, n0, 0, n0 + 32);
-    float xb[2] = {0.f, 0.f}, wr[2] = {0.f, 0.f}, wc[4][2];
+    wm::pgemm<1, 2, false, false, true, true>(xx, p4, p4 + PLN, PP, cm, cm + PLN, PP, m0, n0, 0, n0 + 16);
+    float xb[2] = {0.f, 0.f}, wr[2] = {0.f, 0.f}, wc[2][2];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
+    for (int jj = 0; jj < 2; ++jj) {
       wc[jj][0] = wc[jj][1] = 0.f;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -1476,7 +1483,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
     }
     __syncthreads();  // vcolp free again (d beta read it above)
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
+    for (int jj = 0; jj < 2; ++jj)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float s = col_sum(wc[jj][u]);
@@ -1486,7 +1493,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   __syncthreads();
   // A = (Gamma . M^{-1}) diag(beta) in place of M^{-1}; Y = diag(1/|k|) combination of X for the key
   // gradient: Y[i][c] = (beta_i X_ic + beta_c X_ci) / |k_c| -> p4; d beta and the row/column sums of d g
-  for (int e = tid; e < C * C / 2; e += 256) {
+  for (int e = tid; e < C * C / 2; e += kLocalThreads) {
     const int i = e / (C / 2), c = (e % (C / 2)) * 2;
     float a2[2], y2[2];
 #pragma unroll
@@ -1501,14 +1508,14 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   }
   if (tid < C) {
     const int i = tid;
-    vdb[i] += vxb[i] + vxb[C + i];
-    vdg[i] = (vrow[i] + vrow[C + i]) - (vcolp[i] + vcolp[C + i] + vcolp[2 * C + i] + vcolp[3 * C + i]);
+    vdb[i] += sum4(vxb, i);
+    vdg[i] = sum4(vrow, i) - sum4(vcolp, i);
   }
   __syncthreads();
 
   // ---- C x D stage: warp tiles rows m0 .. m0 + 15, columns nd .. nd + D/2
-  constexpr int NT = D / 16;
-  const int nd = (D / 2) * (warp >> 2);
+  constexpr int NT = D / 32;
+  const int nd = (D / 4) * (warp >> 2);
   {
     // dv = A^T dU   (A^T[j][i] = A[i][j], zero for i < j)
     float acc[1][NT][4];
@@ -1552,7 +1559,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
     wm::pgemm<1, NT, true, true, true, false>(acc, p3, p3 + PLN, PP, tq, tq, DP, m0, nd, m0, C);
     wm::pgemm<1, NT, false, true, true, false>(acc, p4, p4 + PLN, PP, tk, tk, DP, m0, nd, 0, C);
     if (fused_norm)
-      norm_backward<D, NT>(acc, tk, vrk, vnk, m0, nd, len, p.dk + (t0 * p.H + h) * D, (int64_t)p.H * D);
+      norm_backward<D, NT, NCW>(acc, tk, vrk, vnk, m0, nd, len, p.dk + (t0 * p.H + h) * D, (int64_t)p.H * D);
     else
       wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
         if (i < len) *reinterpret_cast<float2*>(p.dkh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
@@ -1580,7 +1587,7 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
     }
     wm::pgemm<1, NT, false, true, true, false>(acc, p2, p2 + PLN, PP, tk, tk, DP, m0, nd, 0, m0 + 16);
     if (fused_norm)
-      norm_backward<D, NT>(acc, tq, vrq, vnq, m0, nd, len, p.dq + (t0 * p.H + h) * D, (int64_t)p.H * D);
+      norm_backward<D, NT, NCW>(acc, tq, vrq, vnq, m0, nd, len, p.dq + (t0 * p.H + h) * D, (int64_t)p.H * D);
     else
       wm::for_each_pair(acc, m0, nd, [&](int i, int c, float& x0, float& x1) {
         if (i < len) *reinterpret_cast<float2*>(p.dqh + ((t0 + i) * p.HV + hv) * D + c) = make_float2(x0, x1);
@@ -1589,8 +1596,8 @@ __global__ void __launch_bounds__(256, 1) bwd_local_fast_kernel(BwdParams p) {
   __syncthreads();
   if (tid < C) {
     const int i = tid;
-    const float rb = vpB[i] + vpB[C + i];
-    vdg[i] += (vpC[i] + vpC[C + i]) - rb + (vpA[i] + vpA[C + i]);
+    const float rb = sum4(vpB, i);
+    vdg[i] += sum4(vpC, i) - rb + sum4(vpA, i);
     vrow[i] = rb;  // r_i, for the chunk-end term
   }
   __syncthreads();
@@ -1737,7 +1744,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
     bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
   } else {
     if ((e = set_smem(bwd_local_fast_kernel<D>, LoFastSmem<D>::bytes)) != cudaSuccess) return e;
-    bwd_local_fast_kernel<D><<<items, 256, LoFastSmem<D>::bytes, s>>>(p);
+    bwd_local_fast_kernel<D><<<items, kLocalThreads, LoFastSmem<D>::bytes, s>>>(p);
   }
   n += 2;
   const int64_t rows = p.T * p.H;
