@@ -113,39 +113,46 @@ __device__ __forceinline__ void cp_async_16z(void* smem, const void* gmem, bool 
                "r"(valid ? 16 : 0));
 }
 
+// f(i, q) for every (row i < ROWS, 16-byte piece q < PER) of a tile, spread over NTHR threads. A
+// thread keeps one piece column and steps through rows NTHR / PER apart, so the loop unrolls and the
+// row addresses reduce to one base plus constant strides.
+template <int ROWS, int PER, int NTHR, class F>
+__device__ __forceinline__ void for_pieces(int tid, const F& f) {
+  static_assert(NTHR % PER == 0, "a thread keeps its piece column");
+  constexpr int RP = NTHR / PER;  // rows per sweep of all threads
+  const int q = tid % PER, i0 = tid / PER;
+#pragma unroll
+  for (int m = 0; m < (ROWS + RP - 1) / RP; ++m) {
+    const int i = i0 + m * RP;
+    if (ROWS % RP != 0 && i >= ROWS) break;
+    f(i, q);
+  }
+}
+
 // Token rows t0 .. t0 + C - 1 of a [T][heads][D] 16-bit array (head offset folded into src, row
-// stride ld elements) into smem rows of pitch DP elements; rows at or past len are zero-filled.
-template <int D, typename E>
-__device__ __forceinline__ void load_tokens(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid,
-                                            int nthr) {
-  constexpr int DP = D + 8, PER = D / 8;  // 16-byte pieces per row
-  for (int e = tid; e < C * PER; e += nthr) {
-    const int i = e / PER, q = e % PER;
+// stride ld elements) into smem rows of pitch D + 8 elements; rows at or past len are zero-filled.
+template <int D, int NTHR, typename E>
+__device__ __forceinline__ void load_tokens(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid) {
+  constexpr int DP = D + 8;
+  const E* base = src + t0 * ld;
+  for_pieces<C, D / 8, NTHR>(tid, [&](int i, int q) {
     const bool ok = i < len;
-    const E* s = src + (ok ? (t0 + i) * ld : t0 * ld) + q * 8;
-    cp_async_16z(dst + i * DP + q * 8, s, ok);
-  }
+    cp_async_16z(dst + i * DP + q * 8, base + (ok ? i * ld : 0) + q * 8, ok);
+  });
 }
-// Column block [c0, c0 + W) of the same rows (W a multiple of 8), pitch WP elements.
-template <int W, int WP, typename E>
-__device__ __forceinline__ void load_tokens_cols(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid,
-                                                 int nthr) {
-  constexpr int PER = W / 8;
-  for (int e = tid; e < C * PER; e += nthr) {
-    const int i = e / PER, q = e % PER;
+// Column block [c0, c0 + W) of the same rows (W a multiple of 8, c0 folded into src), pitch WP elements.
+template <int W, int WP, int NTHR, typename E>
+__device__ __forceinline__ void load_tokens_cols(E* dst, const E* src, int64_t ld, int64_t t0, int len, int tid) {
+  const E* base = src + t0 * ld;
+  for_pieces<C, W / 8, NTHR>(tid, [&](int i, int q) {
     const bool ok = i < len;
-    const E* s = src + (ok ? (t0 + i) * ld : t0 * ld) + q * 8;
-    cp_async_16z(dst + i * WP + q * 8, s, ok);
-  }
+    cp_async_16z(dst + i * WP + q * 8, base + (ok ? i * ld : 0) + q * 8, ok);
+  });
 }
-// rows x W fp32 (W a multiple of 4) from a row-major array of row stride ld floats, pitch LD.
-template <int W, int LD>
-__device__ __forceinline__ void load_f32(float* dst, const float* src, int64_t ld, int rows, int tid, int nthr) {
-  constexpr int PER = W / 4;
-  for (int e = tid; e < rows * PER; e += nthr) {
-    const int i = e / PER, q = e % PER;
-    cp_async_16(dst + i * LD + q * 4, src + i * ld + q * 4);
-  }
+// ROWS x W fp32 (W a multiple of 4) from a row-major array of row stride ld floats, pitch LD.
+template <int W, int LD, int ROWS, int NTHR>
+__device__ __forceinline__ void load_f32(float* dst, const float* src, int64_t ld, int tid) {
+  for_pieces<ROWS, W / 4, NTHR>(tid, [&](int i, int q) { cp_async_16(dst + i * LD + q * 4, src + i * ld + q * 4); });
 }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -184,14 +191,10 @@ __device__ __forceinline__ void split_inplace(bf16*, bf16*, int, int, int) {}
 
 // ----------------------------------------------------------------------------- factor
 
-// rows x W bf16 planes (W a multiple of 8) from a row-major array of row stride ld, pitch P.
-template <int W, int P>
-__device__ __forceinline__ void load_rows(bf16* dst, const bf16* src, int64_t ld, int rows, int tid, int nthr) {
-  constexpr int PER = W / 8;
-  for (int e = tid; e < rows * PER; e += nthr) {
-    const int i = e / PER, q = e % PER;
-    cp_async_16(dst + i * P + q * 8, src + i * ld + q * 8);
-  }
+// ROWS x W bf16 plane rows (W a multiple of 8) from a row-major array of row stride ld, pitch P.
+template <int W, int P, int ROWS, int NTHR>
+__device__ __forceinline__ void load_rows(bf16* dst, const bf16* src, int64_t ld, int tid) {
+  for_pieces<ROWS, W / 8, NTHR>(tid, [&](int i, int q) { cp_async_16(dst + i * P + q * 8, src + i * ld + q * 8); });
 }
 
 template <int D, bool XS>
@@ -241,9 +244,9 @@ __global__ void __launch_bounds__(256) bwd_factor_kernel(BwdParams p) {
   float* vrk = vrq + C;
   float* vek = vrk + C;
 
-  load_tokens<D>(sq, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(sk, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(sv, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_tokens<D, 256>(sq, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, 256>(sk, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, 256>(sv, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid);
   cp_async_commit();
   const int64_t item = (int64_t)j * p.HV + hv;
   if (tid < C) {
@@ -448,11 +451,10 @@ __global__ void __launch_bounds__(2 * kSeqThreads) bwd_state_kernel(BwdParams p)
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
     const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
-    load_f32<VB, UP>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, C, ptid,
-                     kSeqThreads);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid);
+    load_f32<VB, UP, C, kSeqThreads>(reinterpret_cast<float*>(base + S::UT), p.ut + item * C * D + jb.vb, D, ptid);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
     if (ptid < 16) cp_async_16(vec + 4 * ptid, p.g + item * C + 4 * ptid);
     else if (ptid < 32) cp_async_16(vec + C + 4 * (ptid - 16), p.rk + item * C + 4 * (ptid - 16));
@@ -611,15 +613,14 @@ __global__ void __launch_bounds__(2 * kSeqThreads) bwd_dstate_kernel(BwdParams p
     const int4 ct = p.chunk_tab[c];
     const int64_t item = (int64_t)c * p.HV + jb.hv;
     const bf16* pp = reinterpret_cast<const bf16*>(p.pm) + item * 2 * C * C;
-    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PH), pp, C, 0, C, ptid, kSeqThreads);
-    load_tokens<C>(reinterpret_cast<bf16*>(base + S::PL), pp + C * C, C, 0, C, ptid, kSeqThreads);
-    load_tokens_cols<VB, HP>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, ptid,
-                             kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, ptid, kSeqThreads);
+    load_tokens<C, kSeqThreads>(reinterpret_cast<bf16*>(base + S::PH), pp, C, 0, C, ptid);
+    load_tokens<C, kSeqThreads>(reinterpret_cast<bf16*>(base + S::PL), pp + C * C, C, 0, C, ptid);
+    load_tokens_cols<VB, HP, kSeqThreads>(reinterpret_cast<E*>(base + S::DO), doin, (int64_t)p.HV * D, ct.y, ct.z, ptid);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<E*>(base + S::K), kin, (int64_t)p.H * D, ct.y, ct.z, ptid);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<E*>(base + S::Q), qin, (int64_t)p.H * D, ct.y, ct.z, ptid);
     const bf16* wp = reinterpret_cast<const bf16*>(p.w) + item * 2 * C * D;
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid, kSeqThreads);
-    load_tokens<D>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid, kSeqThreads);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<bf16*>(base + S::WH), wp, D, 0, C, ptid);
+    load_tokens<D, kSeqThreads>(reinterpret_cast<bf16*>(base + S::WL), wp + C * D, D, 0, C, ptid);
     float* vec = reinterpret_cast<float*>(base + S::VEC);
     if (ptid < 16) cp_async_16(vec + 4 * ptid, p.g + item * C + 4 * ptid);
     else if (ptid < 32) cp_async_16(vec + C + 4 * (ptid - 16), p.rq + item * C + 4 * (ptid - 16));
@@ -755,7 +756,10 @@ __global__ void __launch_bounds__(2 * kSeqThreads) bwd_dstate_kernel(BwdParams p
     }
     if (S::NST == 1 && c - 1 >= jb.c0) {  // one stage: refill it once this chunk is done with it
       __syncthreads();
-      if (producer) issue(c - 1, 0);
+      if (producer) {
+        issue(c - 1, 0);
+        cp_async_commit();  // committed now, so that the next iteration's wait covers it
+      }
     }
   }
   if (!producer) {
@@ -813,11 +817,11 @@ __global__ void __launch_bounds__(256, 2) bwd_sgrad_kernel(BwdParams p) {
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
 
-  load_rows<HD, HPD>(sSH, sin_g, D, D, tid, 256);
-  load_rows<HD, HPD>(sSL, sin_g + D * D, D, D, tid, 256);
-  load_tokens<D>(sDO, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, ct.y, ct.z, tid, 256);
-  load_rows<D, DP>(sDUH, du_g, D, C, tid, 256);
-  load_rows<D, DP>(sDUL, du_g + C * D, D, C, tid, 256);
+  load_rows<HD, HPD, D, 256>(sSH, sin_g, D, tid);
+  load_rows<HD, HPD, D, 256>(sSL, sin_g + D * D, D, tid);
+  load_tokens<D, 256>(sDO, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, ct.y, ct.z, tid);
+  load_rows<D, DP, C, 256>(sDUH, du_g, D, tid);
+  load_rows<D, DP, C, 256>(sDUL, du_g + C * D, D, tid);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   cp_async_commit();
   cp_async_wait<0>();
@@ -852,8 +856,8 @@ __global__ void __launch_bounds__(256, 2) bwd_sgrad_kernel(BwdParams p) {
   }
   __syncthreads();
   // U planes over dO and dU; dS_out half planes over the S_in half planes, with <dS_out, S_in> on the half
-  load_rows<D, DP>(sUH, u_g, D, C, tid, 256);
-  load_rows<D, DP>(sUL, u_g + C * D, D, C, tid, 256);
+  load_rows<D, DP, C, 256>(sUH, u_g, D, tid);
+  load_rows<D, DP, C, 256>(sUL, u_g + C * D, D, tid);
   cp_async_commit();
   {
     const bf16* src = reinterpret_cast<const bf16*>(p.ds_out) + item * 2 * D * D + col0;
@@ -1002,18 +1006,18 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   float* vnq = vnk + 2 * C;     // [2][C] <q, dq^>
   const bool fused_norm = p.HV == p.H;
 
-  load_tokens<D>(rq_t, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(rk_t, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid, 256);
-  load_tokens<D>(rv_t, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
-  load_tokens<D>(rdo_t, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, 256);
+  load_tokens<D, 256>(rq_t, static_cast<const E*>(p.q) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, 256>(rk_t, static_cast<const E*>(p.k) + (int64_t)h * D, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, 256>(rv_t, static_cast<const E*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid);
+  load_tokens<D, 256>(rdo_t, static_cast<const E*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid);
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
-  load_rows<D, DP>(F1, u_g, D, C, tid, 256);
-  load_rows<D, DP>(F1 + FPL, u_g + C * D, D, C, tid, 256);
-  load_rows<D, DP>(F2, du_g, D, C, tid, 256);
-  load_rows<D, DP>(F2 + FPL, du_g + C * D, D, C, tid, 256);
+  load_rows<D, DP, C, 256>(F1, u_g, D, tid);
+  load_rows<D, DP, C, 256>(F1 + FPL, u_g + C * D, D, tid);
+  load_rows<D, DP, C, 256>(F2, du_g, D, tid);
+  load_rows<D, DP, C, 256>(F2 + FPL, du_g + C * D, D, tid);
   bf16* mi_s = reinterpret_cast<bf16*>(C3);  // M^{-1} planes land in C3 (written later) and widen into C1
-  load_rows<C, C>(mi_s, reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C, C, 2 * C, tid, 256);
+  load_rows<C, C, 2 * C, 256>(mi_s, reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C, C, tid);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
   else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
@@ -1057,8 +1061,8 @@ __global__ void __launch_bounds__(256, 1) bwd_local_kernel(BwdParams p) {
   }
   __syncthreads();  // U, v and dO tiles no longer read
   const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
-  load_rows<D, DP>(F1, dw_g, D, C, tid, 256);
-  load_rows<D, DP>(F1 + FPL, dw_g + C * D, D, C, tid, 256);
+  load_rows<D, DP, C, 256>(F1, dw_g, D, tid);
+  load_rows<D, DP, C, 256>(F1 + FPL, dw_g + C * D, D, tid);
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
@@ -1346,19 +1350,19 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
 
   const bf16* qin = static_cast<const bf16*>(p.q) + (int64_t)h * D;
   const bf16* kin = static_cast<const bf16*>(p.k) + (int64_t)h * D;
-  load_tokens<D>(tq, qin, (int64_t)p.H * D, t0, len, tid, kLocalThreads);
-  load_tokens<D>(tk, kin, (int64_t)p.H * D, t0, len, tid, kLocalThreads);
-  load_tokens<D>(tv, static_cast<const bf16*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, kLocalThreads);
-  load_tokens<D>(tdo, static_cast<const bf16*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid, kLocalThreads);
+  load_tokens<D, kLocalThreads>(tq, qin, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, kLocalThreads>(tk, kin, (int64_t)p.H * D, t0, len, tid);
+  load_tokens<D, kLocalThreads>(tv, static_cast<const bf16*>(p.v) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid);
+  load_tokens<D, kLocalThreads>(tdo, static_cast<const bf16*>(p.d_out) + (int64_t)hv * D, (int64_t)p.HV * D, t0, len, tid);
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
   const bf16* mi_g = reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C;
-  load_rows<D, DP>(pu, u_g, D, C, tid, kLocalThreads);
-  load_rows<D, DP>(pu + TPL, u_g + C * D, D, C, tid, kLocalThreads);
-  load_rows<D, DP>(pdu, du_g, D, C, tid, kLocalThreads);
-  load_rows<D, DP>(pdu + TPL, du_g + C * D, D, C, tid, kLocalThreads);
-  load_rows<C, PP>(cm, mi_g, C, C, tid, kLocalThreads);
-  load_rows<C, PP>(cm + PLN, mi_g + C * C, C, C, tid, kLocalThreads);
+  load_rows<D, DP, C, kLocalThreads>(pu, u_g, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pu + TPL, u_g + C * D, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pdu, du_g, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pdu + TPL, du_g + C * D, D, tid);
+  load_rows<C, PP, C, kLocalThreads>(cm, mi_g, C, tid);
+  load_rows<C, PP, C, kLocalThreads>(cm + PLN, mi_g + C * C, C, tid);
   if (tid < 16) cp_async_16(vg + 4 * tid, p.g + item * C + 4 * tid);
   else if (tid < 32) cp_async_16(vbt + 4 * (tid - 16), p.beta + item * C + 4 * (tid - 16));
   else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
@@ -1386,8 +1390,8 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
   __syncthreads();  // U, v and dO no longer read; veg, vdec visible
   {
     const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
-    load_rows<D, DP>(pu, dw_g, D, C, tid, kLocalThreads);
-    load_rows<D, DP>(pu + TPL, dw_g + C * D, D, C, tid, kLocalThreads);
+    load_rows<D, DP, C, kLocalThreads>(pu, dw_g, D, tid);
+    load_rows<D, DP, C, kLocalThreads>(pu + TPL, dw_g + C * D, D, tid);
     cp_async_commit();
     cp_async_wait<0>();
   }
