@@ -773,7 +773,9 @@ __global__ void __launch_bounds__(2 * kSeqThreads) bwd_dstate_kernel(BwdParams p
 // ----------------------------------------------------------------------------- sgrad
 
 // Two CTAs per (chunk, value head), each computing one half of the output columns (the key
-// dimension), so that two CTAs fit on an SM and one's loads overlap the other's products.
+// dimension), so that two CTAs fit on an SM and one's loads overlap the other's products. The two
+// halves of an item are neighbouring blocks (blockIdx.x = 2 chunk + half), so they run at the same
+// time and the second one's reads of dO, dU and U hit L2.
 template <int D, bool XS>
 struct SgSmem {
   static constexpr int DP = D + 8;                   // pitch of C x D tiles and planes
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(256, 2) bwd_sgrad_kernel(BwdParams p) {
   constexpr int DP = S::DP, HD = S::HD, HPD = S::HPD;
   extern __shared__ __align__(128) unsigned char smem[];
   if (p.status[0] != GDN_OK) return;
-  const int j = blockIdx.x, hv = blockIdx.y, half = blockIdx.z;
+  const int j = blockIdx.x >> 1, hv = blockIdx.y, half = blockIdx.x & 1;
   if (j >= p.status[1]) return;
   const int4 ct = p.chunk_tab[j];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -862,24 +864,35 @@ __global__ void __launch_bounds__(256, 2) bwd_sgrad_kernel(BwdParams p) {
   {
     const bf16* src = reinterpret_cast<const bf16*>(p.ds_out) + item * 2 * D * D + col0;
     float part = 0.f;
-    for (int e = tid; e < D * HD / 8; e += 256) {
-      const int i = e / (HD / 8), c = (e % (HD / 8)) * 8;
-      const uint4 gh = *reinterpret_cast<const uint4*>(src + i * D + c);
-      const uint4 gl = *reinterpret_cast<const uint4*>(src + D * D + i * D + c);
-      uint4* yh = reinterpret_cast<uint4*>(sSH + i * HPD + c);
-      uint4* yl = reinterpret_cast<uint4*>(sSL + i * HPD + c);
-      const uint4 sh = *yh, sl = *yl;
-      const uint32_t a[4] = {gh.x, gh.y, gh.z, gh.w}, b[4] = {gl.x, gl.y, gl.z, gl.w};
-      const uint32_t x[4] = {sh.x, sh.y, sh.z, sh.w}, y[4] = {sl.x, sl.y, sl.z, sl.w};
+    constexpr int NPC = D * HD / 8 / 256;           // 16-byte pieces per thread and plane
+    constexpr int BAT = NPC < 4 ? NPC : 4;          // loaded together, before any is used
+    static_assert(NPC % BAT == 0, "piece batches");
+    for (int e0 = 0; e0 < NPC; e0 += BAT) {
+      uint4 gh[BAT], gl[BAT];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 g0 = ElemT<bf16>::unpack(a[u]), g1 = ElemT<bf16>::unpack(b[u]);
-        const float2 s0 = ElemT<bf16>::unpack(x[u]), s1 = ElemT<bf16>::unpack(y[u]);
-        part = fmaf(g0.x + g1.x, s0.x + s1.x, part);
-        part = fmaf(g0.y + g1.y, s0.y + s1.y, part);
+      for (int q = 0; q < BAT; ++q) {
+        const int e = tid + 256 * (e0 + q), i = e / (HD / 8), c = (e % (HD / 8)) * 8;
+        gh[q] = *reinterpret_cast<const uint4*>(src + i * D + c);
+        gl[q] = *reinterpret_cast<const uint4*>(src + D * D + i * D + c);
       }
-      *yh = gh;
-      *yl = gl;
+#pragma unroll
+      for (int q = 0; q < BAT; ++q) {
+        const int e = tid + 256 * (e0 + q), i = e / (HD / 8), c = (e % (HD / 8)) * 8;
+        uint4* yh = reinterpret_cast<uint4*>(sSH + i * HPD + c);
+        uint4* yl = reinterpret_cast<uint4*>(sSL + i * HPD + c);
+        const uint4 sh = *yh, sl = *yl;
+        const uint32_t a[4] = {gh[q].x, gh[q].y, gh[q].z, gh[q].w}, b[4] = {gl[q].x, gl[q].y, gl[q].z, gl[q].w};
+        const uint32_t x[4] = {sh.x, sh.y, sh.z, sh.w}, y[4] = {sl.x, sl.y, sl.z, sl.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 g0 = ElemT<bf16>::unpack(a[u]), g1 = ElemT<bf16>::unpack(b[u]);
+          const float2 s0 = ElemT<bf16>::unpack(x[u]), s1 = ElemT<bf16>::unpack(y[u]);
+          part = fmaf(g0.x + g1.x, s0.x + s1.x, part);
+          part = fmaf(g0.y + g1.y, s0.y + s1.y, part);
+        }
+        *yh = gh[q];
+        *yl = gl[q];
+      }
     }
     part = warp_sum(part);
     if (lane == 0) vred[warp] = part;
@@ -1290,11 +1303,12 @@ struct LoFastSmem {
   static constexpr uint32_t TK = TQ + TILE;
   static constexpr uint32_t R1 = TK + TILE;          // v, dO tiles; after their last use: pairs P1, P2
   static constexpr uint32_t R1B = 2 * TILE > 2 * PAIR ? 2 * TILE : 2 * PAIR;
-  static constexpr uint32_t PU = R1 + R1B;           // U planes, then dW planes
+  static constexpr uint32_t PU = R1 + R1B;           // dW planes
   static constexpr uint32_t PDU = PU + 2 * TILE;     // dU planes
   static constexpr uint32_t CM = PDU + 2 * TILE;     // M^{-1} planes, then A planes
-  static constexpr uint32_t P3 = CM + PAIR;
-  static constexpr uint32_t P4 = P3 + PAIR;
+  static constexpr uint32_t P3 = CM + PAIR;          // U planes (pitch DP, over P3 and P4) until the
+  static constexpr uint32_t P4 = P3 + PAIR;          // first products; then two C x C pairs
+  static_assert(2 * TILE <= 2 * PAIR, "U planes fit over P3, P4");
   static constexpr int NVEC = 40;                     // vectors of C floats (carved below, in order)
   static constexpr uint32_t VEC = P4 + PAIR;
   static constexpr uint32_t bytes = VEC + NVEC * C * 4;
@@ -1322,7 +1336,8 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
   bf16* tdo = reinterpret_cast<bf16*>(smem + S::R1 + S::TILE);
   bf16* p1 = reinterpret_cast<bf16*>(smem + S::R1);           // dM^{-1}, then X
   bf16* p2 = reinterpret_cast<bf16*>(smem + S::R1 + S::PAIR);  // (Gamma . dP) diag(1/|k|)
-  bf16* pu = reinterpret_cast<bf16*>(smem + S::PU);
+  bf16* pu = reinterpret_cast<bf16*>(smem + S::PU);  // dW
+  bf16* pu0 = reinterpret_cast<bf16*>(smem + S::P3);  // U (first products only)
   bf16* pdu = reinterpret_cast<bf16*>(smem + S::PDU);
   bf16* cm = reinterpret_cast<bf16*>(smem + S::CM);
   bf16* p3 = reinterpret_cast<bf16*>(smem + S::P3);  // diag(1/|q|) (Gamma . dP)
@@ -1357,8 +1372,11 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
   const bf16* u_g = reinterpret_cast<const bf16*>(p.u) + item * 2 * C * D;
   const bf16* du_g = reinterpret_cast<const bf16*>(p.du) + item * 2 * C * D;
   const bf16* mi_g = reinterpret_cast<const bf16*>(p.minv) + item * 2 * C * C;
-  load_rows<D, DP, C, kLocalThreads>(pu, u_g, D, tid);
-  load_rows<D, DP, C, kLocalThreads>(pu + TPL, u_g + C * D, D, tid);
+  const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
+  load_rows<D, DP, C, kLocalThreads>(pu0, u_g, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pu0 + TPL, u_g + C * D, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pu, dw_g, D, tid);
+  load_rows<D, DP, C, kLocalThreads>(pu + TPL, dw_g + C * D, D, tid);
   load_rows<D, DP, C, kLocalThreads>(pdu, du_g, D, tid);
   load_rows<D, DP, C, kLocalThreads>(pdu + TPL, du_g + C * D, D, tid);
   load_rows<C, PP, C, kLocalThreads>(cm, mi_g, C, tid);
@@ -1385,17 +1403,9 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
   wm::zero(da);
   wm::pgemm<1, 2, false, false, false, false>(qk, tq, tq, DP, tk, tk, DP, m0, n0, 0, D);
   wm::pgemm<1, 2, false, false, false, false>(kk, tk, tk, DP, tk, tk, DP, m0, n0, 0, D);
-  wm::pgemm<1, 2, false, false, false, true>(dp, tdo, tdo, DP, pu, pu + TPL, DP, m0, n0, 0, D);  // dO U^T
+  wm::pgemm<1, 2, false, false, false, true>(dp, tdo, tdo, DP, pu0, pu0 + TPL, DP, m0, n0, 0, D);  // dO U^T
   wm::pgemm<1, 2, false, false, true, false>(da, pdu, pdu + TPL, DP, tv, tv, DP, m0, n0, 0, D);  // dU V^T
   __syncthreads();  // U, v and dO no longer read; veg, vdec visible
-  {
-    const bf16* dw_g = reinterpret_cast<const bf16*>(p.dw) + item * 2 * C * D;
-    load_rows<D, DP, C, kLocalThreads>(pu, dw_g, D, tid);
-    load_rows<D, DP, C, kLocalThreads>(pu + TPL, dw_g + C * D, D, tid);
-    cp_async_commit();
-    cp_async_wait<0>();
-  }
-  __syncthreads();
   {
     float da2[1][2][4];
     wm::zero(da2);
@@ -1726,6 +1736,7 @@ template <int D, typename E>
 cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
   cudaError_t e;
   int n = 0;
+  if (p.max_chunks > 0x3fffffff) return cudaErrorInvalidConfiguration;  // 2 blocks per chunk in x
   const dim3 items((unsigned)p.max_chunks, (unsigned)p.HV);
   const unsigned chains = (unsigned)((int64_t)p.B * p.HV * (D / VB));
   constexpr bool f16in = kSplitSrc<E>;
@@ -1742,7 +1753,7 @@ cudaError_t launch_all(const BwdParams& p, cudaStream_t s, int* kernels) {
     n += 2;
   }
   if ((e = set_smem(bwd_sgrad_kernel<D, E>, SgSmem<D, f16in>::bytes)) != cudaSuccess) return e;
-  bwd_sgrad_kernel<D, E><<<dim3(items.x, items.y, 2), 256, SgSmem<D, f16in>::bytes, s>>>(p);
+  bwd_sgrad_kernel<D, E><<<dim3(2 * items.x, items.y), 256, SgSmem<D, f16in>::bytes, s>>>(p);
   if (f16in) {  // fp16 inputs: the generic local kernel
     if ((e = set_smem(bwd_local_kernel<D, E>, LoSmem<D>::bytes)) != cudaSuccess) return e;
     bwd_local_kernel<D, E><<<items, 256, LoSmem<D>::bytes, s>>>(p);
