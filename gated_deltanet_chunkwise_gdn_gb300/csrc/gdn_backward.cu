@@ -1386,6 +1386,13 @@ __global__ void __launch_bounds__(kLocalThreads, 1) bwd_local_fast_kernel(BwdPar
   else if (tid < 48) cp_async_16(vrq + 4 * (tid - 32), p.rq + item * C + 4 * (tid - 32));
   else if (tid < 64) cp_async_16(vrk + 4 * (tid - 48), p.rk + item * C + 4 * (tid - 48));
   cp_async_commit();
+  {  // dKr and dQa (fp32, read by the C x D stage's epilogues) into L2 meanwhile: a 128-byte line per thread
+    constexpr int LINES = C * D / 32;  // 128-byte lines of one C x D fp32 tile
+    for (int l = tid; l < 2 * LINES; l += kLocalThreads) {
+      const float* src = l < LINES ? p.dkr + item * C * D + 32 * l : p.dqa + item * C * D + 32 * (l - LINES);
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(src));
+    }
+  }
   cp_async_wait<0>();
   __syncthreads();
   if (tid < C) {
