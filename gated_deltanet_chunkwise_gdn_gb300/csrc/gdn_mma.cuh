@@ -216,12 +216,7 @@ __device__ __forceinline__ float plane_val(const bf16* hi, int64_t off, int64_t 
   return __bfloat162float(hi[off]) + __bfloat162float(hi[off + plane]);
 }
 
-// x (fp32) as the bf16 pair hi + lo, stored to two planes.
-__device__ __forceinline__ void store_split(bf16* hi, bf16* lo, float x) {
-  const bf16 h = __float2bfloat16_rn(x);
-  *hi = h;
-  *lo = __float2bfloat16_rn(x - __bfloat162float(h));
-}
+// (x0, x1) (fp32) as bf16 pairs hi + lo, stored to two planes (4-byte aligned).
 __device__ __forceinline__ void store_split2(bf16* hi, bf16* lo, float x0, float x1) {
   uint32_t h, l;
   split2<bf16>(x0, x1, h, l);
